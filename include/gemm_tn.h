@@ -1,0 +1,154 @@
+/*
+ * gemm_tn.h — C ABI of the GB300 (sm_103a) dense BF16 TN GEMM library.
+ *
+ * Operation (all entry points):
+ *
+ *     D = alpha * A * B^T + beta * C
+ *
+ *   A  M x K bf16, row-major with leading dimension lda >= K (K contiguous)
+ *   B  N x K bf16, row-major with leading dimension ldb >= K (K contiguous)
+ *   C  M x N, same element type as D, row-major, ldc >= N; not read when
+ *      beta == 0 (it may then be NULL and NaN/Inf in it do not propagate)
+ *   D  M x N bf16 or fp32 (out_dtype), row-major, ldd >= N
+ *
+ * Both operands are K-major — the "TN" convention of the
+ * SM80_16x8x16_F32F16F16F32_TN atom named on the FlashAttention SM80 kernel
+ * page (section on the SM80 mainloop).  Products are accumulated in fp32 on
+ * the tensor cores (the GEMM whose work the H100 Nsight Compute page counts
+ * as F = 2MNK, section 7); the epilogue computes alpha*acc + beta*c in fp32
+ * and rounds once to bf16 (round-to-nearest-even) or stores fp32.  The
+ * summation order over K is unspecified.
+ *
+ * Memory: every pointer is a DEVICE pointer owned by the caller.  A, B, C
+ * and D must be 16-byte aligned and lda*2, ldb*2, ldc*esize, ldd*esize must
+ * be multiples of 16 bytes (tensor-memory-accelerator addressing rules);
+ * otherwise GEMM_ERR_MISALIGNED.  D may be the same buffer as C with
+ * ldc == ldd (in-place beta); D must not overlap A or B.
+ *
+ * Asynchrony: calls enqueue work on `stream` (a cudaStream_t, NULL = the
+ * legacy default stream) and return.  The return value covers argument
+ * validation and the launch only.  A device-side failure (a bounded wait
+ * that gave up) is recorded in a per-device status word that
+ * gemm_get_status() reads.
+ *
+ * Degenerate shapes: M == 0 or N == 0 returns GEMM_OK with no launch;
+ * K == 0 gives D = beta * C (or zeros).
+ *
+ * Library-owned memory: the skinny path (M <= 64) uses an fp32 partial-sum
+ * workspace and arrival counters, allocated on the first such call for a
+ * (device, stream) pair and kept until gemm_shutdown().  That first call
+ * must not happen during stream capture.  Calls on different streams use
+ * different workspaces.
+ *
+ * Thread safety: calls may come from several host threads; the last-error
+ * string is per thread.
+ *
+ * Requires a compute capability 10.3 device (sm_103); anything else returns
+ * GEMM_ERR_UNSUPPORTED_DEVICE.
+ */
+#ifndef GEMM_TN_H_
+#define GEMM_TN_H_
+
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef enum {
+  GEMM_OUT_BF16 = 0,
+  GEMM_OUT_F32 = 1
+} gemm_out_dtype;
+
+typedef enum {
+  GEMM_OK = 0,
+  GEMM_ERR_INVALID_VALUE = -1,      /* bad size, stride, dtype or NULL pointer */
+  GEMM_ERR_MISALIGNED = -2,         /* pointer or stride breaks the 16-byte rule */
+  GEMM_ERR_UNSUPPORTED_DEVICE = -3, /* current device is not sm_103 */
+  GEMM_ERR_LAUNCH = -4,             /* CUDA launch or tensor-map encoding failed */
+  GEMM_ERR_TIMEOUT = -5,            /* device: a bounded wait gave up */
+  GEMM_ERR_NOT_IMPLEMENTED = -6,    /* requested path cannot run this shape */
+  GEMM_ERR_OUT_OF_MEMORY = -7,      /* workspace allocation failed */
+  GEMM_ERR_CUDA = -8                /* another CUDA runtime error */
+} gemm_status;
+
+typedef enum {
+  GEMM_PATH_AUTO = 0,   /* choose by shape */
+  GEMM_PATH_1SM = 1,    /* persistent tiled kernel, 128x256 tile, one CTA per SM */
+  GEMM_PATH_2SM = 2,    /* persistent tiled kernel, 256x256 tile per CTA pair */
+  GEMM_PATH_SKINNY = 3  /* M <= 64: swap-AB stream-K HBM streaming of B */
+} gemm_path;
+
+/* Overrides for gemm_bf16_tn_ex (benchmarks, ablations, tests).
+ * Zero-initialise and set only what is needed; 0 means "library default". */
+typedef struct gemm_tn_config {
+  int path;                 /* gemm_path */
+  int grid;                 /* persistent grid size in CTAs (tiled paths), 0 = auto */
+  int raster_group;         /* tiled paths: tiles along M per raster strip, 0 = auto */
+  int skinny_grid;          /* skinny path: number of CTAs (stream-K ranges), 0 = auto */
+  uint64_t wait_timeout_ns; /* device-side wait limit, 0 = default (2 s, or env GEMM_WAIT_TIMEOUT_NS) */
+  int test_fault;           /* tests only: 1 = the producer of CTA 0 drops one stage's loads,
+                               so the consumer's bounded wait must expire (GEMM_ERR_TIMEOUT) */
+} gemm_tn_config;
+
+/* What the last successful launch on this host thread ran. */
+typedef struct gemm_launch_info {
+  int path;          /* gemm_path actually used (0 if no launch) */
+  int grid;          /* CTAs launched */
+  int cluster;       /* CTAs per cluster */
+  int block;         /* threads per CTA */
+  int tile_m;        /* output rows per tile (pair tile for the 2-SM path; 128 for skinny) */
+  int tile_n;        /* output columns per tile (skinny: padded M) */
+  int stages;        /* shared-memory ring depth */
+  int smem_bytes;    /* dynamic shared memory per CTA */
+  const char *kernel;/* kernel name (static string) */
+} gemm_launch_info;
+
+/* D = alpha * A * B^T + beta * C (see the file comment for every argument).
+ * Returns a gemm_status. */
+int gemm_bf16_tn(int64_t M, int64_t N, int64_t K,
+                 const void *A, int64_t lda,
+                 const void *B, int64_t ldb,
+                 const void *C, int64_t ldc,
+                 void *D, int64_t ldd,
+                 float alpha, float beta, int out_dtype, void *stream);
+
+/* Same operation with explicit overrides; cfg may be NULL (= gemm_bf16_tn).
+ * A forced path that cannot run the shape returns GEMM_ERR_NOT_IMPLEMENTED
+ * (GEMM_PATH_SKINNY needs M <= 64). */
+int gemm_bf16_tn_ex(int64_t M, int64_t N, int64_t K,
+                    const void *A, int64_t lda,
+                    const void *B, int64_t ldb,
+                    const void *C, int64_t ldc,
+                    void *D, int64_t ldd,
+                    float alpha, float beta, int out_dtype, void *stream,
+                    const gemm_tn_config *cfg);
+
+/* Synchronises `stream`, then returns and clears the current device's status
+ * word: GEMM_OK, or GEMM_ERR_TIMEOUT if a kernel's bounded wait gave up since
+ * the last call (its output is then undefined).  A CUDA error from the
+ * synchronisation is returned as GEMM_ERR_CUDA. */
+int gemm_get_status(void *stream);
+
+/* Detail word of the last device error: (role << 24) | block index, with
+ * role 1 = producer, 2 = MMA issuer, 3 = epilogue.  0 if none. */
+int gemm_get_status_detail(void);
+
+/* Human-readable text for the last error on this host thread ("" if none). */
+const char *gemm_last_error_string(void);
+
+/* Launch details of the last successful call on this host thread. */
+int gemm_last_launch_info(gemm_launch_info *out);
+
+/* Frees library-owned device memory (skinny workspaces).  Call only when no
+ * GEMM is in flight. */
+void gemm_shutdown(void);
+
+/* Library version, major * 10000 + minor * 100 + patch. */
+int gemm_version(void);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* GEMM_TN_H_ */

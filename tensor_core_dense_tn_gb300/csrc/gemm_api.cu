@@ -1,0 +1,383 @@
+// C-ABI layer: argument validation, tensor-map encoding, path selection,
+// library workspace and the device status word.  See include/gemm_tn.h.
+//
+// Tensor maps (Ampere-to-Hopper page, section "TMA: from copying addresses to
+// copying tensor tiles": base, shape, stride, box, swizzle and out-of-bounds
+// policy in one descriptor) are encoded on the host for every call: A and B
+// with 64x(rows) boxes and 128-byte swizzle so that the shared-memory image
+// is the canonical K-major layout the tcgen05 descriptors describe; C and D
+// with 32x32 boxes for the epilogue.  Out-of-range boxes are zero-filled on
+// load and clipped on store, which is how ragged M, N and K are handled.
+#include <cuda.h>
+#include <cuda_runtime.h>
+
+#include <cstdarg>
+#include <cstdint>
+#include <cstdio>
+#include <cstdlib>
+#include <cstring>
+#include <map>
+#include <mutex>
+#include <string>
+#include <utility>
+
+#include "../../include/gemm_tn.h"
+#include "kernels.h"
+
+namespace gtn {
+namespace {
+
+// Device status word ([0] = code, [1] = detail), one copy per device.
+__device__ int g_status[kStatusWords];
+
+constexpr int kMaxDevices = 64;
+constexpr uint64_t kDefaultTimeoutNs = 2000000000ull;
+
+thread_local std::string t_error;
+thread_local gemm_launch_info t_info = {};
+thread_local int t_last_detail = 0;
+
+int fail(int code, const char* fmt, ...) {
+  char buf[512];
+  va_list ap;
+  va_start(ap, fmt);
+  vsnprintf(buf, sizeof buf, fmt, ap);
+  va_end(ap);
+  t_error = buf;
+  return code;
+}
+
+struct DeviceState {
+  bool ready = false;
+  int cc_major = 0, cc_minor = 0, sms = 0;
+  int* status = nullptr;  // device address of g_status
+};
+
+std::mutex g_mu;
+DeviceState g_dev[kMaxDevices];
+
+struct Workspace {
+  float* partials = nullptr;
+  size_t partial_floats = 0;
+  int* counters = nullptr;
+  size_t counter_ints = 0;
+};
+std::map<std::pair<int, uintptr_t>, Workspace> g_ws;
+
+using EncodeTiledFn = CUresult (*)(CUtensorMap*, CUtensorMapDataType, cuuint32_t, void*, const cuuint64_t*,
+                                   const cuuint64_t*, const cuuint32_t*, const cuuint32_t*, CUtensorMapInterleave,
+                                   CUtensorMapSwizzle, CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
+EncodeTiledFn g_encode = nullptr;
+
+int init_device(int* dev_out, DeviceState** st_out) {
+  int dev = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) return fail(GEMM_ERR_CUDA, "cudaGetDevice: %s", cudaGetErrorString(e));
+  if (dev < 0 || dev >= kMaxDevices) return fail(GEMM_ERR_UNSUPPORTED_DEVICE, "device index %d out of range", dev);
+  std::lock_guard<std::mutex> lk(g_mu);
+  DeviceState& st = g_dev[dev];
+  if (!st.ready) {
+    cudaDeviceProp prop;
+    e = cudaGetDeviceProperties(&prop, dev);
+    if (e != cudaSuccess) return fail(GEMM_ERR_CUDA, "cudaGetDeviceProperties: %s", cudaGetErrorString(e));
+    st.cc_major = prop.major;
+    st.cc_minor = prop.minor;
+    st.sms = prop.multiProcessorCount;
+    if (!(st.cc_major == 10 && st.cc_minor == 3))
+      return fail(GEMM_ERR_UNSUPPORTED_DEVICE, "device %d is sm_%d%d; this library is built for sm_103a", dev,
+                  st.cc_major, st.cc_minor);
+    void* p = nullptr;
+    e = cudaGetSymbolAddress(&p, g_status);
+    if (e != cudaSuccess) return fail(GEMM_ERR_CUDA, "cudaGetSymbolAddress(status): %s", cudaGetErrorString(e));
+    st.status = static_cast<int*>(p);
+    if (!g_encode) {
+      void* fn = nullptr;
+      cudaDriverEntryPointQueryResult q;
+      e = cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &fn, 12000, cudaEnableDefault, &q);
+      if (e != cudaSuccess || q != cudaDriverEntryPointSuccess || !fn)
+        return fail(GEMM_ERR_CUDA, "cuTensorMapEncodeTiled entry point unavailable");
+      g_encode = reinterpret_cast<EncodeTiledFn>(fn);
+    }
+    st.ready = true;
+  }
+  *dev_out = dev;
+  *st_out = &st;
+  return GEMM_OK;
+}
+
+// 2D tensor map over a row-major matrix (inner = contiguous dimension).
+int encode_2d(CUtensorMap* m, CUtensorMapDataType dt, int esize, const void* base, uint64_t inner, uint64_t outer,
+              uint64_t ld_elems, uint32_t box_inner, uint32_t box_outer, CUtensorMapSwizzle sw, const char* what) {
+  cuuint64_t dims[2] = {inner, outer};
+  cuuint64_t strides[1] = {ld_elems * (uint64_t)esize};
+  cuuint32_t box[2] = {box_inner, box_outer};
+  cuuint32_t estr[2] = {1, 1};
+  CUresult r = g_encode(m, dt, 2, const_cast<void*>(base), dims, strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE, sw,
+                        CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  if (r != CUDA_SUCCESS) return fail(GEMM_ERR_LAUNCH, "cuTensorMapEncodeTiled(%s) failed with %d", what, (int)r);
+  return GEMM_OK;
+}
+
+bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+
+uint64_t timeout_ns(const gemm_tn_config* cfg) {
+  if (cfg && cfg->wait_timeout_ns) return cfg->wait_timeout_ns;
+  static uint64_t env = [] {
+    const char* s = getenv("GEMM_WAIT_TIMEOUT_NS");
+    if (s && *s) {
+      unsigned long long v = strtoull(s, nullptr, 10);
+      if (v > 0) return (uint64_t)v;
+    }
+    return kDefaultTimeoutNs;
+  }();
+  return env;
+}
+
+int get_workspace(int dev, cudaStream_t stream, size_t partial_floats, size_t counter_ints, Workspace** out) {
+  std::lock_guard<std::mutex> lk(g_mu);
+  Workspace& w = g_ws[{dev, reinterpret_cast<uintptr_t>(stream)}];
+  if (w.partial_floats < partial_floats || w.counter_ints < counter_ints) {
+    cudaStreamCaptureStatus cs = cudaStreamCaptureStatusNone;
+    cudaStreamIsCapturing(stream, &cs);
+    if (cs != cudaStreamCaptureStatusNone)
+      return fail(GEMM_ERR_INVALID_VALUE, "skinny workspace must be created outside stream capture");
+    // Work already queued may still use the old buffers.
+    cudaError_t e = cudaStreamSynchronize(stream);
+    if (e != cudaSuccess) return fail(GEMM_ERR_CUDA, "cudaStreamSynchronize: %s", cudaGetErrorString(e));
+    if (w.partials) cudaFree(w.partials);
+    if (w.counters) cudaFree(w.counters);
+    w = Workspace{};
+    size_t pf = partial_floats < (1u << 16) ? (1u << 16) : partial_floats;
+    size_t ci = counter_ints < 4096 ? 4096 : counter_ints;
+    if (cudaMalloc(&w.partials, pf * sizeof(float)) != cudaSuccess ||
+        cudaMalloc(&w.counters, ci * sizeof(int)) != cudaSuccess) {
+      if (w.partials) cudaFree(w.partials);
+      w = Workspace{};
+      cudaGetLastError();
+      return fail(GEMM_ERR_OUT_OF_MEMORY, "skinny workspace allocation failed");
+    }
+    e = cudaMemset(w.counters, 0, ci * sizeof(int));
+    if (e != cudaSuccess) return fail(GEMM_ERR_CUDA, "cudaMemset: %s", cudaGetErrorString(e));
+    e = cudaDeviceSynchronize();
+    if (e != cudaSuccess) return fail(GEMM_ERR_CUDA, "cudaDeviceSynchronize: %s", cudaGetErrorString(e));
+    w.partial_floats = pf;
+    w.counter_ints = ci;
+  }
+  *out = &w;
+  return GEMM_OK;
+}
+
+int run(int64_t M, int64_t N, int64_t K, const void* A, int64_t lda, const void* B, int64_t ldb, const void* C,
+        int64_t ldc, void* D, int64_t ldd, float alpha, float beta, int out_dtype, void* stream_v,
+        const gemm_tn_config* cfg) {
+  t_error.clear();
+  cudaStream_t stream = static_cast<cudaStream_t>(stream_v);
+  // ---- argument validation
+  if (out_dtype != GEMM_OUT_BF16 && out_dtype != GEMM_OUT_F32)
+    return fail(GEMM_ERR_INVALID_VALUE, "out_dtype must be 0 (bf16) or 1 (fp32), got %d", out_dtype);
+  if (M < 0 || N < 0 || K < 0) return fail(GEMM_ERR_INVALID_VALUE, "negative size M=%lld N=%lld K=%lld",
+                                           (long long)M, (long long)N, (long long)K);
+  const int path_req = cfg ? cfg->path : GEMM_PATH_AUTO;
+  if (path_req < GEMM_PATH_AUTO || path_req > GEMM_PATH_SKINNY)
+    return fail(GEMM_ERR_INVALID_VALUE, "unknown path %d", path_req);
+  if (M == 0 || N == 0) return GEMM_OK;
+  const int64_t kMaxDim = (int64_t)1 << 31;
+  if (M >= kMaxDim || N >= kMaxDim || K >= kMaxDim)
+    return fail(GEMM_ERR_INVALID_VALUE, "sizes must be below 2^31");
+  const bool has_c = (beta != 0.0f);
+  const int esize = out_dtype == GEMM_OUT_F32 ? 4 : 2;
+  if (!D) return fail(GEMM_ERR_INVALID_VALUE, "D is NULL");
+  if (ldd < N) return fail(GEMM_ERR_INVALID_VALUE, "ldd (%lld) < N (%lld)", (long long)ldd, (long long)N);
+  if (has_c) {
+    if (!C) return fail(GEMM_ERR_INVALID_VALUE, "beta != 0 but C is NULL");
+    if (ldc < N) return fail(GEMM_ERR_INVALID_VALUE, "ldc (%lld) < N (%lld)", (long long)ldc, (long long)N);
+  }
+  if (K > 0) {
+    if (!A || !B) return fail(GEMM_ERR_INVALID_VALUE, "A or B is NULL");
+    if (lda < K || ldb < K)
+      return fail(GEMM_ERR_INVALID_VALUE, "lda (%lld) and ldb (%lld) must be >= K (%lld)", (long long)lda,
+                  (long long)ldb, (long long)K);
+    if (!aligned16(A) || !aligned16(B)) return fail(GEMM_ERR_MISALIGNED, "A and B must be 16-byte aligned");
+    if ((lda * 2) % 16 || (ldb * 2) % 16)
+      return fail(GEMM_ERR_MISALIGNED, "lda and ldb must be multiples of 8 elements");
+  }
+  if (!aligned16(D) || (ldd * esize) % 16)
+    return fail(GEMM_ERR_MISALIGNED, "D must be 16-byte aligned with ldd*%d a multiple of 16", esize);
+  if (has_c && (!aligned16(C) || (ldc * esize) % 16))
+    return fail(GEMM_ERR_MISALIGNED, "C must be 16-byte aligned with ldc*%d a multiple of 16", esize);
+
+  int dev = 0;
+  DeviceState* st = nullptr;
+  int rc = init_device(&dev, &st);
+  if (rc != GEMM_OK) return rc;
+
+  // ---- path
+  int path = path_req;
+  if (path == GEMM_PATH_AUTO) {
+    if (K == 0) path = GEMM_PATH_1SM;
+    else if (M <= 64) path = GEMM_PATH_SKINNY;
+    else if (M <= 128) path = GEMM_PATH_1SM;
+    else path = GEMM_PATH_2SM;
+  }
+  if (path == GEMM_PATH_SKINNY && (M > 64 || K == 0))
+    return fail(GEMM_ERR_NOT_IMPLEMENTED, "skinny path needs 1 <= M <= 64 and K > 0");
+
+  const CUtensorMapDataType out_dt = out_dtype == GEMM_OUT_F32 ? CU_TENSOR_MAP_DATA_TYPE_FLOAT32
+                                                                : CU_TENSOR_MAP_DATA_TYPE_BFLOAT16;
+  const uint64_t tmo = timeout_ns(cfg);
+  const int fault = cfg ? cfg->test_fault : 0;
+  LaunchInfo li = {};
+  cudaError_t e;
+
+  if (path == GEMM_PATH_SKINNY) {
+    const int np = (int)((M + 15) / 16) * 16;
+    SkinnyParams p = {};
+    p.M = (int)M; p.N = (int)N; p.K = (int)K; p.np = np;
+    p.num_kb = (int)((K + 63) / 64);
+    p.n_tiles = (int)((N + 127) / 128);
+    p.units = (long long)p.n_tiles * p.num_kb;
+    int grid = (cfg && cfg->skinny_grid > 0) ? cfg->skinny_grid : skinny_max_grid(np, st->sms);
+    if ((long long)grid > p.units) grid = (int)p.units;
+    if (grid < 1) grid = 1;
+    p.grid = grid;
+    p.alpha = alpha; p.beta = beta; p.has_c = has_c;
+    p.C = C; p.ldc = ldc; p.D = D; p.ldd = ldd; p.out_f32 = out_dtype == GEMM_OUT_F32;
+    p.fault = fault; p.timeout_ns = tmo; p.status = st->status;
+    Workspace* w = nullptr;
+    rc = get_workspace(dev, stream, (size_t)grid * 2 * np * 128, (size_t)p.n_tiles * 4, &w);
+    if (rc != GEMM_OK) return rc;
+    p.partials = w->partials;
+    p.counters = w->counters;
+    CUtensorMap tA, tB;
+    if ((rc = encode_2d(&tA, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, A, K, M, lda, 64, np, CU_TENSOR_MAP_SWIZZLE_128B, "A")))
+      return rc;
+    if ((rc = encode_2d(&tB, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, B, K, N, ldb, 64, 128, CU_TENSOR_MAP_SWIZZLE_128B, "B")))
+      return rc;
+    e = launch_skinny(tA, tB, p, stream, &li);
+  } else {
+    const int cg = path == GEMM_PATH_2SM ? 2 : 1;
+    int tile_m, tile_n, b_rows, epi_r, epi_c;
+    tiled_shape(cg, out_dtype == GEMM_OUT_F32, &tile_m, &tile_n, &b_rows, &epi_r, &epi_c);
+    TileParams p = {};
+    p.M = (int)M; p.N = (int)N; p.K = (int)K;
+    p.num_kb = (int)((K + 63) / 64);
+    p.tiles_m = (int)((M + tile_m - 1) / tile_m);
+    p.tiles_n = (int)((N + tile_n - 1) / tile_n);
+    const long long nt = (long long)p.tiles_m * p.tiles_n;
+    if (nt >= kMaxDim) return fail(GEMM_ERR_INVALID_VALUE, "too many tiles");
+    p.num_tiles = (int)nt;
+    int group = cfg && cfg->raster_group > 0 ? cfg->raster_group : 0;
+    if (group == 0) {
+      // keep the A rows of one raster strip within ~64 MiB of L2
+      const long long strip_bytes = (long long)tile_m * (K > 0 ? K : 1) * 2;
+      long long g = (64ll << 20) / strip_bytes;
+      group = (int)(g < 1 ? 1 : g);
+    }
+    if (group > p.tiles_m) group = p.tiles_m;
+    p.raster_group = group;
+    p.alpha = alpha; p.beta = beta; p.has_c = has_c;
+    p.fault = fault; p.timeout_ns = tmo; p.status = st->status;
+    CUtensorMap tA, tB, tC, tD;
+    memset(&tA, 0, sizeof tA);
+    memset(&tB, 0, sizeof tB);
+    memset(&tC, 0, sizeof tC);
+    const CUtensorMapSwizzle out_sw = out_dtype == GEMM_OUT_F32 ? CU_TENSOR_MAP_SWIZZLE_128B : CU_TENSOR_MAP_SWIZZLE_64B;
+    if (K > 0) {
+      if ((rc = encode_2d(&tA, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, A, K, M, lda, 64, 128, CU_TENSOR_MAP_SWIZZLE_128B, "A")))
+        return rc;
+      if ((rc = encode_2d(&tB, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, B, K, N, ldb, 64, b_rows, CU_TENSOR_MAP_SWIZZLE_128B,
+                          "B")))
+        return rc;
+    }
+    if (has_c && (rc = encode_2d(&tC, out_dt, esize, C, N, M, ldc, epi_c, epi_r, out_sw, "C"))) return rc;
+    if ((rc = encode_2d(&tD, out_dt, esize, D, N, M, ldd, epi_c, epi_r, out_sw, "D"))) return rc;
+    e = launch_tiled(cg, out_dtype == GEMM_OUT_F32, tA, tB, tC, tD, p, cfg ? cfg->grid : 0, stream, &li);
+  }
+  if (e != cudaSuccess) {
+    cudaGetLastError();
+    return fail(GEMM_ERR_LAUNCH, "kernel launch failed: %s", cudaGetErrorString(e));
+  }
+  t_info.path = li.path == 3 ? GEMM_PATH_SKINNY : li.path;
+  t_info.grid = li.grid;
+  t_info.cluster = li.cluster;
+  t_info.block = li.block;
+  t_info.tile_m = li.tile_m;
+  t_info.tile_n = li.tile_n;
+  t_info.stages = li.stages;
+  t_info.smem_bytes = li.smem_bytes;
+  t_info.kernel = li.kernel;
+  return GEMM_OK;
+}
+
+}  // namespace
+}  // namespace gtn
+
+extern "C" {
+
+int gemm_bf16_tn(int64_t M, int64_t N, int64_t K, const void* A, int64_t lda, const void* B, int64_t ldb,
+                 const void* C, int64_t ldc, void* D, int64_t ldd, float alpha, float beta, int out_dtype,
+                 void* stream) {
+  return gtn::run(M, N, K, A, lda, B, ldb, C, ldc, D, ldd, alpha, beta, out_dtype, stream, nullptr);
+}
+
+int gemm_bf16_tn_ex(int64_t M, int64_t N, int64_t K, const void* A, int64_t lda, const void* B, int64_t ldb,
+                    const void* C, int64_t ldc, void* D, int64_t ldd, float alpha, float beta, int out_dtype,
+                    void* stream, const gemm_tn_config* cfg) {
+  return gtn::run(M, N, K, A, lda, B, ldb, C, ldc, D, ldd, alpha, beta, out_dtype, stream, cfg);
+}
+
+int gemm_get_status(void* stream) {
+  using namespace gtn;
+  t_error.clear();
+  int dev = 0;
+  DeviceState* st = nullptr;
+  int rc = init_device(&dev, &st);
+  if (rc != GEMM_OK) return rc;
+  cudaError_t e = cudaStreamSynchronize(static_cast<cudaStream_t>(stream));
+  if (e != cudaSuccess) return fail(GEMM_ERR_CUDA, "cudaStreamSynchronize: %s", cudaGetErrorString(e));
+  int h[kStatusWords] = {0, 0};
+  e = cudaMemcpy(h, st->status, sizeof h, cudaMemcpyDeviceToHost);
+  if (e != cudaSuccess) return fail(GEMM_ERR_CUDA, "status read: %s", cudaGetErrorString(e));
+  if (h[0] == 0) return GEMM_OK;
+  int z[kStatusWords] = {0, 0};
+  e = cudaMemcpy(st->status, z, sizeof z, cudaMemcpyHostToDevice);
+  if (e != cudaSuccess) return fail(GEMM_ERR_CUDA, "status clear: %s", cudaGetErrorString(e));
+  {
+    // An aborted skinny kernel can leave arrival counters set: clear them.
+    std::lock_guard<std::mutex> lk(g_mu);
+    for (auto& kv : g_ws)
+      if (kv.first.first == dev && kv.second.counters)
+        cudaMemset(kv.second.counters, 0, kv.second.counter_ints * sizeof(int));
+  }
+  cudaDeviceSynchronize();
+  t_last_detail = h[1];
+  return fail(h[0], "device wait timed out (role %d, block %d)", h[1] >> 24, h[1] & 0xFFFFFF);
+}
+
+int gemm_get_status_detail(void) { return gtn::t_last_detail; }
+
+const char* gemm_last_error_string(void) { return gtn::t_error.c_str(); }
+
+int gemm_last_launch_info(gemm_launch_info* out) {
+  if (!out) return GEMM_ERR_INVALID_VALUE;
+  *out = gtn::t_info;
+  return GEMM_OK;
+}
+
+void gemm_shutdown(void) {
+  using namespace gtn;
+  std::lock_guard<std::mutex> lk(g_mu);
+  int cur = 0;
+  cudaGetDevice(&cur);
+  for (auto& kv : g_ws) {
+    cudaSetDevice(kv.first.first);
+    if (kv.second.partials) cudaFree(kv.second.partials);
+    if (kv.second.counters) cudaFree(kv.second.counters);
+  }
+  g_ws.clear();
+  cudaSetDevice(cur);
+}
+
+int gemm_version(void) { return 100; }
+
+}  // extern "C"

@@ -1,0 +1,472 @@
+// Persistent, warp-specialised BF16 TN GEMM on tcgen05 (sm_103a).
+//
+//   D[M,N] = alpha * A[M,K] * B[N,K]^T + beta * C[M,N]     (fp32 accumulate)
+//
+// Structure (one CTA per SM, 6 warps):
+//   warp 0 lane 0   TMA producer: fills a ring of shared-memory stages with
+//                   128x64 A tiles and (BN/CG)x64 B tiles (128-byte swizzle),
+//                   each stage guarded by a FULL / EMPTY mbarrier pair — the
+//                   per-stage ownership state machine of the Ampere-to-Hopper
+//                   page (section "a stage maintains two kinds of ownership")
+//                   and the transaction-count completion of its section
+//                   "Transaction Barrier".
+//   warp 1          allocates Tensor Memory; lane 0 issues tcgen05.mma for
+//                   the whole CTA (or CTA pair) into one of two TMEM
+//                   accumulators and releases stages with tcgen05.commit —
+//                   the single-thread MMA issue, TMEM accumulator and 2-SM
+//                   pair MMA of the SemiAnalysis Blackwell page ("Blackwell
+//                   architecture features", "5th-generation tensor core MMA").
+//   warps 2..5      epilogue: tcgen05.ld 32 columns at a time, alpha/beta,
+//                   bf16 rounding, swizzled staging in shared memory and a TMA
+//                   store that clips rows/columns outside D (the hardware
+//                   out-of-bounds handling of the Ampere-to-Hopper page's TMA
+//                   section).  Two TMEM accumulators let the epilogue of tile
+//                   i overlap the mainloop of tile i+1.
+//
+// CG = 2 runs the pair form: cluster of two CTAs on one TPC, MMA M = 256,
+// each CTA loads its own 128 rows of A and half of the B tile, the leader
+// CTA issues the MMA for both and the accumulator rows stay in each CTA's
+// own TMEM.  No TMA multicast is used; each CTA loads its own tiles.
+//
+// Every mbarrier wait is bounded by %globaltimer.  A wait that gives up sets
+// a CTA abort flag and the device status word; all roles then leave their
+// loops, drain what they issued and free TMEM, so the kernel always returns.
+#include <cuda.h>
+#include <cuda_runtime.h>
+
+#include <cstdint>
+
+#include "kernels.h"
+#include "ptx.cuh"
+
+namespace gtn {
+
+namespace {
+
+constexpr int kBK = 64;           // K elements per stage (128 bytes of bf16)
+constexpr int kUmmaK = 16;        // K per tcgen05.mma (kind::f16)
+constexpr int kEpiWarps = 4;
+constexpr int kThreads = 64 + 32 * kEpiWarps;
+constexpr int kErrTimeout = -5;   // GEMM_ERR_TIMEOUT
+
+template <int CG, bool OUT_F32>
+struct Cfg {
+  static constexpr int BN = 256;                      // tile N (MMA N)
+  static constexpr int TILE_M = 128 * CG;             // rows per (pair) tile = MMA M
+  static constexpr int B_ROWS = BN / CG;              // B rows loaded per CTA
+  static constexpr int A_BYTES = 128 * kBK * 2;       // 16 KiB
+  static constexpr int B_BYTES = B_ROWS * kBK * 2;
+  static constexpr int STAGES = (CG == 1) ? 4 : 6;
+  static constexpr uint32_t STAGE_TX = (A_BYTES + B_BYTES) * CG;
+  static constexpr int OUT_BYTES = OUT_F32 ? 4 : 2;
+  static constexpr int EPI_COLS = 32;
+  static constexpr int EPI_BYTES = 32 * EPI_COLS * OUT_BYTES;   // one 32x32 box
+  static constexpr int TMEM_COLS = 2 * BN;            // two accumulators
+  static constexpr int NUM_BARS = 2 * STAGES + 4 + 2 * kEpiWarps + 1;
+  static constexpr int RING_BYTES = STAGES * (A_BYTES + B_BYTES);
+  static constexpr int EPI_TOTAL = kEpiWarps * 2 * EPI_BYTES;
+  static constexpr int SMEM = 1024 + RING_BYTES + EPI_TOTAL + NUM_BARS * 8 + 16;
+  static_assert(SMEM <= 232448, "shared memory budget");
+  static_assert(TMEM_COLS <= 512, "TMEM columns");
+};
+
+struct Abort {
+  volatile uint32_t* flag;
+  uint64_t timeout_ns;
+  int* status;
+  int role;
+};
+
+template <bool CLUSTER>
+__device__ __forceinline__ bool try_wait(uint32_t bar, uint32_t parity) {
+  if constexpr (CLUSTER) return mbar_try_wait_cluster(bar, parity);
+  else return mbar_try_wait(bar, parity);
+}
+
+// Bounded wait on an mbarrier phase.  Returns false if this CTA is aborting.
+template <bool CLUSTER>
+__device__ __noinline__ bool wait_bar(uint32_t bar, uint32_t parity, const Abort& ab) {
+  if (try_wait<CLUSTER>(bar, parity)) return true;
+  const uint64_t t0 = globaltimer();
+  while (true) {
+#pragma unroll 1
+    for (int i = 0; i < 32; ++i)
+      if (try_wait<CLUSTER>(bar, parity)) return true;
+    if (ab.flag && *ab.flag) return false;
+    if (globaltimer() - t0 > ab.timeout_ns) {
+      if (ab.flag) *ab.flag = 1;
+      if (atomicCAS(ab.status, 0, kErrTimeout) == 0)
+        atomicExch(ab.status + 1, (ab.role << 24) | (int)blockIdx.x);
+      return false;
+    }
+  }
+}
+
+// Spin for `ns` nanoseconds (lets copies already in flight land before exit).
+__device__ __noinline__ void settle(uint64_t ns) {
+  const uint64_t t0 = globaltimer();
+  while (globaltimer() - t0 < ns) __nanosleep(1000);
+}
+
+__device__ __forceinline__ void tile_coords(int t, const TileParams& p, int& tm, int& tn) {
+  const int per_group = p.raster_group * p.tiles_n;
+  const int g = t / per_group;
+  const int first_m = g * p.raster_group;
+  const int gm = min(p.raster_group, p.tiles_m - first_m);
+  const int r = t - g * per_group;
+  tm = first_m + r % gm;
+  tn = r / gm;
+}
+
+template <int CG, bool OUT_F32>
+__global__ void __launch_bounds__(kThreads, 1)
+    gemm_tn_tiled_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
+                         const __grid_constant__ CUtensorMap tmC, const __grid_constant__ CUtensorMap tmD,
+                         const TileParams p) {
+  using C_ = Cfg<CG, OUT_F32>;
+  constexpr bool kCluster = (CG == 2);
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+  const uint32_t sA = smem_u32(smem);
+  const uint32_t sB = sA + C_::STAGES * C_::A_BYTES;
+  const uint32_t sE = sA + C_::RING_BYTES;
+  uint64_t* bars = reinterpret_cast<uint64_t*>(smem + C_::RING_BYTES + C_::EPI_TOTAL);
+  const uint32_t bar0 = smem_u32(bars);
+  auto full_bar = [&](int s) { return bar0 + 8u * s; };
+  auto empty_bar = [&](int s) { return bar0 + 8u * (C_::STAGES + s); };
+  auto accf_bar = [&](int b) { return bar0 + 8u * (2 * C_::STAGES + b); };
+  auto acce_bar = [&](int b) { return bar0 + 8u * (2 * C_::STAGES + 2 + b); };
+  auto c_bar = [&](int w, int b) { return bar0 + 8u * (2 * C_::STAGES + 4 + 2 * w + b); };
+  const uint32_t drain_bar = bar0 + 8u * (C_::NUM_BARS - 1);
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bars + C_::NUM_BARS);
+  volatile uint32_t* abort_flag = tmem_slot + 1;
+
+  const int warp = threadIdx.x >> 5;
+  const int lane = threadIdx.x & 31;
+  const uint32_t rank = kCluster ? cluster_ctarank() : 0;
+  const bool leader = (rank == 0);
+  const int cluster_id = blockIdx.x / CG;
+  const int num_clusters = gridDim.x / CG;
+
+  if (threadIdx.x == 0) {
+    for (int s = 0; s < C_::STAGES; ++s) {
+      mbar_init(full_bar(s), 1);
+      mbar_init(empty_bar(s), 1);
+    }
+    for (int b = 0; b < 2; ++b) {
+      mbar_init(accf_bar(b), 1);
+      mbar_init(acce_bar(b), kEpiWarps * CG);
+    }
+    for (int w = 0; w < kEpiWarps; ++w)
+      for (int b = 0; b < 2; ++b) mbar_init(c_bar(w, b), 1);
+    mbar_init(drain_bar, 1);
+    *abort_flag = 0;
+    fence_mbar_init();
+    fence_proxy_async_smem();
+  }
+  if (warp == 0 && lane == 0) {
+    if (p.num_kb > 0) {
+      tma_prefetch_desc(&tmA);
+      tma_prefetch_desc(&tmB);
+    }
+    if (p.has_c) tma_prefetch_desc(&tmC);
+    tma_prefetch_desc(&tmD);
+  }
+  if (warp == 1) tmem_alloc<CG>(smem_u32(tmem_slot), C_::TMEM_COLS);
+  tc_fence_before();
+  __syncthreads();
+  if constexpr (kCluster) cluster_sync();
+  tc_fence_after();
+  const uint32_t tmem_base = *tmem_slot;
+
+  if (warp == 0) {
+    // ------------------------------------------------------------ producer
+    if (lane == 0) {
+      Abort ab{abort_flag, p.timeout_ns, p.status, kRoleProducer};
+      bool ok = true;
+      bool skip_once = (p.fault & kFaultSkipTmaOnce) && blockIdx.x == 0;
+      int stage = 0;
+      uint32_t phase = 0;
+      for (int t = cluster_id; t < p.num_tiles && ok; t += num_clusters) {
+        int tm, tn;
+        tile_coords(t, p, tm, tn);
+        const int a_row = tm * C_::TILE_M + (int)rank * 128;
+        const int b_row = tn * C_::BN + (int)rank * C_::B_ROWS;
+        for (int kb = 0; kb < p.num_kb; ++kb) {
+          if (!wait_bar<kCluster>(empty_bar(stage), phase ^ 1, ab)) {
+            ok = false;
+            break;
+          }
+          const uint32_t fb = full_bar(stage);
+          if (leader) mbar_arrive_expect_tx(fb, C_::STAGE_TX);
+          if (skip_once) {
+            skip_once = false;  // test-only: leave this stage's bytes missing
+          } else if constexpr (CG == 1) {
+            tma_load_2d(sA + stage * C_::A_BYTES, &tmA, kb * kBK, a_row, fb);
+            tma_load_2d(sB + stage * C_::B_BYTES, &tmB, kb * kBK, b_row, fb);
+          } else {
+            const uint32_t fb_leader = mapa_shared(fb, 0);
+            tma_load_2d_pair(sA + stage * C_::A_BYTES, &tmA, kb * kBK, a_row, fb_leader);
+            tma_load_2d_pair(sB + stage * C_::B_BYTES, &tmB, kb * kBK, b_row, fb_leader);
+          }
+          if (++stage == C_::STAGES) {
+            stage = 0;
+            phase ^= 1;
+          }
+        }
+      }
+      if (!ok) settle(2000000);  // copies already issued land before teardown
+    }
+  } else if (warp == 1) {
+    // ------------------------------------------------------------ MMA issuer
+    if (lane == 0 && leader) {
+      Abort ab{abort_flag, p.timeout_ns, p.status, kRoleMma};
+      constexpr uint32_t idesc = instr_desc_bf16_f32(C_::TILE_M, C_::BN);
+      bool ok = true;
+      int stage = 0;
+      uint32_t phase = 0;
+      int acc = 0;
+      uint32_t acc_phase = 0;
+      for (int t = cluster_id; t < p.num_tiles && ok; t += num_clusters) {
+        if (!wait_bar<kCluster>(acce_bar(acc), acc_phase ^ 1, ab)) break;
+        tc_fence_after();
+        const uint32_t d_tmem = tmem_base + (uint32_t)(acc * C_::BN);
+        for (int kb = 0; kb < p.num_kb; ++kb) {
+          if (!wait_bar<kCluster>(full_bar(stage), phase, ab)) {
+            ok = false;
+            break;
+          }
+          tc_fence_after();
+          const uint64_t a0 = smem_desc_sw128(sA + stage * C_::A_BYTES);
+          const uint64_t b0 = smem_desc_sw128(sB + stage * C_::B_BYTES);
+#pragma unroll
+          for (int k = 0; k < kBK / kUmmaK; ++k) {
+            // +32 bytes along K inside the swizzle atom = +2 in the encoded address
+            mma_bf16<CG>(d_tmem, a0 + 2 * k, b0 + 2 * k, idesc, (kb | k) != 0);
+          }
+          if constexpr (CG == 1) mma_commit(empty_bar(stage));
+          else mma_commit_pair(empty_bar(stage), 0x3);
+          if (++stage == C_::STAGES) {
+            stage = 0;
+            phase ^= 1;
+          }
+        }
+        if (!ok) break;
+        if constexpr (CG == 1) mma_commit(accf_bar(acc));
+        else mma_commit_pair(accf_bar(acc), 0x3);
+        acc ^= 1;
+        if (acc == 0) acc_phase ^= 1;
+      }
+      // All MMAs issued by this thread complete before TMEM is released.
+      if constexpr (CG == 1) mma_commit(drain_bar);
+      else mma_commit_pair(drain_bar, 0x1);
+      Abort ab_drain{nullptr, p.timeout_ns, p.status, kRoleMma};
+      wait_bar<kCluster>(drain_bar, 0, ab_drain);
+    }
+  } else {
+    // ------------------------------------------------------------ epilogue
+    const int ew = warp - 2;          // staging slot 0..3
+    const int q = warp & 3;           // TMEM lane quarter this warp may access
+    Abort ab{abort_flag, p.timeout_ns, p.status, kRoleEpilogue};
+    int acc = 0;
+    uint32_t acc_phase = 0;
+    uint32_t cphase0 = 0, cphase1 = 0;
+    int buf = 0;
+    const uint32_t acce_target = kCluster ? mapa_shared(acce_bar(0), 0) : acce_bar(0);
+    for (int t = cluster_id; t < p.num_tiles; t += num_clusters) {
+      int tm, tn;
+      tile_coords(t, p, tm, tn);
+      const int row0 = tm * C_::TILE_M + (int)rank * 128 + q * 32;
+      if (!wait_bar<kCluster>(accf_bar(acc), acc_phase, ab)) break;
+      tc_fence_after();
+#pragma unroll 1
+      for (int c = 0; c < C_::BN / C_::EPI_COLS; ++c) {
+        const int col0 = tn * C_::BN + c * C_::EPI_COLS;
+        uint32_t r[32];
+        if (p.num_kb > 0) {
+          tmem_ld_32x32b_x32(tmem_base + ((uint32_t)(q * 32) << 16) + (uint32_t)(acc * C_::BN + c * 32), r);
+          tmem_wait_ld();
+        } else {
+#pragma unroll
+          for (int j = 0; j < 32; ++j) r[j] = 0;
+        }
+        if (c == C_::BN / C_::EPI_COLS - 1) {
+          // accumulator fully read: hand it back to the MMA warp
+          tc_fence_before();
+          __syncwarp();
+          if (lane == 0) {
+            if constexpr (kCluster) mbar_arrive_cluster(acce_target + 8u * acc);
+            else mbar_arrive(acce_bar(acc));
+          }
+        }
+        if (row0 >= p.M || col0 >= p.N) continue;  // box entirely outside D
+        const uint32_t sbuf = sE + (uint32_t)((ew * 2 + buf) * C_::EPI_BYTES);
+        if (lane == 0) bulk_wait_read<1>();       // buffer's previous store has read it
+        __syncwarp();
+        float v[32];
+#pragma unroll
+        for (int j = 0; j < 32; ++j) v[j] = p.alpha * __uint_as_float(r[j]);
+        if (p.has_c) {
+          const uint32_t cb = c_bar(ew, buf);
+          if (lane == 0) {
+            mbar_arrive_expect_tx(cb, C_::EPI_BYTES);
+            tma_load_2d(sbuf, &tmC, col0, row0, cb);
+          }
+          const uint32_t par = buf ? cphase1 : cphase0;
+          if (!wait_bar<false>(cb, par, ab)) break;
+          if (buf) cphase1 ^= 1; else cphase0 ^= 1;
+          if constexpr (OUT_F32) {
+#pragma unroll
+            for (int j = 0; j < 8; ++j) {
+              uint32_t x0, x1, x2, x3;
+              ld_shared_v4(sbuf + lane * 128 + ((j ^ (lane & 7)) << 4), x0, x1, x2, x3);
+              v[4 * j + 0] = fmaf(p.beta, __uint_as_float(x0), v[4 * j + 0]);
+              v[4 * j + 1] = fmaf(p.beta, __uint_as_float(x1), v[4 * j + 1]);
+              v[4 * j + 2] = fmaf(p.beta, __uint_as_float(x2), v[4 * j + 2]);
+              v[4 * j + 3] = fmaf(p.beta, __uint_as_float(x3), v[4 * j + 3]);
+            }
+          } else {
+#pragma unroll
+            for (int j = 0; j < 4; ++j) {
+              uint32_t x[4];
+              ld_shared_v4(sbuf + lane * 64 + ((j ^ ((lane >> 1) & 3)) << 4), x[0], x[1], x[2], x[3]);
+#pragma unroll
+              for (int e = 0; e < 4; ++e) {
+                v[8 * j + 2 * e + 0] = fmaf(p.beta, __uint_as_float(x[e] << 16), v[8 * j + 2 * e + 0]);
+                v[8 * j + 2 * e + 1] = fmaf(p.beta, __uint_as_float(x[e] & 0xFFFF0000u), v[8 * j + 2 * e + 1]);
+              }
+            }
+          }
+        }
+        if constexpr (OUT_F32) {
+          // 128-byte rows, 128-byte swizzle: 16-byte chunk j sits at j ^ (row % 8)
+#pragma unroll
+          for (int j = 0; j < 8; ++j)
+            st_shared_v4(sbuf + lane * 128 + ((j ^ (lane & 7)) << 4), __float_as_uint(v[4 * j]),
+                         __float_as_uint(v[4 * j + 1]), __float_as_uint(v[4 * j + 2]),
+                         __float_as_uint(v[4 * j + 3]));
+        } else {
+          // 64-byte rows, 64-byte swizzle: 16-byte chunk j sits at j ^ ((row / 2) % 4)
+#pragma unroll
+          for (int j = 0; j < 4; ++j)
+            st_shared_v4(sbuf + lane * 64 + ((j ^ ((lane >> 1) & 3)) << 4), pack_bf16x2(v[8 * j], v[8 * j + 1]),
+                         pack_bf16x2(v[8 * j + 2], v[8 * j + 3]), pack_bf16x2(v[8 * j + 4], v[8 * j + 5]),
+                         pack_bf16x2(v[8 * j + 6], v[8 * j + 7]));
+        }
+        fence_proxy_async_smem();
+        __syncwarp();
+        if (lane == 0) {
+          tma_store_2d(&tmD, col0, row0, sbuf);
+          bulk_commit();
+        }
+        buf ^= 1;
+      }
+      if (*abort_flag) break;
+      acc ^= 1;
+      if (acc == 0) acc_phase ^= 1;
+    }
+    if (lane == 0) bulk_wait<0>();
+  }
+
+  __syncthreads();
+  if constexpr (kCluster) cluster_sync();
+  if (warp == 1) {
+    tc_fence_after();
+    tmem_dealloc<CG>(tmem_base, C_::TMEM_COLS);
+  }
+}
+
+template <int CG, bool OUT_F32>
+cudaError_t launch_impl(const CUtensorMap& tmA, const CUtensorMap& tmB, const CUtensorMap& tmC,
+                        const CUtensorMap& tmD, const TileParams& p, int grid_override,
+                        cudaStream_t stream, LaunchInfo* info) {
+  using C_ = Cfg<CG, OUT_F32>;
+  auto kern = gemm_tn_tiled_kernel<CG, OUT_F32>;
+  static bool configured[64] = {};
+  int dev = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) return e;
+  if (dev < 64 && !configured[dev]) {
+    e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, C_::SMEM);
+    if (e != cudaSuccess) return e;
+    if (CG == 2) {
+      e = cudaFuncSetAttribute(kern, cudaFuncAttributeNonPortableClusterSizeAllowed, 0);
+      (void)e;
+    }
+    configured[dev] = true;
+  }
+  cudaLaunchConfig_t cfg = {};
+  cudaLaunchAttribute attr[1];
+  cfg.blockDim = dim3(kThreads, 1, 1);
+  cfg.dynamicSmemBytes = C_::SMEM;
+  cfg.stream = stream;
+  int num_attrs = 0;
+  if (CG == 2) {
+    attr[0].id = cudaLaunchAttributeClusterDimension;
+    attr[0].val.clusterDim.x = 2;
+    attr[0].val.clusterDim.y = 1;
+    attr[0].val.clusterDim.z = 1;
+    num_attrs = 1;
+  }
+  cfg.attrs = attr;
+  cfg.numAttrs = num_attrs;
+
+  // Persistent grid: as many CTAs (pairs) as can be co-resident, never more
+  // than there are tiles.
+  int max_units = 0;
+  if (CG == 2) {
+    cfg.gridDim = dim3(2, 1, 1);
+    int clusters = 0;
+    e = cudaOccupancyMaxActiveClusters(&clusters, kern, &cfg);
+    if (e != cudaSuccess) return e;
+    max_units = clusters;
+  } else {
+    int sms = 0;
+    e = cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
+    if (e != cudaSuccess) return e;
+    max_units = sms;
+  }
+  if (max_units < 1) return cudaErrorInvalidConfiguration;
+  int units = p.num_tiles < max_units ? p.num_tiles : max_units;
+  if (grid_override > 0) units = grid_override / CG;
+  if (units < 1) units = 1;
+  cfg.gridDim = dim3(units * CG, 1, 1);
+  if (info) {
+    info->path = CG;
+    info->grid = units * CG;
+    info->cluster = CG;
+    info->block = kThreads;
+    info->tile_m = C_::TILE_M;
+    info->tile_n = C_::BN;
+    info->stages = C_::STAGES;
+    info->smem_bytes = C_::SMEM;
+    info->kernel = CG == 2 ? (OUT_F32 ? "gemm_tn_tiled_kernel<2,f32>" : "gemm_tn_tiled_kernel<2,bf16>")
+                           : (OUT_F32 ? "gemm_tn_tiled_kernel<1,f32>" : "gemm_tn_tiled_kernel<1,bf16>");
+  }
+  return cudaLaunchKernelEx(&cfg, kern, tmA, tmB, tmC, tmD, p);
+}
+
+}  // namespace
+
+void tiled_shape(int cta_group, int out_f32, int* tile_m, int* tile_n, int* b_rows_per_cta, int* epi_rows,
+                 int* epi_cols) {
+  (void)out_f32;
+  *tile_m = 128 * cta_group;
+  *tile_n = 256;
+  *b_rows_per_cta = 256 / cta_group;
+  *epi_rows = 32;
+  *epi_cols = 32;
+}
+
+cudaError_t launch_tiled(int cta_group, int out_f32, const CUtensorMap& tmA, const CUtensorMap& tmB,
+                         const CUtensorMap& tmC, const CUtensorMap& tmD, TileParams p, int grid_override,
+                         cudaStream_t stream, LaunchInfo* info) {
+  if (cta_group == 2) {
+    return out_f32 ? launch_impl<2, true>(tmA, tmB, tmC, tmD, p, grid_override, stream, info)
+                   : launch_impl<2, false>(tmA, tmB, tmC, tmD, p, grid_override, stream, info);
+  }
+  return out_f32 ? launch_impl<1, true>(tmA, tmB, tmC, tmD, p, grid_override, stream, info)
+                 : launch_impl<1, false>(tmA, tmB, tmC, tmD, p, grid_override, stream, info);
+}
+
+}  // namespace gtn

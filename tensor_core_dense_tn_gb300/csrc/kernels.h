@@ -1,0 +1,77 @@
+// Internal interface between the C-ABI layer (gemm_api.cu) and the kernel
+// translation units.  Not installed; the public surface is include/gemm_tn.h.
+#pragma once
+
+#include <cstdint>
+#include <cuda.h>
+#include <cuda_runtime.h>
+
+namespace gtn {
+
+// Device status word: [0] = first error code (0 = none), [1] = detail
+// (role << 24 | block index) of the wait that gave up.
+constexpr int kStatusWords = 2;
+
+enum Role : int { kRoleProducer = 1, kRoleMma = 2, kRoleEpilogue = 3, kRoleFixup = 4 };
+
+// Test-only fault injection bits.
+constexpr int kFaultSkipTmaOnce = 1;
+
+struct TileParams {
+  int M, N, K;
+  int num_kb;          // ceil(K / 64)
+  int tiles_m, tiles_n, num_tiles;
+  int raster_group;    // tiles along M per grouped-raster strip
+  float alpha, beta;
+  int has_c;           // beta != 0
+  int fault;           // kFault* bits (tests only)
+  uint64_t timeout_ns;
+  int* status;
+};
+
+struct SkinnyParams {
+  int M, N, K;
+  int np;              // M rounded up to 16 (MMA N), 16..64
+  int num_kb;          // ceil(K / 64)
+  int n_tiles;         // ceil(N / 128)
+  long long units;     // n_tiles * num_kb
+  int grid;            // CTAs; each owns a contiguous range of units
+  int stages;
+  float alpha, beta;
+  int has_c;
+  const void* C; long long ldc;
+  void* D; long long ldd;
+  int out_f32;
+  float* partials;     // grid * 2 slots * np * 128 floats
+  int* counters;       // 4 per n-tile (one per epilogue warp), zero between calls
+  int fault;
+  uint64_t timeout_ns;
+  int* status;
+};
+
+struct LaunchInfo {
+  int path;            // 1 = 1-SM tiled, 2 = 2-SM tiled, 3 = skinny
+  int grid, cluster, block;
+  int tile_m, tile_n, stages;
+  int smem_bytes;
+  const char* kernel;
+};
+
+// Tiled persistent kernels (1-SM or 2-SM).  Returns a cudaError_t.
+cudaError_t launch_tiled(int cta_group, int out_f32, const CUtensorMap& tmA, const CUtensorMap& tmB,
+                         const CUtensorMap& tmC, const CUtensorMap& tmD, TileParams p, int grid_override,
+                         cudaStream_t stream, LaunchInfo* info);
+
+// Tile shape of the tiled kernels for a CTA group size (for host set-up).
+void tiled_shape(int cta_group, int out_f32, int* tile_m, int* tile_n, int* b_rows_per_cta,
+                 int* epi_rows, int* epi_cols);
+
+// Skinny (M <= 64) swap-AB stream-K kernel.
+cudaError_t launch_skinny(const CUtensorMap& tmA, const CUtensorMap& tmB, SkinnyParams p,
+                          cudaStream_t stream, LaunchInfo* info);
+
+// Largest co-resident grid for the skinny kernel at this np.
+int skinny_max_grid(int np, int num_sms);
+int skinny_stages(int np);
+
+}  // namespace gtn

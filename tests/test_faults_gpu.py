@@ -1,0 +1,42 @@
+"""Bounded device waits: a dropped TMA load must end in GEMM_ERR_TIMEOUT, not a hang.
+
+The test-only fault makes CTA 0's producer arm a stage's transaction count
+without issuing its loads, so the consumer's wait on that stage can never
+complete.  With a short wait limit every role of the kernel gives up, frees
+Tensor Memory and returns; the host reads the status word, and the context
+stays usable for a correct GEMM right after.
+"""
+import numpy as np
+import pytest
+
+import gemm_inputs as gi
+import oracle
+
+pytestmark = pytest.mark.gpu
+
+g = pytest.importorskip("tensor_core_dense_tn_gb300")
+from gpu_util import call, empty_out, from_dev, to_dev_bf16  # noqa: E402
+
+
+@pytest.mark.parametrize("path", [1, 2, 3])
+def test_dropped_load_times_out_then_recovers(path):
+    import torch
+    M = 32 if path == 3 else 512
+    N, K = 768, 512
+    A = gi.draw_bf16(M, K, gi.Dist("int", -4, 4), 77)
+    B = gi.draw_bf16(N, K, gi.Dist("int", -4, 4), 78)
+    dA, dB = to_dev_bf16(A), to_dev_bf16(B)
+    dD, ldd = empty_out(M, N, gi.OUT_F32)
+    rc, st = call(M, N, K, dA, K, dB, K, None, 0, dD, ldd, 1.0, 0.0, gi.OUT_F32, path=path,
+                  timeout_ns=20_000_000, fault=1)
+    assert rc == 0
+    assert st == g.GEMM_ERR_TIMEOUT, (st, g.last_error())
+    assert (g.gemm_get_status_detail() >> 24) in (1, 2, 3)
+    # status is cleared by the read, and the next call is correct
+    s = torch.cuda.current_stream().cuda_stream
+    assert g.gemm_get_status(s) == 0
+    ref, _ = oracle.gemm_ref(A, B)
+    dD2, _ = empty_out(M, N, gi.OUT_F32)
+    rc, st = call(M, N, K, dA, K, dB, K, None, 0, dD2, ldd, 1.0, 0.0, gi.OUT_F32, path=path)
+    assert rc == 0 and st == 0
+    assert np.array_equal(from_dev(dD2, gi.OUT_F32), oracle.exact_f32(ref))

@@ -1,0 +1,322 @@
+"""GPU parity: the CUDA path (through the C ABI) against the CPU oracle.
+
+* integer-valued inputs: bit-exact (every partial sum is an integer < 2^24);
+* real-valued inputs: |D - ref| <= 1e-4 (sum_k |a b| + |beta c|) (+ 1 bf16 ulp);
+* the five workloads at full size — element by element where the oracle is
+  quick, on sampled elements (tile edges included) for the 8192x28672x4096
+  up-projection — in the launch configuration the benchmark uses;
+* edge cases: ragged M/N/K, K = 0, NaN in an unread C, in-place C == D,
+  padding and rows beyond M untouched, determinism, small persistent grids,
+  stream-K splits of the skinny path.
+"""
+import numpy as np
+import pytest
+
+import gemm_inputs as gi
+import oracle
+
+pytestmark = pytest.mark.gpu
+
+g = pytest.importorskip("tensor_core_dense_tn_gb300")
+from gpu_util import call, empty_out, from_dev, sample_positions, to_dev_bf16, to_dev_f32  # noqa: E402
+
+P1, P2, PS = 1, 2, 3
+
+
+def expect_exact(ref, out_dtype):
+    f = oracle.exact_f32(ref)
+    if out_dtype == gi.OUT_F32:
+        return f
+    return gi.f32_to_bf16_bits(f)
+
+
+def up8(x):
+    """Leading dimensions must be multiples of 16 bytes: pad to 8 elements."""
+    return (x + 7) // 8 * 8
+
+
+def run_int(M, N, K, path, out_dtype, seed, lda=None, ldb=None, grid=0, skinny_grid=0, alpha=1.0):
+    lda = up8(K) if lda is None else lda
+    ldb = up8(K) if ldb is None else ldb
+    A = gi.draw_bf16(M, K, gi.Dist("int", -4, 4), seed, ld=lda)
+    B = gi.draw_bf16(N, K, gi.Dist("int", -4, 4), seed + 1, ld=ldb)
+    ref, _ = oracle.gemm_ref(A, B, alpha=alpha, M=M, N=N, K=K, lda=lda, ldb=ldb)
+    dA, dB = to_dev_bf16(A), to_dev_bf16(B)
+    dD, ldd = empty_out(M, N, out_dtype, ld=up8(N))
+    rc, st = call(M, N, K, dA, lda, dB, ldb, None, 0, dD, ldd, alpha, 0.0, out_dtype, path=path,
+                  grid=grid, skinny_grid=skinny_grid)
+    assert rc == 0, g.last_error()
+    assert st == 0, g.last_error()
+    return from_dev(dD, out_dtype)[:, :N], expect_exact(ref, out_dtype)
+
+
+def assert_same(got, exp):
+    if not np.array_equal(got.view(np.uint32) if got.dtype == np.float32 else got,
+                          exp.view(np.uint32) if exp.dtype == np.float32 else exp):
+        bad = np.argwhere(got != exp)
+        pytest.fail(f"{len(bad)} mismatches; first {bad[:5].tolist()}: got {got[tuple(bad[0])]} "
+                    f"expected {exp[tuple(bad[0])]}")
+
+
+# ----------------------------------------------------------------------------- exact
+
+
+@pytest.mark.parametrize("path", [P1, P2, 0])
+def test_tiny_exact_workload(path):
+    w = gi.WORKLOADS[0]
+    A, B, _ = gi.operands(w)
+    ref, _ = oracle.gemm_ref(A, B)
+    dD, ldd = empty_out(w.M, w.N, w.out_dtype)
+    rc, st = call(w.M, w.N, w.K, to_dev_bf16(A), w.K, to_dev_bf16(B), w.K, None, 0, dD, ldd,
+                  w.alpha, w.beta, w.out_dtype, path=path)
+    assert rc == 0 and st == 0, g.last_error()
+    assert_same(from_dev(dD, w.out_dtype), oracle.exact_f32(ref))
+
+
+TILED_SHAPES = [(128, 256, 64), (129, 257, 65), (127, 255, 63), (255, 129, 130), (257, 300, 1),
+                (7, 9, 17), (513, 520, 200), (384, 1024, 320), (1, 1, 1), (96, 40, 8)]
+
+
+@pytest.mark.parametrize("shape", TILED_SHAPES)
+@pytest.mark.parametrize("path", [P1, P2])
+@pytest.mark.parametrize("out_dtype", [gi.OUT_F32, gi.OUT_BF16])
+def test_integer_ragged_tiled(shape, path, out_dtype):
+    M, N, K = shape
+    got, exp = run_int(M, N, K, path, out_dtype, seed=100 + M + 7 * N + 13 * K)
+    assert_same(got, exp)
+
+
+SKINNY_SHAPES = [(16, 256, 256), (1, 300, 70), (16, 1000, 640), (33, 129, 1000), (64, 260, 513),
+                 (5, 8192, 64), (48, 128, 8192)]
+
+
+@pytest.mark.parametrize("shape", SKINNY_SHAPES)
+@pytest.mark.parametrize("out_dtype", [gi.OUT_F32, gi.OUT_BF16])
+def test_integer_ragged_skinny(shape, out_dtype):
+    M, N, K = shape
+    got, exp = run_int(M, N, K, PS, out_dtype, seed=200 + M + 7 * N + 13 * K)
+    assert_same(got, exp)
+
+
+@pytest.mark.parametrize("skinny_grid", [1, 3, 7, 64, 151, 1000])
+def test_skinny_stream_k_partitions(skinny_grid):
+    # every split of the (n-tile, k-block) units must give the same exact result
+    got, exp = run_int(16, 640, 1344, PS, gi.OUT_F32, seed=300, skinny_grid=skinny_grid)
+    assert_same(got, exp)
+
+
+@pytest.mark.parametrize("path,grid", [(P1, 1), (P1, 3), (P2, 2), (P2, 6)])
+def test_small_persistent_grid(path, grid):
+    # few CTAs, many tiles each: ring wrap-around and accumulator double buffering
+    got, exp = run_int(700, 1100, 448, path, gi.OUT_F32, seed=400, grid=grid)
+    assert_same(got, exp)
+
+
+@pytest.mark.parametrize("path", [P1, P2, PS])
+def test_padded_leading_dims(path):
+    M = 40 if path == PS else 300
+    got, exp = run_int(M, 270, 150, path, gi.OUT_BF16, seed=500, lda=168, ldb=256)
+    assert_same(got, exp)
+
+
+@pytest.mark.parametrize("path", [P1, P2, PS])
+def test_alpha_scaling_exact(path):
+    M = 24 if path == PS else 260
+    got1, _ = run_int(M, 300, 200, path, gi.OUT_F32, seed=600)
+    got2, _ = run_int(M, 300, 200, path, gi.OUT_F32, seed=600, alpha=2.0)
+    assert np.array_equal(got2, 2 * got1)
+
+
+# ----------------------------------------------------------------------------- edge cases
+
+
+@pytest.mark.parametrize("out_dtype", [gi.OUT_F32, gi.OUT_BF16])
+def test_k_zero_gives_beta_c(out_dtype):
+    M, N = 300, 264
+    rng = np.random.default_rng(1)
+    Cb = gi.f32_to_bf16_bits(rng.standard_normal((M, N)).astype(np.float32))
+    Cf = gi.bf16_bits_to_f32(Cb)
+    dC = to_dev_bf16(Cb) if out_dtype == gi.OUT_BF16 else to_dev_f32(Cf)
+    dD, ldd = empty_out(M, N, out_dtype)
+    rc, st = call(M, N, 0, None, 0, None, 0, dC, N, dD, ldd, 1.0, 0.5, out_dtype)
+    assert rc == 0 and st == 0, g.last_error()
+    got = oracle.decode_out(from_dev(dD, out_dtype), out_dtype)
+    assert np.array_equal(got, 0.5 * Cf.astype(np.float64))
+    dD2, _ = empty_out(M, N, out_dtype)
+    rc, st = call(M, N, 0, None, 0, None, 0, None, 0, dD2, ldd, 1.0, 0.0, out_dtype)
+    assert rc == 0 and st == 0
+    assert np.all(oracle.decode_out(from_dev(dD2, out_dtype), out_dtype) == 0)
+
+
+@pytest.mark.parametrize("path", [P1, P2, PS])
+def test_beta_zero_does_not_read_nan_c(path):
+    M, N, K = (32 if path == PS else 300), 264, 128
+    A = gi.draw_bf16(M, K, gi.Dist("int", -4, 4), 700)
+    B = gi.draw_bf16(N, K, gi.Dist("int", -4, 4), 701)
+    ref, _ = oracle.gemm_ref(A, B)
+    dC = to_dev_bf16(np.full((M, N), 0x7FC0, dtype=np.uint16))
+    dD, ldd = empty_out(M, N, gi.OUT_BF16)
+    rc, st = call(M, N, K, to_dev_bf16(A), K, to_dev_bf16(B), K, dC, N, dD, ldd, 1.0, 0.0,
+                  gi.OUT_BF16, path=path)
+    assert rc == 0 and st == 0
+    assert_same(from_dev(dD, gi.OUT_BF16), expect_exact(ref, gi.OUT_BF16))
+
+
+@pytest.mark.parametrize("path", [P1, P2, PS])
+def test_in_place_c_equals_d(path):
+    M, N, K = (20 if path == PS else 260), 296, 96
+    A = gi.draw_bf16(M, K, gi.Dist("int", -4, 4), 800)
+    B = gi.draw_bf16(N, K, gi.Dist("int", -4, 4), 801)
+    Cb = gi.draw_bf16(M, N, gi.Dist("int", -8, 8), 802)
+    ref, _ = oracle.gemm_ref(A, B, Cb, 1.0, 0.5)
+    dCD = to_dev_bf16(Cb)
+    rc, st = call(M, N, K, to_dev_bf16(A), K, to_dev_bf16(B), K, dCD, N, dCD, N, 1.0, 0.5,
+                  gi.OUT_BF16, path=path)
+    assert rc == 0 and st == 0
+    assert_same(from_dev(dCD, gi.OUT_BF16), expect_exact(ref, gi.OUT_BF16))
+
+
+@pytest.mark.parametrize("path", [P1, P2, PS])
+@pytest.mark.parametrize("out_dtype", [gi.OUT_F32, gi.OUT_BF16])
+def test_guard_bands_untouched(path, out_dtype):
+    """Row padding (ldd > N) and rows past M keep their canary bits."""
+    import torch
+    M, N, K = (40 if path == PS else 300), 200, 136
+    extra_rows, ldd = 9, 264
+    A = gi.draw_bf16(M, K, gi.Dist("int", -4, 4), 900)
+    B = gi.draw_bf16(N, K, gi.Dist("int", -4, 4), 901)
+    ref, _ = oracle.gemm_ref(A, B)
+    dD, _ = empty_out(M + extra_rows, N, out_dtype, ld=ldd)
+    canary = from_dev(dD, out_dtype).copy()
+    rc, st = call(M, N, K, to_dev_bf16(A), K, to_dev_bf16(B), K, None, 0, dD, ldd, 1.0, 0.0,
+                  out_dtype, path=path)
+    assert rc == 0 and st == 0
+    torch.cuda.synchronize()
+    got = from_dev(dD, out_dtype)
+    assert_same(got[:M, :N], expect_exact(ref, out_dtype))
+    as_bits = (lambda x: x.view(np.uint32)) if out_dtype == gi.OUT_F32 else (lambda x: x)
+    assert np.array_equal(as_bits(got[:M, N:]), as_bits(canary[:M, N:]))
+    assert np.array_equal(as_bits(got[M:]), as_bits(canary[M:]))
+
+
+@pytest.mark.parametrize("path", [P1, P2, PS])
+def test_deterministic(path):
+    M, N, K = (16 if path == PS else 520), 1024, 2048
+    A = gi.draw_bf16(M, K, gi.Dist("normal", 1.0), 1000)
+    B = gi.draw_bf16(N, K, gi.Dist("normal", 1.0 / K), 1001)
+    dA, dB = to_dev_bf16(A), to_dev_bf16(B)
+    outs = []
+    for _ in range(3):
+        dD, ldd = empty_out(M, N, gi.OUT_F32)
+        rc, st = call(M, N, K, dA, K, dB, K, None, 0, dD, ldd, 1.0, 0.0, gi.OUT_F32, path=path)
+        assert rc == 0 and st == 0
+        outs.append(from_dev(dD, gi.OUT_F32).view(np.uint32))
+    assert np.array_equal(outs[0], outs[1]) and np.array_equal(outs[0], outs[2])
+
+
+def test_argument_errors():
+    import torch
+    dA = torch.zeros((64, 64), dtype=torch.bfloat16, device="cuda")
+    dD = torch.zeros((64, 64), dtype=torch.bfloat16, device="cuda")
+    s = torch.cuda.current_stream().cuda_stream
+    base = dict(M=64, N=64, K=64, A=dA.data_ptr(), lda=64, B=dA.data_ptr(), ldb=64, C=0, ldc=0,
+                D=dD.data_ptr(), ldd=64, alpha=1.0, beta=0.0, out_dtype=0, stream=s)
+
+    def rc(**kw):
+        a = dict(base, **kw)
+        return g.gemm_bf16_tn(*a.values())
+
+    assert rc() == g.GEMM_OK
+    assert rc(A=dA.data_ptr() + 2) == g.GEMM_ERR_MISALIGNED
+    assert rc(lda=65) == g.GEMM_ERR_MISALIGNED
+    assert rc(lda=32) == g.GEMM_ERR_INVALID_VALUE
+    assert rc(beta=1.0) == g.GEMM_ERR_INVALID_VALUE
+    assert rc(out_dtype=2) == g.GEMM_ERR_INVALID_VALUE
+    assert rc(M=0) == g.GEMM_OK
+    cfg = g.GemmConfig(path=g.PATH_SKINNY)
+    a = dict(base, M=65)
+    assert g.gemm_bf16_tn_ex(*a.values(), cfg) == g.GEMM_ERR_NOT_IMPLEMENTED
+    torch.cuda.synchronize()
+    assert g.gemm_get_status(s) == 0
+
+
+# ----------------------------------------------------------------------------- tolerance
+
+
+@pytest.mark.parametrize("path", [P1, P2])
+@pytest.mark.parametrize("out_dtype", [gi.OUT_F32, gi.OUT_BF16])
+def test_random_with_beta_tolerance(path, out_dtype):
+    M, N, K = 1000, 1504, 704
+    A = gi.draw_bf16(M, K, gi.Dist("normal", 1.0), 1100)
+    B = gi.draw_bf16(N, K, gi.Dist("normal", 1.0), 1101)
+    if out_dtype == gi.OUT_BF16:
+        C = gi.draw_bf16(M, N, gi.Dist("normal", 1.0), 1102)
+        dC = to_dev_bf16(C)
+        cvals = gi.bf16_bits_to_f32(C)
+    else:
+        C = gi.draw_f32(M, N, gi.Dist("normal", 1.0), 1102)
+        dC = to_dev_f32(C)
+        cvals = C
+    ref, absdot = oracle.gemm_ref(A, B, C, 0.75, -1.25)
+    dD, ldd = empty_out(M, N, out_dtype)
+    rc, st = call(M, N, K, to_dev_bf16(A), K, to_dev_bf16(B), K, dC, N, dD, ldd, 0.75, -1.25,
+                  out_dtype, path=path)
+    assert rc == 0 and st == 0
+    ok, worst, where = oracle.check(from_dev(dD, out_dtype), ref, absdot, out_dtype, -1.25, cvals)
+    assert ok, (worst, where)
+
+
+# ----------------------------------------------------------------------------- workloads
+
+
+def _run_workload(w, path=0):
+    A, B, C = gi.operands(w)
+    dA, dB = to_dev_bf16(A), to_dev_bf16(B)
+    dC = None
+    if C is not None:
+        dC = to_dev_bf16(C) if w.out_dtype == gi.OUT_BF16 else to_dev_f32(C)
+    dD, ldd = empty_out(w.M, w.N, w.out_dtype)
+    rc, st = call(w.M, w.N, w.K, dA, w.K, dB, w.K, dC, w.N if C is not None else 0, dD, ldd,
+                  w.alpha, w.beta, w.out_dtype, path=path)
+    assert rc == 0 and st == 0, g.last_error()
+    return A, B, C, from_dev(dD, w.out_dtype)
+
+
+def _cvals(w, C):
+    if C is None:
+        return None
+    return gi.bf16_bits_to_f32(C) if w.out_dtype == gi.OUT_BF16 else C
+
+
+def test_workload_square_full():
+    w = gi.WORKLOADS[1]
+    A, B, C, D = _run_workload(w)
+    ref, absdot = oracle.gemm_ref(A, B, C, w.alpha, w.beta)
+    ok, worst, where = oracle.check(D, ref, absdot, w.out_dtype, w.beta, _cvals(w, C))
+    assert ok, (worst, where)
+
+
+def test_workload_ragged_full():
+    w = gi.WORKLOADS[2]
+    A, B, C, D = _run_workload(w)
+    ref, absdot = oracle.gemm_ref(A, B, C, w.alpha, w.beta)
+    ok, worst, where = oracle.check(D, ref, absdot, w.out_dtype)
+    assert ok, (worst, where)
+
+
+def test_workload_mlp_up_projection_sampled():
+    w = gi.WORKLOADS[3]
+    A, B, C, D = _run_workload(w)
+    rows, cols = sample_positions(w.M, w.N, n_random=6000, seed=3)
+    ref, absdot = oracle.gemm_ref_sampled(A, B, rows, cols, C, w.alpha, w.beta)
+    ok, worst, where = oracle.check(D[rows, cols], ref, absdot, w.out_dtype)
+    assert ok, (worst, where)
+    assert np.all(np.isfinite(oracle.decode_out(D, w.out_dtype)))
+
+
+def test_workload_decode_full():
+    w = gi.WORKLOADS[4]
+    A, B, C, D = _run_workload(w)
+    ref, absdot = oracle.gemm_ref(A, B, C, w.alpha, w.beta)
+    ok, worst, where = oracle.check(D, ref, absdot, w.out_dtype)
+    assert ok, (worst, where)

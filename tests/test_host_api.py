@@ -1,0 +1,84 @@
+"""Host-side checks that need no GPU: the library builds, loads, exports every
+entry point the header declares, and rejects bad arguments before touching a
+device."""
+import ctypes
+import os
+import re
+
+import pytest
+
+import tensor_core_dense_tn_gb300 as g
+from tensor_core_dense_tn_gb300 import build as gbuild
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+HEADER = os.path.join(ROOT, "include", "gemm_tn.h")
+
+
+@pytest.fixture(scope="module")
+def lib():
+    gbuild.build()
+    return g.load()
+
+
+def declared_functions():
+    text = open(HEADER).read()
+    text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
+    return sorted(set(re.findall(r"\b(gemm_[a-z0-9_]+)\s*\(", text)))
+
+
+def test_header_declares_the_binding_names():
+    assert declared_functions() == sorted(g.EXPORTED)
+
+
+def test_every_declared_symbol_is_exported(lib):
+    for name in declared_functions():
+        assert hasattr(lib, name), name
+        assert ctypes.cast(getattr(lib, name), ctypes.c_void_p).value
+
+
+def test_version(lib):
+    assert g.version() == 100
+
+
+def test_no_torch_or_oracle_in_product_sources():
+    csrc = os.path.join(ROOT, "tensor_core_dense_tn_gb300", "csrc")
+    for f in os.listdir(csrc):
+        src = open(os.path.join(csrc, f)).read()
+        assert "torch" not in src and "oracle" not in src, f
+    pkg = open(os.path.join(ROOT, "tensor_core_dense_tn_gb300", "__init__.py")).read()
+    assert "import oracle" not in pkg and "from oracle" not in pkg
+
+
+@pytest.mark.parametrize("kw,code", [
+    (dict(out_dtype=2), g.GEMM_ERR_INVALID_VALUE),
+    (dict(M=-1), g.GEMM_ERR_INVALID_VALUE),
+    (dict(D=0), g.GEMM_ERR_INVALID_VALUE),
+    (dict(ldd=8), g.GEMM_ERR_INVALID_VALUE),
+    (dict(beta=1.0), g.GEMM_ERR_INVALID_VALUE),         # C is NULL
+    (dict(lda=32), g.GEMM_ERR_INVALID_VALUE),           # lda < K
+    (dict(A=0x1008), g.GEMM_ERR_MISALIGNED),
+    (dict(lda=68), g.GEMM_ERR_MISALIGNED),              # 136 B rows
+    (dict(D=0x3004), g.GEMM_ERR_MISALIGNED),
+    (dict(ldd=20, N=20), g.GEMM_ERR_MISALIGNED),        # 40 B rows of bf16
+    (dict(M=0), g.GEMM_OK),                             # empty: no launch
+    (dict(N=0), g.GEMM_OK),
+])
+def test_validation_before_any_device_call(lib, kw, code):
+    a = dict(M=64, N=64, K=64, A=0x1000, lda=64, B=0x2000, ldb=64, C=0, ldc=0, D=0x3000, ldd=64,
+             alpha=1.0, beta=0.0, out_dtype=0, stream=0)
+    a.update(kw)
+    assert g.gemm_bf16_tn(*a.values()) == code
+    if code != g.GEMM_OK:
+        assert g.last_error() != ""
+
+
+def test_forced_unknown_path_rejected(lib):
+    a = (64, 64, 64, 0x1000, 64, 0x2000, 64, 0, 0, 0x3000, 64, 1.0, 0.0, 0, 0)
+    assert g.gemm_bf16_tn_ex(*a, config=g.GemmConfig(path=9)) == g.GEMM_ERR_INVALID_VALUE
+
+
+def test_gemm_wrapper_checks_types():
+    torch = pytest.importorskip("torch")
+    A = torch.zeros((4, 8), dtype=torch.float32)
+    with pytest.raises(ValueError):
+        g.gemm(A, A)
