@@ -1,0 +1,477 @@
+#!/usr/bin/env python3
+"""Benchmark of the BF16 TN GEMM library on GB300.
+
+One step = one call of the hot path (gemm_bf16_tn through the C ABI) on the
+8192 x 28672 x 4096 MLP up-projection (A ~ N(0,1), B ~ N(0,1/4096), bf16
+out), operands resident in HBM.  Operands (288 MiB) exceed L2 (126 MiB), so
+no flush is needed between steps.  Alongside it, in the same run:
+
+* ``secondary``: the 16 x 8192 x 8192 decode GEMM in GB/s (B rotated over
+  four copies, 512 MiB, so it never sits in L2);
+* ``e2e``: the same metric with host buffers — pinned host->device copies
+  of A and B and the device->host copy of D inside every timed step;
+* ``cpu_baseline``: the FP64 CPU oracle timed on a bounded row sample of
+  the workload on the host's cores (its rows also double as a parity spot
+  check of the GPU result);
+* ``roofline``: achieved FLOP/s of the GEMM kernel (CUDA events on the
+  launching stream) against the measured dense bf16 peak.
+
+``--impl reference`` times the reference arm instead: the CPU oracle, on
+bounded row samples of the same workload, one sample per step.
+
+Multi-GPU (``torchrun --nproc-per-node N bench.py --gpus N``): every rank
+runs the full workload on its own GPU (weak scaling, no data exchange);
+elapsed time is the maximum over ranks and ``value`` sums all ranks' work.
+"""
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import os
+import statistics
+import subprocess
+import sys
+import threading
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+import numpy as np  # noqa: E402
+
+import gemm_inputs as gi  # noqa: E402
+from tensor_core_dense_tn_gb300 import roofline as rl  # noqa: E402
+
+METRIC = "BF16 GEMM TFLOP/s at 8192×28672×4096 (% of tensor peak); GB/s at M=16"
+MAIN = 3       # index of the 8192x28672x4096 workload
+DECODE = 4     # index of the 16x8192x8192 workload
+KERNEL_SOURCES = ("gemm_api.cu", "gemm_tiled.cu", "gemm_skinny.cu", "ptx.cuh", "kernels.h")
+PATH_NAMES = {1: "1sm", 2: "2sm", 3: "skinny"}
+
+
+def log(*a):
+    print(*a, file=sys.stderr, flush=True)
+
+
+# ----------------------------------------------------------------------------- distributed
+
+
+class Dist:
+    def __init__(self):
+        self.world = int(os.environ.get("WORLD_SIZE", "1"))
+        self.rank = int(os.environ.get("RANK", "0"))
+        self.local_rank = int(os.environ.get("LOCAL_RANK", "0"))
+        self.pg = None
+
+    def init(self, backend):
+        if self.world > 1:
+            import torch.distributed as dist
+            dist.init_process_group(backend)
+            self.pg = dist
+
+    def barrier(self):
+        if self.pg:
+            self.pg.barrier()
+
+    def max(self, x: float) -> float:
+        if not self.pg:
+            return x
+        import torch
+        t = torch.tensor([x], dtype=torch.float64, device="cuda" if torch.cuda.is_available() else "cpu")
+        self.pg.all_reduce(t, op=self.pg.ReduceOp.MAX)
+        return float(t.item())
+
+    def finish(self):
+        if self.pg:
+            self.pg.destroy_process_group()
+
+
+# ----------------------------------------------------------------------------- clocks
+
+
+class ClockSampler:
+    """nvidia-smi samples of SM clock and throttle reasons while running."""
+    FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_index: int, period_ms: int = 50):
+        self.gpu = gpu_index
+        self.period = period_ms
+        self.proc = None
+        self.lines = []
+        self.thread = None
+
+    def start(self):
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", f"--query-gpu={self.FIELDS}", "--format=csv,noheader,nounits",
+                 f"-lms", str(self.period), "-i", str(self.gpu)],
+                stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+        except OSError:
+            self.proc = None
+            return
+        self.thread = threading.Thread(target=self._read, daemon=True)
+        self.thread.start()
+        time.sleep(0.3)  # let the sampler come up before the timed region
+
+    def _read(self):
+        for line in self.proc.stdout:
+            self.lines.append((time.time(), line.strip()))
+
+    def stop(self):
+        if self.proc:
+            time.sleep(0.05)
+            self.proc.terminate()
+            try:
+                self.proc.wait(timeout=5)
+            except subprocess.TimeoutExpired:
+                self.proc.kill()
+            if self.thread:
+                self.thread.join(timeout=2)
+
+    def summary(self, t0: float, t1: float) -> dict:
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        sms, maxes, reasons, n = [], [], set(), 0
+        for ts, line in self.lines:
+            if not (t0 <= ts <= t1 + 0.06):
+                continue
+            parts = [p.strip() for p in line.split(",")]
+            if len(parts) < 9:
+                continue
+            try:
+                sms.append(float(parts[1]))
+                maxes.append(float(parts[2]))
+            except ValueError:
+                continue
+            n += 1
+            for nm, v in zip(names, parts[5:9]):
+                if v.lower() == "active":
+                    reasons.add(nm)
+        return {"sm_mhz": statistics.median(sms) if sms else None,
+                "sm_max_mhz": max(maxes) if maxes else None,
+                "reasons": sorted(reasons), "samples": n}
+
+
+# ----------------------------------------------------------------------------- helpers
+
+
+def kernel_source_hash() -> str:
+    h = hashlib.sha256()
+    for f in KERNEL_SOURCES:
+        with open(os.path.join(ROOT, "tensor_core_dense_tn_gb300", "csrc", f), "rb") as fh:
+            h.update(fh.read())
+    return h.hexdigest()[:16]
+
+
+def profiled_traffic(workload_name: str):
+    """DRAM bytes per launch from the committed ncu summary, if the kernels are unchanged."""
+    p = os.path.join(ROOT, "profiles", "ncu_traffic.json")
+    try:
+        d = json.load(open(p))
+    except (OSError, ValueError):
+        return None
+    e = d.get(workload_name)
+    if not e or e.get("source_hash") != kernel_source_hash():
+        return None
+    return e.get("dram_bytes_per_launch")
+
+
+def dev_bf16(bits, torch, device):
+    return torch.from_numpy(np.ascontiguousarray(bits).view(np.int16)).to(device).view(torch.bfloat16)
+
+
+# ----------------------------------------------------------------------------- our arm
+
+
+def time_steps(torch, stream, fn, steps):
+    """CUDA-event time of `steps` back-to-back calls on `stream` (ms total)."""
+    start = torch.cuda.Event(enable_timing=True)
+    end = torch.cuda.Event(enable_timing=True)
+    torch.cuda.synchronize()
+    start.record(stream)
+    for i in range(steps):
+        fn(i)
+    end.record(stream)
+    torch.cuda.synchronize()
+    return start.elapsed_time(end)
+
+
+def run_ours(args, dist):
+    import torch
+    import tensor_core_dense_tn_gb300 as g
+
+    g.load()  # fail loudly without the CUDA library
+    device = torch.device("cuda", dist.local_rank)
+    torch.cuda.set_device(device)
+    dist.init("nccl")
+    stream = torch.cuda.current_stream(device)
+    s_handle = stream.cuda_stream
+    peaks = rl.load_peaks()
+    warmup = max(args.warmup, 3)
+
+    w = gi.WORKLOADS[args.workload]
+    if args.shape:
+        M, N, K = (int(x) for x in args.shape.split(","))
+        w = gi.Workload(w.index, f"custom {M}x{N}x{K}", M, N, K, w.dist_a, w.dist_b, w.dist_c,
+                        w.alpha, w.beta, w.out_dtype)
+    t_gen = time.time()
+    A, B, C = gi.operands(w)
+    log(f"[bench] inputs for {w.name} generated in {time.time() - t_gen:.1f}s")
+    dA, dB = dev_bf16(A, torch, device), dev_bf16(B, torch, device)
+    out_t = torch.float32 if w.out_dtype == gi.OUT_F32 else torch.bfloat16
+    dC = None
+    if C is not None:
+        dC = dev_bf16(C, torch, device) if w.out_dtype == gi.OUT_BF16 else torch.from_numpy(C).to(device)
+    dD = torch.empty((w.M, w.N), dtype=out_t, device=device)
+    cfg = g.GemmConfig(path=args.path)
+    c_ptr = dC.data_ptr() if dC is not None else 0
+    ldc = w.N if dC is not None else 0
+
+    def step(_i):
+        rc = g.gemm_bf16_tn_ex(w.M, w.N, w.K, dA.data_ptr(), w.K, dB.data_ptr(), w.K, c_ptr, ldc,
+                               dD.data_ptr(), w.N, w.alpha, w.beta, w.out_dtype, s_handle, cfg)
+        if rc != 0:
+            raise RuntimeError(f"gemm failed: {rc} {g.last_error()}")
+
+    for i in range(warmup):
+        step(i)
+    st = g.gemm_get_status(s_handle)
+    if st != 0:
+        raise RuntimeError(f"device status {st}: {g.last_error()}")
+    info = g.last_launch_info()
+
+    vis = [v for v in os.environ.get("CUDA_VISIBLE_DEVICES", "").split(",") if v.strip()]
+    smi_index = int(vis[dist.local_rank]) if len(vis) > dist.local_rank and vis[dist.local_rank].isdigit() \
+        else dist.local_rank
+    sampler = ClockSampler(smi_index)
+    sampler.start()
+    dist.barrier()
+    t0 = time.time()
+    ms = time_steps(torch, stream, step, args.steps)
+    t1 = time.time()
+    dist.barrier()
+    sampler.stop()
+    st = g.gemm_get_status(s_handle)
+    if st != 0:
+        raise RuntimeError(f"device status {st}: {g.last_error()}")
+    ms = dist.max(ms)
+    clocks = sampler.summary(t0, t1)
+
+    flops = rl.gemm_flops(w.M, w.N, w.K)
+    qbytes = rl.gemm_bytes(w.M, w.N, w.K, 4 if w.out_dtype == gi.OUT_F32 else 2, w.beta != 0)
+    per_step_s = ms / 1e3 / args.steps
+    value = dist.world * flops / per_step_s / 1e12
+    achieved = flops / per_step_s / 1e12          # per launch, per GPU
+    traffic = profiled_traffic(w.name)
+    roof = {"bound": "tensor", "achieved": round(achieved, 2), "peak": peaks["bf16_tflops"],
+            "unit": "TFLOP/s", "frac": round(achieved / peaks["bf16_tflops"], 4),
+            "traffic": traffic, "algorithmic_flops": flops, "algorithmic_bytes": qbytes,
+            "peak_source": f"{peaks['source']} burst bf16 (MEASURED_PEAKS.json)"
+                           if peaks["source"] == "measured" else "fallback 1.9 PFLOP/s",
+            "frac_of_sustained": round(achieved / peaks["bf16_tflops_sustained"], 4),
+            "kernel": info.get("kernel")}
+
+    result = {
+        "metric": METRIC, "value": round(value, 2), "unit": "TFLOP/s", "n_gpus": dist.world,
+        "steps": args.steps, "warmup": warmup, "ms_per_step": round(ms / args.steps, 4),
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "bf16",
+        "data": "synthetic",
+        "config": dict(w.describe(), path=PATH_NAMES.get(info.get("path"), info.get("path")),
+                       grid=info.get("grid"), cluster=info.get("cluster"),
+                       tile=[info.get("tile_m"), info.get("tile_n")], stages=info.get("stages"),
+                       l2="operands (288 MiB) larger than L2; no flush" if args.workload == MAIN
+                       else "see workload", parallelism=f"replicas x{dist.world}"),
+        "roofline": roof,
+        "gpu_launches": args.steps,
+        "clocks": clocks,
+    }
+
+    # ---------------------------------------------------------------- e2e (host buffers)
+    if not args.no_e2e:
+        hA = torch.from_numpy(A.view(np.int16)).pin_memory()
+        hB = torch.from_numpy(B.view(np.int16)).pin_memory()
+        hD = torch.empty((w.M, w.N), dtype=torch.int16 if out_t == torch.bfloat16 else torch.float32).pin_memory()
+        dA16, dB16 = dA.view(torch.int16), dB.view(torch.int16)
+        dDv = dD.view(torch.int16) if out_t == torch.bfloat16 else dD
+
+        def e2e_step(i):
+            dA16.copy_(hA, non_blocking=True)
+            dB16.copy_(hB, non_blocking=True)
+            step(i)
+            hD.copy_(dDv, non_blocking=True)
+
+        e_steps = max(3, min(args.steps, 20))
+        for i in range(2):
+            e2e_step(i)
+        e_ms = dist.max(time_steps(torch, stream, e2e_step, e_steps))
+        g.gemm_get_status(s_handle)
+        e_per = e_ms / 1e3 / e_steps
+        result["e2e"] = {"value": round(dist.world * flops / e_per / 1e12, 2), "unit": "TFLOP/s",
+                         "h2d_bytes_per_step": hA.numel() * 2 + hB.numel() * 2,
+                         "d2h_bytes_per_step": hD.numel() * hD.element_size(),
+                         "ms_per_step": round(e_ms / e_steps, 3), "steps": e_steps,
+                         "api": "gemm_bf16_tn (C ABI) with pinned host operands"}
+        del hA, hB, hD
+
+    # ---------------------------------------------------------------- decode secondary
+    if not args.no_secondary:
+        result["secondary"] = run_decode(args, g, torch, device, peaks, dist)
+
+    # ---------------------------------------------------------------- CPU oracle baseline
+    if not args.no_cpu_baseline and dist.rank == 0:
+        result["cpu_baseline"] = cpu_baseline(w, A, B, C, dD, out_t, torch, args.cpu_seconds)
+
+    dist.finish()
+    return result
+
+
+def run_decode(args, g, torch, device, peaks, dist):
+    w = gi.WORKLOADS[DECODE]
+    # own stream: graph capture needs a non-default stream
+    stream = torch.cuda.Stream(device)
+    s_handle = stream.cuda_stream
+    A, B, _ = gi.operands(w)
+    dA = dev_bf16(A, torch, device)
+    copies = 4
+    dBs = [dev_bf16(B, torch, device) for _ in range(copies)]
+    dD = torch.empty((w.M, w.N), dtype=torch.bfloat16, device=device)
+    cfg = g.GemmConfig(path=0)
+
+    def step(i):
+        rc = g.gemm_bf16_tn_ex(w.M, w.N, w.K, dA.data_ptr(), w.K, dBs[i % copies].data_ptr(), w.K, 0, 0,
+                               dD.data_ptr(), w.N, w.alpha, w.beta, w.out_dtype, s_handle, cfg)
+        if rc != 0:
+            raise RuntimeError(f"decode gemm failed: {rc} {g.last_error()}")
+
+    with torch.cuda.stream(stream):
+        for i in range(max(args.warmup, 3)):
+            step(i)
+    torch.cuda.synchronize()
+    info = g.last_launch_info()
+    steps = max(args.steps, 50)
+    ms_eager = dist.max(time_steps(torch, stream, step, steps))
+    # The same launches replayed from a CUDA graph (how a decode loop runs):
+    # every step is still one full GEMM on a rotated copy of B.
+    graph = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(graph, stream=stream):
+        for i in range(steps):
+            step(i)
+    with torch.cuda.stream(stream):  # replay() launches on the current stream
+        graph.replay()
+        ms = dist.max(time_steps(torch, stream, lambda _i: graph.replay(), 1))
+    st = g.gemm_get_status(s_handle)
+    if st != 0:
+        raise RuntimeError(f"device status {st}: {g.last_error()}")
+    per = ms / 1e3 / steps
+    qbytes = rl.gemm_bytes(w.M, w.N, w.K)
+    gbs = qbytes / per / 1e9
+    traffic = profiled_traffic(w.name)
+    gbs_eager = qbytes / (ms_eager / 1e3 / steps) / 1e9
+    return {"metric": "BF16 GEMM GB/s at 16x8192x8192", "value": round(dist.world * gbs, 1),
+            "unit": "GB/s", "ms_per_step": round(ms / steps, 5), "steps": steps,
+            "launch": "CUDA graph of the steps' launches",
+            "eager": {"value": round(dist.world * gbs_eager, 1), "ms_per_step": round(ms_eager / steps, 5)},
+            "tflops": round(rl.gemm_flops(w.M, w.N, w.K) / per / 1e12, 2),
+            "config": dict(w.describe(), path=PATH_NAMES.get(info.get("path")), grid=info.get("grid"),
+                           stages=info.get("stages"), l2=f"B rotated over {copies} copies (512 MiB)"),
+            "roofline": {"bound": "hbm", "achieved": round(gbs, 1), "peak": peaks["hbm_gbs"], "unit": "GB/s",
+                         "frac": round(gbs / peaks["hbm_gbs"], 4), "traffic": traffic,
+                         "algorithmic_bytes": qbytes, "kernel": info.get("kernel"),
+                         "peak_source": "measured copy bandwidth (MEASURED_PEAKS.json)"
+                         if peaks["source"] == "measured" else "fallback 6.8 TB/s"}}
+
+
+def cpu_baseline(w, A, B, C, dD, out_t, torch, seconds):
+    """Time the CPU oracle on a row sample sized to ~`seconds`; compare those rows with the GPU."""
+    import oracle
+    threads = oracle.default_threads()
+    per_row = 2.0 * w.N * w.K
+    t = time.time()
+    oracle.gemm_ref(A[:threads], B, None if C is None else C[:threads], w.alpha, w.beta)
+    rate = threads * per_row / max(time.time() - t, 1e-3)
+    rows = int(max(threads, min(w.M, seconds * rate / per_row)))
+    r0 = (w.M - rows) // 2
+    t = time.time()
+    ref, absdot = oracle.gemm_ref(A[r0:r0 + rows], B, None if C is None else C[r0:r0 + rows], w.alpha, w.beta)
+    dt = time.time() - t
+    if out_t == torch.bfloat16:
+        got = dD[r0:r0 + rows].view(torch.int16).cpu().numpy().view(np.uint16)
+        od = gi.OUT_BF16
+    else:
+        got = dD[r0:r0 + rows].cpu().numpy()
+        od = gi.OUT_F32
+    cvals = None if C is None else (gi.bf16_bits_to_f32(C[r0:r0 + rows]) if od == gi.OUT_BF16 else C[r0:r0 + rows])
+    ok, worst, _ = oracle.check(got, ref, absdot, od, w.beta, cvals)
+    return {"value": round(rows * per_row / dt / 1e12, 6), "unit": "TFLOP/s", "cores": threads,
+            "kind": "oracle", "sample": f"rows {r0}..{r0 + rows - 1} of {w.M} ({rows} x {w.N} outputs, "
+                                        f"K={w.K}) in {dt:.1f}s",
+            "parity_on_sample": {"ok": bool(ok), "worst_err_over_bound": round(worst, 4)}}
+
+
+# ----------------------------------------------------------------------------- reference arm
+
+
+def run_reference(args, dist):
+    """The CPU oracle as the reference arm: one bounded row sample per step."""
+    if dist.rank != 0:
+        return None
+    import oracle
+    w = gi.WORKLOADS[args.workload]
+    A, B, C = gi.operands(w)
+    threads = oracle.default_threads()
+    per_row = 2.0 * w.N * w.K
+    t = time.time()
+    oracle.gemm_ref(A[:threads], B, None if C is None else C[:threads], w.alpha, w.beta)
+    rate = threads * per_row / max(time.time() - t, 1e-3)
+    warmup = max(args.warmup, 3)
+    budget = args.reference_seconds / (args.steps + warmup)
+    rows = int(max(1, min(4 * threads, budget * rate / per_row)))
+    for i in range(warmup):
+        r0 = (i * rows) % (w.M - rows + 1)
+        oracle.gemm_ref(A[r0:r0 + rows], B, None if C is None else C[r0:r0 + rows], w.alpha, w.beta)
+    t = time.time()
+    for i in range(args.steps):
+        r0 = ((warmup + i) * rows) % (w.M - rows + 1)
+        oracle.gemm_ref(A[r0:r0 + rows], B, None if C is None else C[r0:r0 + rows], w.alpha, w.beta)
+    dt = time.time() - t
+    value = args.steps * rows * per_row / dt / 1e12
+    sample = f"{rows} rows x {w.N} outputs x K={w.K} per step"
+    return {"impl": "reference", "metric": METRIC, "value": round(value, 6), "unit": "TFLOP/s",
+            "n_gpus": dist.world, "steps": args.steps, "warmup": warmup,
+            "ms_per_step": round(dt / args.steps * 1e3, 2), "higher_is_better": True, "scaling": "weak",
+            "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+            "config": w.describe(),
+            "cpu_baseline": {"value": round(value, 6), "unit": "TFLOP/s", "cores": threads, "kind": "oracle",
+                             "sample": sample},
+            "e2e": {"value": round(value, 6), "unit": "TFLOP/s", "h2d_bytes_per_step": 0,
+                    "d2h_bytes_per_step": 0}}
+
+
+def main():
+    ap = argparse.ArgumentParser(description=__doc__, formatter_class=argparse.RawDescriptionHelpFormatter)
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=200)
+    ap.add_argument("--warmup", type=int, default=10)
+    ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
+    ap.add_argument("--workload", type=int, default=MAIN, help="index into gemm_inputs.WORKLOADS")
+    ap.add_argument("--shape", default="", help="M,N,K override (profiling runs)")
+    ap.add_argument("--path", type=int, default=0, help="0 auto, 1 1-SM, 2 2-SM, 3 skinny")
+    ap.add_argument("--no-e2e", action="store_true")
+    ap.add_argument("--no-secondary", action="store_true")
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--cpu-seconds", type=float, default=12.0)
+    ap.add_argument("--reference-seconds", type=float, default=120.0)
+    args = ap.parse_args()
+    dist = Dist()
+    if args.impl == "reference":
+        res = run_reference(args, dist)
+    else:
+        res = run_ours(args, dist)
+    if res is not None and dist.rank == 0:
+        print(json.dumps(res), flush=True)
+
+
+if __name__ == "__main__":
+    main()

@@ -40,6 +40,12 @@
  * must not happen during stream capture.  Calls on different streams use
  * different workspaces.
  *
+ * Launch: kernels are launched with programmatic stream serialisation, so
+ * their set-up (barrier initialisation, Tensor Memory allocation) may overlap
+ * the tail of the previous kernel on the stream.  Each kernel waits for the
+ * previous kernel's completion (griddepcontrol.wait) before its first global
+ * memory access, so stream order is preserved for inputs and outputs.
+ *
  * Thread safety: calls may come from several host threads; the last-error
  * string is per thread.
  *
@@ -89,6 +95,7 @@ typedef struct gemm_tn_config {
   uint64_t wait_timeout_ns; /* device-side wait limit, 0 = default (2 s, or env GEMM_WAIT_TIMEOUT_NS) */
   int test_fault;           /* tests only: 1 = the producer of CTA 0 drops one stage's loads,
                                so the consumer's bounded wait must expire (GEMM_ERR_TIMEOUT) */
+  int disable_pdl;          /* 1 = launch without programmatic dependent launch (see below) */
 } gemm_tn_config;
 
 /* What the last successful launch on this host thread ran. */

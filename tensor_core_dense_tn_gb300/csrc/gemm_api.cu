@@ -226,6 +226,7 @@ int run(int64_t M, int64_t N, int64_t K, const void* A, int64_t lda, const void*
                                                                 : CU_TENSOR_MAP_DATA_TYPE_BFLOAT16;
   const uint64_t tmo = timeout_ns(cfg);
   const int fault = cfg ? cfg->test_fault : 0;
+  const bool pdl = !(cfg && cfg->disable_pdl);
   LaunchInfo li = {};
   cudaError_t e;
 
@@ -244,7 +245,7 @@ int run(int64_t M, int64_t N, int64_t K, const void* A, int64_t lda, const void*
     p.C = C; p.ldc = ldc; p.D = D; p.ldd = ldd; p.out_f32 = out_dtype == GEMM_OUT_F32;
     p.fault = fault; p.timeout_ns = tmo; p.status = st->status;
     Workspace* w = nullptr;
-    rc = get_workspace(dev, stream, (size_t)grid * 2 * np * 128, (size_t)p.n_tiles * 4, &w);
+    rc = get_workspace(dev, stream, (size_t)grid * 2 * 128 * np, (size_t)p.n_tiles * 4, &w);
     if (rc != GEMM_OK) return rc;
     p.partials = w->partials;
     p.counters = w->counters;
@@ -253,7 +254,7 @@ int run(int64_t M, int64_t N, int64_t K, const void* A, int64_t lda, const void*
       return rc;
     if ((rc = encode_2d(&tB, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, B, K, N, ldb, 64, 128, CU_TENSOR_MAP_SWIZZLE_128B, "B")))
       return rc;
-    e = launch_skinny(tA, tB, p, stream, &li);
+    e = launch_skinny(tA, tB, p, pdl, stream, &li);
   } else {
     const int cg = path == GEMM_PATH_2SM ? 2 : 1;
     int tile_m, tile_n, b_rows, epi_r, epi_c;
@@ -291,7 +292,7 @@ int run(int64_t M, int64_t N, int64_t K, const void* A, int64_t lda, const void*
     }
     if (has_c && (rc = encode_2d(&tC, out_dt, esize, C, N, M, ldc, epi_c, epi_r, out_sw, "C"))) return rc;
     if ((rc = encode_2d(&tD, out_dt, esize, D, N, M, ldd, epi_c, epi_r, out_sw, "D"))) return rc;
-    e = launch_tiled(cg, out_dtype == GEMM_OUT_F32, tA, tB, tC, tD, p, cfg ? cfg->grid : 0, stream, &li);
+    e = launch_tiled(cg, out_dtype == GEMM_OUT_F32, tA, tB, tC, tD, p, cfg ? cfg->grid : 0, pdl, stream, &li);
   }
   if (e != cudaSuccess) {
     cudaGetLastError();

@@ -2,20 +2,27 @@
 //
 // With M tokens this small the arithmetic intensity is ~M FLOP per byte of B
 // (the GEMV/decode bound of the Ampere-to-Hopper page, section on decode:
-// performance ~ intensity x HBM bandwidth), so the kernel's only job is to
-// keep enough bytes of B in flight on every SM (Little's law, H100 Nsight
-// Compute page, section on bytes in flight; TMA needs 64-128 KiB in flight
-// per SM on Blackwell, SemiAnalysis Blackwell page, section "TMA").
+// performance ~ intensity x HBM bandwidth), so the kernel's job is to keep
+// enough bytes of B in flight on every SM (Little's law, H100 Nsight Compute
+// page, section on bytes in flight; TMA needs 64-128 KiB in flight per SM on
+// Blackwell, SemiAnalysis Blackwell page, section "TMA") from the first
+// cycle to the last.
 //
 // Swap-AB: the tensor core computes D^T = B * A^T, so the 128 rows of a B
 // tile fill the MMA's M = 128 and the (padded) M tokens become MMA N = np.
-// Work is the list of (n-tile, k-block) units, split into `grid` contiguous
-// ranges, one per CTA (stream-K).  A CTA that covers a whole n-tile writes D
-// directly; a tile split between CTAs leaves fp32 partials in a workspace and
-// the last CTA to finish it (per-tile arrival counter) sums them in fixed
-// k order, so the result does not depend on timing.
 //
-// Roles and bounded waits are as in the tiled kernel (gemm_tiled.cu).
+// Work is the list of (n-tile, k-block) units, split into `grid` contiguous
+// ranges, one per CTA (stream-K), so every SM streams the same number of
+// bytes.  A CTA that covers a whole n-tile writes D directly.  A tile split
+// between CTAs leaves fp32 partials in a workspace; the last CTA to finish a
+// part of that tile (per-tile arrival counters) adds the parts in k order,
+// so the result does not depend on timing.  No CTA ever waits for another.
+//
+// Roles: warp 0 lane 0 issues TMA loads into a deep ring (its first loads go
+// out before the block-wide start-up sync); warp 1 lane 0 issues tcgen05.mma
+// into TMEM accumulators; warps 2..5 read them back (tcgen05.ld) and finish
+// each segment.  Every wait is bounded as in the tiled kernel
+// (gemm_tiled.cu).
 #include <cuda.h>
 #include <cuda_runtime.h>
 
@@ -33,10 +40,12 @@ constexpr int kUmmaK = 16;
 constexpr int kEpiWarps = 4;
 constexpr int kThreads = 64 + 32 * kEpiWarps;
 constexpr int kMaxStages = 16;
-constexpr int kBTileBytes = 128 * kBK * 2;  // 16 KiB
-constexpr int kTmemCols = 128;              // two accumulators of up to 64 columns
+constexpr int kNumAcc = 4;                   // TMEM accumulators (64 columns each)
+constexpr int kBTileBytes = 128 * kBK * 2;   // 16 KiB
+constexpr int kTmemCols = 64 * kNumAcc;
 constexpr int kErrTimeout = -5;
-constexpr int kSmemBudget = 200 * 1024;
+constexpr int kSmemBudget = 216 * 1024;
+constexpr int kNumBars = 2 * kMaxStages + 2 * kNumAcc + 1;
 
 __host__ __device__ inline int stage_bytes(int np) { return kBTileBytes + np * kBK * 2; }
 
@@ -46,7 +55,7 @@ __host__ __device__ inline int stages_for(int np) {
 }
 
 __host__ __device__ inline int smem_for(int np) {
-  return 1024 + stages_for(np) * stage_bytes(np) + (2 * kMaxStages + 4 + 1) * 8 + 16;
+  return 1024 + stages_for(np) * stage_bytes(np) + kNumBars * 8 + 16;
 }
 
 // First unit owned by CTA c when U units are split into G contiguous ranges.
@@ -57,9 +66,8 @@ __device__ __forceinline__ long long owner_of(long long x, long long U, long lon
   return ((x + 1) * G + U - 1) / U - 1;
 }
 
-__device__ __noinline__ bool wait_bar(uint32_t bar, uint32_t parity, volatile uint32_t* flag, uint64_t timeout_ns,
-                                      int* status, int role) {
-  if (mbar_try_wait(bar, parity)) return true;
+__device__ __noinline__ bool wait_bar_slow(uint32_t bar, uint32_t parity, volatile uint32_t* flag,
+                                           uint64_t timeout_ns, int* status, int role) {
   const uint64_t t0 = globaltimer();
   while (true) {
 #pragma unroll 1
@@ -74,15 +82,17 @@ __device__ __noinline__ bool wait_bar(uint32_t bar, uint32_t parity, volatile ui
   }
 }
 
+// Bounded wait on an mbarrier phase (inline fast path).  Returns false if
+// this CTA is aborting or the limit expired.
+__device__ __forceinline__ bool wait_bar(uint32_t bar, uint32_t parity, volatile uint32_t* flag,
+                                         uint64_t timeout_ns, int* status, int role) {
+  if (mbar_try_wait(bar, parity)) return true;
+  return wait_bar_slow(bar, parity, flag, timeout_ns, status, role);
+}
+
 __device__ __noinline__ void settle(uint64_t ns) {
   const uint64_t t0 = globaltimer();
   while (globaltimer() - t0 < ns) __nanosleep(1000);
-}
-
-__device__ __forceinline__ float ld_cg_f32(const float* p) {
-  float v;
-  asm volatile("ld.global.cg.f32 %0, [%1];" : "=f"(v) : "l"(p));
-  return v;
 }
 
 __device__ __forceinline__ float load_c(const SkinnyParams& p, int m, int n) {
@@ -100,6 +110,14 @@ __device__ __forceinline__ void store_d(const SkinnyParams& p, int m, int n, flo
   }
 }
 
+// Partial of CTA c's segment of a tile: slot 0 = the CTA's first tile,
+// slot 1 = its last (only the first and last segment of a range can be
+// partial).  Layout [cta][slot][row][np] so a thread's np values are
+// contiguous (16-byte vectors).
+__device__ __forceinline__ float* partial_ptr(const SkinnyParams& p, long long c, int slot, int row) {
+  return p.partials + ((c * 2 + slot) * 128 + row) * (long long)p.np;
+}
+
 __global__ void __launch_bounds__(kThreads, 1)
     gemm_tn_skinny_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
                           const SkinnyParams p) {
@@ -114,9 +132,9 @@ __global__ void __launch_bounds__(kThreads, 1)
   auto full_bar = [&](int s) { return bar0 + 8u * s; };
   auto empty_bar = [&](int s) { return bar0 + 8u * (kMaxStages + s); };
   auto accf_bar = [&](int b) { return bar0 + 8u * (2 * kMaxStages + b); };
-  auto acce_bar = [&](int b) { return bar0 + 8u * (2 * kMaxStages + 2 + b); };
-  const uint32_t drain_bar = bar0 + 8u * (2 * kMaxStages + 4);
-  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bars + 2 * kMaxStages + 5);
+  auto acce_bar = [&](int b) { return bar0 + 8u * (2 * kMaxStages + kNumAcc + b); };
+  const uint32_t drain_bar = bar0 + 8u * (kNumBars - 1);
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bars + kNumBars);
   volatile uint32_t* abort_flag = tmem_slot + 1;
 
   const int warp = threadIdx.x >> 5;
@@ -125,12 +143,32 @@ __global__ void __launch_bounds__(kThreads, 1)
   const long long c = blockIdx.x;
   const long long u_begin = range_start(c, U, G), u_end = range_start(c + 1, U, G);
 
+  // ---- producer state (thread 0).  The first ring's worth of loads is
+  // issued right after the barriers exist, before the block-wide sync, so
+  // that it overlaps TMEM allocation and the other warps' start-up.
+  const uint32_t tx = (uint32_t)(kBTileBytes + a_bytes);
+  bool skip_once = (p.fault & kFaultSkipTmaOnce) && blockIdx.x == 0;
+  int p_stage = 0;
+  uint32_t p_phase = 0;
+  long long p_u = u_begin;
+  auto issue = [&](long long u, int stage) {
+    const int n = (int)(u / KB), kb = (int)(u % KB);
+    const uint32_t fb = full_bar(stage);
+    mbar_arrive_expect_tx(fb, tx);
+    if (skip_once) {
+      skip_once = false;  // test-only: leave this stage's bytes missing
+    } else {
+      tma_load_2d(sB + stage * kBTileBytes, &tmB, kb * kBK, n * 128, fb);
+      tma_load_2d(sA + stage * a_bytes, &tmA, kb * kBK, 0, fb);
+    }
+  };
+
   if (threadIdx.x == 0) {
     for (int s = 0; s < S; ++s) {
       mbar_init(full_bar(s), 1);
       mbar_init(empty_bar(s), 1);
     }
-    for (int b = 0; b < 2; ++b) {
+    for (int b = 0; b < kNumAcc; ++b) {
       mbar_init(accf_bar(b), 1);
       mbar_init(acce_bar(b), kEpiWarps);
     }
@@ -138,10 +176,19 @@ __global__ void __launch_bounds__(kThreads, 1)
     *abort_flag = 0;
     fence_mbar_init();
     fence_proxy_async_smem();
-  }
-  if (warp == 0 && lane == 0) {
     tma_prefetch_desc(&tmA);
     tma_prefetch_desc(&tmB);
+  }
+  // Inputs may come from the previous kernel on the stream: no global memory
+  // access before this point.
+  griddep_wait();
+  griddep_launch_dependents();
+  if (threadIdx.x == 0) {
+    while (p_u < u_end && p_stage < S) issue(p_u++, p_stage++);  // every stage starts empty
+    if (p_stage == S) {
+      p_stage = 0;
+      p_phase = 1;
+    }
   }
   if (warp == 1) tmem_alloc<1>(smem_u32(tmem_slot), kTmemCols);
   tc_fence_before();
@@ -152,27 +199,16 @@ __global__ void __launch_bounds__(kThreads, 1)
   if (warp == 0) {
     if (lane == 0) {
       // -------------------------------------------------------- producer
-      const uint32_t tx = (uint32_t)(kBTileBytes + a_bytes);
-      bool ok = true, skip_once = (p.fault & kFaultSkipTmaOnce) && blockIdx.x == 0;
-      int stage = 0;
-      uint32_t phase = 0;
-      for (long long u = u_begin; u < u_end && ok; ++u) {
-        const int n = (int)(u / KB), kb = (int)(u % KB);
-        if (!wait_bar(empty_bar(stage), phase ^ 1, abort_flag, p.timeout_ns, p.status, kRoleProducer)) {
+      bool ok = true;
+      for (; p_u < u_end; ++p_u) {
+        if (!wait_bar(empty_bar(p_stage), p_phase ^ 1, abort_flag, p.timeout_ns, p.status, kRoleProducer)) {
           ok = false;
           break;
         }
-        const uint32_t fb = full_bar(stage);
-        mbar_arrive_expect_tx(fb, tx);
-        if (skip_once) {
-          skip_once = false;
-        } else {
-          tma_load_2d(sB + stage * kBTileBytes, &tmB, kb * kBK, n * 128, fb);
-          tma_load_2d(sA + stage * a_bytes, &tmA, kb * kBK, 0, fb);
-        }
-        if (++stage == S) {
-          stage = 0;
-          phase ^= 1;
+        issue(p_u, p_stage);
+        if (++p_stage == S) {
+          p_stage = 0;
+          p_phase ^= 1;
         }
       }
       if (!ok) settle(2000000);
@@ -210,8 +246,10 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
         if (!ok) break;
         mma_commit(accf_bar(acc));
-        acc ^= 1;
-        if (acc == 0) acc_phase ^= 1;
+        if (++acc == kNumAcc) {
+          acc = 0;
+          acc_phase ^= 1;
+        }
         u = seg_end;
       }
       mma_commit(drain_bar);
@@ -221,7 +259,8 @@ __global__ void __launch_bounds__(kThreads, 1)
     // ---------------------------------------------------------- epilogue
     // Each warp owns 32 of the tile's 128 rows of D^T (TMEM lane quarter q)
     // and finishes them on its own: split tiles keep one arrival counter per
-    // (tile, warp), so no barrier is shared between epilogue warps.
+    // (tile, warp), so no barrier is shared between epilogue warps and no
+    // warp ever waits for another CTA.
     const int q = warp & 3;
     const int n_local = q * 32 + lane;
     int acc = 0;
@@ -243,50 +282,85 @@ __global__ void __launch_bounds__(kThreads, 1)
           tmem_wait_ld();
         } else {
 #pragma unroll
-          for (int j = 0; j < 16; ++j) r[j] = 0;
+          for (int t = 0; t < 16; ++t) r[t] = 0;
         }
 #pragma unroll
-        for (int j = 0; j < 16; ++j) vals[g * 16 + j] = __uint_as_float(r[j]);
+        for (int t = 0; t < 16; ++t) vals[g * 16 + t] = __uint_as_float(r[t]);
       }
       tc_fence_before();
       __syncwarp();
       if (lane == 0) mbar_arrive(acce_bar(acc));
-      acc ^= 1;
-      if (acc == 0) acc_phase ^= 1;
+      if (++acc == kNumAcc) {
+        acc = 0;
+        acc_phase ^= 1;
+      }
 
       const int ng = (int)(n * 128) + n_local;
       bool finish = whole;
       if (!whole) {
-        // fp32 partial of this k-range into the CTA's slot for the tile
         const int slot = (n == first_tile) ? 0 : 1;
-        float* mine = p.partials + ((c * 2 + slot) * (long long)p.np) * 128;
+        float4* mine = reinterpret_cast<float4*>(partial_ptr(p, c, slot, n_local));
 #pragma unroll
-        for (int m = 0; m < 64; ++m)
-          if (m < p.M) mine[m * 128 + n_local] = vals[m];
-        __threadfence();
+        for (int g4 = 0; g4 < 16; ++g4)
+          if (g4 * 4 < p.np) mine[g4] = make_float4(vals[4 * g4], vals[4 * g4 + 1], vals[4 * g4 + 2], vals[4 * g4 + 3]);
+        // The warp barrier orders every lane's partial before lane 0's
+        // release; lane 0's acquire is passed back to the lanes the same way.
         __syncwarp();
+        const long long c_first = owner_of(n * KB, U, G);
+        const long long c_last = owner_of((n + 1) * KB - 1, U, G);
+        const int nseg = (int)(c_last - c_first + 1);
         int last = 0;
         if (lane == 0) {
-          const long long c_first = owner_of(n * KB, U, G);
-          const long long c_last = owner_of((n + 1) * KB - 1, U, G);
-          const int nseg = (int)(c_last - c_first + 1);
-          const int prev = atomicAdd(p.counters + n * 4 + q, 1);
+          const int prev = atom_add_acq_rel_gpu(p.counters + n * 4 + q, 1);
           last = (prev == nseg - 1);
           if (last) p.counters[n * 4 + q] = 0;  // ready for the next call
         }
         finish = __shfl_sync(0xffffffffu, last, 0) != 0;
+        __syncwarp();
         if (finish) {
-          __threadfence();
-          const long long c_first = owner_of(n * KB, U, G);
-          const long long c_last = owner_of((n + 1) * KB - 1, U, G);
+          // Add the tile's parts in k order (CTA order), this CTA's own part
+          // from registers.  Loads go out in batches of kBatch parts x 16
+          // values so that their latencies overlap.
+          constexpr int kBatch = 4;
 #pragma unroll
-          for (int m = 0; m < 64; ++m) vals[m] = 0.0f;
-          for (long long cc = c_first; cc <= c_last; ++cc) {
-            const int sl = (n == range_start(cc, U, G) / KB) ? 0 : 1;
-            const float* part = p.partials + ((cc * 2 + sl) * (long long)p.np) * 128 + n_local;
+          for (int g16 = 0; g16 < 4; ++g16) {
+            if (g16 * 16 >= p.np) break;
+            float acc16[16];
 #pragma unroll
-            for (int m = 0; m < 64; ++m)
-              if (m < p.M) vals[m] += ld_cg_f32(part + m * 128);
+            for (int t = 0; t < 16; ++t) acc16[t] = 0.0f;
+            for (long long cc0 = c_first; cc0 <= c_last; cc0 += kBatch) {
+              float4 buf[kBatch][4];
+#pragma unroll
+              for (int b = 0; b < kBatch; ++b) {
+                const long long cc = cc0 + b;
+                if (cc <= c_last && cc != c) {
+                  const int sl = (n == range_start(cc, U, G) / KB) ? 0 : 1;
+                  const float4* part = reinterpret_cast<const float4*>(partial_ptr(p, cc, sl, n_local) + g16 * 16);
+#pragma unroll
+                  for (int v = 0; v < 4; ++v) buf[b][v] = __ldcg(part + v);
+                }
+              }
+#pragma unroll
+              for (int b = 0; b < kBatch; ++b) {
+                const long long cc = cc0 + b;
+                if (cc <= c_last) {
+                  if (cc == c) {
+#pragma unroll
+                    for (int t = 0; t < 16; ++t) acc16[t] += vals[g16 * 16 + t];
+                  } else {
+#pragma unroll
+                    for (int v = 0; v < 4; ++v) {
+                      acc16[4 * v + 0] += buf[b][v].x;
+                      acc16[4 * v + 1] += buf[b][v].y;
+                      acc16[4 * v + 2] += buf[b][v].z;
+                      acc16[4 * v + 3] += buf[b][v].w;
+                    }
+                  }
+                }
+              }
+            }
+#pragma unroll
+            for (int t = 0; t < 16; ++t) vals[g16 * 16 + t] = acc16[t];
           }
         }
       }
@@ -320,15 +394,14 @@ int skinny_max_grid(int np, int num_sms) {
   return num_sms;  // one CTA per SM (shared memory bound)
 }
 
-cudaError_t launch_skinny(const CUtensorMap& tmA, const CUtensorMap& tmB, SkinnyParams p, cudaStream_t stream,
-                          LaunchInfo* info) {
+cudaError_t launch_skinny(const CUtensorMap& tmA, const CUtensorMap& tmB, SkinnyParams p, bool pdl,
+                          cudaStream_t stream, LaunchInfo* info) {
   static bool configured[64] = {};
   int dev = 0;
   cudaError_t e = cudaGetDevice(&dev);
   if (e != cudaSuccess) return e;
-  const int smem_max = smem_for(16);  // the largest footprint over np = 16..64
   if (dev < 64 && !configured[dev]) {
-    int worst = smem_max;
+    int worst = 0;
     for (int np = 16; np <= 64; np += 16) worst = smem_for(np) > worst ? smem_for(np) : worst;
     e = cudaFuncSetAttribute(gemm_tn_skinny_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, worst);
     if (e != cudaSuccess) return e;
@@ -347,8 +420,19 @@ cudaError_t launch_skinny(const CUtensorMap& tmA, const CUtensorMap& tmB, Skinny
     info->smem_bytes = smem;
     info->kernel = "gemm_tn_skinny_kernel";
   }
-  gemm_tn_skinny_kernel<<<p.grid, kThreads, smem, stream>>>(tmA, tmB, p);
-  return cudaGetLastError();
+  cudaLaunchConfig_t cfg = {};
+  cudaLaunchAttribute attr[1];
+  cfg.gridDim = dim3(p.grid, 1, 1);
+  cfg.blockDim = dim3(kThreads, 1, 1);
+  cfg.dynamicSmemBytes = smem;
+  cfg.stream = stream;
+  if (pdl) {
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+  }
+  return cudaLaunchKernelEx(&cfg, gemm_tn_skinny_kernel, tmA, tmB, p);
 }
 
 }  // namespace gtn

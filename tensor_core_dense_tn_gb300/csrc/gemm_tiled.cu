@@ -83,23 +83,29 @@ __device__ __forceinline__ bool try_wait(uint32_t bar, uint32_t parity) {
   else return mbar_try_wait(bar, parity);
 }
 
-// Bounded wait on an mbarrier phase.  Returns false if this CTA is aborting.
+// Slow path of a bounded wait: spin on the phase with a %globaltimer limit.
 template <bool CLUSTER>
-__device__ __noinline__ bool wait_bar(uint32_t bar, uint32_t parity, const Abort& ab) {
-  if (try_wait<CLUSTER>(bar, parity)) return true;
+__device__ __noinline__ bool wait_bar_slow(uint32_t bar, uint32_t parity, volatile uint32_t* flag,
+                                           uint64_t timeout_ns, int* status, int role) {
   const uint64_t t0 = globaltimer();
   while (true) {
 #pragma unroll 1
     for (int i = 0; i < 32; ++i)
       if (try_wait<CLUSTER>(bar, parity)) return true;
-    if (ab.flag && *ab.flag) return false;
-    if (globaltimer() - t0 > ab.timeout_ns) {
-      if (ab.flag) *ab.flag = 1;
-      if (atomicCAS(ab.status, 0, kErrTimeout) == 0)
-        atomicExch(ab.status + 1, (ab.role << 24) | (int)blockIdx.x);
+    if (flag && *flag) return false;
+    if (globaltimer() - t0 > timeout_ns) {
+      if (flag) *flag = 1;
+      if (atomicCAS(status, 0, kErrTimeout) == 0) atomicExch(status + 1, (role << 24) | (int)blockIdx.x);
       return false;
     }
   }
+}
+
+// Bounded wait on an mbarrier phase.  Returns false if this CTA is aborting.
+template <bool CLUSTER>
+__device__ __forceinline__ bool wait_bar(uint32_t bar, uint32_t parity, const Abort& ab) {
+  if (try_wait<CLUSTER>(bar, parity)) return true;
+  return wait_bar_slow<CLUSTER>(bar, parity, ab.flag, ab.timeout_ns, ab.status, ab.role);
 }
 
 // Spin for `ns` nanoseconds (lets copies already in flight land before exit).
@@ -178,6 +184,10 @@ __global__ void __launch_bounds__(kThreads, 1)
   if constexpr (kCluster) cluster_sync();
   tc_fence_after();
   const uint32_t tmem_base = *tmem_slot;
+  // Inputs may come from the previous kernel on the stream: no global memory
+  // access before this point (the set-up above overlaps that kernel's tail).
+  griddep_wait();
+  griddep_launch_dependents();
 
   if (warp == 0) {
     // ------------------------------------------------------------ producer
@@ -378,7 +388,7 @@ __global__ void __launch_bounds__(kThreads, 1)
 
 template <int CG, bool OUT_F32>
 cudaError_t launch_impl(const CUtensorMap& tmA, const CUtensorMap& tmB, const CUtensorMap& tmC,
-                        const CUtensorMap& tmD, const TileParams& p, int grid_override,
+                        const CUtensorMap& tmD, const TileParams& p, int grid_override, bool pdl,
                         cudaStream_t stream, LaunchInfo* info) {
   using C_ = Cfg<CG, OUT_F32>;
   auto kern = gemm_tn_tiled_kernel<CG, OUT_F32>;
@@ -396,7 +406,7 @@ cudaError_t launch_impl(const CUtensorMap& tmA, const CUtensorMap& tmB, const CU
     configured[dev] = true;
   }
   cudaLaunchConfig_t cfg = {};
-  cudaLaunchAttribute attr[1];
+  cudaLaunchAttribute attr[2];
   cfg.blockDim = dim3(kThreads, 1, 1);
   cfg.dynamicSmemBytes = C_::SMEM;
   cfg.stream = stream;
@@ -408,6 +418,12 @@ cudaError_t launch_impl(const CUtensorMap& tmA, const CUtensorMap& tmB, const CU
     attr[0].val.clusterDim.z = 1;
     num_attrs = 1;
   }
+  const int n_occupancy_attrs = num_attrs;
+  if (pdl) {
+    attr[num_attrs].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[num_attrs].val.programmaticStreamSerializationAllowed = 1;
+    ++num_attrs;
+  }
   cfg.attrs = attr;
   cfg.numAttrs = num_attrs;
 
@@ -416,8 +432,10 @@ cudaError_t launch_impl(const CUtensorMap& tmA, const CUtensorMap& tmB, const CU
   int max_units = 0;
   if (CG == 2) {
     cfg.gridDim = dim3(2, 1, 1);
+    cfg.numAttrs = n_occupancy_attrs;
     int clusters = 0;
     e = cudaOccupancyMaxActiveClusters(&clusters, kern, &cfg);
+    cfg.numAttrs = num_attrs;
     if (e != cudaSuccess) return e;
     max_units = clusters;
   } else {
@@ -460,13 +478,13 @@ void tiled_shape(int cta_group, int out_f32, int* tile_m, int* tile_n, int* b_ro
 
 cudaError_t launch_tiled(int cta_group, int out_f32, const CUtensorMap& tmA, const CUtensorMap& tmB,
                          const CUtensorMap& tmC, const CUtensorMap& tmD, TileParams p, int grid_override,
-                         cudaStream_t stream, LaunchInfo* info) {
+                         bool pdl, cudaStream_t stream, LaunchInfo* info) {
   if (cta_group == 2) {
-    return out_f32 ? launch_impl<2, true>(tmA, tmB, tmC, tmD, p, grid_override, stream, info)
-                   : launch_impl<2, false>(tmA, tmB, tmC, tmD, p, grid_override, stream, info);
+    return out_f32 ? launch_impl<2, true>(tmA, tmB, tmC, tmD, p, grid_override, pdl, stream, info)
+                   : launch_impl<2, false>(tmA, tmB, tmC, tmD, p, grid_override, pdl, stream, info);
   }
-  return out_f32 ? launch_impl<1, true>(tmA, tmB, tmC, tmD, p, grid_override, stream, info)
-                 : launch_impl<1, false>(tmA, tmB, tmC, tmD, p, grid_override, stream, info);
+  return out_f32 ? launch_impl<1, true>(tmA, tmB, tmC, tmD, p, grid_override, pdl, stream, info)
+                 : launch_impl<1, false>(tmA, tmB, tmC, tmD, p, grid_override, pdl, stream, info);
 }
 
 }  // namespace gtn

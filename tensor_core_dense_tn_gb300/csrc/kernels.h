@@ -42,7 +42,7 @@ struct SkinnyParams {
   const void* C; long long ldc;
   void* D; long long ldd;
   int out_f32;
-  float* partials;     // grid * 2 slots * np * 128 floats
+  float* partials;     // grid * 2 slots * 128 * np floats
   int* counters;       // 4 per n-tile (one per epilogue warp), zero between calls
   int fault;
   uint64_t timeout_ns;
@@ -57,17 +57,20 @@ struct LaunchInfo {
   const char* kernel;
 };
 
-// Tiled persistent kernels (1-SM or 2-SM).  Returns a cudaError_t.
+// Tiled persistent kernels (1-SM or 2-SM).  Returns a cudaError_t.  `pdl`
+// launches with programmatic stream serialisation: the kernel's set-up may
+// overlap the previous kernel on the stream; it waits for that kernel's
+// completion (griddepcontrol.wait) before touching global memory.
 cudaError_t launch_tiled(int cta_group, int out_f32, const CUtensorMap& tmA, const CUtensorMap& tmB,
                          const CUtensorMap& tmC, const CUtensorMap& tmD, TileParams p, int grid_override,
-                         cudaStream_t stream, LaunchInfo* info);
+                         bool pdl, cudaStream_t stream, LaunchInfo* info);
 
 // Tile shape of the tiled kernels for a CTA group size (for host set-up).
 void tiled_shape(int cta_group, int out_f32, int* tile_m, int* tile_n, int* b_rows_per_cta,
                  int* epi_rows, int* epi_cols);
 
 // Skinny (M <= 64) swap-AB stream-K kernel.
-cudaError_t launch_skinny(const CUtensorMap& tmA, const CUtensorMap& tmB, SkinnyParams p,
+cudaError_t launch_skinny(const CUtensorMap& tmA, const CUtensorMap& tmB, SkinnyParams p, bool pdl,
                           cudaStream_t stream, LaunchInfo* info);
 
 // Largest co-resident grid for the skinny kernel at this np.

@@ -35,7 +35,8 @@ def up8(x):
     return (x + 7) // 8 * 8
 
 
-def run_int(M, N, K, path, out_dtype, seed, lda=None, ldb=None, grid=0, skinny_grid=0, alpha=1.0):
+def run_int(M, N, K, path, out_dtype, seed, lda=None, ldb=None, grid=0, skinny_grid=0, alpha=1.0,
+            disable_pdl=0):
     lda = up8(K) if lda is None else lda
     ldb = up8(K) if ldb is None else ldb
     A = gi.draw_bf16(M, K, gi.Dist("int", -4, 4), seed, ld=lda)
@@ -44,7 +45,7 @@ def run_int(M, N, K, path, out_dtype, seed, lda=None, ldb=None, grid=0, skinny_g
     dA, dB = to_dev_bf16(A), to_dev_bf16(B)
     dD, ldd = empty_out(M, N, out_dtype, ld=up8(N))
     rc, st = call(M, N, K, dA, lda, dB, ldb, None, 0, dD, ldd, alpha, 0.0, out_dtype, path=path,
-                  grid=grid, skinny_grid=skinny_grid)
+                  grid=grid, skinny_grid=skinny_grid, disable_pdl=disable_pdl)
     assert rc == 0, g.last_error()
     assert st == 0, g.last_error()
     return from_dev(dD, out_dtype)[:, :N], expect_exact(ref, out_dtype)
@@ -98,10 +99,20 @@ def test_integer_ragged_skinny(shape, out_dtype):
     assert_same(got, exp)
 
 
-@pytest.mark.parametrize("skinny_grid", [1, 3, 7, 64, 151, 1000])
-def test_skinny_stream_k_partitions(skinny_grid):
-    # every split of the (n-tile, k-block) units must give the same exact result
-    got, exp = run_int(16, 640, 1344, PS, gi.OUT_F32, seed=300, skinny_grid=skinny_grid)
+@pytest.mark.parametrize("skinny_grid", [1, 3, 7, 64, 100, 151, 1000])
+@pytest.mark.parametrize("K", [64, 1344, 4160])
+def test_skinny_stream_k_partitions(skinny_grid, K):
+    # every split of the (n-tile, k-block) units gives the same exact result, and the
+    # arrival counters are left clean for the next call
+    for rep in range(2):
+        got, exp = run_int(16, 640, K, PS, gi.OUT_F32, seed=300 + rep, skinny_grid=skinny_grid)
+        assert_same(got, exp)
+
+
+@pytest.mark.parametrize("path", [P1, P2, PS])
+def test_without_programmatic_launch(path):
+    M = 16 if path == PS else 300
+    got, exp = run_int(M, 520, 640, path, gi.OUT_BF16, seed=310, disable_pdl=1)
     assert_same(got, exp)
 
 
