@@ -154,6 +154,36 @@ void gemm_shutdown(void);
 /* Library version, major * 10000 + minor * 100 + patch. */
 int gemm_version(void);
 
+/* The skinny path (1 <= M <= 64) without any allocation at call time.
+ *
+ * The pages have no counterpart to this entry point; it exists for callers
+ * that cannot allocate device memory when they call a GEMM: code that runs
+ * under a memory budget reserved up front (a serving process that owns all
+ * of HBM through its own pool), latency-critical code that cannot afford
+ * cudaMalloc's implicit device synchronisation, and plug-ins whose host
+ * framework owns every allocation.  gemm_bf16_tn allocates the skinny
+ * path's workspace on first use; this entry point calls no cudaMalloc,
+ * cudaFree or other allocating routine.
+ *
+ * Same operation and argument rules as gemm_bf16_tn, restricted to
+ * 1 <= M <= 64, 1 <= N <= 131072 and K >= 1; larger sizes return
+ * GEMM_ERR_INVALID_VALUE (text in gemm_last_error_string).  Its scratch (fp32
+ * partial sums and arrival counters, about 10 MiB) is a fixed device array
+ * inside the library, held by every device that loads the library until the
+ * process exits.  The first call on a device looks up that array's device
+ * address (cudaGetSymbolAddress) with the device current; make that first
+ * call before any stream capture.  Every call on a device shares the array:
+ * each call clears the counters on its stream before its kernel, so calls
+ * ordered in one stream are safe, but calls whose kernels overlap on the GPU
+ * (unordered streams) race and give wrong results.  Device-side timeouts are
+ * reported by gemm_get_status. */
+int gemm_bf16_tn_skinny_noalloc(int64_t M, int64_t N, int64_t K,
+                                const void *A, int64_t lda,
+                                const void *B, int64_t ldb,
+                                const void *C, int64_t ldc,
+                                void *D, int64_t ldd,
+                                float alpha, float beta, int out_dtype, void *stream);
+
 #ifdef __cplusplus
 }
 #endif

@@ -36,7 +36,8 @@ GEMM_ERR_OUT_OF_MEMORY = -7
 GEMM_ERR_CUDA = -8
 
 EXPORTED = ["gemm_bf16_tn", "gemm_bf16_tn_ex", "gemm_get_status", "gemm_get_status_detail",
-            "gemm_last_error_string", "gemm_last_launch_info", "gemm_shutdown", "gemm_version"]
+            "gemm_last_error_string", "gemm_last_launch_info", "gemm_shutdown", "gemm_version",
+            "gemm_bf16_tn_skinny_noalloc"]
 
 
 class GemmError(RuntimeError):
@@ -78,6 +79,8 @@ def load(path: str = LIB_PATH):
         args = [i64, i64, i64, vp, i64, vp, i64, vp, i64, vp, i64, f32, f32, i32, vp]
         lib.gemm_bf16_tn.argtypes = args
         lib.gemm_bf16_tn.restype = i32
+        lib.gemm_bf16_tn_skinny_noalloc.argtypes = args
+        lib.gemm_bf16_tn_skinny_noalloc.restype = i32
         lib.gemm_bf16_tn_ex.argtypes = args + [ctypes.POINTER(GemmConfig)]
         lib.gemm_bf16_tn_ex.restype = i32
         lib.gemm_get_status.argtypes = [vp]
@@ -114,6 +117,13 @@ def gemm_bf16_tn_ex(M, N, K, A, lda, B, ldb, C, ldc, D, ldd, alpha, beta, out_dt
     cfg = ctypes.byref(config) if config is not None else None
     return load().gemm_bf16_tn_ex(M, N, K, A, lda, B, ldb, C or None, ldc, D, ldd, alpha, beta,
                                   out_dtype, stream or None, cfg)
+
+
+def gemm_bf16_tn_skinny_noalloc(M, N, K, A, lda, B, ldb, C, ldc, D, ldd, alpha, beta, out_dtype,
+                                stream) -> int:
+    """Raw C-ABI call of the allocation-free skinny entry point (1 <= M <= 64)."""
+    return load().gemm_bf16_tn_skinny_noalloc(M, N, K, A, lda, B, ldb, C or None, ldc, D, ldd, alpha,
+                                              beta, out_dtype, stream or None)
 
 
 def gemm_get_status(stream=None) -> int:

@@ -311,6 +311,20 @@ int run(int64_t M, int64_t N, int64_t K, const void* A, int64_t lda, const void*
 }
 
 }  // namespace
+
+// Sets the text gemm_last_error_string returns on this thread, for entry
+// points defined in other files.
+void set_error_text(const char* msg) { t_error = msg ? msg : ""; }
+
+// Device address of the current device's status word (the one
+// gemm_get_status reads), for entry points defined in other files.
+cudaError_t status_word_address(int** out) {
+  void* p = nullptr;
+  cudaError_t e = cudaGetSymbolAddress(&p, g_status);
+  if (e == cudaSuccess) *out = static_cast<int*>(p);
+  return e;
+}
+
 }  // namespace gtn
 
 extern "C" {

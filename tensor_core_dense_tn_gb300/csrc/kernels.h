@@ -73,6 +73,11 @@ void tiled_shape(int cta_group, int out_f32, int* tile_m, int* tile_n, int* b_ro
 cudaError_t launch_skinny(const CUtensorMap& tmA, const CUtensorMap& tmB, SkinnyParams p, bool pdl,
                           cudaStream_t stream, LaunchInfo* info);
 
+// Device address of the current device's status word (gemm_api.cu).
+cudaError_t status_word_address(int** out);
+// Text returned by gemm_last_error_string on this thread (gemm_api.cu).
+void set_error_text(const char* msg);
+
 // Largest co-resident grid for the skinny kernel at this np.
 int skinny_max_grid(int np, int num_sms);
 int skinny_stages(int np);
