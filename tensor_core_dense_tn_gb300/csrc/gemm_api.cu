@@ -269,9 +269,10 @@ int run(int64_t M, int64_t N, int64_t K, const void* A, int64_t lda, const void*
     p.num_tiles = (int)nt;
     int group = cfg && cfg->raster_group > 0 ? cfg->raster_group : 0;
     if (group == 0) {
-      // keep the A rows of one raster strip within ~64 MiB of L2
+      // keep the A rows of one raster strip within ~32 MiB of L2 (the
+      // strip is then re-read from L2 for every tile column it meets)
       const long long strip_bytes = (long long)tile_m * (K > 0 ? K : 1) * 2;
-      long long g = (64ll << 20) / strip_bytes;
+      long long g = (32ll << 20) / strip_bytes;
       group = (int)(g < 1 ? 1 : g);
     }
     if (group > p.tiles_m) group = p.tiles_m;
