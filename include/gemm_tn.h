@@ -138,7 +138,8 @@ int gemm_bf16_tn_ex(int64_t M, int64_t N, int64_t K,
 int gemm_get_status(void *stream);
 
 /* Detail word of the last device error: (role << 24) | block index, with
- * role 1 = producer, 2 = MMA issuer, 3 = epilogue.  0 if none. */
+ * role 1 = producer, 2 = MMA issuer, 3 = epilogue, 4 = skinny-path wait for
+ * the other parts of a split tile.  0 if none. */
 int gemm_get_status_detail(void);
 
 /* Human-readable text for the last error on this host thread ("" if none). */

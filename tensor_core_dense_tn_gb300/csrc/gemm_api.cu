@@ -237,7 +237,8 @@ int run(int64_t M, int64_t N, int64_t K, const void* A, int64_t lda, const void*
     p.num_kb = (int)((K + 63) / 64);
     p.n_tiles = (int)((N + 127) / 128);
     p.units = (long long)p.n_tiles * p.num_kb;
-    int grid = (cfg && cfg->skinny_grid > 0) ? cfg->skinny_grid : skinny_max_grid(np, st->sms);
+    int grid = (cfg && cfg->skinny_grid > 0) ? cfg->skinny_grid
+                                              : skinny_default_grid(p.n_tiles, p.num_kb, skinny_max_grid(np, st->sms));
     if ((long long)grid > p.units) grid = (int)p.units;
     if (grid < 1) grid = 1;
     p.grid = grid;

@@ -13,10 +13,14 @@
 //
 // Work is the list of (n-tile, k-block) units, split into `grid` contiguous
 // ranges, one per CTA (stream-K), so every SM streams the same number of
-// bytes.  A CTA that covers a whole n-tile writes D directly.  A tile split
-// between CTAs leaves fp32 partials in a workspace; the last CTA to finish a
-// part of that tile (per-tile arrival counters) adds the parts in k order,
-// so the result does not depend on timing.  No CTA ever waits for another.
+// bytes.  A CTA that covers a whole n-tile writes D directly.  In a tile
+// split between CTAs, the CTA holding the tile's first k-blocks finishes it:
+// that part is always the last segment of its range, so by the time it gets
+// there the other parts (first segments, or whole ranges, of later CTAs) are
+// done or nearly so.  Those write fp32 partials to a workspace and count
+// them without waiting; the finisher waits (bounded) for the count and adds
+// the parts in k order, so the result does not depend on timing.  No CTA
+// waits in front of a part another CTA needs, so waits never chain.
 //
 // Roles: warp 0 lane 0 issues TMA loads into a deep ring (its first loads go
 // out before the block-wide start-up sync); warp 1 lane 0 issues tcgen05.mma
@@ -298,25 +302,53 @@ __global__ void __launch_bounds__(kThreads, 1)
       const int ng = (int)(n * 128) + n_local;
       bool finish = whole;
       if (!whole) {
-        const int slot = (n == first_tile) ? 0 : 1;
-        float4* mine = reinterpret_cast<float4*>(partial_ptr(p, c, slot, n_local));
-#pragma unroll
-        for (int g4 = 0; g4 < 16; ++g4)
-          if (g4 * 4 < p.np) mine[g4] = make_float4(vals[4 * g4], vals[4 * g4 + 1], vals[4 * g4 + 2], vals[4 * g4 + 3]);
-        // The warp barrier orders every lane's partial before lane 0's
-        // release; lane 0's acquire is passed back to the lanes the same way.
-        __syncwarp();
+        // A split tile's parts: the head belongs to c_first and is always
+        // the last segment of c_first's range; every other part is the only
+        // segment of a CTA inside the tile or the first segment of c_last.
+        // c_first finishes the tile; the others publish a partial and go on.
         const long long c_first = owner_of(n * KB, U, G);
         const long long c_last = owner_of((n + 1) * KB - 1, U, G);
         const int nseg = (int)(c_last - c_first + 1);
-        int last = 0;
-        if (lane == 0) {
-          const int prev = atom_add_acq_rel_gpu(p.counters + n * 4 + q, 1);
-          last = (prev == nseg - 1);
-          if (last) p.counters[n * 4 + q] = 0;  // ready for the next call
+        int* arrivals = p.counters + n * 4 + q;
+        if (c != c_first) {
+          // Partial laid out so each thread writes 16-byte vectors.  The warp
+          // barrier orders every lane's partial before lane 0's release.
+          const int slot = (n == first_tile) ? 0 : 1;
+          float4* mine = reinterpret_cast<float4*>(partial_ptr(p, c, slot, n_local));
+#pragma unroll
+          for (int g4 = 0; g4 < 16; ++g4)
+            if (g4 * 4 < p.np)
+              mine[g4] = make_float4(vals[4 * g4], vals[4 * g4 + 1], vals[4 * g4 + 2], vals[4 * g4 + 3]);
+          __syncwarp();
+          if (lane == 0) red_add_release_gpu(arrivals, 1);
+        } else {
+          // Wait (bounded) for the other nseg-1 parts.  They are segments no
+          // CTA waits in front of, so this wait never chains into another.
+          int ok = 1;
+          if (lane == 0) {
+            if (ld_acquire_gpu(arrivals) != nseg - 1) {
+              const uint64_t t0 = globaltimer();
+              while (ld_acquire_gpu(arrivals) != nseg - 1) {
+                if (*abort_flag || globaltimer() - t0 > p.timeout_ns) {
+                  if (!*abort_flag) {
+                    *abort_flag = 1;
+                    if (atomicCAS(p.status, 0, kErrTimeout) == 0)
+                      atomicExch(p.status + 1, (kRoleFixup << 24) | (int)blockIdx.x);
+                  }
+                  ok = 0;
+                  break;
+                }
+                __nanosleep(32);
+              }
+            }
+            if (ok) *arrivals = 0;  // every part is in: ready for the next call
+          }
+          ok = __shfl_sync(0xffffffffu, ok, 0);
+          // lane 0's acquire is passed to the other lanes by the warp barrier
+          __syncwarp();
+          if (!ok) break;
+          finish = true;
         }
-        finish = __shfl_sync(0xffffffffu, last, 0) != 0;
-        __syncwarp();
         if (finish) {
           // Add the tile's parts in k order (CTA order), this CTA's own part
           // from registers.  Loads go out in batches of kBatch parts x 16
@@ -392,6 +424,18 @@ int skinny_stages(int np) { return stages_for(np); }
 int skinny_max_grid(int np, int num_sms) {
   (void)np;
   return num_sms;  // one CTA per SM (shared memory bound)
+}
+
+int skinny_default_grid(int n_tiles, int num_kb, int num_sms) {
+  // Splitting every tile into the same number s of equal k-ranges (one CTA
+  // each) leaves every split tile with exactly s parts and every CTA with one
+  // segment; it wins over a full-GPU stream-K split as long as it keeps at
+  // least 80% of the SMs streaming.
+  if (n_tiles < num_sms) {
+    const int s = num_sms / n_tiles;
+    if (s <= num_kb && 5 * n_tiles * s >= 4 * num_sms) return n_tiles * s;
+  }
+  return num_sms;
 }
 
 cudaError_t launch_skinny(const CUtensorMap& tmA, const CUtensorMap& tmB, SkinnyParams p, bool pdl,

@@ -80,6 +80,8 @@ void set_error_text(const char* msg);
 
 // Largest co-resident grid for the skinny kernel at this np.
 int skinny_max_grid(int np, int num_sms);
+// Default number of CTAs (stream-K ranges) for the skinny kernel.
+int skinny_default_grid(int n_tiles, int num_kb, int num_sms);
 int skinny_stages(int np);
 
 }  // namespace gtn
