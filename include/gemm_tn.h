@@ -96,6 +96,8 @@ typedef struct gemm_tn_config {
   int test_fault;           /* tests only: 1 = the producer of CTA 0 drops one stage's loads,
                                so the consumer's bounded wait must expire (GEMM_ERR_TIMEOUT) */
   int disable_pdl;          /* 1 = launch without programmatic dependent launch (see below) */
+  int skinny_skew_kb;       /* skinny path, equal-split mode: k-blocks (of 64) moved to the part that
+                               finishes each tile; 0 = default (K/4096), < 0 = none */
 } gemm_tn_config;
 
 /* What the last successful launch on this host thread ran. */

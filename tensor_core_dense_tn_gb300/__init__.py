@@ -49,7 +49,8 @@ class GemmError(RuntimeError):
 class GemmConfig(ctypes.Structure):
     _fields_ = [("path", ctypes.c_int), ("grid", ctypes.c_int), ("raster_group", ctypes.c_int),
                 ("skinny_grid", ctypes.c_int), ("wait_timeout_ns", ctypes.c_uint64),
-                ("test_fault", ctypes.c_int), ("disable_pdl", ctypes.c_int)]
+                ("test_fault", ctypes.c_int), ("disable_pdl", ctypes.c_int),
+                ("skinny_skew_kb", ctypes.c_int)]
 
 
 class LaunchInfo(ctypes.Structure):

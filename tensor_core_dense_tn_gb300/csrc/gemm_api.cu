@@ -237,11 +237,8 @@ int run(int64_t M, int64_t N, int64_t K, const void* A, int64_t lda, const void*
     p.num_kb = (int)((K + 63) / 64);
     p.n_tiles = (int)((N + 127) / 128);
     p.units = (long long)p.n_tiles * p.num_kb;
-    int grid = (cfg && cfg->skinny_grid > 0) ? cfg->skinny_grid
-                                              : skinny_default_grid(p.n_tiles, p.num_kb, skinny_max_grid(np, st->sms));
-    if ((long long)grid > p.units) grid = (int)p.units;
-    if (grid < 1) grid = 1;
-    p.grid = grid;
+    skinny_partition(&p, skinny_max_grid(np, st->sms), cfg ? cfg->skinny_grid : 0, cfg ? cfg->skinny_skew_kb : 0);
+    const int grid = p.grid;
     p.alpha = alpha; p.beta = beta; p.has_c = has_c;
     p.C = C; p.ldc = ldc; p.D = D; p.ldd = ldd; p.out_f32 = out_dtype == GEMM_OUT_F32;
     p.fault = fault; p.timeout_ns = tmo; p.status = st->status;

@@ -143,10 +143,9 @@ extern "C" int gemm_bf16_tn_skinny_noalloc(int64_t M, int64_t N, int64_t K, cons
   p.num_kb = (int)((K + 63) / 64);
   p.n_tiles = (int)((N + 127) / 128);
   p.units = (long long)p.n_tiles * p.num_kb;
-  int grid = skinny_default_grid(p.n_tiles, p.num_kb, skinny_max_grid(p.np, d->sms));
-  if (grid > kNaMaxGrid) grid = kNaMaxGrid;
-  if ((long long)grid > p.units) grid = (int)p.units;
-  p.grid = grid;
+  int sms = skinny_max_grid(p.np, d->sms);
+  if (sms > kNaMaxGrid) sms = kNaMaxGrid;
+  skinny_partition(&p, sms, 0, 0);
   p.alpha = alpha;
   p.beta = beta;
   p.has_c = has_c;

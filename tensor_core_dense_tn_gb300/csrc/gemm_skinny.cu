@@ -70,6 +70,36 @@ __device__ __forceinline__ long long owner_of(long long x, long long U, long lon
   return ((x + 1) * G + U - 1) / U - 1;
 }
 
+// Split mode: first k-block of part j of a tile (part 0 gets `skew` extra
+// k-blocks, the last part as many fewer).
+__device__ __forceinline__ long long split_bound(const SkinnyParams& p, long long j) {
+  if (j <= 0) return 0;
+  if (j >= p.split) return p.num_kb;
+  return j * p.num_kb / p.split + p.skew;
+}
+
+// First and one-past-last unit of CTA c's range.
+__device__ __forceinline__ long long cta_begin(const SkinnyParams& p, long long c) {
+  if (p.split == 0) return range_start(c, p.units, p.grid);
+  return (c % p.n_tiles) * p.num_kb + split_bound(p, c / p.n_tiles);
+}
+__device__ __forceinline__ long long cta_end(const SkinnyParams& p, long long c) {
+  if (p.split == 0) return range_start(c + 1, p.units, p.grid);
+  return (c % p.n_tiles) * p.num_kb + split_bound(p, c / p.n_tiles + 1);
+}
+
+// Number of CTAs holding a part of tile n, and the CTA holding part j
+// (part 0 = the tile's first k-blocks).
+__device__ __forceinline__ int tile_parts(const SkinnyParams& p, long long n) {
+  if (p.split) return p.split;
+  const long long KB = p.num_kb;
+  return (int)(owner_of((n + 1) * KB - 1, p.units, p.grid) - owner_of(n * KB, p.units, p.grid) + 1);
+}
+__device__ __forceinline__ long long tile_part_cta(const SkinnyParams& p, long long n, int j) {
+  if (p.split) return n + (long long)j * p.n_tiles;
+  return owner_of(n * p.num_kb, p.units, p.grid) + j;
+}
+
 __device__ __noinline__ bool wait_bar_slow(uint32_t bar, uint32_t parity, volatile uint32_t* flag,
                                            uint64_t timeout_ns, int* status, int role) {
   const uint64_t t0 = globaltimer();
@@ -145,7 +175,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   const int lane = threadIdx.x & 31;
   const long long U = p.units, G = p.grid, KB = p.num_kb;
   const long long c = blockIdx.x;
-  const long long u_begin = range_start(c, U, G), u_end = range_start(c + 1, U, G);
+  const long long u_begin = cta_begin(p, c), u_end = cta_end(p, c);
 
   // ---- producer state (thread 0).  The first ring's worth of loads is
   // issued right after the barriers exist, before the block-wide sync, so
@@ -302,13 +332,12 @@ __global__ void __launch_bounds__(kThreads, 1)
       const int ng = (int)(n * 128) + n_local;
       bool finish = whole;
       if (!whole) {
-        // A split tile's parts: the head belongs to c_first and is always
-        // the last segment of c_first's range; every other part is the only
-        // segment of a CTA inside the tile or the first segment of c_last.
-        // c_first finishes the tile; the others publish a partial and go on.
-        const long long c_first = owner_of(n * KB, U, G);
-        const long long c_last = owner_of((n + 1) * KB - 1, U, G);
-        const int nseg = (int)(c_last - c_first + 1);
+        // A split tile's parts.  Part 0 (the tile's first k-blocks) is
+        // always the last segment of its CTA's range; every other part is the
+        // only segment of its CTA or that CTA's first segment.  Part 0's CTA
+        // finishes the tile; the others publish a partial and go on.
+        const long long c_first = tile_part_cta(p, n, 0);
+        const int nseg = tile_parts(p, n);
         int* arrivals = p.counters + n * 4 + q;
         if (c != c_first) {
           // Partial laid out so each thread writes 16-byte vectors.  The warp
@@ -360,13 +389,13 @@ __global__ void __launch_bounds__(kThreads, 1)
             float acc16[16];
 #pragma unroll
             for (int t = 0; t < 16; ++t) acc16[t] = 0.0f;
-            for (long long cc0 = c_first; cc0 <= c_last; cc0 += kBatch) {
+            for (int j0 = 0; j0 < nseg; j0 += kBatch) {
               float4 buf[kBatch][4];
 #pragma unroll
               for (int b = 0; b < kBatch; ++b) {
-                const long long cc = cc0 + b;
-                if (cc <= c_last && cc != c) {
-                  const int sl = (n == range_start(cc, U, G) / KB) ? 0 : 1;
+                const long long cc = j0 + b < nseg ? tile_part_cta(p, n, j0 + b) : -1;
+                if (cc >= 0 && cc != c) {
+                  const int sl = (n == cta_begin(p, cc) / KB) ? 0 : 1;
                   const float4* part = reinterpret_cast<const float4*>(partial_ptr(p, cc, sl, n_local) + g16 * 16);
 #pragma unroll
                   for (int v = 0; v < 4; ++v) buf[b][v] = __ldcg(part + v);
@@ -374,9 +403,8 @@ __global__ void __launch_bounds__(kThreads, 1)
               }
 #pragma unroll
               for (int b = 0; b < kBatch; ++b) {
-                const long long cc = cc0 + b;
-                if (cc <= c_last) {
-                  if (cc == c) {
+                if (j0 + b < nseg) {
+                  if (j0 + b == 0) {  // part 0 is this CTA's own
 #pragma unroll
                     for (int t = 0; t < 16; ++t) acc16[t] += vals[g16 * 16 + t];
                   } else {
@@ -426,16 +454,33 @@ int skinny_max_grid(int np, int num_sms) {
   return num_sms;  // one CTA per SM (shared memory bound)
 }
 
-int skinny_default_grid(int n_tiles, int num_kb, int num_sms) {
-  // Splitting every tile into the same number s of equal k-ranges (one CTA
-  // each) leaves every split tile with exactly s parts and every CTA with one
-  // segment; it wins over a full-GPU stream-K split as long as it keeps at
-  // least 80% of the SMs streaming.
-  if (n_tiles < num_sms) {
-    const int s = num_sms / n_tiles;
-    if (s <= num_kb && 5 * n_tiles * s >= 4 * num_sms) return n_tiles * s;
+void skinny_partition(SkinnyParams* p, int num_sms, int grid_override, int skew_kb) {
+  p->split = 0;
+  p->skew = 0;
+  if (grid_override > 0) {
+    const long long g = grid_override < p->units ? grid_override : p->units;
+    p->grid = (int)(g < 1 ? 1 : g);
+    return;
   }
-  return num_sms;
+  // Splitting every tile into the same number s of k-ranges (one CTA each)
+  // leaves every CTA with one segment; it wins over a full-GPU stream-K split
+  // as long as it keeps at least 80% of the SMs streaming.  Part j of tile n
+  // goes to CTA n + j * n_tiles, so the parts of a tile sit on SMs spread
+  // across the grid.  Part 0's CTA finishes the tile after the other parts
+  // land, so it gets a few more k-blocks.
+  if (p->n_tiles < num_sms) {
+    const int s = num_sms / p->n_tiles;
+    if (s >= 2 && s <= p->num_kb && 5 * p->n_tiles * s >= 4 * num_sms) {
+      p->grid = p->n_tiles * s;
+      p->split = s;
+      int skew = skew_kb > 0 ? skew_kb : (skew_kb < 0 ? 0 : p->num_kb / 64);
+      const int room = p->num_kb / s - 1;  // every part keeps at least one k-block
+      p->skew = skew < room ? skew : (room > 0 ? room : 0);
+      return;
+    }
+  }
+  const long long g = num_sms < p->units ? num_sms : p->units;
+  p->grid = (int)(g < 1 ? 1 : g);
 }
 
 cudaError_t launch_skinny(const CUtensorMap& tmA, const CUtensorMap& tmB, SkinnyParams p, bool pdl,

@@ -36,6 +36,9 @@ struct SkinnyParams {
   int n_tiles;         // ceil(N / 128)
   long long units;     // n_tiles * num_kb
   int grid;            // CTAs; each owns a contiguous range of units
+  int split;           // 0: stream-K ranges over the grid; s >= 2: every tile in s parts,
+                       //    CTA c holds part c / n_tiles of tile c % n_tiles
+  int skew;            // split mode: k-blocks moved from the last part to part 0
   int stages;
   float alpha, beta;
   int has_c;
@@ -80,8 +83,10 @@ void set_error_text(const char* msg);
 
 // Largest co-resident grid for the skinny kernel at this np.
 int skinny_max_grid(int np, int num_sms);
-// Default number of CTAs (stream-K ranges) for the skinny kernel.
-int skinny_default_grid(int n_tiles, int num_kb, int num_sms);
+// Work partition of the skinny kernel: fills p->grid, p->split and p->skew
+// from p->n_tiles and p->num_kb.  grid_override > 0 forces a stream-K grid;
+// skew_kb: 0 = default, > 0 = that many k-blocks, < 0 = none.
+void skinny_partition(SkinnyParams* p, int num_sms, int grid_override, int skew_kb);
 int skinny_stages(int np);
 
 }  // namespace gtn

@@ -109,6 +109,26 @@ def test_skinny_stream_k_partitions(skinny_grid, K):
         assert_same(got, exp)
 
 
+@pytest.mark.parametrize("skew", [-1, 1, 5, 1000])
+def test_skinny_equal_split_skew(skew):
+    # default grid on 16 x 1024 x 4096 is the equal-split mode (8 tiles x 19 parts on 152 SMs);
+    # every skew (clamped so each part keeps a k-block) gives the exact result
+    import torch
+    M, N, K = 16, 1024, 4096
+    A = gi.draw_bf16(M, K, gi.Dist("int", -4, 4), 320)
+    B = gi.draw_bf16(N, K, gi.Dist("int", -4, 4), 321)
+    ref, _ = oracle.gemm_ref(A, B)
+    for rep in range(2):
+        dD, ldd = empty_out(M, N, gi.OUT_F32)
+        cfg = g.GemmConfig(path=PS, skinny_skew_kb=skew)
+        rc = g.gemm_bf16_tn_ex(M, N, K, to_dev_bf16(A).data_ptr(), K, to_dev_bf16(B).data_ptr(), K, 0, 0,
+                               dD.data_ptr(), ldd, 1.0, 0.0, gi.OUT_F32,
+                               torch.cuda.current_stream().cuda_stream, cfg)
+        assert rc == 0, g.last_error()
+        assert g.gemm_get_status(torch.cuda.current_stream().cuda_stream) == 0
+        assert_same(from_dev(dD, gi.OUT_F32), oracle.exact_f32(ref))
+
+
 @pytest.mark.parametrize("path", [P1, P2, PS])
 def test_without_programmatic_launch(path):
     M = 16 if path == PS else 300
