@@ -46,7 +46,7 @@ from tensor_core_dense_tn_gb300 import roofline as rl  # noqa: E402
 METRIC = "BF16 GEMM TFLOP/s at 8192×28672×4096 (% of tensor peak); GB/s at M=16"
 MAIN = 3       # index of the 8192x28672x4096 workload
 DECODE = 4     # index of the 16x8192x8192 workload
-KERNEL_SOURCES = ("gemm_api.cu", "gemm_tiled.cu", "gemm_skinny.cu", "ptx.cuh", "kernels.h")
+KERNEL_SOURCES = ("gemm_api.cu", "gemm_tiled.cu", "gemm_skinny.cu", "ptx.cuh", "kernels.h", "epilogue.cuh")
 PATH_NAMES = {1: "1sm", 2: "2sm", 3: "skinny"}
 
 
@@ -287,6 +287,29 @@ def run_ours(args, dist):
         "gpu_launches": args.steps,
         "clocks": clocks,
     }
+
+    # ---------------------------------------------------------------- fused bias + GELU
+    if not args.no_secondary:
+        hb = gi.draw_bf16(w.N, 1, gi.Dist("normal", 1.0), w.seed(gi.TENSOR_C)).reshape(w.N)
+        dbias = dev_bf16(hb, torch, device)
+
+        def fused(_i):
+            rc = g.gemm_bf16_tn_bias_act(w.M, w.N, w.K, dA.data_ptr(), w.K, dB.data_ptr(), w.K, c_ptr, ldc,
+                                         dD.data_ptr(), w.N, w.alpha, w.beta, w.out_dtype,
+                                         dbias.data_ptr(), 0, g.ACT_GELU_TANH, s_handle)
+            if rc != 0:
+                raise RuntimeError(f"fused gemm failed: {rc} {g.last_error()}")
+
+        for i in range(3):
+            fused(i)
+        f_steps = max(10, min(args.steps, 50))
+        f_ms = dist.max(time_steps(torch, stream, fused, f_steps))
+        if g.gemm_get_status(s_handle) != 0:
+            raise RuntimeError(g.last_error())
+        result["fused_bias_gelu"] = {
+            "value": round(dist.world * flops / (f_ms / 1e3 / f_steps) / 1e12, 2), "unit": "TFLOP/s",
+            "ms_per_step": round(f_ms / f_steps, 4), "steps": f_steps,
+            "op": "D = gelu_tanh(A B^T + bias) in the GEMM epilogue (gemm_bf16_tn_bias_act)"}
 
     # ---------------------------------------------------------------- e2e (host buffers)
     if not args.no_e2e:

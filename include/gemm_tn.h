@@ -79,6 +79,14 @@ typedef enum {
 } gemm_status;
 
 typedef enum {
+  GEMM_ACT_NONE = 0,
+  GEMM_ACT_RELU = 1,       /* max(x, 0) */
+  GEMM_ACT_GELU = 2,       /* x * Phi(x) = 0.5 x (1 + erf(x / sqrt 2)) */
+  GEMM_ACT_GELU_TANH = 3,  /* 0.5 x (1 + tanh(sqrt(2/pi) (x + 0.044715 x^3))) */
+  GEMM_ACT_SILU = 4        /* x / (1 + exp(-x)) */
+} gemm_activation;
+
+typedef enum {
   GEMM_PATH_AUTO = 0,   /* choose by shape */
   GEMM_PATH_1SM = 1,    /* persistent tiled kernel, 128x256 tile, one CTA per SM */
   GEMM_PATH_2SM = 2,    /* persistent tiled kernel, 256x256 tile per CTA pair */
@@ -132,6 +140,25 @@ int gemm_bf16_tn_ex(int64_t M, int64_t N, int64_t K,
                     void *D, int64_t ldd,
                     float alpha, float beta, int out_dtype, void *stream,
                     const gemm_tn_config *cfg);
+
+/* Fused epilogue for MLP layers:
+ *
+ *     D = act(alpha * A * B^T + beta * C + bias)
+ *
+ * bias holds N values (one per output column, i.e. per row of B), in bf16
+ * (bias_dtype 0) or fp32 (bias_dtype 1), device memory, aligned to its
+ * element size; NULL means no bias.  activation is a gemm_activation; it is
+ * evaluated in fp32 before the single rounding to out_dtype.  Every other
+ * argument, and the error behaviour, are those of gemm_bf16_tn.  It fuses
+ * the step after the GEMM in an MLP up-projection (the epilogue fusion the
+ * H100 Nsight Compute page lists among GEMM optimisations, section 7). */
+int gemm_bf16_tn_bias_act(int64_t M, int64_t N, int64_t K,
+                          const void *A, int64_t lda,
+                          const void *B, int64_t ldb,
+                          const void *C, int64_t ldc,
+                          void *D, int64_t ldd,
+                          float alpha, float beta, int out_dtype,
+                          const void *bias, int bias_dtype, int activation, void *stream);
 
 /* Synchronises `stream`, then returns and clears the current device's status
  * word: GEMM_OK, or GEMM_ERR_TIMEOUT if a kernel's bounded wait gave up since

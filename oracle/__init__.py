@@ -62,6 +62,8 @@ def _load():
                                                     i32, d, d, i64, p, p, p, p, i32]
             lib.oracle_gemm_f64_sampled.restype = i32
             lib.oracle_nthreads_default.restype = i32
+            lib.oracle_epilogue_f64.argtypes = [i64, i64, p, i64, p, i32, i32]
+            lib.oracle_epilogue_f64.restype = i32
             _lib = lib
     return _lib
 
@@ -135,6 +137,52 @@ def gemm_ref_sampled(A, B, rows, cols, C=None, alpha=1.0, beta=0.0, M=None, N=No
     if rc != 0:
         raise ValueError("oracle_gemm_f64_sampled rejected its arguments")
     return ref, absdot
+
+
+def epilogue(ref, bias=None, act=0):
+    """act(ref + bias[n]) in FP64 (see gemm_ref.c); returns a new array.
+
+    bias: N values as bf16 bits (uint16) or float32, or None.
+    act: 0 none, 1 ReLU, 2 GELU (erf), 3 GELU (tanh), 4 SiLU.
+    """
+    out = np.array(ref, dtype=np.float64, order="C", copy=True)
+    if out.ndim != 2:
+        raise ValueError("ref must be 2-D")
+    M, N = out.shape
+    bd = 0
+    if bias is not None:
+        bias = np.ascontiguousarray(bias)
+        if bias.shape != (N,):
+            raise ValueError("bias must hold N values")
+        if bias.dtype == np.float32:
+            bd = 1
+        elif bias.dtype != np.uint16:
+            raise TypeError("bias must be bf16 bits (uint16) or float32")
+    rc = _load().oracle_epilogue_f64(M, N, _ptr(out), N, _ptr(bias), bd, int(act))
+    if rc != 0:
+        raise ValueError("oracle_epilogue_f64 rejected its arguments")
+    return out
+
+
+# Largest slope of each activation (bounds how a pre-activation error grows).
+ACT_LIPSCHITZ = {0: 1.0, 1: 1.0, 2: 1.13, 3: 1.13, 4: 1.1}
+
+
+def bound_act(z, fz, absdot, out_dtype, act, beta=0.0, c=None):
+    """Allowed |D - act(z)| when D = act(alpha A B^T + beta C + bias) is computed
+    with fp32 accumulation and an fp32 activation: the pre-activation bound
+    (1e-4 (absdot + |beta c|) plus fp32 rounding of the epilogue sums) times the
+    activation's slope, plus the fp32 evaluation error of the activation
+    (cancellation in 1 + erf / 1 + tanh costs up to ~2^-22 |z|), plus one bf16
+    ulp of |act(z)| for bf16 output."""
+    z = np.asarray(z, dtype=np.float64)
+    pre = 1e-4 * np.asarray(absdot, dtype=np.float64) + 2.0 ** -22 * np.abs(z)
+    if beta != 0.0 and c is not None:
+        pre = pre + 1e-4 * np.abs(beta * np.asarray(c, dtype=np.float64))
+    b = ACT_LIPSCHITZ[act] * pre + 2.0 ** -21 * (np.abs(z) + np.abs(fz))
+    if out_dtype == 0:
+        b = b + ulp_bf16(fz)
+    return b
 
 
 # ---------------------------------------------------------------------------

@@ -169,3 +169,39 @@ int oracle_gemm_f64_sampled(int64_t M, int64_t N, int64_t K, const uint16_t *A,
 }
 
 int oracle_nthreads_default(void) { return nthreads_or_default(0); }
+
+/*
+ * Fused MLP epilogue, in FP64: ref[i][j] <- act(ref[i][j] + bias[j]).
+ *
+ * bias holds N values (bf16 bits, bias_dtype 0, or float, bias_dtype 1) or
+ * is NULL.  act: 0 none, 1 ReLU max(x, 0), 2 GELU x * Phi(x) with
+ * Phi(x) = (1 + erf(x / sqrt 2)) / 2, 3 the tanh approximation of GELU
+ * 0.5 x (1 + tanh(sqrt(2/pi) (x + 0.044715 x^3))), 4 SiLU x / (1 + e^-x).
+ * These are the usual definitions of the activations an MLP up-projection
+ * applies after adding its bias (the epilogue-fusion step the H100 Nsight
+ * Compute page lists among GEMM optimisations, section 7).
+ */
+static double act_f64(double x, int act) {
+  switch (act) {
+    case 1: return x > 0.0 ? x : 0.0;
+    case 2: return 0.5 * x * (1.0 + erf(x / sqrt(2.0)));
+    case 3: {
+      const double k = sqrt(2.0 / 3.14159265358979323846);
+      return 0.5 * x * (1.0 + tanh(k * (x + 0.044715 * x * x * x)));
+    }
+    case 4: return x / (1.0 + exp(-x));
+    default: return x;
+  }
+}
+
+int oracle_epilogue_f64(int64_t M, int64_t N, double *ref, int64_t ldr,
+                        const void *bias, int bias_dtype, int act) {
+  if (M < 0 || N < 0 || ldr < N || act < 0 || act > 4) return -1;
+  for (int64_t i = 0; i < M; ++i)
+    for (int64_t j = 0; j < N; ++j) {
+      double b = 0.0;
+      if (bias) b = bias_dtype == 0 ? dec_bf16(((const uint16_t *)bias)[j]) : (double)((const float *)bias)[j];
+      ref[i * ldr + j] = act_f64(ref[i * ldr + j] + b, act);
+    }
+  return 0;
+}

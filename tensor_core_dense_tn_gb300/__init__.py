@@ -37,7 +37,9 @@ GEMM_ERR_CUDA = -8
 
 EXPORTED = ["gemm_bf16_tn", "gemm_bf16_tn_ex", "gemm_get_status", "gemm_get_status_detail",
             "gemm_last_error_string", "gemm_last_launch_info", "gemm_shutdown", "gemm_version",
-            "gemm_bf16_tn_skinny_noalloc"]
+            "gemm_bf16_tn_skinny_noalloc", "gemm_bf16_tn_bias_act"]
+
+ACT_NONE, ACT_RELU, ACT_GELU, ACT_GELU_TANH, ACT_SILU = 0, 1, 2, 3, 4
 
 
 class GemmError(RuntimeError):
@@ -80,6 +82,8 @@ def load(path: str = LIB_PATH):
         args = [i64, i64, i64, vp, i64, vp, i64, vp, i64, vp, i64, f32, f32, i32, vp]
         lib.gemm_bf16_tn.argtypes = args
         lib.gemm_bf16_tn.restype = i32
+        lib.gemm_bf16_tn_bias_act.argtypes = args[:-1] + [vp, i32, i32, vp]
+        lib.gemm_bf16_tn_bias_act.restype = i32
         lib.gemm_bf16_tn_skinny_noalloc.argtypes = args
         lib.gemm_bf16_tn_skinny_noalloc.restype = i32
         lib.gemm_bf16_tn_ex.argtypes = args + [ctypes.POINTER(GemmConfig)]
@@ -125,6 +129,13 @@ def gemm_bf16_tn_skinny_noalloc(M, N, K, A, lda, B, ldb, C, ldc, D, ldd, alpha, 
     """Raw C-ABI call of the allocation-free skinny entry point (1 <= M <= 64)."""
     return load().gemm_bf16_tn_skinny_noalloc(M, N, K, A, lda, B, ldb, C or None, ldc, D, ldd, alpha,
                                               beta, out_dtype, stream or None)
+
+
+def gemm_bf16_tn_bias_act(M, N, K, A, lda, B, ldb, C, ldc, D, ldd, alpha, beta, out_dtype, bias,
+                          bias_dtype, activation, stream) -> int:
+    """Raw C-ABI call: D = act(alpha * A B^T + beta * C + bias)."""
+    return load().gemm_bf16_tn_bias_act(M, N, K, A, lda, B, ldb, C or None, ldc, D, ldd, alpha, beta,
+                                        out_dtype, bias or None, bias_dtype, activation, stream or None)
 
 
 def gemm_get_status(stream=None) -> int:

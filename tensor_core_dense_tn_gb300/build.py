@@ -18,7 +18,7 @@ OUT_DIR = os.path.join(PKG, "_lib")
 BUILD_DIR = os.path.join(PKG, "_build")
 LIB = os.path.join(OUT_DIR, "libgemm_tn.so")
 SOURCES = ["gemm_api.cu", "gemm_tiled.cu", "gemm_skinny.cu", "gemm_noalloc.cu"]
-HEADERS = ["ptx.cuh", "kernels.h"]
+HEADERS = ["ptx.cuh", "kernels.h", "epilogue.cuh"]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 
 

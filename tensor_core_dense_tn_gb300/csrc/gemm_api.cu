@@ -169,7 +169,7 @@ int get_workspace(int dev, cudaStream_t stream, size_t partial_floats, size_t co
 
 int run(int64_t M, int64_t N, int64_t K, const void* A, int64_t lda, const void* B, int64_t ldb, const void* C,
         int64_t ldc, void* D, int64_t ldd, float alpha, float beta, int out_dtype, void* stream_v,
-        const gemm_tn_config* cfg) {
+        const gemm_tn_config* cfg, Epilogue epi = Epilogue{nullptr, 0, kActNone}) {
   t_error.clear();
   cudaStream_t stream = static_cast<cudaStream_t>(stream_v);
   // ---- argument validation
@@ -239,7 +239,7 @@ int run(int64_t M, int64_t N, int64_t K, const void* A, int64_t lda, const void*
     p.units = (long long)p.n_tiles * p.num_kb;
     skinny_partition(&p, skinny_max_grid(np, st->sms), cfg ? cfg->skinny_grid : 0, cfg ? cfg->skinny_skew_kb : 0);
     const int grid = p.grid;
-    p.alpha = alpha; p.beta = beta; p.has_c = has_c;
+    p.alpha = alpha; p.beta = beta; p.has_c = has_c; p.epi = epi;
     p.C = C; p.ldc = ldc; p.D = D; p.ldd = ldd; p.out_f32 = out_dtype == GEMM_OUT_F32;
     p.fault = fault; p.timeout_ns = tmo; p.status = st->status;
     Workspace* w = nullptr;
@@ -275,7 +275,7 @@ int run(int64_t M, int64_t N, int64_t K, const void* A, int64_t lda, const void*
     }
     if (group > p.tiles_m) group = p.tiles_m;
     p.raster_group = group;
-    p.alpha = alpha; p.beta = beta; p.has_c = has_c;
+    p.alpha = alpha; p.beta = beta; p.has_c = has_c; p.epi = epi;
     p.fault = fault; p.timeout_ns = tmo; p.status = st->status;
     CUtensorMap tA, tB, tC, tD;
     memset(&tA, 0, sizeof tA);
@@ -338,6 +338,20 @@ int gemm_bf16_tn_ex(int64_t M, int64_t N, int64_t K, const void* A, int64_t lda,
                     const void* C, int64_t ldc, void* D, int64_t ldd, float alpha, float beta, int out_dtype,
                     void* stream, const gemm_tn_config* cfg) {
   return gtn::run(M, N, K, A, lda, B, ldb, C, ldc, D, ldd, alpha, beta, out_dtype, stream, cfg);
+}
+
+int gemm_bf16_tn_bias_act(int64_t M, int64_t N, int64_t K, const void* A, int64_t lda, const void* B, int64_t ldb,
+                          const void* C, int64_t ldc, void* D, int64_t ldd, float alpha, float beta, int out_dtype,
+                          const void* bias, int bias_dtype, int activation, void* stream) {
+  using namespace gtn;
+  if (activation < GEMM_ACT_NONE || activation > GEMM_ACT_SILU)
+    return fail(GEMM_ERR_INVALID_VALUE, "unknown activation %d", activation);
+  if (bias && bias_dtype != GEMM_OUT_BF16 && bias_dtype != GEMM_OUT_F32)
+    return fail(GEMM_ERR_INVALID_VALUE, "bias_dtype must be 0 (bf16) or 1 (fp32), got %d", bias_dtype);
+  if (bias && (reinterpret_cast<uintptr_t>(bias) & (bias_dtype == GEMM_OUT_F32 ? 3u : 1u)))
+    return fail(GEMM_ERR_MISALIGNED, "bias must be aligned to its element size");
+  const Epilogue epi{bias, bias_dtype == GEMM_OUT_F32 ? 1 : 0, activation};
+  return run(M, N, K, A, lda, B, ldb, C, ldc, D, ldd, alpha, beta, out_dtype, stream, nullptr, epi);
 }
 
 int gemm_get_status(void* stream) {

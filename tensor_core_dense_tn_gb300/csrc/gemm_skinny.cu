@@ -32,6 +32,7 @@
 
 #include <cstdint>
 
+#include "epilogue.cuh"
 #include "kernels.h"
 #include "ptx.cuh"
 
@@ -425,11 +426,13 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
       }
       if (finish && ng < p.N) {
+        const float bias_n = p.epi.bias ? load_bias(p.epi, ng) : 0.0f;
 #pragma unroll
         for (int m = 0; m < 64; ++m) {
           if (m < p.M) {
             float v = p.alpha * vals[m];
             if (p.has_c) v = fmaf(p.beta, load_c(p, m, ng), v);
+            if (p.epi.bias || p.epi.act) v = activate(v + bias_n, p.epi.act);
             store_d(p, m, ng, v);
           }
         }

@@ -36,6 +36,7 @@
 
 #include <cstdint>
 
+#include "epilogue.cuh"
 #include "kernels.h"
 #include "ptx.cuh"
 
@@ -346,6 +347,18 @@ __global__ void __launch_bounds__(kThreads, 1)
                 v[8 * j + 2 * e + 1] = fmaf(p.beta, __uint_as_float(x[e] & 0xFFFF0000u), v[8 * j + 2 * e + 1]);
               }
             }
+          }
+        }
+        if (p.epi.bias || p.epi.act) {
+          // bias is per column: lane l fetches column col0 + l, every lane
+          // then takes the 32 values by shuffle
+          float bl = 0.0f;
+          if (p.epi.bias && col0 + lane < p.N) bl = load_bias(p.epi, col0 + lane);
+#pragma unroll
+          for (int j = 0; j < 32; ++j) {
+            float x = v[j];
+            if (p.epi.bias) x += __shfl_sync(0xffffffffu, bl, j);
+            v[j] = activate(x, p.epi.act);
           }
         }
         if constexpr (OUT_F32) {

@@ -17,6 +17,16 @@ enum Role : int { kRoleProducer = 1, kRoleMma = 2, kRoleEpilogue = 3, kRoleFixup
 // Test-only fault injection bits.
 constexpr int kFaultSkipTmaOnce = 1;
 
+// Activation codes (same values as gemm_activation in gemm_tn.h).
+constexpr int kActNone = 0, kActRelu = 1, kActGelu = 2, kActGeluTanh = 3, kActSilu = 4;
+
+// Fused epilogue: D = act(alpha * acc + beta * C + bias[n]).
+struct Epilogue {
+  const void* bias;    // N values (bf16 or fp32) or nullptr
+  int bias_f32;
+  int act;             // kAct*
+};
+
 struct TileParams {
   int M, N, K;
   int num_kb;          // ceil(K / 64)
@@ -24,6 +34,7 @@ struct TileParams {
   int raster_group;    // tiles along M per grouped-raster strip
   float alpha, beta;
   int has_c;           // beta != 0
+  Epilogue epi;
   int fault;           // kFault* bits (tests only)
   uint64_t timeout_ns;
   int* status;
@@ -45,6 +56,7 @@ struct SkinnyParams {
   const void* C; long long ldc;
   void* D; long long ldd;
   int out_f32;
+  Epilogue epi;
   float* partials;     // grid * 2 slots * 128 * np floats
   int* counters;       // 4 per n-tile (one per epilogue warp), zero between calls
   int fault;

@@ -118,10 +118,11 @@ def test_skinny_equal_split_skew(skew):
     A = gi.draw_bf16(M, K, gi.Dist("int", -4, 4), 320)
     B = gi.draw_bf16(N, K, gi.Dist("int", -4, 4), 321)
     ref, _ = oracle.gemm_ref(A, B)
+    dA, dB = to_dev_bf16(A), to_dev_bf16(B)   # keep the buffers alive across the calls
     for rep in range(2):
         dD, ldd = empty_out(M, N, gi.OUT_F32)
         cfg = g.GemmConfig(path=PS, skinny_skew_kb=skew)
-        rc = g.gemm_bf16_tn_ex(M, N, K, to_dev_bf16(A).data_ptr(), K, to_dev_bf16(B).data_ptr(), K, 0, 0,
+        rc = g.gemm_bf16_tn_ex(M, N, K, dA.data_ptr(), K, dB.data_ptr(), K, 0, 0,
                                dD.data_ptr(), ldd, 1.0, 0.0, gi.OUT_F32,
                                torch.cuda.current_stream().cuda_stream, cfg)
         assert rc == 0, g.last_error()

@@ -258,3 +258,49 @@ def test_rne_rounding_of_inputs():
                  dtype=np.float32)
     got = gi.bf16_bits_to_f32(gi.f32_to_bf16_bits(x))
     assert got.tolist() == [1.0, 1.0 + 2 ** -6, 1.0 + 2 ** -7, -1.0]
+
+
+# ----------------------------------------------------------------------------- fused epilogue
+
+
+def test_epilogue_matches_library_activations():
+    """The FP64 activations against torch's own (float64, CPU) implementations."""
+    torch = pytest.importorskip("torch")
+    x = np.concatenate([np.linspace(-12, 12, 4001), [0.0, -0.0, 1e-8, -1e-8, 30.0, -30.0]])
+    ref = x[None, :]
+    t = torch.from_numpy(x)
+    lib = {1: torch.relu(t), 2: torch.nn.functional.gelu(t),
+           3: torch.nn.functional.gelu(t, approximate="tanh"), 4: torch.nn.functional.silu(t)}
+    for act, want in lib.items():
+        got = oracle.epilogue(ref, act=act)[0]
+        # 1 + erf and 1 + tanh cancel for x < 0: agreement to FP64 rounding of the formula
+        assert np.allclose(got, want.numpy(), rtol=1e-12, atol=1e-14), act
+    assert np.array_equal(oracle.epilogue(ref, act=0)[0], x)
+
+
+def test_epilogue_gelu_is_x_times_normal_cdf():
+    """GELU(x) = x * Phi(x), Phi from scipy's normal distribution."""
+    stats = pytest.importorskip("scipy.stats")
+    x = np.linspace(-8, 8, 1601)
+    got = oracle.epilogue(x[None, :], act=2)[0]
+    assert np.allclose(got, x * stats.norm.cdf(x), rtol=1e-13, atol=1e-15)
+
+
+def test_epilogue_bias_is_per_column_and_exact():
+    rng = np.random.default_rng(21)
+    ref = rng.standard_normal((5, 7))
+    b16 = gi.f32_to_bf16_bits(rng.standard_normal(7).astype(np.float32))
+    b32 = rng.standard_normal(7).astype(np.float32)
+    assert np.array_equal(oracle.epilogue(ref, b16, 0), ref + gi.bf16_bits_to_f32(b16).astype(np.float64)[None, :])
+    assert np.array_equal(oracle.epilogue(ref, b32, 0), ref + b32.astype(np.float64)[None, :])
+    relu = oracle.epilogue(ref, b32, 1)
+    assert np.array_equal(relu, np.maximum(ref + b32.astype(np.float64)[None, :], 0.0))
+    with pytest.raises(ValueError):
+        oracle.epilogue(ref, b32[:3], 0)
+
+
+def test_epilogue_special_values():
+    x = np.array([[0.0, 50.0, -50.0]])
+    for act in (2, 3, 4):
+        y = oracle.epilogue(x, act=act)[0]
+        assert y[0] == 0.0 and y[1] == 50.0 and abs(y[2]) < 1e-20
