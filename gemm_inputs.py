@@ -49,6 +49,66 @@ def bf16_bits_to_f32(h: np.ndarray) -> np.ndarray:
     return (h.astype(np.uint32) << 16).view(np.float32)
 
 
+FP8_E4M3 = 0
+FP8_E5M2 = 1
+
+
+def _fp8_positive_table(fmt: int):
+    """(codes, values) of the non-negative finite fp8 codes, ascending."""
+    codes = np.arange(0x80, dtype=np.int64)
+    if fmt == FP8_E4M3:          # 4 exponent bits (bias 7), 3 mantissa bits, 0x7F = NaN
+        e, m = codes >> 3, codes & 7
+        vals = np.where(e == 0, m / 8.0 * 2.0 ** -6, (1 + m / 8.0) * 2.0 ** (e - 7))
+        keep = codes != 0x7F
+    else:                        # 5 exponent bits (bias 15), 2 mantissa bits, e = 31 inf/NaN
+        e, m = codes >> 2, codes & 3
+        vals = np.where(e == 0, m / 4.0 * 2.0 ** -14, (1 + m / 4.0) * 2.0 ** (e - 15))
+        keep = e != 31
+    return codes[keep], vals[keep]
+
+
+def f32_to_fp8_bits(x: np.ndarray, fmt: int) -> np.ndarray:
+    """Round to the nearest fp8 value (ties to the even code), saturating at the
+    largest finite value; returns uint8 codes."""
+    codes, vals = _fp8_positive_table(fmt)
+    x = np.asarray(x, dtype=np.float64)
+    ax = np.minimum(np.abs(x), vals[-1])
+    hi = np.clip(np.searchsorted(vals, ax), 1, len(vals) - 1)
+    lo = hi - 1
+    dlo, dhi = ax - vals[lo], vals[hi] - ax
+    pick_hi = (dhi < dlo) | ((dhi == dlo) & (codes[hi] % 2 == 0))
+    out = np.where(pick_hi, codes[hi], codes[lo]).astype(np.uint8)
+    return np.where(np.signbit(x) & (out != 0), out | 0x80, out).astype(np.uint8)
+
+
+def fp8_bits_to_f64(b: np.ndarray, fmt: int) -> np.ndarray:
+    """Decode finite fp8 codes to float64 (exact)."""
+    codes, vals = _fp8_positive_table(fmt)
+    lut = np.full(256, np.nan)
+    lut[codes] = vals
+    lut[codes | 0x80] = -vals
+    return lut[np.asarray(b, dtype=np.uint8)]
+
+
+def draw_fp8(rows: int, cols: int, dist: "Dist", seed: int, fmt: int, ld: Optional[int] = None) -> np.ndarray:
+    """A rows x ld array of fp8 codes drawn from dist (padding filled with 0x7F)."""
+    ld = cols if ld is None else ld
+    rng = np.random.Generator(np.random.PCG64(seed))
+    n = rows * cols
+    if dist.kind == "int":
+        vals = rng.integers(int(dist.a), int(dist.b) + 1, size=n).astype(np.float64)
+    elif dist.kind == "normal":
+        vals = rng.standard_normal(size=n) * math.sqrt(dist.a)
+    else:
+        vals = rng.uniform(dist.a, dist.b, size=n)
+    bits = f32_to_fp8_bits(vals, fmt).reshape(rows, cols)
+    if ld == cols:
+        return bits
+    out = np.full((rows, ld), 0x7F, dtype=np.uint8)
+    out[:, :cols] = bits
+    return out
+
+
 @dataclasses.dataclass(frozen=True)
 class Dist:
     kind: str            # "int", "normal", "uniform"

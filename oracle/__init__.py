@@ -62,6 +62,12 @@ def _load():
                                                     i32, d, d, i64, p, p, p, p, i32]
             lib.oracle_gemm_f64_sampled.restype = i32
             lib.oracle_nthreads_default.restype = i32
+            lib.oracle_gemm_fp8_f64.argtypes = [i64, i64, i64, p, i64, p, i64, i32, p, i64, i32,
+                                                d, d, p, p, i64, i32]
+            lib.oracle_gemm_fp8_f64.restype = i32
+            lib.oracle_gemm_fp8_f64_sampled.argtypes = [i64, i64, i64, p, i64, p, i64, i32, p, i64, i32,
+                                                        d, d, i64, p, p, p, p, i32]
+            lib.oracle_gemm_fp8_f64_sampled.restype = i32
             lib.oracle_epilogue_f64.argtypes = [i64, i64, p, i64, p, i32, i32]
             lib.oracle_epilogue_f64.restype = i32
             _lib = lib
@@ -136,6 +142,53 @@ def gemm_ref_sampled(A, B, rows, cols, C=None, alpha=1.0, beta=0.0, M=None, N=No
                                          int(nthreads))
     if rc != 0:
         raise ValueError("oracle_gemm_f64_sampled rejected its arguments")
+    return ref, absdot
+
+
+def gemm_ref_fp8(A, B, fmt, C=None, alpha=1.0, beta=0.0, M=None, N=None, K=None, lda=None, ldb=None,
+                 ldc=None, nthreads=0):
+    """FP64 reference for fp8 operands (uint8 codes; fmt 0 = e4m3, 1 = e5m2): (ref, absdot)."""
+    A = np.ascontiguousarray(A, dtype=np.uint8)
+    B = np.ascontiguousarray(B, dtype=np.uint8)
+    M = A.shape[0] if M is None else M
+    N = B.shape[0] if N is None else N
+    K = A.shape[1] if K is None else K
+    lda = A.shape[1] if lda is None else lda
+    ldb = B.shape[1] if ldb is None else ldb
+    if C is not None:
+        C = np.ascontiguousarray(C)
+    Cc, ldc_, cd = _c_args(C, ldc)
+    ref = np.empty((M, N), dtype=np.float64)
+    absdot = np.empty((M, N), dtype=np.float64)
+    rc = _load().oracle_gemm_fp8_f64(M, N, K, _ptr(A), lda, _ptr(B), ldb, int(fmt), _ptr(Cc), ldc_, cd,
+                                     float(alpha), float(beta), _ptr(ref), _ptr(absdot), N, int(nthreads))
+    if rc != 0:
+        raise ValueError("oracle_gemm_fp8_f64 rejected its arguments")
+    return ref, absdot
+
+
+def gemm_ref_fp8_sampled(A, B, fmt, rows, cols, C=None, alpha=1.0, beta=0.0, M=None, N=None, K=None,
+                         lda=None, ldb=None, ldc=None, nthreads=0):
+    """FP64 fp8 reference at the listed (rows[s], cols[s]) only: (ref, absdot) 1-D."""
+    A = np.ascontiguousarray(A, dtype=np.uint8)
+    B = np.ascontiguousarray(B, dtype=np.uint8)
+    M = A.shape[0] if M is None else M
+    N = B.shape[0] if N is None else N
+    K = A.shape[1] if K is None else K
+    lda = A.shape[1] if lda is None else lda
+    ldb = B.shape[1] if ldb is None else ldb
+    rows = np.ascontiguousarray(rows, dtype=np.int64)
+    cols = np.ascontiguousarray(cols, dtype=np.int64)
+    if C is not None:
+        C = np.ascontiguousarray(C)
+    Cc, ldc_, cd = _c_args(C, ldc)
+    ref = np.empty(rows.shape, dtype=np.float64)
+    absdot = np.empty(rows.shape, dtype=np.float64)
+    rc = _load().oracle_gemm_fp8_f64_sampled(M, N, K, _ptr(A), lda, _ptr(B), ldb, int(fmt), _ptr(Cc), ldc_,
+                                             cd, float(alpha), float(beta), rows.size, _ptr(rows),
+                                             _ptr(cols), _ptr(ref), _ptr(absdot), int(nthreads))
+    if rc != 0:
+        raise ValueError("oracle_gemm_fp8_f64_sampled rejected its arguments")
     return ref, absdot
 
 

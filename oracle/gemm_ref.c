@@ -171,6 +171,123 @@ int oracle_gemm_f64_sampled(int64_t M, int64_t N, int64_t K, const uint16_t *A,
 int oracle_nthreads_default(void) { return nthreads_or_default(0); }
 
 /*
+ * FP8 operands.  A one-byte value decodes by its format's definition:
+ *   e4m3 (fmt 0): sign, 4 exponent bits (bias 7), 3 mantissa bits; exponent
+ *     field 0 is subnormal (2^-6 * m/8); all-ones exponent with mantissa 7 is
+ *     NaN, the other all-ones codes are finite (max 448); no infinities.
+ *   e5m2 (fmt 1): sign, 5 exponent bits (bias 15), 2 mantissa bits; exponent
+ *     field 0 is subnormal (2^-14 * m/4); all-ones exponent is infinity
+ *     (mantissa 0) or NaN.
+ * Products of two fp8 values are exact in double, as is their k-order sum
+ * for the sizes used here.
+ */
+static double dec_fp8(uint8_t v, int fmt) {
+  const int s = v >> 7;
+  double x;
+  if (fmt == 0) {
+    const int e = (v >> 3) & 0xF, m = v & 7;
+    if (e == 0xF && m == 7) x = NAN;
+    else if (e == 0) x = ldexp((double)m / 8.0, -6);
+    else x = ldexp(1.0 + (double)m / 8.0, e - 7);
+  } else {
+    const int e = (v >> 2) & 0x1F, m = v & 3;
+    if (e == 0x1F) x = m == 0 ? INFINITY : NAN;
+    else if (e == 0) x = ldexp((double)m / 4.0, -14);
+    else x = ldexp(1.0 + (double)m / 4.0, e - 15);
+  }
+  return s ? -x : x;
+}
+
+typedef struct {
+  int64_t N, K, lda, ldb, ldc, ldr;
+  const uint8_t *A, *B;
+  int fmt;
+  const void *C;
+  int c_dtype;
+  double alpha, beta;
+  double *ref, *absdot;
+  const int64_t *rows, *cols; /* sampled mode when non-NULL */
+  int64_t begin, end;
+} job8_t;
+
+/* One output element, D[i][c] in FP64, and sum |alpha a_ik b_ck| beside it. */
+static void one_fp8(const job8_t *j, int64_t i, int64_t c, double *ref, double *absdot) {
+  double acc = 0.0, mag = 0.0;
+  for (int64_t k = 0; k < j->K; ++k) {
+    double pr = dec_fp8(j->A[i * j->lda + k], j->fmt) * dec_fp8(j->B[c * j->ldb + k], j->fmt);
+    acc += pr;
+    mag += fabs(pr);
+  }
+  double r = j->alpha * acc;
+  if (j->beta != 0.0) r += j->beta * dec_c(j->C, i * j->ldc + c, j->c_dtype);
+  *ref = r;
+  if (absdot) *absdot = fabs(j->alpha) * mag;
+}
+
+static void *run_fp8(void *p) {
+  job8_t *j = (job8_t *)p;
+  if (j->rows) {
+    for (int64_t s = j->begin; s < j->end; ++s)
+      one_fp8(j, j->rows[s], j->cols[s], &j->ref[s], j->absdot ? &j->absdot[s] : NULL);
+    return NULL;
+  }
+  for (int64_t i = j->begin; i < j->end; ++i)
+    for (int64_t c = 0; c < j->N; ++c)
+      one_fp8(j, i, c, &j->ref[i * j->ldr + c], j->absdot ? &j->absdot[i * j->ldr + c] : NULL);
+  return NULL;
+}
+
+static int spawn_fp8(job8_t base, int64_t total, int nthreads) {
+  nthreads = nthreads_or_default(nthreads);
+  if (nthreads > total) nthreads = total > 0 ? (int)total : 1;
+  pthread_t *th = (pthread_t *)calloc((size_t)nthreads, sizeof(pthread_t));
+  job8_t *jobs = (job8_t *)calloc((size_t)nthreads, sizeof(job8_t));
+  if (!th || !jobs) {
+    free(th);
+    free(jobs);
+    return -1;
+  }
+  for (int t = 0; t < nthreads; ++t) {
+    jobs[t] = base;
+    jobs[t].begin = total * t / nthreads;
+    jobs[t].end = total * (t + 1) / nthreads;
+    if (pthread_create(&th[t], NULL, run_fp8, &jobs[t]) != 0) {
+      run_fp8(&jobs[t]);
+      th[t] = 0;
+    }
+  }
+  for (int t = 0; t < nthreads; ++t)
+    if (th[t]) pthread_join(th[t], NULL);
+  free(th);
+  free(jobs);
+  return 0;
+}
+
+/* Full FP64 reference for fp8 A (M x lda bytes) and B (N x ldb bytes). */
+int oracle_gemm_fp8_f64(int64_t M, int64_t N, int64_t K, const uint8_t *A, int64_t lda, const uint8_t *B,
+                        int64_t ldb, int fmt, const void *C, int64_t ldc, int c_dtype, double alpha,
+                        double beta, double *ref, double *absdot, int64_t ldr, int nthreads) {
+  if (M < 0 || N < 0 || K < 0 || ldr < N || (fmt != 0 && fmt != 1)) return -1;
+  if (beta != 0.0 && C == NULL) return -1;
+  job8_t b = {N, K, lda, ldb, ldc, ldr, A, B, fmt, C, c_dtype, alpha, beta, ref, absdot, NULL, NULL, 0, 0};
+  return spawn_fp8(b, M, nthreads);
+}
+
+/* The same at the listed (rows[s], cols[s]) only; ref and absdot hold nsamples values. */
+int oracle_gemm_fp8_f64_sampled(int64_t M, int64_t N, int64_t K, const uint8_t *A, int64_t lda,
+                                const uint8_t *B, int64_t ldb, int fmt, const void *C, int64_t ldc,
+                                int c_dtype, double alpha, double beta, int64_t nsamples,
+                                const int64_t *rows, const int64_t *cols, double *ref, double *absdot,
+                                int nthreads) {
+  if (M < 0 || N < 0 || K < 0 || nsamples < 0 || (fmt != 0 && fmt != 1)) return -1;
+  if (beta != 0.0 && C == NULL) return -1;
+  for (int64_t s = 0; s < nsamples; ++s)
+    if (rows[s] < 0 || rows[s] >= M || cols[s] < 0 || cols[s] >= N) return -1;
+  job8_t b = {N, K, lda, ldb, ldc, 0, A, B, fmt, C, c_dtype, alpha, beta, ref, absdot, rows, cols, 0, 0};
+  return spawn_fp8(b, nsamples, nthreads);
+}
+
+/*
  * Fused MLP epilogue, in FP64: ref[i][j] <- act(ref[i][j] + bias[j]).
  *
  * bias holds N values (bf16 bits, bias_dtype 0, or float, bias_dtype 1) or

@@ -304,3 +304,82 @@ def test_epilogue_special_values():
     for act in (2, 3, 4):
         y = oracle.epilogue(x, act=act)[0]
         assert y[0] == 0.0 and y[1] == 50.0 and abs(y[2]) < 1e-20
+
+
+# ----------------------------------------------------------------------------- fp8 operands
+
+
+def _fp8_golden():
+    rows = []
+    with open(os.path.join(GOLDEN, "fp8_values.txt")) as f:
+        for line in f:
+            line = line.split("#")[0].strip()
+            if line:
+                fmt, code, val = line.split()
+                rows.append((0 if fmt == "e4m3" else 1, int(code, 16), float(val)))
+    return rows
+
+
+def test_fp8_decode_golden():
+    for fmt, code, val in _fp8_golden():
+        A = np.array([[code]], dtype=np.uint8)
+        one = 0x38 if fmt == 0 else 0x3C
+        B = np.array([[one]], dtype=np.uint8)
+        ref, _ = oracle.gemm_ref_fp8(A, B, fmt)
+        assert ref[0, 0] == val, (fmt, hex(code), ref[0, 0], val)
+
+
+@pytest.mark.parametrize("fmt", [0, 1])
+def test_fp8_decode_all_codes_against_torch(fmt):
+    torch = pytest.importorskip("torch")
+    dt = torch.float8_e4m3fn if fmt == 0 else torch.float8_e5m2
+    codes = np.arange(256, dtype=np.uint8)
+    want = torch.from_numpy(codes).view(dt).to(torch.float64).numpy()
+    one = 0x38 if fmt == 0 else 0x3C
+    ref, _ = oracle.gemm_ref_fp8(codes[:, None], np.array([[one]], dtype=np.uint8), fmt)
+    got = ref[:, 0]
+    same = (got == want) | (np.isnan(got) & np.isnan(want))
+    assert np.all(same), codes[~same]
+    # the input encoder inverts the decoder on every finite code
+    fin = np.isfinite(want)
+    enc = gi.f32_to_fp8_bits(want[fin], fmt)
+    assert np.array_equal(gi.fp8_bits_to_f64(enc, fmt), want[fin])
+
+
+@pytest.mark.parametrize("fmt", [0, 1])
+def test_fp8_integer_gemm_exact_and_identity(fmt):
+    rng = np.random.default_rng(31 + fmt)
+    M, N, K = 23, 17, 96
+    Ai = rng.integers(-4, 5, size=(M, K))
+    Bi = rng.integers(-4, 5, size=(N, K))
+    A = gi.f32_to_fp8_bits(Ai, fmt)
+    B = gi.f32_to_fp8_bits(Bi, fmt)
+    ref, absdot = oracle.gemm_ref_fp8(A, B, fmt)
+    assert np.array_equal(ref, (Ai @ Bi.T).astype(np.float64))
+    eye = gi.f32_to_fp8_bits(np.eye(K), fmt)
+    ref, _ = oracle.gemm_ref_fp8(eye, B, fmt)
+    assert np.array_equal(ref, gi.fp8_bits_to_f64(B, fmt).T)
+
+
+def test_fp8_rounding_ties_and_saturation():
+    # e4m3 around 1: spacing 1/8; 1 + 1/16 ties to the even code (1.0)
+    x = np.array([1.0 + 1 / 16, 1.0 + 3 / 16, 1000.0, -1000.0, 1e-9])
+    got = gi.fp8_bits_to_f64(gi.f32_to_fp8_bits(x, 0), 0)
+    assert got.tolist() == [1.0, 1.25, 448.0, -448.0, 0.0]
+
+
+def test_fp8_sampled_matches_full():
+    rng = np.random.default_rng(77)
+    M, N, K = 37, 29, 160
+    for fmt in (0, 1):
+        A = gi.draw_fp8(M, K, gi.Dist("normal", 1.0), 900 + fmt, fmt)
+        B = gi.draw_fp8(N, K, gi.Dist("normal", 1.0), 910 + fmt, fmt)
+        C = gi.draw_f32(M, N, gi.Dist("normal", 1.0), 920)
+        full, fabs_ = oracle.gemm_ref_fp8(A, B, fmt, C=C, alpha=0.75, beta=-0.5)
+        r, c = rng.integers(0, M, 50), rng.integers(0, N, 50)
+        s, sabs = oracle.gemm_ref_fp8_sampled(A, B, fmt, r, c, C=C, alpha=0.75, beta=-0.5)
+        assert np.array_equal(s, full[r, c]) and np.array_equal(sabs, fabs_[r, c])
+        # beta * C is the only other term: against the decoded operands' plain product
+        a64 = gi.fp8_bits_to_f64(A, fmt)
+        b64 = gi.fp8_bits_to_f64(B, fmt)
+        assert np.allclose(full, 0.75 * (a64 @ b64.T) - 0.5 * C, rtol=1e-12, atol=1e-12)
