@@ -8,6 +8,9 @@ no flush is needed between steps.  Alongside it, in the same run:
 
 * ``secondary``: the 16 x 8192 x 8192 decode GEMM in GB/s (B rotated over
   four copies, 512 MiB, so it never sits in L2);
+* ``fused_bias_gelu``: the same GEMM with bias + tanh-GELU in its epilogue;
+* ``fp8``: the e4m3 variant on both shapes (per-tensor scales folded into
+  alpha), against twice the measured bf16 peak and the copy bandwidth;
 * ``e2e``: the same metric with host buffers — pinned host->device copies
   of A and B and the device->host copy of D inside every timed step;
 * ``cpu_baseline``: the FP64 CPU oracle timed on a bounded row sample of
@@ -216,10 +219,17 @@ def run_ours(args, dist):
         M, N, K = (int(x) for x in args.shape.split(","))
         w = gi.Workload(w.index, f"custom {M}x{N}x{K}", M, N, K, w.dist_a, w.dist_b, w.dist_c,
                         w.alpha, w.beta, w.out_dtype)
+    fp8 = args.in_dtype != "bf16"
+    fmt = gi.FP8_E5M2 if args.in_dtype == "e5m2" else gi.FP8_E4M3
     t_gen = time.time()
     A, B, C = gi.operands(w)
+    if fp8:  # the fp8 variant of the same workload: codes plus per-tensor scales
+        A8, B8, scale_a, scale_b = gi.fp8_operands(w, fmt)
+        dA, dB = torch.from_numpy(A8).to(device), torch.from_numpy(B8).to(device)
+        del A8, B8
+    else:
+        dA, dB = dev_bf16(A, torch, device), dev_bf16(B, torch, device)
     log(f"[bench] inputs for {w.name} generated in {time.time() - t_gen:.1f}s")
-    dA, dB = dev_bf16(A, torch, device), dev_bf16(B, torch, device)
     out_t = torch.float32 if w.out_dtype == gi.OUT_F32 else torch.bfloat16
     dC = None
     if C is not None:
@@ -230,8 +240,12 @@ def run_ours(args, dist):
     ldc = w.N if dC is not None else 0
 
     def step(_i):
-        rc = g.gemm_bf16_tn_ex(w.M, w.N, w.K, dA.data_ptr(), w.K, dB.data_ptr(), w.K, c_ptr, ldc,
-                               dD.data_ptr(), w.N, w.alpha, w.beta, w.out_dtype, s_handle, cfg)
+        if fp8:
+            rc = g.gemm_fp8_tn(w.M, w.N, w.K, dA.data_ptr(), w.K, dB.data_ptr(), w.K, fmt, scale_a, scale_b,
+                               c_ptr, ldc, dD.data_ptr(), w.N, w.alpha, w.beta, w.out_dtype, s_handle)
+        else:
+            rc = g.gemm_bf16_tn_ex(w.M, w.N, w.K, dA.data_ptr(), w.K, dB.data_ptr(), w.K, c_ptr, ldc,
+                                   dD.data_ptr(), w.N, w.alpha, w.beta, w.out_dtype, s_handle, cfg)
         if rc != 0:
             raise RuntimeError(f"gemm failed: {rc} {g.last_error()}")
 
@@ -260,24 +274,28 @@ def run_ours(args, dist):
     clocks = sampler.summary(t0, t1)
 
     flops = rl.gemm_flops(w.M, w.N, w.K)
-    qbytes = rl.gemm_bytes(w.M, w.N, w.K, 4 if w.out_dtype == gi.OUT_F32 else 2, w.beta != 0)
+    qbytes = rl.gemm_bytes(w.M, w.N, w.K, 4 if w.out_dtype == gi.OUT_F32 else 2, w.beta != 0,
+                           in_bytes=1 if fp8 else 2)
     per_step_s = ms / 1e3 / args.steps
     value = dist.world * flops / per_step_s / 1e12
     achieved = flops / per_step_s / 1e12          # per launch, per GPU
-    traffic = profiled_traffic(w.name)
-    roof = {"bound": "tensor", "achieved": round(achieved, 2), "peak": peaks["bf16_tflops"],
-            "unit": "TFLOP/s", "frac": round(achieved / peaks["bf16_tflops"], 4),
+    traffic = profiled_traffic(w.name if not fp8 else f"{w.name} [{args.in_dtype}]")
+    ratio = 2.0 if fp8 else 1.0                   # nominal fp8 : bf16 dense ratio (4.5 : 2.25 PFLOP/s)
+    peak = ratio * peaks["bf16_tflops"]
+    roof = {"bound": "tensor", "achieved": round(achieved, 2), "peak": peak,
+            "unit": "TFLOP/s", "frac": round(achieved / peak, 4),
             "traffic": traffic, "algorithmic_flops": flops, "algorithmic_bytes": qbytes,
-            "peak_source": f"{peaks['source']} burst bf16 (MEASURED_PEAKS.json)"
-                           if peaks["source"] == "measured" else "fallback 1.9 PFLOP/s",
-            "frac_of_sustained": round(achieved / peaks["bf16_tflops_sustained"], 4),
+            "peak_source": (f"{'2 x ' if fp8 else ''}{peaks['source']} burst bf16 (MEASURED_PEAKS.json)"
+                            if peaks["source"] == "measured" else "fallback 1.9 PFLOP/s"),
+            "frac_of_sustained": round(achieved / (ratio * peaks["bf16_tflops_sustained"]), 4),
             "kernel": info.get("kernel")}
 
     result = {
-        "metric": METRIC, "value": round(value, 2), "unit": "TFLOP/s", "n_gpus": dist.world,
+        "metric": METRIC if not fp8 else f"FP8 ({args.in_dtype}) GEMM TFLOP/s at {w.M}x{w.N}x{w.K}",
+        "value": round(value, 2), "unit": "TFLOP/s", "n_gpus": dist.world,
         "steps": args.steps, "warmup": warmup, "ms_per_step": round(ms / args.steps, 4),
-        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "bf16",
-        "data": "synthetic",
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
+        "dtype": args.in_dtype, "data": "synthetic",
         "config": dict(w.describe(), path=PATH_NAMES.get(info.get("path"), info.get("path")),
                        grid=info.get("grid"), cluster=info.get("cluster"),
                        tile=[info.get("tile_m"), info.get("tile_n")], stages=info.get("stages"),
@@ -288,14 +306,21 @@ def run_ours(args, dist):
         "clocks": clocks,
     }
 
+    if fp8:  # the other legs are the bf16 path's; the fp8 main step stands alone
+        result["config"].update(A=f"{args.in_dtype} codes, scale {scale_a:g}",
+                                B=f"{args.in_dtype} codes, scale {scale_b:g}")
+        dist.finish()
+        return result
+
     # ---------------------------------------------------------------- fused bias + GELU
     if not args.no_secondary:
         hb = gi.draw_bf16(w.N, 1, gi.Dist("normal", 1.0), w.seed(gi.TENSOR_C)).reshape(w.N)
         dbias = dev_bf16(hb, torch, device)
+        dDf = torch.empty_like(dD)   # own output: dD keeps the plain GEMM for the CPU-sample check
 
         def fused(_i):
             rc = g.gemm_bf16_tn_bias_act(w.M, w.N, w.K, dA.data_ptr(), w.K, dB.data_ptr(), w.K, c_ptr, ldc,
-                                         dD.data_ptr(), w.N, w.alpha, w.beta, w.out_dtype,
+                                         dDf.data_ptr(), w.N, w.alpha, w.beta, w.out_dtype,
                                          dbias.data_ptr(), 0, g.ACT_GELU_TANH, s_handle)
             if rc != 0:
                 raise RuntimeError(f"fused gemm failed: {rc} {g.last_error()}")
@@ -310,6 +335,7 @@ def run_ours(args, dist):
             "value": round(dist.world * flops / (f_ms / 1e3 / f_steps) / 1e12, 2), "unit": "TFLOP/s",
             "ms_per_step": round(f_ms / f_steps, 4), "steps": f_steps,
             "op": "D = gelu_tanh(A B^T + bias) in the GEMM epilogue (gemm_bf16_tn_bias_act)"}
+        del dDf
 
     # ---------------------------------------------------------------- e2e (host buffers)
     if not args.no_e2e:
@@ -318,6 +344,7 @@ def run_ours(args, dist):
     # ---------------------------------------------------------------- decode secondary
     if not args.no_secondary:
         result["secondary"] = run_decode(args, g, torch, device, peaks, dist)
+        result["fp8"] = run_fp8(args, g, torch, device, peaks, dist)
 
     # ---------------------------------------------------------------- CPU oracle baseline
     if not args.no_cpu_baseline and dist.rank == 0:
@@ -391,6 +418,21 @@ def run_e2e(args, g, torch, device, w, A, B, out_t, flops, dist):
                    "copies on their own streams, two device buffers"}
 
 
+def time_eager_and_graph(torch, stream, step, steps, dist):
+    """(ms eager, ms graph) for `steps` launches on `stream`: first launched one
+    by one from Python, then the same launches captured once in a CUDA graph
+    and replayed (how a decode loop runs).  Each is the max over ranks."""
+    ms_eager = dist.max(time_steps(torch, stream, step, steps))
+    graph = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(graph, stream=stream):
+        for i in range(steps):
+            step(i)
+    with torch.cuda.stream(stream):  # replay() launches on the current stream
+        graph.replay()
+        ms = dist.max(time_steps(torch, stream, lambda _i: graph.replay(), 1))
+    return ms_eager, ms
+
+
 def run_decode(args, g, torch, device, peaks, dist):
     w = gi.WORKLOADS[DECODE]
     # own stream: graph capture needs a non-default stream
@@ -415,16 +457,8 @@ def run_decode(args, g, torch, device, peaks, dist):
     torch.cuda.synchronize()
     info = g.last_launch_info()
     steps = max(args.steps, 50)
-    ms_eager = dist.max(time_steps(torch, stream, step, steps))
-    # The same launches replayed from a CUDA graph (how a decode loop runs):
-    # every step is still one full GEMM on a rotated copy of B.
-    graph = torch.cuda.CUDAGraph()
-    with torch.cuda.graph(graph, stream=stream):
-        for i in range(steps):
-            step(i)
-    with torch.cuda.stream(stream):  # replay() launches on the current stream
-        graph.replay()
-        ms = dist.max(time_steps(torch, stream, lambda _i: graph.replay(), 1))
+    # every step, eager or replayed, is one full GEMM on a rotated copy of B
+    ms_eager, ms = time_eager_and_graph(torch, stream, step, steps, dist)
     st = g.gemm_get_status(s_handle)
     if st != 0:
         raise RuntimeError(f"device status {st}: {g.last_error()}")
@@ -445,6 +479,78 @@ def run_decode(args, g, torch, device, peaks, dist):
                          "algorithmic_bytes": qbytes, "kernel": info.get("kernel"),
                          "peak_source": "measured copy bandwidth (MEASURED_PEAKS.json)"
                          if peaks["source"] == "measured" else "fallback 6.8 TB/s"}}
+
+
+def run_fp8(args, g, torch, device, peaks, dist):
+    """The FP8 (e4m3) variant on the two headline shapes: the 8192x28672x4096
+    up-projection (tensor bound) and the 16x8192x8192 decode (HBM bound), with
+    per-tensor scales folded into alpha."""
+    fmt = gi.FP8_E4M3
+    stream = torch.cuda.Stream(device)
+    s_handle = stream.cuda_stream
+    out = {}
+    fp8_peak = 2.0 * peaks["bf16_tflops"]
+    for name, idx in (("mlp_e4m3", MAIN), ("decode_e4m3", DECODE)):
+        w = gi.WORKLOADS[idx]
+        A, B, sa, sb = gi.fp8_operands(w, fmt)
+        dA = torch.from_numpy(A).to(device)
+        copies = 8 if idx == DECODE else 1
+        dBs = [torch.from_numpy(B).to(device) for _ in range(copies)]
+        dD = torch.empty((w.M, w.N), dtype=torch.bfloat16, device=device)
+
+        def step(i, w=w, dA=dA, dBs=dBs, dD=dD, sa=sa, sb=sb):
+            rc = g.gemm_fp8_tn(w.M, w.N, w.K, dA.data_ptr(), w.K, dBs[i % len(dBs)].data_ptr(), w.K, fmt, sa, sb,
+                               0, 0, dD.data_ptr(), w.N, 1.0, 0.0, gi.OUT_BF16, s_handle)
+            if rc != 0:
+                raise RuntimeError(f"fp8 gemm failed: {rc} {g.last_error()}")
+
+        with torch.cuda.stream(stream):
+            for i in range(max(args.warmup, 3)):
+                step(i)
+        torch.cuda.synchronize()
+        info = g.last_launch_info()
+        flops = rl.gemm_flops(w.M, w.N, w.K)
+        qbytes = rl.gemm_bytes(w.M, w.N, w.K, in_bytes=1)
+        if idx == DECODE:
+            steps = max(args.steps, 50)
+            ms_eager, ms = time_eager_and_graph(torch, stream, step, steps, dist)
+        else:
+            steps = max(10, min(args.steps, 100))
+            ms = dist.max(time_steps(torch, stream, step, steps))
+            ms_eager = ms
+        st = g.gemm_get_status(s_handle)
+        if st != 0:
+            raise RuntimeError(f"device status {st}: {g.last_error()}")
+        per = ms / 1e3 / steps
+        tf, gbs = flops / per / 1e12, qbytes / per / 1e9
+        entry = {"op": f"D = (alpha*scale_a*scale_b) A B^T, A and B e4m3, bf16 out ({w.M}x{w.N}x{w.K})",
+                 "ms_per_step": round(ms / steps, 5), "steps": steps,
+                 "config": dict(w.describe(), A="e4m3 codes of N(0,1)", B="e4m3 codes of N(0,1)",
+                                scale_a=sa, scale_b=sb, path=PATH_NAMES.get(info.get("path")),
+                                grid=info.get("grid"), stages=info.get("stages"))}
+        if idx == DECODE:
+            entry.update({"value": round(dist.world * gbs, 1), "unit": "GB/s", "tflops": round(tf, 2),
+                          "launch": "CUDA graph of the steps' launches",
+                          "eager": {"value": round(dist.world * qbytes / (ms_eager / 1e3 / steps) / 1e9, 1),
+                                    "ms_per_step": round(ms_eager / steps, 5)},
+                          "roofline": {"bound": "hbm", "achieved": round(gbs, 1), "peak": peaks["hbm_gbs"],
+                                       "unit": "GB/s", "frac": round(gbs / peaks["hbm_gbs"], 4),
+                                       "traffic": profiled_traffic(f"{w.name} [e4m3]"),
+                                       "algorithmic_bytes": qbytes, "kernel": info.get("kernel"),
+                                       "peak_source": "measured copy bandwidth"}})
+            entry["config"]["l2"] = f"B rotated over {copies} copies ({copies * w.N * w.K >> 20} MiB)"
+        else:
+            entry.update({"value": round(dist.world * tf, 2), "unit": "TFLOP/s",
+                          "roofline": {"bound": "tensor", "achieved": round(tf, 2), "peak": fp8_peak,
+                                       "unit": "TFLOP/s", "frac": round(tf / fp8_peak, 4),
+                                       "traffic": profiled_traffic(f"{w.name} [e4m3]"),
+                                       "algorithmic_flops": flops, "kernel": info.get("kernel"),
+                                       "peak_source": "2 x measured burst bf16 (the nominal fp8:bf16 "
+                                                      "dense ratio, 4.5:2.25 PFLOP/s)"}})
+            entry["config"]["l2"] = "operands 144 MiB + D 448 MiB per step, larger than L2; no flush"
+        out[name] = entry
+        del dA, dBs, dD
+    return out
 
 
 def cpu_baseline(w, A, B, C, dD, out_t, torch, seconds):
@@ -468,10 +574,13 @@ def cpu_baseline(w, A, B, C, dD, out_t, torch, seconds):
         od = gi.OUT_F32
     cvals = None if C is None else (gi.bf16_bits_to_f32(C[r0:r0 + rows]) if od == gi.OUT_BF16 else C[r0:r0 + rows])
     ok, worst, _ = oracle.check(got, ref, absdot, od, w.beta, cvals)
+    if not ok:
+        log(f"[bench] WARNING: GPU rows disagree with the oracle on the CPU sample (worst {worst:.3g} x bound)")
     return {"value": round(rows * per_row / dt / 1e12, 6), "unit": "TFLOP/s", "cores": threads,
             "kind": "oracle", "sample": f"rows {r0}..{r0 + rows - 1} of {w.M} ({rows} x {w.N} outputs, "
                                         f"K={w.K}) in {dt:.1f}s",
             "parity_on_sample": {"ok": bool(ok), "worst_err_over_bound": round(worst, 4)}}
+
 
 
 # ----------------------------------------------------------------------------- reference arm
@@ -522,6 +631,8 @@ def main():
     ap.add_argument("--workload", type=int, default=MAIN, help="index into gemm_inputs.WORKLOADS")
     ap.add_argument("--shape", default="", help="M,N,K override (profiling runs)")
     ap.add_argument("--path", type=int, default=0, help="0 auto, 1 1-SM, 2 2-SM, 3 skinny")
+    ap.add_argument("--in-dtype", choices=["bf16", "e4m3", "e5m2"], default="bf16",
+                    help="input type of the main step (fp8 runs the main step alone)")
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--no-secondary", action="store_true")
     ap.add_argument("--no-cpu-baseline", action="store_true")

@@ -1,6 +1,7 @@
 """Seeded synthetic inputs for the BF16 TN GEMM workloads.
 
-This module only draws random numbers and stores them as bf16 bit patterns.
+This module only draws random numbers and stores them as bf16 bit patterns
+(or, for the FP8 variant, as e4m3/e5m2 codes).
 It holds none of the GEMM's arithmetic, so both the CPU oracle's tests and the
 GPU path's tests/bench can take their operands from it without sharing any of
 the computation.
@@ -68,17 +69,33 @@ def _fp8_positive_table(fmt: int):
 
 
 def f32_to_fp8_bits(x: np.ndarray, fmt: int) -> np.ndarray:
-    """Round to the nearest fp8 value (ties to the even code), saturating at the
-    largest finite value; returns uint8 codes."""
-    codes, vals = _fp8_positive_table(fmt)
-    x = np.asarray(x, dtype=np.float64)
-    ax = np.minimum(np.abs(x), vals[-1])
-    hi = np.clip(np.searchsorted(vals, ax), 1, len(vals) - 1)
-    lo = hi - 1
-    dlo, dhi = ax - vals[lo], vals[hi] - ax
-    pick_hi = (dhi < dlo) | ((dhi == dlo) & (codes[hi] % 2 == 0))
-    out = np.where(pick_hi, codes[hi], codes[lo]).astype(np.uint8)
-    return np.where(np.signbit(x) & (out != 0), out | 0x80, out).astype(np.uint8)
+    """Round float32 values to fp8 codes: nearest value, ties to the even code,
+    saturating at the largest finite value (448 e4m3, 57344 e5m2).
+
+    Normal results round the float32 bit pattern's mantissa to 3 (e4m3) or 2
+    (e5m2) bits, the carry moving into the exponent; results below the smallest
+    normal (2^-6 e4m3, 2^-14 e5m2) are whole multiples of the subnormal step,
+    rounded with numpy's half-to-even rint."""
+    mbits, bias, max_code = (3, 7, 0x7E) if fmt == FP8_E4M3 else (2, 15, 0x7B)
+    shift = 23 - mbits
+    min_normal = np.float32(2.0 ** (1 - bias))
+    sub_scale = np.float32(2.0 ** (bias - 1 + mbits))   # 1 / subnormal step
+    x = np.ascontiguousarray(x, dtype=np.float32)
+    flat = x.reshape(-1)
+    out = np.empty(flat.shape, dtype=np.uint8)
+    for s in range(0, flat.size, _CHUNK):
+        v = flat[s:s + _CHUNK]
+        u = v.view(np.uint32)
+        sign = ((u >> 31) << 7).astype(np.uint8)
+        a = (u & 0x7FFFFFFF).astype(np.int64)
+        r = (a + ((1 << (shift - 1)) - 1) + ((a >> shift) & 1)) >> shift
+        code = r - ((127 - bias) << mbits)
+        av = np.abs(v)
+        sub = av < min_normal
+        code = np.where(sub, np.rint(np.where(sub, av, 0) * sub_scale).astype(np.int64), code)
+        code = np.minimum(code, max_code)
+        out[s:s + _CHUNK] = np.where(code == 0, 0, code.astype(np.uint8) | sign)
+    return out.reshape(x.shape)
 
 
 def fp8_bits_to_f64(b: np.ndarray, fmt: int) -> np.ndarray:
@@ -91,16 +108,23 @@ def fp8_bits_to_f64(b: np.ndarray, fmt: int) -> np.ndarray:
 
 
 def draw_fp8(rows: int, cols: int, dist: "Dist", seed: int, fmt: int, ld: Optional[int] = None) -> np.ndarray:
-    """A rows x ld array of fp8 codes drawn from dist (padding filled with 0x7F)."""
+    """A rows x ld array of fp8 codes drawn from dist in float32, then rounded
+    to the format (padding filled with 0x7F, a NaN in e4m3 and e5m2)."""
     ld = cols if ld is None else ld
+    if ld < cols:
+        raise ValueError("ld < cols")
     rng = np.random.Generator(np.random.PCG64(seed))
     n = rows * cols
     if dist.kind == "int":
-        vals = rng.integers(int(dist.a), int(dist.b) + 1, size=n).astype(np.float64)
+        vals = rng.integers(int(dist.a), int(dist.b) + 1, size=n, dtype=np.int64).astype(np.float32)
     elif dist.kind == "normal":
-        vals = rng.standard_normal(size=n) * math.sqrt(dist.a)
+        vals = rng.standard_normal(size=n, dtype=np.float32)
+        if dist.a != 1.0:
+            vals *= np.float32(math.sqrt(dist.a))
+    elif dist.kind == "uniform":
+        vals = rng.uniform(dist.a, dist.b, size=n).astype(np.float32)
     else:
-        vals = rng.uniform(dist.a, dist.b, size=n)
+        raise ValueError(dist.kind)
     bits = f32_to_fp8_bits(vals, fmt).reshape(rows, cols)
     if ld == cols:
         return bits
@@ -214,3 +238,23 @@ def operands(w: Workload):
         else:
             C = draw_f32(w.M, w.N, w.dist_c, w.seed(TENSOR_C))
     return A, B, C
+
+
+TENSOR_A_FP8, TENSOR_B_FP8 = 3, 4
+
+
+def fp8_operands(w: Workload, fmt: int = FP8_E4M3):
+    """(A codes MxK, B codes NxK, scale_a, scale_b) for workload w in fp8.
+
+    Per-tensor scaling: an operand drawn from N(0, v) is stored as codes of
+    N(0, 1) values with scale sqrt(v), so that scale * code has the
+    workload's distribution while the codes use the format's normal range;
+    integer and uniform operands are stored as they are with scale 1."""
+    out = []
+    for dist, tid, rows in ((w.dist_a, TENSOR_A_FP8, w.M), (w.dist_b, TENSOR_B_FP8, w.N)):
+        if dist.kind == "normal":
+            out.append((draw_fp8(rows, w.K, Dist("normal", 1.0), w.seed(tid), fmt), math.sqrt(dist.a)))
+        else:
+            out.append((draw_fp8(rows, w.K, dist, w.seed(tid), fmt), 1.0))
+    (A, sa), (B, sb) = out
+    return A, B, sa, sb

@@ -79,6 +79,11 @@ typedef enum {
 } gemm_status;
 
 typedef enum {
+  GEMM_FP8_E4M3 = 0,  /* 1 sign, 4 exponent (bias 7), 3 mantissa bits; max 448; no infinities */
+  GEMM_FP8_E5M2 = 1   /* 1 sign, 5 exponent (bias 15), 2 mantissa bits; max 57344; IEEE inf/NaN */
+} gemm_fp8_format;
+
+typedef enum {
   GEMM_ACT_NONE = 0,
   GEMM_ACT_RELU = 1,       /* max(x, 0) */
   GEMM_ACT_GELU = 2,       /* x * Phi(x) = 0.5 x (1 + erf(x / sqrt 2)) */
@@ -159,6 +164,27 @@ int gemm_bf16_tn_bias_act(int64_t M, int64_t N, int64_t K,
                           void *D, int64_t ldd,
                           float alpha, float beta, int out_dtype,
                           const void *bias, int bias_dtype, int activation, void *stream);
+
+/* FP8 TN GEMM with per-tensor scales:
+ *
+ *     D = alpha * (scale_a * scale_b) * A * B^T + beta * C
+ *
+ * A (M x K) and B (N x K) hold one-byte fp8 values of the same format
+ * (fp8_format: GEMM_FP8_E4M3 or GEMM_FP8_E5M2), K contiguous; lda and ldb
+ * count elements (bytes) and must be multiples of 16.  Products accumulate in
+ * fp32 on the tensor cores (tcgen05.mma kind::f8f6f4, twice the bf16 rate);
+ * C, D, out_dtype, the paths and the error behaviour are those of
+ * gemm_bf16_tn.  FP8 with per-tensor scaling is the reduced-precision
+ * variant the Ampere-to-Hopper page discusses for Ada and Hopper (sections on
+ * FP8 and the Transformer Engine); it halves the bytes a decode GEMM
+ * streams. */
+int gemm_fp8_tn(int64_t M, int64_t N, int64_t K,
+                const void *A, int64_t lda,
+                const void *B, int64_t ldb,
+                int fp8_format, float scale_a, float scale_b,
+                const void *C, int64_t ldc,
+                void *D, int64_t ldd,
+                float alpha, float beta, int out_dtype, void *stream);
 
 /* Synchronises `stream`, then returns and clears the current device's status
  * word: GEMM_OK, or GEMM_ERR_TIMEOUT if a kernel's bounded wait gave up since

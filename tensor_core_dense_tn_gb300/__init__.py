@@ -37,7 +37,9 @@ GEMM_ERR_CUDA = -8
 
 EXPORTED = ["gemm_bf16_tn", "gemm_bf16_tn_ex", "gemm_get_status", "gemm_get_status_detail",
             "gemm_last_error_string", "gemm_last_launch_info", "gemm_shutdown", "gemm_version",
-            "gemm_bf16_tn_skinny_noalloc", "gemm_bf16_tn_bias_act"]
+            "gemm_bf16_tn_skinny_noalloc", "gemm_bf16_tn_bias_act", "gemm_fp8_tn"]
+
+FP8_E4M3, FP8_E5M2 = 0, 1
 
 ACT_NONE, ACT_RELU, ACT_GELU, ACT_GELU_TANH, ACT_SILU = 0, 1, 2, 3, 4
 
@@ -82,6 +84,9 @@ def load(path: str = LIB_PATH):
         args = [i64, i64, i64, vp, i64, vp, i64, vp, i64, vp, i64, f32, f32, i32, vp]
         lib.gemm_bf16_tn.argtypes = args
         lib.gemm_bf16_tn.restype = i32
+        lib.gemm_fp8_tn.argtypes = [i64, i64, i64, vp, i64, vp, i64, i32, f32, f32, vp, i64, vp, i64,
+                                    f32, f32, i32, vp]
+        lib.gemm_fp8_tn.restype = i32
         lib.gemm_bf16_tn_bias_act.argtypes = args[:-1] + [vp, i32, i32, vp]
         lib.gemm_bf16_tn_bias_act.restype = i32
         lib.gemm_bf16_tn_skinny_noalloc.argtypes = args
@@ -136,6 +141,13 @@ def gemm_bf16_tn_bias_act(M, N, K, A, lda, B, ldb, C, ldc, D, ldd, alpha, beta, 
     """Raw C-ABI call: D = act(alpha * A B^T + beta * C + bias)."""
     return load().gemm_bf16_tn_bias_act(M, N, K, A, lda, B, ldb, C or None, ldc, D, ldd, alpha, beta,
                                         out_dtype, bias or None, bias_dtype, activation, stream or None)
+
+
+def gemm_fp8_tn(M, N, K, A, lda, B, ldb, fp8_format, scale_a, scale_b, C, ldc, D, ldd, alpha, beta,
+                out_dtype, stream) -> int:
+    """Raw C-ABI call: D = alpha * scale_a * scale_b * A B^T + beta * C, fp8 A and B."""
+    return load().gemm_fp8_tn(M, N, K, A, lda, B, ldb, fp8_format, scale_a, scale_b, C or None, ldc, D,
+                              ldd, alpha, beta, out_dtype, stream or None)
 
 
 def gemm_get_status(stream=None) -> int:

@@ -169,7 +169,12 @@ int get_workspace(int dev, cudaStream_t stream, size_t partial_floats, size_t co
 
 int run(int64_t M, int64_t N, int64_t K, const void* A, int64_t lda, const void* B, int64_t ldb, const void* C,
         int64_t ldc, void* D, int64_t ldd, float alpha, float beta, int out_dtype, void* stream_v,
-        const gemm_tn_config* cfg, Epilogue epi = Epilogue{nullptr, 0, kActNone}) {
+        const gemm_tn_config* cfg, Epilogue epi = Epilogue{nullptr, 0, kActNone}, int in_kind = kInBf16,
+        int fp8_format = 0) {
+  // Input element: bf16 (2 bytes, 64 per 128-byte stage row) or fp8 (1 byte, 128).
+  const int in_bytes = in_kind == kInFp8 ? 1 : 2;
+  const int kbe = 128 / in_bytes;
+  const CUtensorMapDataType in_dt = in_kind == kInFp8 ? CU_TENSOR_MAP_DATA_TYPE_UINT8 : CU_TENSOR_MAP_DATA_TYPE_BFLOAT16;
   t_error.clear();
   cudaStream_t stream = static_cast<cudaStream_t>(stream_v);
   // ---- argument validation
@@ -198,8 +203,8 @@ int run(int64_t M, int64_t N, int64_t K, const void* A, int64_t lda, const void*
       return fail(GEMM_ERR_INVALID_VALUE, "lda (%lld) and ldb (%lld) must be >= K (%lld)", (long long)lda,
                   (long long)ldb, (long long)K);
     if (!aligned16(A) || !aligned16(B)) return fail(GEMM_ERR_MISALIGNED, "A and B must be 16-byte aligned");
-    if ((lda * 2) % 16 || (ldb * 2) % 16)
-      return fail(GEMM_ERR_MISALIGNED, "lda and ldb must be multiples of 8 elements");
+    if ((lda * in_bytes) % 16 || (ldb * in_bytes) % 16)
+      return fail(GEMM_ERR_MISALIGNED, "lda and ldb must be multiples of %d elements", 16 / in_bytes);
   }
   if (!aligned16(D) || (ldd * esize) % 16)
     return fail(GEMM_ERR_MISALIGNED, "D must be 16-byte aligned with ldd*%d a multiple of 16", esize);
@@ -234,8 +239,11 @@ int run(int64_t M, int64_t N, int64_t K, const void* A, int64_t lda, const void*
     const int np = (int)((M + 15) / 16) * 16;
     SkinnyParams p = {};
     p.M = (int)M; p.N = (int)N; p.K = (int)K; p.np = np;
-    p.num_kb = (int)((K + 63) / 64);
+    p.num_kb = (int)((K + kbe - 1) / kbe);
     p.n_tiles = (int)((N + 127) / 128);
+    p.kind = in_kind;
+    p.a_fmt = fp8_format;
+    p.b_fmt = fp8_format;
     p.units = (long long)p.n_tiles * p.num_kb;
     skinny_partition(&p, skinny_max_grid(np, st->sms), cfg ? cfg->skinny_grid : 0, cfg ? cfg->skinny_skew_kb : 0);
     const int grid = p.grid;
@@ -248,9 +256,9 @@ int run(int64_t M, int64_t N, int64_t K, const void* A, int64_t lda, const void*
     p.partials = w->partials;
     p.counters = w->counters;
     CUtensorMap tA, tB;
-    if ((rc = encode_2d(&tA, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, A, K, M, lda, 64, np, CU_TENSOR_MAP_SWIZZLE_128B, "A")))
+    if ((rc = encode_2d(&tA, in_dt, in_bytes, A, K, M, lda, kbe, np, CU_TENSOR_MAP_SWIZZLE_128B, "A")))
       return rc;
-    if ((rc = encode_2d(&tB, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, B, K, N, ldb, 64, 128, CU_TENSOR_MAP_SWIZZLE_128B, "B")))
+    if ((rc = encode_2d(&tB, in_dt, in_bytes, B, K, N, ldb, kbe, 128, CU_TENSOR_MAP_SWIZZLE_128B, "B")))
       return rc;
     e = launch_skinny(tA, tB, p, pdl, stream, &li);
   } else {
@@ -259,7 +267,9 @@ int run(int64_t M, int64_t N, int64_t K, const void* A, int64_t lda, const void*
     tiled_shape(cg, out_dtype == GEMM_OUT_F32, &tile_m, &tile_n, &b_rows, &epi_r, &epi_c);
     TileParams p = {};
     p.M = (int)M; p.N = (int)N; p.K = (int)K;
-    p.num_kb = (int)((K + 63) / 64);
+    p.num_kb = (int)((K + kbe - 1) / kbe);
+    p.a_fmt = fp8_format;
+    p.b_fmt = fp8_format;
     p.tiles_m = (int)((M + tile_m - 1) / tile_m);
     p.tiles_n = (int)((N + tile_n - 1) / tile_n);
     const long long nt = (long long)p.tiles_m * p.tiles_n;
@@ -269,7 +279,7 @@ int run(int64_t M, int64_t N, int64_t K, const void* A, int64_t lda, const void*
     if (group == 0) {
       // keep the A rows of one raster strip within ~32 MiB of L2 (the
       // strip is then re-read from L2 for every tile column it meets)
-      const long long strip_bytes = (long long)tile_m * (K > 0 ? K : 1) * 2;
+      const long long strip_bytes = (long long)tile_m * (K > 0 ? K : 1) * in_bytes;
       long long g = (32ll << 20) / strip_bytes;
       group = (int)(g < 1 ? 1 : g);
     }
@@ -283,15 +293,15 @@ int run(int64_t M, int64_t N, int64_t K, const void* A, int64_t lda, const void*
     memset(&tC, 0, sizeof tC);
     const CUtensorMapSwizzle out_sw = out_dtype == GEMM_OUT_F32 ? CU_TENSOR_MAP_SWIZZLE_128B : CU_TENSOR_MAP_SWIZZLE_64B;
     if (K > 0) {
-      if ((rc = encode_2d(&tA, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, A, K, M, lda, 64, 128, CU_TENSOR_MAP_SWIZZLE_128B, "A")))
+      if ((rc = encode_2d(&tA, in_dt, in_bytes, A, K, M, lda, kbe, 128, CU_TENSOR_MAP_SWIZZLE_128B, "A")))
         return rc;
-      if ((rc = encode_2d(&tB, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, B, K, N, ldb, 64, b_rows, CU_TENSOR_MAP_SWIZZLE_128B,
+      if ((rc = encode_2d(&tB, in_dt, in_bytes, B, K, N, ldb, kbe, b_rows, CU_TENSOR_MAP_SWIZZLE_128B,
                           "B")))
         return rc;
     }
     if (has_c && (rc = encode_2d(&tC, out_dt, esize, C, N, M, ldc, epi_c, epi_r, out_sw, "C"))) return rc;
     if ((rc = encode_2d(&tD, out_dt, esize, D, N, M, ldd, epi_c, epi_r, out_sw, "D"))) return rc;
-    e = launch_tiled(cg, out_dtype == GEMM_OUT_F32, tA, tB, tC, tD, p, cfg ? cfg->grid : 0, pdl, stream, &li);
+    e = launch_tiled(cg, out_dtype == GEMM_OUT_F32, in_kind, tA, tB, tC, tD, p, cfg ? cfg->grid : 0, pdl, stream, &li);
   }
   if (e != cudaSuccess) {
     cudaGetLastError();
@@ -352,6 +362,16 @@ int gemm_bf16_tn_bias_act(int64_t M, int64_t N, int64_t K, const void* A, int64_
     return fail(GEMM_ERR_MISALIGNED, "bias must be aligned to its element size");
   const Epilogue epi{bias, bias_dtype == GEMM_OUT_F32 ? 1 : 0, activation};
   return run(M, N, K, A, lda, B, ldb, C, ldc, D, ldd, alpha, beta, out_dtype, stream, nullptr, epi);
+}
+
+int gemm_fp8_tn(int64_t M, int64_t N, int64_t K, const void* A, int64_t lda, const void* B, int64_t ldb,
+                int fp8_format, float scale_a, float scale_b, const void* C, int64_t ldc, void* D, int64_t ldd,
+                float alpha, float beta, int out_dtype, void* stream) {
+  using namespace gtn;
+  if (fp8_format != GEMM_FP8_E4M3 && fp8_format != GEMM_FP8_E5M2)
+    return fail(GEMM_ERR_INVALID_VALUE, "fp8_format must be 0 (e4m3) or 1 (e5m2), got %d", fp8_format);
+  return run(M, N, K, A, lda, B, ldb, C, ldc, D, ldd, alpha * scale_a * scale_b, beta, out_dtype, stream, nullptr,
+             Epilogue{nullptr, 0, kActNone}, kInFp8, fp8_format);
 }
 
 int gemm_get_status(void* stream) {

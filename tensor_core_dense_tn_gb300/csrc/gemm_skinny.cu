@@ -40,19 +40,19 @@ namespace gtn {
 
 namespace {
 
-constexpr int kBK = 64;
-constexpr int kUmmaK = 16;
+constexpr int kStageK = 128;      // bytes of K per operand row per stage
+constexpr int kMmaPerStage = 4;   // tcgen05.mma per stage, 32 bytes of K each
 constexpr int kEpiWarps = 4;
 constexpr int kThreads = 64 + 32 * kEpiWarps;
 constexpr int kMaxStages = 16;
 constexpr int kNumAcc = 4;                   // TMEM accumulators (64 columns each)
-constexpr int kBTileBytes = 128 * kBK * 2;   // 16 KiB
+constexpr int kBTileBytes = 128 * kStageK;   // 16 KiB
 constexpr int kTmemCols = 64 * kNumAcc;
 constexpr int kErrTimeout = -5;
 constexpr int kSmemBudget = 216 * 1024;
 constexpr int kNumBars = 2 * kMaxStages + 2 * kNumAcc + 1;
 
-__host__ __device__ inline int stage_bytes(int np) { return kBTileBytes + np * kBK * 2; }
+__host__ __device__ inline int stage_bytes(int np) { return kBTileBytes + np * kStageK; }
 
 __host__ __device__ inline int stages_for(int np) {
   int s = kSmemBudget / stage_bytes(np);
@@ -153,13 +153,15 @@ __device__ __forceinline__ float* partial_ptr(const SkinnyParams& p, long long c
   return p.partials + ((c * 2 + slot) * 128 + row) * (long long)p.np;
 }
 
+template <int KIND>
 __global__ void __launch_bounds__(kThreads, 1)
     gemm_tn_skinny_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
                           const SkinnyParams p) {
+  constexpr int kBK = KIND == kKindF16 ? 64 : 128;  // K elements per stage
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
   const int S = p.stages;
-  const int a_bytes = p.np * kBK * 2;
+  const int a_bytes = p.np * kStageK;
   const uint32_t sB = smem_u32(smem);
   const uint32_t sA = sB + S * kBTileBytes;
   uint64_t* bars = reinterpret_cast<uint64_t*>(smem + S * (kBTileBytes + a_bytes));
@@ -251,7 +253,8 @@ __global__ void __launch_bounds__(kThreads, 1)
   } else if (warp == 1) {
     if (lane == 0) {
       // -------------------------------------------------------- MMA
-      const uint32_t idesc = instr_desc_bf16_f32(128, (uint32_t)p.np);
+      const uint32_t idesc = KIND == kKindF16 ? instr_desc_bf16_f32(128, (uint32_t)p.np)
+                                              : instr_desc_f32acc(128, (uint32_t)p.np, p.b_fmt, p.a_fmt);
       bool ok = true;
       int stage = 0, acc = 0;
       uint32_t phase = 0, acc_phase = 0;
@@ -271,8 +274,8 @@ __global__ void __launch_bounds__(kThreads, 1)
           const uint64_t a0 = smem_desc_sw128(sB + stage * kBTileBytes);
           const uint64_t b0 = smem_desc_sw128(sA + stage * a_bytes);
 #pragma unroll
-          for (int k = 0; k < kBK / kUmmaK; ++k)
-            mma_bf16<1>(d_tmem, a0 + 2 * k, b0 + 2 * k, idesc, (v != u || k != 0) ? 1u : 0u);
+          for (int k = 0; k < kMmaPerStage; ++k)
+            mma_issue<1, KIND>(d_tmem, a0 + 2 * k, b0 + 2 * k, idesc, (v != u || k != 0) ? 1u : 0u);
           mma_commit(empty_bar(stage));
           if (++stage == S) {
             stage = 0;
@@ -425,15 +428,26 @@ __global__ void __launch_bounds__(kThreads, 1)
           }
         }
       }
-      if (finish && ng < p.N) {
+      // The fused bias/activation gets a loop of its own: with the test
+      // inside the unrolled plain loop the activation code is scheduled
+      // into it and the plain decode GEMM ran 1.7x slower (measured).
+      if (finish && ng < p.N && !(p.epi.bias || p.epi.act)) {
+#pragma unroll
+        for (int m = 0; m < 64; ++m) {
+          if (m < p.M) {
+            float v = p.alpha * vals[m];
+            if (p.has_c) v = fmaf(p.beta, load_c(p, m, ng), v);
+            store_d(p, m, ng, v);
+          }
+        }
+      } else if (finish && ng < p.N) {
         const float bias_n = p.epi.bias ? load_bias(p.epi, ng) : 0.0f;
 #pragma unroll
         for (int m = 0; m < 64; ++m) {
           if (m < p.M) {
             float v = p.alpha * vals[m];
             if (p.has_c) v = fmaf(p.beta, load_c(p, m, ng), v);
-            if (p.epi.bias || p.epi.act) v = activate(v + bias_n, p.epi.act);
-            store_d(p, m, ng, v);
+            store_d(p, m, ng, activate(v + bias_n, p.epi.act));
           }
         }
       }
@@ -495,7 +509,9 @@ cudaError_t launch_skinny(const CUtensorMap& tmA, const CUtensorMap& tmB, Skinny
   if (dev < 64 && !configured[dev]) {
     int worst = 0;
     for (int np = 16; np <= 64; np += 16) worst = smem_for(np) > worst ? smem_for(np) : worst;
-    e = cudaFuncSetAttribute(gemm_tn_skinny_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, worst);
+    e = cudaFuncSetAttribute(gemm_tn_skinny_kernel<kKindF16>, cudaFuncAttributeMaxDynamicSharedMemorySize, worst);
+    if (e != cudaSuccess) return e;
+    e = cudaFuncSetAttribute(gemm_tn_skinny_kernel<kKindF8F6F4>, cudaFuncAttributeMaxDynamicSharedMemorySize, worst);
     if (e != cudaSuccess) return e;
     configured[dev] = true;
   }
@@ -510,7 +526,7 @@ cudaError_t launch_skinny(const CUtensorMap& tmA, const CUtensorMap& tmB, Skinny
     info->tile_n = p.np;
     info->stages = p.stages;
     info->smem_bytes = smem;
-    info->kernel = "gemm_tn_skinny_kernel";
+    info->kernel = p.kind == kKindF8F6F4 ? "gemm_tn_skinny_kernel<fp8 in>" : "gemm_tn_skinny_kernel";
   }
   cudaLaunchConfig_t cfg = {};
   cudaLaunchAttribute attr[1];
@@ -524,7 +540,8 @@ cudaError_t launch_skinny(const CUtensorMap& tmA, const CUtensorMap& tmB, Skinny
     cfg.attrs = attr;
     cfg.numAttrs = 1;
   }
-  return cudaLaunchKernelEx(&cfg, gemm_tn_skinny_kernel, tmA, tmB, p);
+  return p.kind == kKindF8F6F4 ? cudaLaunchKernelEx(&cfg, gemm_tn_skinny_kernel<kKindF8F6F4>, tmA, tmB, p)
+                               : cudaLaunchKernelEx(&cfg, gemm_tn_skinny_kernel<kKindF16>, tmA, tmB, p);
 }
 
 }  // namespace gtn

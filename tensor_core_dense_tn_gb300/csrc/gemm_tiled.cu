@@ -44,8 +44,12 @@ namespace gtn {
 
 namespace {
 
-constexpr int kBK = 64;           // K elements per stage (128 bytes of bf16)
-constexpr int kUmmaK = 16;        // K per tcgen05.mma (kind::f16)
+constexpr int kStageK = 128;      // bytes of K per operand row per stage (one 128-byte swizzle atom)
+constexpr int kMmaPerStage = 4;   // tcgen05.mma instructions per stage, 32 bytes of K each
+
+// K elements per stage: 64 bf16 or 128 fp8.
+template <int KIND>
+constexpr int stage_k_elems() { return KIND == kKindF16 ? 64 : 128; }
 constexpr int kEpiWarps = 4;
 constexpr int kThreads = 64 + 32 * kEpiWarps;
 constexpr int kErrTimeout = -5;   // GEMM_ERR_TIMEOUT
@@ -55,8 +59,8 @@ struct Cfg {
   static constexpr int BN = 256;                      // tile N (MMA N)
   static constexpr int TILE_M = 128 * CG;             // rows per (pair) tile = MMA M
   static constexpr int B_ROWS = BN / CG;              // B rows loaded per CTA
-  static constexpr int A_BYTES = 128 * kBK * 2;       // 16 KiB
-  static constexpr int B_BYTES = B_ROWS * kBK * 2;
+  static constexpr int A_BYTES = 128 * kStageK;       // 16 KiB
+  static constexpr int B_BYTES = B_ROWS * kStageK;
   static constexpr int STAGES = (CG == 1) ? 4 : 6;
   static constexpr uint32_t STAGE_TX = (A_BYTES + B_BYTES) * CG;
   static constexpr int OUT_BYTES = OUT_F32 ? 4 : 2;
@@ -125,13 +129,14 @@ __device__ __forceinline__ void tile_coords(int t, const TileParams& p, int& tm,
   tn = r / gm;
 }
 
-template <int CG, bool OUT_F32>
+template <int CG, bool OUT_F32, int KIND>
 __global__ void __launch_bounds__(kThreads, 1)
     gemm_tn_tiled_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
                          const __grid_constant__ CUtensorMap tmC, const __grid_constant__ CUtensorMap tmD,
                          const TileParams p) {
   using C_ = Cfg<CG, OUT_F32>;
   constexpr bool kCluster = (CG == 2);
+  constexpr int kBK = stage_k_elems<KIND>();
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
   const uint32_t sA = smem_u32(smem);
@@ -232,7 +237,8 @@ __global__ void __launch_bounds__(kThreads, 1)
     // ------------------------------------------------------------ MMA issuer
     if (lane == 0 && leader) {
       Abort ab{abort_flag, p.timeout_ns, p.status, kRoleMma};
-      constexpr uint32_t idesc = instr_desc_bf16_f32(C_::TILE_M, C_::BN);
+      const uint32_t idesc = KIND == kKindF16 ? instr_desc_bf16_f32(C_::TILE_M, C_::BN)
+                                              : instr_desc_f32acc(C_::TILE_M, C_::BN, p.a_fmt, p.b_fmt);
       bool ok = true;
       int stage = 0;
       uint32_t phase = 0;
@@ -251,9 +257,9 @@ __global__ void __launch_bounds__(kThreads, 1)
           const uint64_t a0 = smem_desc_sw128(sA + stage * C_::A_BYTES);
           const uint64_t b0 = smem_desc_sw128(sB + stage * C_::B_BYTES);
 #pragma unroll
-          for (int k = 0; k < kBK / kUmmaK; ++k) {
+          for (int k = 0; k < kMmaPerStage; ++k) {
             // +32 bytes along K inside the swizzle atom = +2 in the encoded address
-            mma_bf16<CG>(d_tmem, a0 + 2 * k, b0 + 2 * k, idesc, (kb | k) != 0);
+            mma_issue<CG, KIND>(d_tmem, a0 + 2 * k, b0 + 2 * k, idesc, (kb | k) != 0);
           }
           if constexpr (CG == 1) mma_commit(empty_bar(stage));
           else mma_commit_pair(empty_bar(stage), 0x3);
@@ -399,12 +405,12 @@ __global__ void __launch_bounds__(kThreads, 1)
   }
 }
 
-template <int CG, bool OUT_F32>
+template <int CG, bool OUT_F32, int KIND>
 cudaError_t launch_impl(const CUtensorMap& tmA, const CUtensorMap& tmB, const CUtensorMap& tmC,
                         const CUtensorMap& tmD, const TileParams& p, int grid_override, bool pdl,
                         cudaStream_t stream, LaunchInfo* info) {
   using C_ = Cfg<CG, OUT_F32>;
-  auto kern = gemm_tn_tiled_kernel<CG, OUT_F32>;
+  auto kern = gemm_tn_tiled_kernel<CG, OUT_F32, KIND>;
   static bool configured[64] = {};
   int dev = 0;
   cudaError_t e = cudaGetDevice(&dev);
@@ -471,8 +477,12 @@ cudaError_t launch_impl(const CUtensorMap& tmA, const CUtensorMap& tmB, const CU
     info->tile_n = C_::BN;
     info->stages = C_::STAGES;
     info->smem_bytes = C_::SMEM;
-    info->kernel = CG == 2 ? (OUT_F32 ? "gemm_tn_tiled_kernel<2,f32>" : "gemm_tn_tiled_kernel<2,bf16>")
-                           : (OUT_F32 ? "gemm_tn_tiled_kernel<1,f32>" : "gemm_tn_tiled_kernel<1,bf16>");
+    static const char* names[2][2][2] = {
+        {{"gemm_tn_tiled_kernel<1,bf16>", "gemm_tn_tiled_kernel<1,f32>"},
+         {"gemm_tn_tiled_kernel<2,bf16>", "gemm_tn_tiled_kernel<2,f32>"}},
+        {{"gemm_tn_tiled_kernel<1,bf16,fp8 in>", "gemm_tn_tiled_kernel<1,f32,fp8 in>"},
+         {"gemm_tn_tiled_kernel<2,bf16,fp8 in>", "gemm_tn_tiled_kernel<2,f32,fp8 in>"}}};
+    info->kernel = names[KIND][CG - 1][OUT_F32 ? 1 : 0];
   }
   return cudaLaunchKernelEx(&cfg, kern, tmA, tmB, tmC, tmD, p);
 }
@@ -489,15 +499,17 @@ void tiled_shape(int cta_group, int out_f32, int* tile_m, int* tile_n, int* b_ro
   *epi_cols = 32;
 }
 
-cudaError_t launch_tiled(int cta_group, int out_f32, const CUtensorMap& tmA, const CUtensorMap& tmB,
+cudaError_t launch_tiled(int cta_group, int out_f32, int kind, const CUtensorMap& tmA, const CUtensorMap& tmB,
                          const CUtensorMap& tmC, const CUtensorMap& tmD, TileParams p, int grid_override,
                          bool pdl, cudaStream_t stream, LaunchInfo* info) {
-  if (cta_group == 2) {
-    return out_f32 ? launch_impl<2, true>(tmA, tmB, tmC, tmD, p, grid_override, pdl, stream, info)
-                   : launch_impl<2, false>(tmA, tmB, tmC, tmD, p, grid_override, pdl, stream, info);
+#define GTN_LAUNCH(CGV, OF, KV) launch_impl<CGV, OF, KV>(tmA, tmB, tmC, tmD, p, grid_override, pdl, stream, info)
+  if (kind == kKindF8F6F4) {
+    if (cta_group == 2) return out_f32 ? GTN_LAUNCH(2, true, kKindF8F6F4) : GTN_LAUNCH(2, false, kKindF8F6F4);
+    return out_f32 ? GTN_LAUNCH(1, true, kKindF8F6F4) : GTN_LAUNCH(1, false, kKindF8F6F4);
   }
-  return out_f32 ? launch_impl<1, true>(tmA, tmB, tmC, tmD, p, grid_override, pdl, stream, info)
-                 : launch_impl<1, false>(tmA, tmB, tmC, tmD, p, grid_override, pdl, stream, info);
+  if (cta_group == 2) return out_f32 ? GTN_LAUNCH(2, true, kKindF16) : GTN_LAUNCH(2, false, kKindF16);
+  return out_f32 ? GTN_LAUNCH(1, true, kKindF16) : GTN_LAUNCH(1, false, kKindF16);
+#undef GTN_LAUNCH
 }
 
 }  // namespace gtn

@@ -8,6 +8,10 @@
 
 namespace gtn {
 
+// Input kinds (match the tcgen05.mma kinds in ptx.cuh).
+constexpr int kInBf16 = 0;
+constexpr int kInFp8 = 1;
+
 // Device status word: [0] = first error code (0 = none), [1] = detail
 // (role << 24 | block index) of the wait that gave up.
 constexpr int kStatusWords = 2;
@@ -34,6 +38,7 @@ struct TileParams {
   int raster_group;    // tiles along M per grouped-raster strip
   float alpha, beta;
   int has_c;           // beta != 0
+  int a_fmt, b_fmt;    // fp8 inputs: kind::f8f6f4 format codes (0 = e4m3, 1 = e5m2)
   Epilogue epi;
   int fault;           // kFault* bits (tests only)
   uint64_t timeout_ns;
@@ -56,6 +61,8 @@ struct SkinnyParams {
   const void* C; long long ldc;
   void* D; long long ldd;
   int out_f32;
+  int kind;            // kKindF16 (bf16 inputs) or kKindF8F6F4 (fp8 inputs)
+  int a_fmt, b_fmt;    // fp8 format codes
   Epilogue epi;
   float* partials;     // grid * 2 slots * 128 * np floats
   int* counters;       // 4 per n-tile (one per epilogue warp), zero between calls
@@ -76,7 +83,7 @@ struct LaunchInfo {
 // launches with programmatic stream serialisation: the kernel's set-up may
 // overlap the previous kernel on the stream; it waits for that kernel's
 // completion (griddepcontrol.wait) before touching global memory.
-cudaError_t launch_tiled(int cta_group, int out_f32, const CUtensorMap& tmA, const CUtensorMap& tmB,
+cudaError_t launch_tiled(int cta_group, int out_f32, int kind, const CUtensorMap& tmA, const CUtensorMap& tmB,
                          const CUtensorMap& tmC, const CUtensorMap& tmD, TileParams p, int grid_override,
                          bool pdl, cudaStream_t stream, LaunchInfo* info);
 

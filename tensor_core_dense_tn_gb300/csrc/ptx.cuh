@@ -215,22 +215,43 @@ __device__ __forceinline__ void tc_fence_after() {
   asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory");
 }
 
-// D[tmem] (+)= A[smem desc] * B[smem desc]^T, kind::f16 (bf16 in, fp32 accumulate).
-template <int CG>
-__device__ __forceinline__ void mma_bf16(uint32_t d_tmem, uint64_t adesc, uint64_t bdesc,
-                                         uint32_t idesc, uint32_t accumulate) {
-  if constexpr (CG == 1) {
-    asm volatile(
-        "{\n\t.reg .pred p;\n\tsetp.ne.b32 p, %4, 0;\n\t"
-        "tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %3, p;\n\t}" ::"r"(d_tmem),
-        "l"(adesc), "l"(bdesc), "r"(idesc), "r"(accumulate)
-        : "memory");
+// Input kinds of tcgen05.mma used here.
+constexpr int kKindF16 = 0;      // kind::f16 (bf16 x bf16), K = 16 per MMA
+constexpr int kKindF8F6F4 = 1;   // kind::f8f6f4 (e4m3 / e5m2), K = 32 per MMA
+
+// D[tmem] (+)= A[smem desc] * B[smem desc]^T with fp32 accumulation.  Either
+// kind reads 32 bytes of K per operand row per instruction.
+template <int CG, int KIND>
+__device__ __forceinline__ void mma_issue(uint32_t d_tmem, uint64_t adesc, uint64_t bdesc, uint32_t idesc,
+                                          uint32_t accumulate) {
+  if constexpr (KIND == kKindF16) {
+    if constexpr (CG == 1) {
+      asm volatile(
+          "{\n\t.reg .pred p;\n\tsetp.ne.b32 p, %4, 0;\n\t"
+          "tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %3, p;\n\t}" ::"r"(d_tmem),
+          "l"(adesc), "l"(bdesc), "r"(idesc), "r"(accumulate)
+          : "memory");
+    } else {
+      asm volatile(
+          "{\n\t.reg .pred p;\n\tsetp.ne.b32 p, %4, 0;\n\t"
+          "tcgen05.mma.cta_group::2.kind::f16 [%0], %1, %2, %3, p;\n\t}" ::"r"(d_tmem),
+          "l"(adesc), "l"(bdesc), "r"(idesc), "r"(accumulate)
+          : "memory");
+    }
   } else {
-    asm volatile(
-        "{\n\t.reg .pred p;\n\tsetp.ne.b32 p, %4, 0;\n\t"
-        "tcgen05.mma.cta_group::2.kind::f16 [%0], %1, %2, %3, p;\n\t}" ::"r"(d_tmem),
-        "l"(adesc), "l"(bdesc), "r"(idesc), "r"(accumulate)
-        : "memory");
+    if constexpr (CG == 1) {
+      asm volatile(
+          "{\n\t.reg .pred p;\n\tsetp.ne.b32 p, %4, 0;\n\t"
+          "tcgen05.mma.cta_group::1.kind::f8f6f4 [%0], %1, %2, %3, p;\n\t}" ::"r"(d_tmem),
+          "l"(adesc), "l"(bdesc), "r"(idesc), "r"(accumulate)
+          : "memory");
+    } else {
+      asm volatile(
+          "{\n\t.reg .pred p;\n\tsetp.ne.b32 p, %4, 0;\n\t"
+          "tcgen05.mma.cta_group::2.kind::f8f6f4 [%0], %1, %2, %3, p;\n\t}" ::"r"(d_tmem),
+          "l"(adesc), "l"(bdesc), "r"(idesc), "r"(accumulate)
+          : "memory");
+    }
   }
 }
 
@@ -292,12 +313,18 @@ __host__ __device__ constexpr uint64_t smem_desc_sw128(uint32_t saddr) {
          ((uint64_t)1 << 46) | ((uint64_t)2 << 61);
 }
 
-// Instruction descriptor for kind::f16 with bf16 A/B, fp32 D, both operands
-// K-major: D format in bits 4-5 (1 = f32), A format 7-9 and B format 10-12
-// (1 = bf16), transpose bits 15/16 clear (K-major), N >> 3 in bits 17-22,
-// M >> 4 in bits 24-28.
+// Instruction descriptor for fp32 accumulation with both operands K-major
+// (PTX ISA, tcgen05 instruction descriptor): D format in bits 4-5 (1 = f32),
+// A format in bits 7-9 and B format in bits 10-12, transpose bits 15/16
+// clear (K-major), N >> 3 in bits 17-22, M >> 4 in bits 24-28.  Format codes:
+// kind::f16 uses 1 = bf16; kind::f8f6f4 uses 0 = e4m3, 1 = e5m2.
+__host__ __device__ constexpr uint32_t instr_desc_f32acc(uint32_t M, uint32_t N, uint32_t a_fmt, uint32_t b_fmt) {
+  return (1u << 4) | (a_fmt << 7) | (b_fmt << 10) | ((N >> 3) << 17) | ((M >> 4) << 24);
+}
+
+// kind::f16 with bf16 A and B.
 __host__ __device__ constexpr uint32_t instr_desc_bf16_f32(uint32_t M, uint32_t N) {
-  return (1u << 4) | (1u << 7) | (1u << 10) | ((N >> 3) << 17) | ((M >> 4) << 24);
+  return instr_desc_f32acc(M, N, 1, 1);
 }
 
 // ---------------------------------------------------------------- numerics

@@ -26,8 +26,9 @@ def gemm_flops(M: int, N: int, K: int) -> int:
     return 2 * M * N * K
 
 
-def gemm_bytes(M: int, N: int, K: int, out_bytes: int = 2, beta_nonzero: bool = False) -> int:
-    q = 2 * (M * K + N * K) + out_bytes * M * N
+def gemm_bytes(M: int, N: int, K: int, out_bytes: int = 2, beta_nonzero: bool = False,
+               in_bytes: int = 2) -> int:
+    q = in_bytes * (M * K + N * K) + out_bytes * M * N
     if beta_nonzero:
         q += out_bytes * M * N
     return q

@@ -1,0 +1,135 @@
+"""GPU parity of the FP8 TN GEMM, D = alpha * scale_a * scale_b * A B^T + beta * C.
+
+A and B are one-byte e4m3 or e5m2 codes (the same format for both); products
+are formed on the tensor cores with FP32 accumulation.  Against the FP64
+oracle, which decodes every code by the formats' definitions:
+* integer inputs in [-4, 4] (exact in both formats): bit-exact on all three
+  kernel paths, ragged M, N and K, and with power-of-two scales;
+* normal inputs, real scales, beta with C: within the oracle's accumulation
+  bound (1e-4 of sum |alpha' a b| plus the output rounding).
+"""
+import numpy as np
+import pytest
+
+import gemm_inputs as gi
+import oracle
+
+pytestmark = pytest.mark.gpu
+
+g = pytest.importorskip("tensor_core_dense_tn_gb300")
+from gpu_util import empty_out, from_dev, sample_positions, to_dev_bf16, to_dev_f32  # noqa: E402
+
+# M picks the kernel path: 48 -> skinny, 100 -> 1-SM tiled, 300 -> 2-SM tiled
+PATH_M = {"skinny": 48, "1sm": 100, "2sm": 300}
+FMTS = [gi.FP8_E4M3, gi.FP8_E5M2]
+
+
+def to_dev_u8(codes):
+    import torch
+    return torch.from_numpy(np.ascontiguousarray(codes, dtype=np.uint8)).to("cuda:0")
+
+
+def _run(M, N, K, A, B, fmt, out_dtype, scale_a=1.0, scale_b=1.0, alpha=1.0, beta=0.0, C=None,
+         lda=None, ldb=None):
+    import torch
+    lda = K if lda is None else lda
+    ldb = K if ldb is None else ldb
+    dA, dB = to_dev_u8(A), to_dev_u8(B)
+    dC = None
+    if C is not None:
+        dC = to_dev_bf16(C) if out_dtype == gi.OUT_BF16 else to_dev_f32(C)
+    dD, ldd = empty_out(M, N, out_dtype)
+    s = torch.cuda.current_stream().cuda_stream
+    rc = g.gemm_fp8_tn(M, N, K, dA.data_ptr(), lda, dB.data_ptr(), ldb, fmt, scale_a, scale_b,
+                       dC.data_ptr() if dC is not None else 0, N if dC is not None else 0,
+                       dD.data_ptr(), ldd, alpha, beta, out_dtype, s)
+    assert rc == 0, g.last_error()
+    assert g.gemm_get_status(s) == 0, g.last_error()
+    return from_dev(dD, out_dtype)
+
+
+@pytest.mark.parametrize("path", list(PATH_M))
+@pytest.mark.parametrize("fmt", FMTS)
+@pytest.mark.parametrize("N,K", [(520, 320), (264, 1040)])
+def test_integer_exact(path, fmt, N, K):
+    M = PATH_M[path]
+    A = gi.draw_fp8(M, K, gi.Dist("int", -4, 4), 5000 + fmt, fmt)
+    B = gi.draw_fp8(N, K, gi.Dist("int", -4, 4), 5010 + fmt, fmt)
+    ref, _ = oracle.gemm_ref_fp8(A, B, fmt)
+    got = _run(M, N, K, A, B, fmt, gi.OUT_F32)
+    assert np.array_equal(got, oracle.exact_f32(ref))
+
+
+@pytest.mark.parametrize("path", list(PATH_M))
+def test_integer_exact_scales_and_padding(path):
+    # power-of-two scales keep the result exact; padded rows (ld > K) hold NaN codes
+    M, N, K, ld = PATH_M[path] + 3, 392, 208, 256
+    fmt = gi.FP8_E4M3
+    A = gi.draw_fp8(M, K, gi.Dist("int", -4, 4), 5100, fmt, ld=ld)
+    B = gi.draw_fp8(N, K, gi.Dist("int", -4, 4), 5101, fmt, ld=ld)
+    ref, _ = oracle.gemm_ref_fp8(A, B, fmt, M=M, N=N, K=K, lda=ld, ldb=ld, alpha=0.5 * 0.25 * 8.0)
+    got = _run(M, N, K, A, B, fmt, gi.OUT_F32, scale_a=0.25, scale_b=8.0, alpha=0.5, lda=ld, ldb=ld)
+    assert np.array_equal(got, oracle.exact_f32(ref))
+
+
+@pytest.mark.parametrize("path", list(PATH_M))
+@pytest.mark.parametrize("fmt", FMTS)
+@pytest.mark.parametrize("out_dtype", [gi.OUT_BF16, gi.OUT_F32])
+def test_normal_within_bound(path, fmt, out_dtype):
+    M, N, K = PATH_M[path], 776, 1536
+    A = gi.draw_fp8(M, K, gi.Dist("normal", 4.0), 5200 + fmt, fmt)
+    B = gi.draw_fp8(N, K, gi.Dist("normal", 4.0), 5210 + fmt, fmt)
+    C = (gi.draw_bf16(M, N, gi.Dist("normal", 1.0), 5220) if out_dtype == gi.OUT_BF16
+         else gi.draw_f32(M, N, gi.Dist("normal", 1.0), 5220))
+    sa, sb, alpha, beta = 0.37, 0.011, 1.25, 0.5
+    c64 = gi.bf16_bits_to_f32(C) if out_dtype == gi.OUT_BF16 else C
+    ref, absdot = oracle.gemm_ref_fp8(A, B, fmt, C=C, alpha=alpha * np.float32(sa) * np.float32(sb),
+                                      beta=beta)
+    got = _run(M, N, K, A, B, fmt, out_dtype, scale_a=sa, scale_b=sb, alpha=alpha, beta=beta, C=C)
+    ok, worst, idx = oracle.check(got, ref, absdot, out_dtype, beta, c64)
+    assert ok, (worst, idx)
+
+
+@pytest.mark.parametrize("M,N,K", [(16, 8192, 8192), (8192, 28672, 4096)])
+def test_full_size_sampled(M, N, K):
+    """The two FP8 bench shapes (decode and MLP up-projection), e4m3, sampled outputs."""
+    fmt = gi.FP8_E4M3
+    A = gi.draw_fp8(M, K, gi.Dist("normal", 1.0), 5300, fmt)
+    B = gi.draw_fp8(N, K, gi.Dist("normal", 1.0), 5301, fmt)
+    sb = 1.0 / K
+    got = _run(M, N, K, A, B, fmt, gi.OUT_BF16, scale_b=sb)
+    rows, cols = sample_positions(M, N, n_random=2048, seed=53)
+    ref, absdot = oracle.gemm_ref_fp8_sampled(A, B, fmt, rows, cols, alpha=sb)
+    ok, worst, idx = oracle.check(got[rows, cols], ref, absdot, gi.OUT_BF16)
+    assert ok, (worst, idx)
+
+
+def test_fp8_matches_bf16_path_on_common_values():
+    """Small integers are exact in bf16 and both fp8 formats: all three inputs
+    kinds must give the same bits through their own kernels."""
+    import torch
+    M, N, K = 300, 520, 512
+    Ai = np.random.default_rng(5400).integers(-4, 5, size=(M, K))
+    Bi = np.random.default_rng(5401).integers(-4, 5, size=(N, K))
+    outs = []
+    for fmt in FMTS:
+        outs.append(_run(M, N, K, gi.f32_to_fp8_bits(Ai, fmt), gi.f32_to_fp8_bits(Bi, fmt), fmt, gi.OUT_F32))
+    dA = to_dev_bf16(gi.f32_to_bf16_bits(Ai.astype(np.float32)))
+    dB = to_dev_bf16(gi.f32_to_bf16_bits(Bi.astype(np.float32)))
+    dD, ldd = empty_out(M, N, gi.OUT_F32)
+    s = torch.cuda.current_stream().cuda_stream
+    rc = g.gemm_bf16_tn(M, N, K, dA.data_ptr(), K, dB.data_ptr(), K, 0, 0, dD.data_ptr(), ldd,
+                        1.0, 0.0, gi.OUT_F32, s)
+    assert rc == 0 and g.gemm_get_status(s) == 0
+    outs.append(from_dev(dD, gi.OUT_F32))
+    assert np.array_equal(outs[0], outs[1]) and np.array_equal(outs[0], outs[2])
+
+
+def test_fp8_argument_errors():
+    a = (64, 64, 64, 0x1000, 64, 0x2000, 64)
+    tail = (1.0, 1.0, 0, 0, 0x3000, 64, 1.0, 0.0, 0, 0)
+    assert g.gemm_fp8_tn(*a, 2, *tail) == g.GEMM_ERR_INVALID_VALUE
+    assert g.gemm_fp8_tn(*a, -1, *tail) == g.GEMM_ERR_INVALID_VALUE
+    # lda must be a multiple of 16 one-byte elements
+    assert g.gemm_fp8_tn(64, 64, 64, 0x1000, 72, 0x2000, 64, 0, *tail) == g.GEMM_ERR_MISALIGNED
+    assert g.gemm_fp8_tn(64, 64, 64, 0x1008, 64, 0x2000, 64, 0, *tail) == g.GEMM_ERR_MISALIGNED

@@ -383,3 +383,27 @@ def test_fp8_sampled_matches_full():
         a64 = gi.fp8_bits_to_f64(A, fmt)
         b64 = gi.fp8_bits_to_f64(B, fmt)
         assert np.allclose(full, 0.75 * (a64 @ b64.T) - 0.5 * C, rtol=1e-12, atol=1e-12)
+
+
+@pytest.mark.parametrize("fmt", [0, 1])
+def test_fp8_encoder_is_nearest_ties_even(fmt):
+    """The input encoder against a brute-force search over every finite code."""
+    rng = np.random.default_rng(88 + fmt)
+    top = 448.0 if fmt == 0 else 57344.0
+    x = np.concatenate([rng.standard_normal(4000) * s for s in (1e-4, 1e-2, 1.0, 30.0, top / 3)]).astype(np.float32)
+    # exact midpoints between neighbouring finite values, and just past the top
+    codes = np.arange(256, dtype=np.uint8)
+    vals = gi.fp8_bits_to_f64(codes, fmt)
+    fin = np.sort(np.unique(vals[np.isfinite(vals)]))
+    mids = ((fin[1:] + fin[:-1]) / 2).astype(np.float32)
+    x = np.concatenate([x, mids, [top * 1.01, -top * 1.5, 1e30, 0.0]]).astype(np.float32)
+    got = gi.fp8_bits_to_f64(gi.f32_to_fp8_bits(x, fmt), fmt)
+    fin_codes = codes[np.isfinite(vals)]
+    fin_vals = vals[np.isfinite(vals)]
+    for xi, gv in zip(x.astype(np.float64), got):
+        xc = min(max(xi, -top), top)
+        d = np.abs(fin_vals - xc)
+        best = fin_codes[d == d.min()]
+        # among equally near codes, ties go to the even one (+0 and -0 both fine)
+        want = {float(gi.fp8_bits_to_f64(np.uint8(c), fmt)) for c in best if c % 2 == 0 or len(best) == 1}
+        assert gv in want or (xc == 0 and gv == 0), (xi, gv, want)
