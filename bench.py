@@ -235,7 +235,8 @@ def run_ours(args, dist):
     if C is not None:
         dC = dev_bf16(C, torch, device) if w.out_dtype == gi.OUT_BF16 else torch.from_numpy(C).to(device)
     dD = torch.empty((w.M, w.N), dtype=out_t, device=device)
-    cfg = g.GemmConfig(path=args.path)
+    sched = {"default": 0, "static": 1, "clc": 2}[args.scheduler]
+    cfg = g.GemmConfig(path=args.path, scheduler=sched)
     c_ptr = dC.data_ptr() if dC is not None else 0
     ldc = w.N if dC is not None else 0
 
@@ -299,6 +300,7 @@ def run_ours(args, dist):
         "config": dict(w.describe(), path=PATH_NAMES.get(info.get("path"), info.get("path")),
                        grid=info.get("grid"), cluster=info.get("cluster"),
                        tile=[info.get("tile_m"), info.get("tile_n")], stages=info.get("stages"),
+                       scheduler={1: "static", 2: "clc"}.get(info.get("scheduler"), None),
                        l2="operands (288 MiB) larger than L2; no flush" if args.workload == MAIN
                        else "see workload", parallelism=f"replicas x{dist.world}"),
         "roofline": roof,
@@ -345,6 +347,7 @@ def run_ours(args, dist):
     if not args.no_secondary:
         result["secondary"] = run_decode(args, g, torch, device, peaks, dist)
         result["fp8"] = run_fp8(args, g, torch, device, peaks, dist)
+        result["scheduler_clc"] = run_scheduler_study(args, g, torch, device, w, dA, dB, dD, flops, peaks, dist)
 
     # ---------------------------------------------------------------- CPU oracle baseline
     if not args.no_cpu_baseline and dist.rank == 0:
@@ -553,6 +556,89 @@ def run_fp8(args, g, torch, device, peaks, dist):
     return out
 
 
+def run_scheduler_study(args, g, torch, device, w, dA, dB, dD, flops, peaks, dist):
+    """The cluster-launch-control tile scheduler against the static persistent
+    grid: (1) the main GEMM under CLC on an idle GPU; (2) an 8192x8192x4096
+    GEMM started while another kernel (a 1-SM GEMM with one long tile per CTA)
+    holds 64 of the SMs for ~0.45 ms, where a static grid cannot place all its
+    CTAs and CLC lets the resident ones take the missing CTAs' tiles."""
+    stream = torch.cuda.current_stream(device)
+    s_handle = stream.cuda_stream
+
+    def stepper(sched):
+        cfg = g.GemmConfig(scheduler=sched)
+
+        def step(_i):
+            rc = g.gemm_bf16_tn_ex(w.M, w.N, w.K, dA.data_ptr(), w.K, dB.data_ptr(), w.K, 0, 0, dD.data_ptr(),
+                                   w.N, w.alpha, w.beta, w.out_dtype, s_handle, cfg)
+            if rc != 0:
+                raise RuntimeError(f"gemm failed: {rc} {g.last_error()}")
+        return step
+
+    # interleaved rounds with equal step counts, so that clock and power
+    # drift over the run falls on both schedulers alike
+    steps = max(10, min(args.steps, 30))
+    tf = {"static": [], "clc": []}
+    for r in range(4):
+        order = (("static", g.SCHED_STATIC), ("clc", g.SCHED_CLC))
+        for name, sched in (order if r % 2 == 0 else order[::-1]):
+            step = stepper(sched)
+            for i in range(2):
+                step(i)
+            ms = dist.max(time_steps(torch, stream, step, steps))
+            tf[name].append(flops / (ms / 1e3 / steps) / 1e12)
+    if g.gemm_get_status(s_handle) != 0:
+        raise RuntimeError(g.last_error())
+    med = {k: statistics.median(v) for k, v in tf.items()}
+    out = {"main_interleaved": {"unit": "TFLOP/s", "steps_per_round": steps, "rounds": 4,
+                                "static": round(dist.world * med["static"], 2),
+                                "clc": round(dist.world * med["clc"], 2),
+                                "clc_over_static": round(med["clc"] / med["static"], 4)}}
+
+    # shared GPU: background kernel on 64 SMs, then the GEMM on its own stream
+    bg_ctas, kb = 64, 65536
+    bgA = torch.zeros((128 * bg_ctas, kb), dtype=torch.bfloat16, device=device)
+    bgB = torch.zeros((256, kb), dtype=torch.bfloat16, device=device)
+    bgD = torch.empty((128 * bg_ctas, 256), dtype=torch.bfloat16, device=device)
+    M = N = 8192
+    K = 4096
+    sA = dA[:M, :K] if dA.shape[0] >= M else None
+    sB = dB[:N, :K] if dB.shape[0] >= N else None
+    if sA is None or sB is None or w.K != K:
+        return out
+    s_bg, s_main = torch.cuda.Stream(device), torch.cuda.Stream(device)
+    bg_cfg = g.GemmConfig(path=g.PATH_1SM, grid=bg_ctas, scheduler=g.SCHED_STATIC)
+    dDs = torch.empty((M, N), dtype=torch.bfloat16, device=device)
+    times = {"static": [], "clc": []}
+    for rep in range(4):
+        for name, sched in (("static", g.SCHED_STATIC), ("clc", g.SCHED_CLC)):
+            torch.cuda.synchronize()
+            e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            rc = g.gemm_bf16_tn_ex(128 * bg_ctas, 256, kb, bgA.data_ptr(), kb, bgB.data_ptr(), kb, 0, 0,
+                                   bgD.data_ptr(), 256, 1.0, 0.0, gi.OUT_BF16, s_bg.cuda_stream, bg_cfg)
+            if rc != 0:
+                raise RuntimeError(g.last_error())
+            with torch.cuda.stream(s_main):
+                torch.cuda._sleep(40000)   # ~20 us: the background CTAs are resident by now
+                e0.record(s_main)
+                rc = g.gemm_bf16_tn_ex(M, N, K, sA.data_ptr(), w.K, sB.data_ptr(), w.K, 0, 0, dDs.data_ptr(), N,
+                                       1.0, 0.0, gi.OUT_BF16, s_main.cuda_stream, g.GemmConfig(scheduler=sched))
+                if rc != 0:
+                    raise RuntimeError(g.last_error())
+                e1.record(s_main)
+            torch.cuda.synchronize()
+            if rep > 0:  # the first round warms both paths up
+                times[name].append(e0.elapsed_time(e1) * 1e3)
+    if g.gemm_get_status(s_main.cuda_stream) != 0:
+        raise RuntimeError(g.last_error())
+    med = {k: statistics.median(v) for k, v in times.items()}
+    out["shared_gpu"] = {"gemm": "8192x8192x4096 bf16", "other_kernel": f"1-SM GEMM on {bg_ctas} SMs, ~0.45 ms",
+                         "static_us": round(med["static"], 1), "clc_us": round(med["clc"], 1),
+                         "clc_speedup": round(med["static"] / med["clc"], 3), "repeats": len(times["clc"])}
+    del bgA, bgB, bgD, dDs
+    return out
+
+
 def cpu_baseline(w, A, B, C, dD, out_t, torch, seconds):
     """Time the CPU oracle on a row sample sized to ~`seconds`; compare those rows with the GPU."""
     import oracle
@@ -631,6 +717,8 @@ def main():
     ap.add_argument("--workload", type=int, default=MAIN, help="index into gemm_inputs.WORKLOADS")
     ap.add_argument("--shape", default="", help="M,N,K override (profiling runs)")
     ap.add_argument("--path", type=int, default=0, help="0 auto, 1 1-SM, 2 2-SM, 3 skinny")
+    ap.add_argument("--scheduler", choices=["default", "static", "clc"], default="default",
+                    help="tile scheduler of the tiled paths (main step)")
     ap.add_argument("--in-dtype", choices=["bf16", "e4m3", "e5m2"], default="bf16",
                     help="input type of the main step (fp8 runs the main step alone)")
     ap.add_argument("--no-e2e", action="store_true")

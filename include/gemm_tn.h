@@ -111,7 +111,21 @@ typedef struct gemm_tn_config {
   int disable_pdl;          /* 1 = launch without programmatic dependent launch (see below) */
   int skinny_skew_kb;       /* skinny path, equal-split mode: k-blocks (of 64) moved to the part that
                                finishes each tile; 0 = default (K/4096), < 0 = none */
+  int scheduler;            /* tiled paths: GEMM_SCHED_* (0 = the default) */
 } gemm_tn_config;
+
+/* Tile schedulers of the tiled paths.
+ * STATIC: a persistent grid of as many CTAs (pairs) as fit on the GPU at
+ *   once; CTA c takes tiles c, c + grid, c + 2 grid, ...
+ * CLC: one CTA (pair) per tile is launched; each running CTA, while it works
+ *   on a tile, asks the hardware (cluster launch control) to cancel a CTA
+ *   that has not started yet and then takes that CTA's tile.  CTAs stay
+ *   resident as long as there is work, as in STATIC, but the split of tiles
+ *   follows the SMs actually available (other kernels on the GPU, uneven
+ *   tiles).  This is the dynamic persistent scheduling with cluster launch
+ *   control that the SemiAnalysis Blackwell page lists among the new
+ *   features ("Blackwell architecture features"). */
+typedef enum { GEMM_SCHED_DEFAULT = 0, GEMM_SCHED_STATIC = 1, GEMM_SCHED_CLC = 2 } gemm_scheduler;
 
 /* What the last successful launch on this host thread ran. */
 typedef struct gemm_launch_info {
@@ -124,6 +138,7 @@ typedef struct gemm_launch_info {
   int stages;        /* shared-memory ring depth */
   int smem_bytes;    /* dynamic shared memory per CTA */
   const char *kernel;/* kernel name (static string) */
+  int scheduler;     /* tiled paths: GEMM_SCHED_STATIC or GEMM_SCHED_CLC; 0 otherwise */
 } gemm_launch_info;
 
 /* D = alpha * A * B^T + beta * C (see the file comment for every argument).

@@ -40,6 +40,7 @@ EXPORTED = ["gemm_bf16_tn", "gemm_bf16_tn_ex", "gemm_get_status", "gemm_get_stat
             "gemm_bf16_tn_skinny_noalloc", "gemm_bf16_tn_bias_act", "gemm_fp8_tn"]
 
 FP8_E4M3, FP8_E5M2 = 0, 1
+SCHED_DEFAULT, SCHED_STATIC, SCHED_CLC = 0, 1, 2
 
 ACT_NONE, ACT_RELU, ACT_GELU, ACT_GELU_TANH, ACT_SILU = 0, 1, 2, 3, 4
 
@@ -54,13 +55,14 @@ class GemmConfig(ctypes.Structure):
     _fields_ = [("path", ctypes.c_int), ("grid", ctypes.c_int), ("raster_group", ctypes.c_int),
                 ("skinny_grid", ctypes.c_int), ("wait_timeout_ns", ctypes.c_uint64),
                 ("test_fault", ctypes.c_int), ("disable_pdl", ctypes.c_int),
-                ("skinny_skew_kb", ctypes.c_int)]
+                ("skinny_skew_kb", ctypes.c_int), ("scheduler", ctypes.c_int)]
 
 
 class LaunchInfo(ctypes.Structure):
     _fields_ = [("path", ctypes.c_int), ("grid", ctypes.c_int), ("cluster", ctypes.c_int),
                 ("block", ctypes.c_int), ("tile_m", ctypes.c_int), ("tile_n", ctypes.c_int),
-                ("stages", ctypes.c_int), ("smem_bytes", ctypes.c_int), ("kernel", ctypes.c_char_p)]
+                ("stages", ctypes.c_int), ("smem_bytes", ctypes.c_int), ("kernel", ctypes.c_char_p),
+                ("scheduler", ctypes.c_int)]
 
     def as_dict(self):
         return {f: (getattr(self, f).decode() if f == "kernel" and getattr(self, f) else getattr(self, f))

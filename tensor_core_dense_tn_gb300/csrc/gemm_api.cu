@@ -185,6 +185,9 @@ int run(int64_t M, int64_t N, int64_t K, const void* A, int64_t lda, const void*
   const int path_req = cfg ? cfg->path : GEMM_PATH_AUTO;
   if (path_req < GEMM_PATH_AUTO || path_req > GEMM_PATH_SKINNY)
     return fail(GEMM_ERR_INVALID_VALUE, "unknown path %d", path_req);
+  const int sched = cfg ? cfg->scheduler : GEMM_SCHED_DEFAULT;
+  if (sched != GEMM_SCHED_DEFAULT && sched != GEMM_SCHED_STATIC && sched != GEMM_SCHED_CLC)
+    return fail(GEMM_ERR_INVALID_VALUE, "unknown scheduler %d", sched);
   if (M == 0 || N == 0) return GEMM_OK;
   const int64_t kMaxDim = (int64_t)1 << 31;
   if (M >= kMaxDim || N >= kMaxDim || K >= kMaxDim)
@@ -287,6 +290,7 @@ int run(int64_t M, int64_t N, int64_t K, const void* A, int64_t lda, const void*
     p.raster_group = group;
     p.alpha = alpha; p.beta = beta; p.has_c = has_c; p.epi = epi;
     p.fault = fault; p.timeout_ns = tmo; p.status = st->status;
+    p.clc = sched == GEMM_SCHED_CLC ? 1 : 0;
     CUtensorMap tA, tB, tC, tD;
     memset(&tA, 0, sizeof tA);
     memset(&tB, 0, sizeof tB);
@@ -316,6 +320,7 @@ int run(int64_t M, int64_t N, int64_t K, const void* A, int64_t lda, const void*
   t_info.stages = li.stages;
   t_info.smem_bytes = li.smem_bytes;
   t_info.kernel = li.kernel;
+  t_info.scheduler = li.scheduler;
   return GEMM_OK;
 }
 

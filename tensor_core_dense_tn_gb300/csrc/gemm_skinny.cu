@@ -176,7 +176,7 @@ __global__ void __launch_bounds__(kThreads, 1)
 
   const int warp = threadIdx.x >> 5;
   const int lane = threadIdx.x & 31;
-  const long long U = p.units, G = p.grid, KB = p.num_kb;
+  const long long KB = p.num_kb;
   const long long c = blockIdx.x;
   const long long u_begin = cta_begin(p, c), u_end = cta_end(p, c);
 

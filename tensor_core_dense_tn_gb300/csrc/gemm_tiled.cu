@@ -28,6 +28,13 @@
 // CTA issues the MMA for both and the accumulator rows stay in each CTA's
 // own TMEM.  No TMA multicast is used; each CTA loads its own tiles.
 //
+// Tile schedule: either a persistent grid with a fixed stride (CTA c takes
+// tiles c, c + G, ...), or one CTA (pair) per tile with cluster launch
+// control: at the start of each tile the producer asks the hardware to cancel
+// a cluster that has not launched yet; the 16-byte answer lands in a small
+// ring in shared memory (in both CTAs of a pair) and every role reads it to
+// learn its next tile, or that there is none.
+//
 // Every mbarrier wait is bounded by %globaltimer.  A wait that gives up sets
 // a CTA abort flag and the device status word; all roles then leave their
 // loops, drain what they issued and free TMEM, so the kernel always returns.
@@ -67,10 +74,15 @@ struct Cfg {
   static constexpr int EPI_COLS = 32;
   static constexpr int EPI_BYTES = 32 * EPI_COLS * OUT_BYTES;   // one 32x32 box
   static constexpr int TMEM_COLS = 2 * BN;            // two accumulators
-  static constexpr int NUM_BARS = 2 * STAGES + 4 + 2 * kEpiWarps + 1;
+  static constexpr int CLC_SLOTS = 4;                 // cluster-launch-control answers in flight
+  // readers of each answer, all arriving on the leader CTA's CLC_EMPTY:
+  // producer + 4 epilogue warps per CTA, and the leader's MMA thread
+  static constexpr int CLC_READERS = CG * (1 + kEpiWarps) + 1;
+  static constexpr int NUM_BARS = 2 * STAGES + 4 + 2 * kEpiWarps + 1 + 2 * CLC_SLOTS;
   static constexpr int RING_BYTES = STAGES * (A_BYTES + B_BYTES);
   static constexpr int EPI_TOTAL = kEpiWarps * 2 * EPI_BYTES;
-  static constexpr int SMEM = 1024 + RING_BYTES + EPI_TOTAL + NUM_BARS * 8 + 16;
+  static constexpr int CLC_BYTES = CLC_SLOTS * 16;
+  static constexpr int SMEM = 1024 + RING_BYTES + EPI_TOTAL + CLC_BYTES + NUM_BARS * 8 + 16;
   static_assert(SMEM <= 232448, "shared memory budget");
   static_assert(TMEM_COLS <= 512, "TMEM columns");
 };
@@ -129,6 +141,39 @@ __device__ __forceinline__ void tile_coords(int t, const TileParams& p, int& tm,
   tn = r / gm;
 }
 
+// Position of one role in the cluster-launch-control answer ring.
+struct ClcCursor {
+  int slot = 0;
+  uint32_t phase = 0;
+  __device__ void advance(int slots) {
+    if (++slot == slots) {
+      slot = 0;
+      phase ^= 1;
+    }
+  }
+};
+
+// Next tile of a role after tile t.  Static schedule: t + stride.  Cluster
+// launch control: wait for the answer in the cursor's slot, read it, hand
+// the slot back (arrive on the leader's CLC_EMPTY; `arrive` is false for the
+// lanes of a warp other than lane 0) and return the cancelled cluster's tile,
+// or num_tiles if no cluster was left.  Returns -1 if the wait gave up.
+template <bool CLUSTER, int CG, int SLOTS, bool WARP>
+__device__ __forceinline__ int next_tile(int t, int stride, const TileParams& p, ClcCursor& cur, uint32_t full0,
+                                         uint32_t empty0_leader, uint32_t resp0, bool arrive, const Abort& ab) {
+  if (!p.clc) return t + stride;
+  if (!wait_bar<CLUSTER>(full0 + 8u * cur.slot, cur.phase, ab)) return -1;
+  uint32_t first_x;
+  const bool got = clc_query(resp0 + 16u * cur.slot, first_x);
+  if constexpr (WARP) __syncwarp();  // every lane has read the answer before lane 0 frees the slot
+  if (arrive) {  // the answer is in registers already: a relaxed arrive suffices
+    if constexpr (CLUSTER) mbar_arrive_relaxed_cluster(empty0_leader + 8u * cur.slot);
+    else mbar_arrive_relaxed(empty0_leader + 8u * cur.slot);
+  }
+  cur.advance(SLOTS);
+  return got ? (int)(first_x / CG) : p.num_tiles;
+}
+
 template <int CG, bool OUT_F32, int KIND>
 __global__ void __launch_bounds__(kThreads, 1)
     gemm_tn_tiled_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
@@ -142,14 +187,17 @@ __global__ void __launch_bounds__(kThreads, 1)
   const uint32_t sA = smem_u32(smem);
   const uint32_t sB = sA + C_::STAGES * C_::A_BYTES;
   const uint32_t sE = sA + C_::RING_BYTES;
-  uint64_t* bars = reinterpret_cast<uint64_t*>(smem + C_::RING_BYTES + C_::EPI_TOTAL);
+  const uint32_t sClc = sE + C_::EPI_TOTAL;           // CLC answers, 16 bytes each
+  uint64_t* bars = reinterpret_cast<uint64_t*>(smem + C_::RING_BYTES + C_::EPI_TOTAL + C_::CLC_BYTES);
   const uint32_t bar0 = smem_u32(bars);
   auto full_bar = [&](int s) { return bar0 + 8u * s; };
   auto empty_bar = [&](int s) { return bar0 + 8u * (C_::STAGES + s); };
   auto accf_bar = [&](int b) { return bar0 + 8u * (2 * C_::STAGES + b); };
   auto acce_bar = [&](int b) { return bar0 + 8u * (2 * C_::STAGES + 2 + b); };
   auto c_bar = [&](int w, int b) { return bar0 + 8u * (2 * C_::STAGES + 4 + 2 * w + b); };
-  const uint32_t drain_bar = bar0 + 8u * (C_::NUM_BARS - 1);
+  const uint32_t drain_bar = bar0 + 8u * (2 * C_::STAGES + 4 + 2 * kEpiWarps);
+  const uint32_t clcf0 = drain_bar + 8u;                          // CLC_FULL[slot]
+  const uint32_t clce0 = clcf0 + 8u * C_::CLC_SLOTS;              // CLC_EMPTY[slot] (used in the leader)
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bars + C_::NUM_BARS);
   volatile uint32_t* abort_flag = tmem_slot + 1;
 
@@ -172,6 +220,10 @@ __global__ void __launch_bounds__(kThreads, 1)
     for (int w = 0; w < kEpiWarps; ++w)
       for (int b = 0; b < 2; ++b) mbar_init(c_bar(w, b), 1);
     mbar_init(drain_bar, 1);
+    for (int s = 0; s < C_::CLC_SLOTS; ++s) {
+      mbar_init(clcf0 + 8u * s, 1);
+      mbar_init(clce0 + 8u * s, C_::CLC_READERS);
+    }
     *abort_flag = 0;
     fence_mbar_init();
     fence_proxy_async_smem();
@@ -203,7 +255,23 @@ __global__ void __launch_bounds__(kThreads, 1)
       bool skip_once = (p.fault & kFaultSkipTmaOnce) && blockIdx.x == 0;
       int stage = 0;
       uint32_t phase = 0;
-      for (int t = cluster_id; t < p.num_tiles && ok; t += num_clusters) {
+      ClcCursor req, rd;  // slot of the next request, slot of the next answer to read
+      const uint32_t clce_leader = kCluster ? mapa_shared(clce0, 0) : clce0;
+      int t = cluster_id;
+      while (t < p.num_tiles && ok) {
+        if (p.clc) {
+          // ask for the tile after this one now; the answer is read once this tile's loads are issued
+          if (leader && !wait_bar<kCluster>(clce0 + 8u * req.slot, req.phase ^ 1, ab)) {
+            ok = false;
+            break;
+          }
+          mbar_arrive_expect_tx(clcf0 + 8u * req.slot, 16);
+          if (leader) {
+            if constexpr (CG == 2) clc_try_cancel_multicast(sClc + 16u * req.slot, clcf0 + 8u * req.slot);
+            else clc_try_cancel(sClc + 16u * req.slot, clcf0 + 8u * req.slot);
+          }
+          req.advance(C_::CLC_SLOTS);
+        }
         int tm, tn;
         tile_coords(t, p, tm, tn);
         const int a_row = tm * C_::TILE_M + (int)rank * 128;
@@ -230,8 +298,11 @@ __global__ void __launch_bounds__(kThreads, 1)
             phase ^= 1;
           }
         }
+        if (!ok) break;
+        t = next_tile<kCluster, CG, C_::CLC_SLOTS, false>(t, num_clusters, p, rd, clcf0, clce_leader, sClc, true, ab);
+        if (t < 0) ok = false;
       }
-      if (!ok) settle(2000000);  // copies already issued land before teardown
+      if (!ok) settle(2000000);  // copies (and a CLC answer) already issued land before teardown
     }
   } else if (warp == 1) {
     // ------------------------------------------------------------ MMA issuer
@@ -244,7 +315,10 @@ __global__ void __launch_bounds__(kThreads, 1)
       uint32_t phase = 0;
       int acc = 0;
       uint32_t acc_phase = 0;
-      for (int t = cluster_id; t < p.num_tiles && ok; t += num_clusters) {
+      ClcCursor rd;
+      const uint32_t clce_leader = kCluster ? mapa_shared(clce0, 0) : clce0;
+      int t = cluster_id;
+      while (t < p.num_tiles && ok) {
         if (!wait_bar<kCluster>(acce_bar(acc), acc_phase ^ 1, ab)) break;
         tc_fence_after();
         const uint32_t d_tmem = tmem_base + (uint32_t)(acc * C_::BN);
@@ -273,6 +347,8 @@ __global__ void __launch_bounds__(kThreads, 1)
         else mma_commit_pair(accf_bar(acc), 0x3);
         acc ^= 1;
         if (acc == 0) acc_phase ^= 1;
+        t = next_tile<kCluster, CG, C_::CLC_SLOTS, false>(t, num_clusters, p, rd, clcf0, clce_leader, sClc, true, ab);
+        if (t < 0) break;
       }
       // All MMAs issued by this thread complete before TMEM is released.
       if constexpr (CG == 1) mma_commit(drain_bar);
@@ -290,7 +366,10 @@ __global__ void __launch_bounds__(kThreads, 1)
     uint32_t cphase0 = 0, cphase1 = 0;
     int buf = 0;
     const uint32_t acce_target = kCluster ? mapa_shared(acce_bar(0), 0) : acce_bar(0);
-    for (int t = cluster_id; t < p.num_tiles; t += num_clusters) {
+    ClcCursor rd;
+    const uint32_t clce_leader = kCluster ? mapa_shared(clce0, 0) : clce0;
+    int t = cluster_id;
+    while (t < p.num_tiles) {
       int tm, tn;
       tile_coords(t, p, tm, tn);
       const int row0 = tm * C_::TILE_M + (int)rank * 128 + q * 32;
@@ -393,6 +472,9 @@ __global__ void __launch_bounds__(kThreads, 1)
       if (*abort_flag) break;
       acc ^= 1;
       if (acc == 0) acc_phase ^= 1;
+      t = next_tile<kCluster, CG, C_::CLC_SLOTS, true>(t, num_clusters, p, rd, clcf0, clce_leader, sClc, lane == 0,
+                                                       ab);
+      if (t < 0) break;
     }
     if (lane == 0) bulk_wait<0>();
   }
@@ -466,10 +548,14 @@ cudaError_t launch_impl(const CUtensorMap& tmA, const CUtensorMap& tmB, const CU
   if (max_units < 1) return cudaErrorInvalidConfiguration;
   int units = p.num_tiles < max_units ? p.num_tiles : max_units;
   if (grid_override > 0) units = grid_override / CG;
+  // cluster launch control: one cluster per tile; the ones that find their
+  // tile already taken over are cancelled before they start
+  if (p.clc) units = p.num_tiles;
   if (units < 1) units = 1;
   cfg.gridDim = dim3(units * CG, 1, 1);
   if (info) {
     info->path = CG;
+    info->scheduler = p.clc ? 2 : 1;
     info->grid = units * CG;
     info->cluster = CG;
     info->block = kThreads;

@@ -39,6 +39,7 @@ struct TileParams {
   float alpha, beta;
   int has_c;           // beta != 0
   int a_fmt, b_fmt;    // fp8 inputs: kind::f8f6f4 format codes (0 = e4m3, 1 = e5m2)
+  int clc;             // 1 = one CTA (pair) launched per tile, work taken over by cluster launch control
   Epilogue epi;
   int fault;           // kFault* bits (tests only)
   uint64_t timeout_ns;
@@ -77,6 +78,7 @@ struct LaunchInfo {
   int tile_m, tile_n, stages;
   int smem_bytes;
   const char* kernel;
+  int scheduler;       // 1 = static persistent, 2 = cluster launch control (tiled paths)
 };
 
 // Tiled persistent kernels (1-SM or 2-SM).  Returns a cudaError_t.  `pdl`

@@ -61,6 +61,17 @@ __device__ __forceinline__ void mbar_arrive_cluster(uint32_t cluster_bar) {
                : "memory");
 }
 
+// Arrive with relaxed ordering, on a barrier of this CTA or (shared::cluster
+// address) of another CTA of the cluster.  For hand-backs that only follow
+// reads whose values the thread has already used: no release fence, which at
+// cluster scope would first wait for the thread's earlier memory operations.
+__device__ __forceinline__ void mbar_arrive_relaxed_cluster(uint32_t cluster_bar) {
+  asm volatile("mbarrier.arrive.relaxed.cluster.shared::cluster.b64 _, [%0];" :: "r"(cluster_bar) : "memory");
+}
+__device__ __forceinline__ void mbar_arrive_relaxed(uint32_t bar) {
+  asm volatile("mbarrier.arrive.relaxed.cta.shared::cta.b64 _, [%0];" :: "r"(bar) : "memory");
+}
+
 __device__ __forceinline__ void mbar_arrive_expect_tx(uint32_t bar, uint32_t bytes) {
   asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;" ::"r"(bar), "r"(bytes)
                : "memory");
@@ -134,6 +145,39 @@ __device__ __forceinline__ int atom_add_acq_rel_gpu(int* p, int v) {
 }
 
 // ---------------------------------------------------------------- TMA
+// ---------------------------------------------------------------- cluster launch control
+// A running CTA asks the hardware to cancel the launch of a cluster that has
+// not started yet and takes over its work.  The 16-byte response lands in
+// shared memory and completes 16 transaction bytes on `bar`.
+__device__ __forceinline__ void clc_try_cancel(uint32_t resp, uint32_t bar) {
+  asm volatile("clusterlaunchcontrol.try_cancel.async.shared::cta.mbarrier::complete_tx::bytes.b128 [%0], [%1];"
+               :: "r"(resp), "r"(bar) : "memory");
+}
+
+// The same, with the response (and the transaction bytes) delivered to the
+// same shared-memory offsets in every CTA of the cluster.
+__device__ __forceinline__ void clc_try_cancel_multicast(uint32_t resp, uint32_t bar) {
+  asm volatile(
+      "clusterlaunchcontrol.try_cancel.async.shared::cta.mbarrier::complete_tx::bytes.multicast::cluster::all.b128 "
+      "[%0], [%1];" :: "r"(resp), "r"(bar) : "memory");
+}
+
+// Decodes a response: true if a cluster was cancelled, with the x index of
+// its first CTA in `first_x`.
+__device__ __forceinline__ bool clc_query(uint32_t resp, uint32_t& first_x) {
+  uint32_t ok, x;
+  asm volatile(
+      "{\n\t.reg .b128 r;\n\t.reg .pred p;\n\t"
+      "ld.shared.b128 r, [%2];\n\t"
+      "clusterlaunchcontrol.query_cancel.is_canceled.pred.b128 p, r;\n\t"
+      "selp.u32 %0, 1, 0, p;\n\t"
+      "mov.u32 %1, 0;\n\t"
+      "@p clusterlaunchcontrol.query_cancel.get_first_ctaid::x.b32.b128 %1, r;\n\t}"
+      : "=r"(ok), "=r"(x) : "r"(resp) : "memory");
+  first_x = x;
+  return ok != 0;
+}
+
 __device__ __forceinline__ void tma_prefetch_desc(const CUtensorMap* m) {
   asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(m)) : "memory");
 }

@@ -18,8 +18,8 @@ g = pytest.importorskip("tensor_core_dense_tn_gb300")
 from gpu_util import call, empty_out, from_dev, to_dev_bf16  # noqa: E402
 
 
-@pytest.mark.parametrize("path", [1, 2, 3])
-def test_dropped_load_times_out_then_recovers(path):
+@pytest.mark.parametrize("path,scheduler", [(1, 0), (2, 0), (3, 0), (1, 2), (2, 2)])
+def test_dropped_load_times_out_then_recovers(path, scheduler):
     import torch
     M = 32 if path == 3 else 512
     N, K = 768, 512
@@ -28,7 +28,7 @@ def test_dropped_load_times_out_then_recovers(path):
     dA, dB = to_dev_bf16(A), to_dev_bf16(B)
     dD, ldd = empty_out(M, N, gi.OUT_F32)
     rc, st = call(M, N, K, dA, K, dB, K, None, 0, dD, ldd, 1.0, 0.0, gi.OUT_F32, path=path,
-                  timeout_ns=20_000_000, fault=1)
+                  timeout_ns=20_000_000, fault=1, scheduler=scheduler)
     assert rc == 0
     assert st == g.GEMM_ERR_TIMEOUT, (st, g.last_error())
     assert (g.gemm_get_status_detail() >> 24) in (1, 2, 3, 4)
@@ -37,6 +37,7 @@ def test_dropped_load_times_out_then_recovers(path):
     assert g.gemm_get_status(s) == 0
     ref, _ = oracle.gemm_ref(A, B)
     dD2, _ = empty_out(M, N, gi.OUT_F32)
-    rc, st = call(M, N, K, dA, K, dB, K, None, 0, dD2, ldd, 1.0, 0.0, gi.OUT_F32, path=path)
+    rc, st = call(M, N, K, dA, K, dB, K, None, 0, dD2, ldd, 1.0, 0.0, gi.OUT_F32, path=path,
+                  scheduler=scheduler)
     assert rc == 0 and st == 0
     assert np.array_equal(from_dev(dD2, gi.OUT_F32), oracle.exact_f32(ref))

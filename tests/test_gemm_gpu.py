@@ -36,7 +36,7 @@ def up8(x):
 
 
 def run_int(M, N, K, path, out_dtype, seed, lda=None, ldb=None, grid=0, skinny_grid=0, alpha=1.0,
-            disable_pdl=0):
+            disable_pdl=0, scheduler=0):
     lda = up8(K) if lda is None else lda
     ldb = up8(K) if ldb is None else ldb
     A = gi.draw_bf16(M, K, gi.Dist("int", -4, 4), seed, ld=lda)
@@ -45,7 +45,7 @@ def run_int(M, N, K, path, out_dtype, seed, lda=None, ldb=None, grid=0, skinny_g
     dA, dB = to_dev_bf16(A), to_dev_bf16(B)
     dD, ldd = empty_out(M, N, out_dtype, ld=up8(N))
     rc, st = call(M, N, K, dA, lda, dB, ldb, None, 0, dD, ldd, alpha, 0.0, out_dtype, path=path,
-                  grid=grid, skinny_grid=skinny_grid, disable_pdl=disable_pdl)
+                  grid=grid, skinny_grid=skinny_grid, disable_pdl=disable_pdl, scheduler=scheduler)
     assert rc == 0, g.last_error()
     assert st == 0, g.last_error()
     return from_dev(dD, out_dtype)[:, :N], expect_exact(ref, out_dtype)

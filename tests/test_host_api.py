@@ -82,3 +82,20 @@ def test_gemm_wrapper_checks_types():
     A = torch.zeros((4, 8), dtype=torch.float32)
     with pytest.raises(ValueError):
         g.gemm(A, A)
+
+
+def test_unknown_scheduler_rejected(lib):
+    a = (64, 64, 64, 0x1000, 64, 0x2000, 64, 0, 0, 0x3000, 64, 1.0, 0.0, 0, 0)
+    assert g.gemm_bf16_tn_ex(*a, config=g.GemmConfig(scheduler=3)) == g.GEMM_ERR_INVALID_VALUE
+    assert "scheduler" in g.last_error()
+
+
+def _struct_fields(name):
+    text = re.sub(r"/\*.*?\*/", "", open(HEADER).read(), flags=re.S)
+    body = re.search(r"typedef struct " + name + r" \{(.*?)\}", text, flags=re.S).group(1)
+    return [re.findall(r"(\w+)\s*;", line)[0] for line in body.split("\n") if ";" in line]
+
+
+@pytest.mark.parametrize("name,cls", [("gemm_tn_config", g.GemmConfig), ("gemm_launch_info", g.LaunchInfo)])
+def test_ctypes_structs_follow_the_header(name, cls):
+    assert _struct_fields(name) == [f for f, _ in cls._fields_]
