@@ -9,6 +9,9 @@ no flush is needed between steps.  Alongside it, in the same run:
 * ``secondary``: the 16 x 8192 x 8192 decode GEMM in GB/s (B rotated over
   four copies, 512 MiB, so it never sits in L2);
 * ``fused_bias_gelu``: the same GEMM with bias + tanh-GELU in its epilogue;
+* ``scheduler_clc`` / ``grouped``: the cluster-launch-control scheduler
+  against the static one, and 64 small GEMMs as separate, batched and
+  grouped calls;
 * ``fp8``: the e4m3 variant on both shapes (per-tensor scales folded into
   alpha), against twice the measured bf16 peak and the copy bandwidth;
 * ``e2e``: the same metric with host buffers — pinned host->device copies
@@ -348,6 +351,7 @@ def run_ours(args, dist):
         result["secondary"] = run_decode(args, g, torch, device, peaks, dist)
         result["fp8"] = run_fp8(args, g, torch, device, peaks, dist)
         result["scheduler_clc"] = run_scheduler_study(args, g, torch, device, w, dA, dB, dD, flops, peaks, dist)
+        result["grouped"] = run_grouped_leg(args, g, torch, device, dist)
 
     # ---------------------------------------------------------------- CPU oracle baseline
     if not args.no_cpu_baseline and dist.rank == 0:
@@ -636,6 +640,63 @@ def run_scheduler_study(args, g, torch, device, w, dA, dB, dD, flops, peaks, dis
                          "static_us": round(med["static"], 1), "clc_us": round(med["clc"], 1),
                          "clc_speedup": round(med["static"] / med["clc"], 3), "repeats": len(times["clc"])}
     del bgA, bgB, bgD, dDs
+    return out
+
+
+def run_grouped_leg(args, g, torch, device, dist):
+    """Many small GEMMs: 64 problems of the 256 x 256 x 256 shape as 64
+    separate launches, as one strided batched call and as one grouped call.
+    Each form is captured in a CUDA graph (10 calls) and replayed, so the
+    numbers are GPU time, not host launch cost; the host time per call is
+    given beside them."""
+    P, M, N, K = 64, 256, 256, 256
+    w0 = gi.WORKLOADS[0]
+    A = dev_bf16(gi.draw_bf16(P * M, K, w0.dist_a, w0.seed(gi.TENSOR_A)), torch, device)
+    B = dev_bf16(gi.draw_bf16(P * N, K, w0.dist_b, w0.seed(gi.TENSOR_B)), torch, device)
+    D = torch.empty((P * M, N), dtype=torch.bfloat16, device=device)
+    stream = torch.cuda.Stream(device)
+    sh = stream.cuda_stream
+    probs = [g.GemmProblem(M=M, N=N, K=K, A=A.data_ptr() + 2 * p * M * K, lda=K, B=B.data_ptr() + 2 * p * N * K,
+                           ldb=K, C=0, ldc=0, D=D.data_ptr() + 2 * p * M * N, ldd=N) for p in range(P)]
+
+    def separate(_i):
+        for q in probs:
+            if g.gemm_bf16_tn(M, N, K, q.A, K, q.B, K, 0, 0, q.D, N, 1.0, 0.0, gi.OUT_BF16, sh) != 0:
+                raise RuntimeError(g.last_error())
+
+    def batched(_i):
+        if g.gemm_bf16_tn_batched(P, M, N, K, A.data_ptr(), K, M * K, B.data_ptr(), K, N * K, 0, 0, 0,
+                                  D.data_ptr(), N, M * N, 1.0, 0.0, gi.OUT_BF16, sh) != 0:
+            raise RuntimeError(g.last_error())
+
+    def grouped(_i):
+        if g.gemm_bf16_tn_grouped(probs, 1.0, 0.0, gi.OUT_BF16, sh) != 0:
+            raise RuntimeError(g.last_error())
+
+    flops = 2.0 * P * M * N * K
+    out = {"problems": f"{P} x {M}x{N}x{K} bf16 (int[-4,4] inputs)", "unit": "TFLOP/s"}
+    calls = 10
+    for name, fn, launches in (("separate", separate, P), ("batched", batched, 1), ("grouped", grouped, 2)):
+        with torch.cuda.stream(stream):
+            fn(0)
+            torch.cuda.synchronize()
+            t0 = time.perf_counter()
+            for i in range(calls):
+                fn(i)
+            torch.cuda.synchronize()
+            host_us = (time.perf_counter() - t0) / calls * 1e6
+            graph = torch.cuda.CUDAGraph()
+            with torch.cuda.graph(graph, stream=stream):
+                for i in range(calls):
+                    fn(i)
+            graph.replay()
+            ms = dist.max(time_steps(torch, stream, lambda _i: graph.replay(), 5)) / 5
+        per = ms / 1e3 / calls
+        out[name] = {"value": round(dist.world * flops / per / 1e12, 2), "us_per_call": round(per * 1e6, 2),
+                     "launches_per_call": launches, "host_us_per_call_eager": round(host_us, 1)}
+    if g.gemm_get_status(sh) != 0:
+        raise RuntimeError(g.last_error())
+    del A, B, D
     return out
 
 

@@ -201,6 +201,51 @@ int gemm_fp8_tn(int64_t M, int64_t N, int64_t K,
                 void *D, int64_t ldd,
                 float alpha, float beta, int out_dtype, void *stream);
 
+/* One GEMM of a grouped call: D = alpha * A * B^T + beta * C with this
+ * problem's own sizes, pointers and leading dimensions (the rules of
+ * gemm_bf16_tn apply to each; M or N = 0 makes it a no-op). */
+typedef struct gemm_problem {
+  int64_t M, N, K;
+  const void *A; int64_t lda;
+  const void *B; int64_t ldb;
+  const void *C; int64_t ldc;
+  void *D; int64_t ldd;
+} gemm_problem;
+
+/* Grouped GEMM: num_problems independent BF16 TN GEMMs of any shapes,
+ * sharing alpha, beta and out_dtype, run by the tiled kernels over one linear
+ * order of all the problems' tiles, so that many small GEMMs fill the GPU
+ * together instead of one launch each.  Grouping, batching and persistent
+ * kernels are the remedies the Ampere-to-Hopper page lists for small GEMMs
+ * that cannot fill the GPU ("why some operators improve a lot and others
+ * hardly at all").
+ *
+ * `problems` is a host array, read during the call only.  Up to 56 non-empty
+ * problems go into one launch (their tensor maps travel in the kernel's
+ * parameters); larger groups take several launches on `stream`, which may
+ * run at the same time, so the problems must be independent: no problem's D
+ * may overlap another problem's A, B, C or D.  Pair tiles
+ * (256 x 256) are used if any problem has M > 128, else 128 x 256 tiles; M <=
+ * 64 problems run on the tiled kernels too.  Errors: the codes of
+ * gemm_bf16_tn, with the failing problem's index in gemm_last_error_string;
+ * nothing is launched if any problem is invalid. */
+int gemm_bf16_tn_grouped(int num_problems, const gemm_problem *problems,
+                         float alpha, float beta, int out_dtype, void *stream);
+
+/* Strided batched GEMM: for b in [0, batch),
+ *   D_b = alpha * A_b * B_b^T + beta * C_b,  X_b = X + b * stride_x
+ * (strides in elements), all problems M x N x K.  One launch reads every
+ * problem through 3D tensor maps whose third coordinate is b.  Each stride
+ * must be at least rows * ld of its matrix (problems do not overlap), and a
+ * multiple of 16 bytes; strides are ignored when batch == 1.  Otherwise the
+ * rules and errors of gemm_bf16_tn apply to every problem. */
+int gemm_bf16_tn_batched(int64_t batch, int64_t M, int64_t N, int64_t K,
+                         const void *A, int64_t lda, int64_t stride_a,
+                         const void *B, int64_t ldb, int64_t stride_b,
+                         const void *C, int64_t ldc, int64_t stride_c,
+                         void *D, int64_t ldd, int64_t stride_d,
+                         float alpha, float beta, int out_dtype, void *stream);
+
 /* Synchronises `stream`, then returns and clears the current device's status
  * word: GEMM_OK, or GEMM_ERR_TIMEOUT if a kernel's bounded wait gave up since
  * the last call (its output is then undefined).  A CUDA error from the

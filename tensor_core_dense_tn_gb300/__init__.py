@@ -37,7 +37,8 @@ GEMM_ERR_CUDA = -8
 
 EXPORTED = ["gemm_bf16_tn", "gemm_bf16_tn_ex", "gemm_get_status", "gemm_get_status_detail",
             "gemm_last_error_string", "gemm_last_launch_info", "gemm_shutdown", "gemm_version",
-            "gemm_bf16_tn_skinny_noalloc", "gemm_bf16_tn_bias_act", "gemm_fp8_tn"]
+            "gemm_bf16_tn_skinny_noalloc", "gemm_bf16_tn_bias_act", "gemm_fp8_tn", "gemm_bf16_tn_grouped",
+            "gemm_bf16_tn_batched"]
 
 FP8_E4M3, FP8_E5M2 = 0, 1
 SCHED_DEFAULT, SCHED_STATIC, SCHED_CLC = 0, 1, 2
@@ -56,6 +57,13 @@ class GemmConfig(ctypes.Structure):
                 ("skinny_grid", ctypes.c_int), ("wait_timeout_ns", ctypes.c_uint64),
                 ("test_fault", ctypes.c_int), ("disable_pdl", ctypes.c_int),
                 ("skinny_skew_kb", ctypes.c_int), ("scheduler", ctypes.c_int)]
+
+
+class GemmProblem(ctypes.Structure):
+    """One problem of gemm_bf16_tn_grouped (device pointers as integers)."""
+    _fields_ = [("M", ctypes.c_int64), ("N", ctypes.c_int64), ("K", ctypes.c_int64),
+                ("A", ctypes.c_void_p), ("lda", ctypes.c_int64), ("B", ctypes.c_void_p), ("ldb", ctypes.c_int64),
+                ("C", ctypes.c_void_p), ("ldc", ctypes.c_int64), ("D", ctypes.c_void_p), ("ldd", ctypes.c_int64)]
 
 
 class LaunchInfo(ctypes.Structure):
@@ -93,6 +101,11 @@ def load(path: str = LIB_PATH):
         lib.gemm_bf16_tn_bias_act.restype = i32
         lib.gemm_bf16_tn_skinny_noalloc.argtypes = args
         lib.gemm_bf16_tn_skinny_noalloc.restype = i32
+        lib.gemm_bf16_tn_grouped.argtypes = [i32, ctypes.POINTER(GemmProblem), f32, f32, i32, vp]
+        lib.gemm_bf16_tn_grouped.restype = i32
+        lib.gemm_bf16_tn_batched.argtypes = [i64, i64, i64, i64, vp, i64, i64, vp, i64, i64, vp, i64, i64,
+                                             vp, i64, i64, f32, f32, i32, vp]
+        lib.gemm_bf16_tn_batched.restype = i32
         lib.gemm_bf16_tn_ex.argtypes = args + [ctypes.POINTER(GemmConfig)]
         lib.gemm_bf16_tn_ex.restype = i32
         lib.gemm_get_status.argtypes = [vp]
@@ -136,6 +149,21 @@ def gemm_bf16_tn_skinny_noalloc(M, N, K, A, lda, B, ldb, C, ldc, D, ldd, alpha, 
     """Raw C-ABI call of the allocation-free skinny entry point (1 <= M <= 64)."""
     return load().gemm_bf16_tn_skinny_noalloc(M, N, K, A, lda, B, ldb, C or None, ldc, D, ldd, alpha,
                                               beta, out_dtype, stream or None)
+
+
+def gemm_bf16_tn_grouped(problems, alpha, beta, out_dtype, stream) -> int:
+    """Raw C-ABI call: `problems` is a sequence of GemmProblem (or of dicts with its fields)."""
+    arr = (GemmProblem * max(1, len(problems)))()
+    for i, q in enumerate(problems):
+        arr[i] = q if isinstance(q, GemmProblem) else GemmProblem(**q)
+    return load().gemm_bf16_tn_grouped(len(problems), arr, alpha, beta, out_dtype, stream or None)
+
+
+def gemm_bf16_tn_batched(batch, M, N, K, A, lda, stride_a, B, ldb, stride_b, C, ldc, stride_c, D, ldd, stride_d,
+                         alpha, beta, out_dtype, stream) -> int:
+    """Raw C-ABI call of the strided batched GEMM (strides in elements)."""
+    return load().gemm_bf16_tn_batched(batch, M, N, K, A, lda, stride_a, B, ldb, stride_b, C or None, ldc,
+                                       stride_c, D, ldd, stride_d, alpha, beta, out_dtype, stream or None)
 
 
 def gemm_bf16_tn_bias_act(M, N, K, A, lda, B, ldb, C, ldc, D, ldd, alpha, beta, out_dtype, bias,

@@ -167,6 +167,58 @@ int get_workspace(int dev, cudaStream_t stream, size_t partial_floats, size_t co
   return GEMM_OK;
 }
 
+// Argument rules shared by every entry point for one problem's operands (the
+// header states them): sizes below 2^31, D present with ldd >= N, C present
+// when beta != 0, A and B present with ld >= K when K > 0, and the 16-byte
+// alignment TMA needs for every base address and row pitch.
+int check_operands(int64_t M, int64_t N, int64_t K, const void* A, int64_t lda, const void* B, int64_t ldb,
+                   const void* C, int64_t ldc, const void* D, int64_t ldd, bool has_c, int esize, int in_bytes) {
+  const int64_t kMaxDim = (int64_t)1 << 31;
+  if (M >= kMaxDim || N >= kMaxDim || K >= kMaxDim) return fail(GEMM_ERR_INVALID_VALUE, "sizes must be below 2^31");
+  if (!D) return fail(GEMM_ERR_INVALID_VALUE, "D is NULL");
+  if (ldd < N) return fail(GEMM_ERR_INVALID_VALUE, "ldd (%lld) < N (%lld)", (long long)ldd, (long long)N);
+  if (has_c) {
+    if (!C) return fail(GEMM_ERR_INVALID_VALUE, "beta != 0 but C is NULL");
+    if (ldc < N) return fail(GEMM_ERR_INVALID_VALUE, "ldc (%lld) < N (%lld)", (long long)ldc, (long long)N);
+  }
+  if (K > 0) {
+    if (!A || !B) return fail(GEMM_ERR_INVALID_VALUE, "A or B is NULL");
+    if (lda < K || ldb < K)
+      return fail(GEMM_ERR_INVALID_VALUE, "lda (%lld) and ldb (%lld) must be >= K (%lld)", (long long)lda,
+                  (long long)ldb, (long long)K);
+    if (!aligned16(A) || !aligned16(B)) return fail(GEMM_ERR_MISALIGNED, "A and B must be 16-byte aligned");
+    if ((lda * in_bytes) % 16 || (ldb * in_bytes) % 16)
+      return fail(GEMM_ERR_MISALIGNED, "lda and ldb must be multiples of %d elements", 16 / in_bytes);
+  }
+  if (!aligned16(D) || (ldd * esize) % 16)
+    return fail(GEMM_ERR_MISALIGNED, "D must be 16-byte aligned with ldd*%d a multiple of 16", esize);
+  if (has_c && (!aligned16(C) || (ldc * esize) % 16))
+    return fail(GEMM_ERR_MISALIGNED, "C must be 16-byte aligned with ldc*%d a multiple of 16", esize);
+  return GEMM_OK;
+}
+
+// Tiles along M per raster strip: keep the strip's A rows within ~32 MiB of
+// L2, so that the strip is re-read from L2 for every tile column it meets.
+int raster_group_for(int tile_m, int64_t K, int in_bytes, int tiles_m) {
+  const long long strip_bytes = (long long)tile_m * (K > 0 ? K : 1) * in_bytes;
+  const long long g = (32ll << 20) / strip_bytes;
+  const int group = (int)(g < 1 ? 1 : g);
+  return group > tiles_m ? tiles_m : group;
+}
+
+void record_launch(const LaunchInfo& li) {
+  t_info.path = li.path == 3 ? GEMM_PATH_SKINNY : li.path;
+  t_info.grid = li.grid;
+  t_info.cluster = li.cluster;
+  t_info.block = li.block;
+  t_info.tile_m = li.tile_m;
+  t_info.tile_n = li.tile_n;
+  t_info.stages = li.stages;
+  t_info.smem_bytes = li.smem_bytes;
+  t_info.kernel = li.kernel;
+  t_info.scheduler = li.scheduler;
+}
+
 int run(int64_t M, int64_t N, int64_t K, const void* A, int64_t lda, const void* B, int64_t ldb, const void* C,
         int64_t ldc, void* D, int64_t ldd, float alpha, float beta, int out_dtype, void* stream_v,
         const gemm_tn_config* cfg, Epilogue epi = Epilogue{nullptr, 0, kActNone}, int in_kind = kInBf16,
@@ -189,34 +241,14 @@ int run(int64_t M, int64_t N, int64_t K, const void* A, int64_t lda, const void*
   if (sched != GEMM_SCHED_DEFAULT && sched != GEMM_SCHED_STATIC && sched != GEMM_SCHED_CLC)
     return fail(GEMM_ERR_INVALID_VALUE, "unknown scheduler %d", sched);
   if (M == 0 || N == 0) return GEMM_OK;
-  const int64_t kMaxDim = (int64_t)1 << 31;
-  if (M >= kMaxDim || N >= kMaxDim || K >= kMaxDim)
-    return fail(GEMM_ERR_INVALID_VALUE, "sizes must be below 2^31");
   const bool has_c = (beta != 0.0f);
   const int esize = out_dtype == GEMM_OUT_F32 ? 4 : 2;
-  if (!D) return fail(GEMM_ERR_INVALID_VALUE, "D is NULL");
-  if (ldd < N) return fail(GEMM_ERR_INVALID_VALUE, "ldd (%lld) < N (%lld)", (long long)ldd, (long long)N);
-  if (has_c) {
-    if (!C) return fail(GEMM_ERR_INVALID_VALUE, "beta != 0 but C is NULL");
-    if (ldc < N) return fail(GEMM_ERR_INVALID_VALUE, "ldc (%lld) < N (%lld)", (long long)ldc, (long long)N);
-  }
-  if (K > 0) {
-    if (!A || !B) return fail(GEMM_ERR_INVALID_VALUE, "A or B is NULL");
-    if (lda < K || ldb < K)
-      return fail(GEMM_ERR_INVALID_VALUE, "lda (%lld) and ldb (%lld) must be >= K (%lld)", (long long)lda,
-                  (long long)ldb, (long long)K);
-    if (!aligned16(A) || !aligned16(B)) return fail(GEMM_ERR_MISALIGNED, "A and B must be 16-byte aligned");
-    if ((lda * in_bytes) % 16 || (ldb * in_bytes) % 16)
-      return fail(GEMM_ERR_MISALIGNED, "lda and ldb must be multiples of %d elements", 16 / in_bytes);
-  }
-  if (!aligned16(D) || (ldd * esize) % 16)
-    return fail(GEMM_ERR_MISALIGNED, "D must be 16-byte aligned with ldd*%d a multiple of 16", esize);
-  if (has_c && (!aligned16(C) || (ldc * esize) % 16))
-    return fail(GEMM_ERR_MISALIGNED, "C must be 16-byte aligned with ldc*%d a multiple of 16", esize);
+  int rc = check_operands(M, N, K, A, lda, B, ldb, C, ldc, D, ldd, has_c, esize, in_bytes);
+  if (rc != GEMM_OK) return rc;
 
   int dev = 0;
   DeviceState* st = nullptr;
-  int rc = init_device(&dev, &st);
+  rc = init_device(&dev, &st);
   if (rc != GEMM_OK) return rc;
 
   // ---- path
@@ -276,16 +308,10 @@ int run(int64_t M, int64_t N, int64_t K, const void* A, int64_t lda, const void*
     p.tiles_m = (int)((M + tile_m - 1) / tile_m);
     p.tiles_n = (int)((N + tile_n - 1) / tile_n);
     const long long nt = (long long)p.tiles_m * p.tiles_n;
-    if (nt >= kMaxDim) return fail(GEMM_ERR_INVALID_VALUE, "too many tiles");
+    if (nt >= ((int64_t)1 << 31)) return fail(GEMM_ERR_INVALID_VALUE, "too many tiles");
     p.num_tiles = (int)nt;
     int group = cfg && cfg->raster_group > 0 ? cfg->raster_group : 0;
-    if (group == 0) {
-      // keep the A rows of one raster strip within ~32 MiB of L2 (the
-      // strip is then re-read from L2 for every tile column it meets)
-      const long long strip_bytes = (long long)tile_m * (K > 0 ? K : 1) * in_bytes;
-      long long g = (32ll << 20) / strip_bytes;
-      group = (int)(g < 1 ? 1 : g);
-    }
+    if (group == 0) group = raster_group_for(tile_m, K, in_bytes, p.tiles_m);
     if (group > p.tiles_m) group = p.tiles_m;
     p.raster_group = group;
     p.alpha = alpha; p.beta = beta; p.has_c = has_c; p.epi = epi;
@@ -311,16 +337,201 @@ int run(int64_t M, int64_t N, int64_t K, const void* A, int64_t lda, const void*
     cudaGetLastError();
     return fail(GEMM_ERR_LAUNCH, "kernel launch failed: %s", cudaGetErrorString(e));
   }
-  t_info.path = li.path == 3 ? GEMM_PATH_SKINNY : li.path;
-  t_info.grid = li.grid;
-  t_info.cluster = li.cluster;
-  t_info.block = li.block;
-  t_info.tile_m = li.tile_m;
-  t_info.tile_n = li.tile_n;
-  t_info.stages = li.stages;
-  t_info.smem_bytes = li.smem_bytes;
-  t_info.kernel = li.kernel;
-  t_info.scheduler = li.scheduler;
+  record_launch(li);
+  return GEMM_OK;
+}
+
+// 3D tensor map over a strided batch of row-major matrices.
+int encode_3d(CUtensorMap* m, CUtensorMapDataType dt, int esize, const void* base, uint64_t inner, uint64_t outer,
+              uint64_t batch, uint64_t ld_elems, uint64_t stride_elems, uint32_t box_inner, uint32_t box_outer,
+              CUtensorMapSwizzle sw, const char* what) {
+  cuuint64_t dims[3] = {inner, outer, batch};
+  cuuint64_t strides[2] = {ld_elems * (uint64_t)esize, stride_elems * (uint64_t)esize};
+  cuuint32_t box[3] = {box_inner, box_outer, 1};
+  cuuint32_t estr[3] = {1, 1, 1};
+  CUresult r = g_encode(m, dt, 3, const_cast<void*>(base), dims, strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE, sw,
+                        CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  if (r != CUDA_SUCCESS) return fail(GEMM_ERR_LAUNCH, "cuTensorMapEncodeTiled(%s, 3D) failed with %d", what, (int)r);
+  return GEMM_OK;
+}
+
+// Per-thread staging of one launch's problem list (tensor maps and sizes).
+// The launch copies it into the kernel's parameters, so it can be reused as
+// soon as the launch call returns.
+thread_local GroupList t_list;
+
+int run_grouped(int count, const gemm_problem* probs, float alpha, float beta, int out_dtype, void* stream_v) {
+  t_error.clear();
+  if (out_dtype != GEMM_OUT_BF16 && out_dtype != GEMM_OUT_F32)
+    return fail(GEMM_ERR_INVALID_VALUE, "out_dtype must be 0 (bf16) or 1 (fp32), got %d", out_dtype);
+  if (count < 0) return fail(GEMM_ERR_INVALID_VALUE, "negative problem count %d", count);
+  if (count == 0) return GEMM_OK;
+  if (!probs) return fail(GEMM_ERR_INVALID_VALUE, "problems is NULL");
+  const bool has_c = (beta != 0.0f);
+  const int esize = out_dtype == GEMM_OUT_F32 ? 4 : 2;
+  bool any_tall = false, any_work = false;
+  for (int i = 0; i < count; ++i) {
+    const gemm_problem& q = probs[i];
+    if (q.M < 0 || q.N < 0 || q.K < 0)
+      return fail(GEMM_ERR_INVALID_VALUE, "problem %d: negative size M=%lld N=%lld K=%lld", i, (long long)q.M,
+                  (long long)q.N, (long long)q.K);
+    if (q.M == 0 || q.N == 0) continue;
+    const int rc = check_operands(q.M, q.N, q.K, q.A, q.lda, q.B, q.ldb, q.C, q.ldc, q.D, q.ldd, has_c, esize, 2);
+    if (rc != GEMM_OK) {
+      t_error = "problem " + std::to_string(i) + ": " + t_error;
+      return rc;
+    }
+    any_tall = any_tall || q.M > 128;
+    any_work = true;
+  }
+  if (!any_work) return GEMM_OK;
+  int dev = 0;
+  DeviceState* st = nullptr;
+  int rc = init_device(&dev, &st);
+  if (rc != GEMM_OK) return rc;
+
+  // One tile shape for the whole list: pair tiles if any problem is taller
+  // than 128 rows, else 1-SM tiles.
+  const int cg = any_tall ? 2 : 1;
+  int tile_m, tile_n, b_rows, epi_r, epi_c;
+  tiled_shape(cg, out_dtype == GEMM_OUT_F32, &tile_m, &tile_n, &b_rows, &epi_r, &epi_c);
+  const CUtensorMapDataType out_dt = out_dtype == GEMM_OUT_F32 ? CU_TENSOR_MAP_DATA_TYPE_FLOAT32
+                                                                : CU_TENSOR_MAP_DATA_TYPE_BFLOAT16;
+  const CUtensorMapSwizzle out_sw = out_dtype == GEMM_OUT_F32 ? CU_TENSOR_MAP_SWIZZLE_128B : CU_TENSOR_MAP_SWIZZLE_64B;
+  cudaStream_t stream = static_cast<cudaStream_t>(stream_v);
+  CUtensorMap unused;
+  memset(&unused, 0, sizeof unused);
+  LaunchInfo li = {};
+  int i = 0, launches = 0;
+  while (i < count) {
+    // the next launch: up to kMaxGroup non-empty problems, below 2^31 tiles
+    GroupList& L = t_list;
+    memset(&L, 0, sizeof L);
+    int n = 0;
+    long long tiles = 0;
+    for (; i < count && n < kMaxGroup; ++i) {
+      const gemm_problem& q = probs[i];
+      if (q.M == 0 || q.N == 0) continue;
+      GroupProblem& P = L.prob[n];
+      P.M = (int)q.M;
+      P.N = (int)q.N;
+      P.num_kb = (int)((q.K + 63) / 64);
+      P.tiles_m = (int)((q.M + tile_m - 1) / tile_m);
+      P.tiles_n = (int)((q.N + tile_n - 1) / tile_n);
+      if (tiles + (long long)P.tiles_m * P.tiles_n >= (1ll << 31)) {
+        if (n == 0) return fail(GEMM_ERR_INVALID_VALUE, "problem %d: too many tiles", i);
+        break;
+      }
+      P.raster_group = raster_group_for(tile_m, q.K, 2, P.tiles_m);
+      P.tile_begin = (int)tiles;
+      if (q.K > 0) {
+        if ((rc = encode_2d(&L.a[n], CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, q.A, q.K, q.M, q.lda, 64, 128,
+                            CU_TENSOR_MAP_SWIZZLE_128B, "A")))
+          return rc;
+        if ((rc = encode_2d(&L.b[n], CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, q.B, q.K, q.N, q.ldb, 64, b_rows,
+                            CU_TENSOR_MAP_SWIZZLE_128B, "B")))
+          return rc;
+      }
+      if (has_c && (rc = encode_2d(&L.c[n], out_dt, esize, q.C, q.N, q.M, q.ldc, epi_c, epi_r, out_sw, "C")))
+        return rc;
+      if ((rc = encode_2d(&L.d[n], out_dt, esize, q.D, q.N, q.M, q.ldd, epi_c, epi_r, out_sw, "D"))) return rc;
+      tiles += (long long)P.tiles_m * P.tiles_n;
+      ++n;
+    }
+    if (n == 0) break;
+    L.count = n;
+    TileParams p = {};
+    p.M = 1; p.N = 1; p.K = 1; p.num_kb = 1;
+    p.tiles_m = 1; p.tiles_n = 1; p.raster_group = 1;
+    p.num_tiles = (int)tiles;
+    p.alpha = alpha; p.beta = beta; p.has_c = has_c;
+    p.timeout_ns = timeout_ns(nullptr); p.status = st->status;
+    p.defer_wait = launches > 0 ? 1 : 0;
+    const cudaError_t e = launch_tiled_group(cg, out_dtype == GEMM_OUT_F32, kModeList, unused, unused, unused, unused,
+                                             &L, p, true, stream, &li);
+    ++launches;
+    if (e != cudaSuccess) {
+      cudaGetLastError();
+      return fail(GEMM_ERR_LAUNCH, "kernel launch failed: %s", cudaGetErrorString(e));
+    }
+  }
+  record_launch(li);
+  return GEMM_OK;
+}
+
+int run_batched(int64_t batch, int64_t M, int64_t N, int64_t K, const void* A, int64_t lda, int64_t sa,
+                const void* B, int64_t ldb, int64_t sb, const void* C, int64_t ldc, int64_t sc, void* D, int64_t ldd,
+                int64_t sd, float alpha, float beta, int out_dtype, void* stream_v) {
+  t_error.clear();
+  if (out_dtype != GEMM_OUT_BF16 && out_dtype != GEMM_OUT_F32)
+    return fail(GEMM_ERR_INVALID_VALUE, "out_dtype must be 0 (bf16) or 1 (fp32), got %d", out_dtype);
+  if (batch < 0 || M < 0 || N < 0 || K < 0)
+    return fail(GEMM_ERR_INVALID_VALUE, "negative size batch=%lld M=%lld N=%lld K=%lld", (long long)batch,
+                (long long)M, (long long)N, (long long)K);
+  if (batch == 0 || M == 0 || N == 0) return GEMM_OK;
+  const bool has_c = (beta != 0.0f);
+  const int esize = out_dtype == GEMM_OUT_F32 ? 4 : 2;
+  int rc = check_operands(M, N, K, A, lda, B, ldb, C, ldc, D, ldd, has_c, esize, 2);
+  if (rc != GEMM_OK) return rc;
+  if (batch >= ((int64_t)1 << 31)) return fail(GEMM_ERR_INVALID_VALUE, "batch must be below 2^31");
+  if (batch == 1) {  // the strides are not used; give the maps valid ones
+    sa = M * lda;
+    sb = N * ldb;
+    sc = M * ldc;
+    sd = M * ldd;
+  }
+  if (K > 0 && (sa < M * lda || sb < N * ldb))
+    return fail(GEMM_ERR_INVALID_VALUE, "stride_a (%lld) must be >= M*lda and stride_b (%lld) >= N*ldb",
+                (long long)sa, (long long)sb);
+  if (sd < M * ldd || (has_c && sc < M * ldc))
+    return fail(GEMM_ERR_INVALID_VALUE, "stride_d (%lld) must be >= M*ldd and stride_c (%lld) >= M*ldc",
+                (long long)sd, (long long)sc);
+  if ((K > 0 && ((sa * 2) % 16 || (sb * 2) % 16)) || (sd * esize) % 16 || (has_c && (sc * esize) % 16))
+    return fail(GEMM_ERR_MISALIGNED, "batch strides must be multiples of 16 bytes");
+  int dev = 0;
+  DeviceState* st = nullptr;
+  if ((rc = init_device(&dev, &st)) != GEMM_OK) return rc;
+
+  const int cg = M > 128 ? 2 : 1;
+  int tile_m, tile_n, b_rows, epi_r, epi_c;
+  tiled_shape(cg, out_dtype == GEMM_OUT_F32, &tile_m, &tile_n, &b_rows, &epi_r, &epi_c);
+  TileParams p = {};
+  p.M = (int)M; p.N = (int)N; p.K = (int)K;
+  p.num_kb = (int)((K + 63) / 64);
+  p.tiles_m = (int)((M + tile_m - 1) / tile_m);
+  p.tiles_n = (int)((N + tile_n - 1) / tile_n);
+  const long long nt = (long long)p.tiles_m * p.tiles_n * batch;
+  if (nt >= ((int64_t)1 << 31)) return fail(GEMM_ERR_INVALID_VALUE, "too many tiles");
+  p.num_tiles = (int)nt;
+  p.batch = (int)batch;
+  p.raster_group = raster_group_for(tile_m, K, 2, p.tiles_m);
+  p.alpha = alpha; p.beta = beta; p.has_c = has_c;
+  p.timeout_ns = timeout_ns(nullptr); p.status = st->status;
+  const CUtensorMapDataType out_dt = out_dtype == GEMM_OUT_F32 ? CU_TENSOR_MAP_DATA_TYPE_FLOAT32
+                                                                : CU_TENSOR_MAP_DATA_TYPE_BFLOAT16;
+  const CUtensorMapSwizzle out_sw = out_dtype == GEMM_OUT_F32 ? CU_TENSOR_MAP_SWIZZLE_128B : CU_TENSOR_MAP_SWIZZLE_64B;
+  CUtensorMap tA, tB, tC, tD;
+  memset(&tA, 0, sizeof tA);
+  memset(&tB, 0, sizeof tB);
+  memset(&tC, 0, sizeof tC);
+  if (K > 0) {
+    if ((rc = encode_3d(&tA, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, A, K, M, batch, lda, sa, 64, 128,
+                        CU_TENSOR_MAP_SWIZZLE_128B, "A")))
+      return rc;
+    if ((rc = encode_3d(&tB, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, B, K, N, batch, ldb, sb, 64, b_rows,
+                        CU_TENSOR_MAP_SWIZZLE_128B, "B")))
+      return rc;
+  }
+  if (has_c && (rc = encode_3d(&tC, out_dt, esize, C, N, M, batch, ldc, sc, epi_c, epi_r, out_sw, "C"))) return rc;
+  if ((rc = encode_3d(&tD, out_dt, esize, D, N, M, batch, ldd, sd, epi_c, epi_r, out_sw, "D"))) return rc;
+  LaunchInfo li = {};
+  const cudaError_t e = launch_tiled_group(cg, out_dtype == GEMM_OUT_F32, kModeStrided, tA, tB, tC, tD, nullptr, p,
+                                           true, static_cast<cudaStream_t>(stream_v), &li);
+  if (e != cudaSuccess) {
+    cudaGetLastError();
+    return fail(GEMM_ERR_LAUNCH, "kernel launch failed: %s", cudaGetErrorString(e));
+  }
+  record_launch(li);
   return GEMM_OK;
 }
 
@@ -353,6 +564,19 @@ int gemm_bf16_tn_ex(int64_t M, int64_t N, int64_t K, const void* A, int64_t lda,
                     const void* C, int64_t ldc, void* D, int64_t ldd, float alpha, float beta, int out_dtype,
                     void* stream, const gemm_tn_config* cfg) {
   return gtn::run(M, N, K, A, lda, B, ldb, C, ldc, D, ldd, alpha, beta, out_dtype, stream, cfg);
+}
+
+int gemm_bf16_tn_grouped(int num_problems, const gemm_problem* problems, float alpha, float beta, int out_dtype,
+                         void* stream) {
+  return gtn::run_grouped(num_problems, problems, alpha, beta, out_dtype, stream);
+}
+
+int gemm_bf16_tn_batched(int64_t batch, int64_t M, int64_t N, int64_t K, const void* A, int64_t lda, int64_t stride_a,
+                         const void* B, int64_t ldb, int64_t stride_b, const void* C, int64_t ldc, int64_t stride_c,
+                         void* D, int64_t ldd, int64_t stride_d, float alpha, float beta, int out_dtype,
+                         void* stream) {
+  return gtn::run_batched(batch, M, N, K, A, lda, stride_a, B, ldb, stride_b, C, ldc, stride_c, D, ldd, stride_d,
+                          alpha, beta, out_dtype, stream);
 }
 
 int gemm_bf16_tn_bias_act(int64_t M, int64_t N, int64_t K, const void* A, int64_t lda, const void* B, int64_t ldb,

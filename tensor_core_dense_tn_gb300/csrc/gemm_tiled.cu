@@ -42,6 +42,7 @@
 #include <cuda_runtime.h>
 
 #include <cstdint>
+#include <type_traits>
 
 #include "epilogue.cuh"
 #include "kernels.h"
@@ -131,14 +132,85 @@ __device__ __noinline__ void settle(uint64_t ns) {
   while (globaltimer() - t0 < ns) __nanosleep(1000);
 }
 
-__device__ __forceinline__ void tile_coords(int t, const TileParams& p, int& tm, int& tn) {
-  const int per_group = p.raster_group * p.tiles_n;
+__device__ __forceinline__ void tile_coords(int t, int raster_group, int tiles_m, int tiles_n, int& tm, int& tn) {
+  const int per_group = raster_group * tiles_n;
   const int g = t / per_group;
-  const int first_m = g * p.raster_group;
-  const int gm = min(p.raster_group, p.tiles_m - first_m);
+  const int first_m = g * raster_group;
+  const int gm = min(raster_group, tiles_m - first_m);
   const int r = t - g * per_group;
   tm = first_m + r % gm;
   tn = r / gm;
+}
+
+template <int MODE>
+using GroupArg = typename std::conditional<MODE == kModeList, GroupList, NoGroup>::type;
+
+// Everything a role needs to know about tile t: its position, the sizes of
+// its problem and that problem's tensor maps (z = batch index for a strided
+// batch, else 0).
+struct TileRef {
+  int tm, tn, z;
+  int M, N, num_kb;
+  const CUtensorMap *a, *b, *c, *d;
+};
+
+template <int MODE>
+__device__ __forceinline__ TileRef resolve(int t, const TileParams& p, const GroupArg<MODE>& ga, const CUtensorMap* tA,
+                                           const CUtensorMap* tB, const CUtensorMap* tC, const CUtensorMap* tD) {
+  TileRef r;
+  if constexpr (MODE == kModeList) {
+    // last problem whose first tile is <= t (tile_begin ascends)
+    int g = 0, hi = ga.count - 1;
+    while (g < hi) {
+      const int mid = (g + hi + 1) >> 1;
+      if (ga.prob[mid].tile_begin <= t) g = mid;
+      else hi = mid - 1;
+    }
+    const GroupProblem& q = ga.prob[g];
+    tile_coords(t - q.tile_begin, q.raster_group, q.tiles_m, q.tiles_n, r.tm, r.tn);
+    r.z = 0;
+    r.M = q.M;
+    r.N = q.N;
+    r.num_kb = q.num_kb;
+    r.a = &ga.a[g];
+    r.b = &ga.b[g];
+    r.c = &ga.c[g];
+    r.d = &ga.d[g];
+  } else {
+    int local = t;
+    r.z = 0;
+    if constexpr (MODE == kModeStrided) {
+      const int per = p.tiles_m * p.tiles_n;
+      r.z = t / per;
+      local = t - r.z * per;
+    }
+    tile_coords(local, p.raster_group, p.tiles_m, p.tiles_n, r.tm, r.tn);
+    r.M = p.M;
+    r.N = p.N;
+    r.num_kb = p.num_kb;
+    r.a = tA;
+    r.b = tB;
+    r.c = tC;
+    r.d = tD;
+  }
+  return r;
+}
+
+// TMA through 2D maps, or 3D maps with the batch index for a strided batch.
+template <int MODE>
+__device__ __forceinline__ void tload(uint32_t dst, const CUtensorMap* m, int x, int y, int z, uint32_t bar) {
+  if constexpr (MODE == kModeStrided) tma_load_3d(dst, m, x, y, z, bar);
+  else tma_load_2d(dst, m, x, y, bar);
+}
+template <int MODE>
+__device__ __forceinline__ void tload_pair(uint32_t dst, const CUtensorMap* m, int x, int y, int z, uint32_t bar) {
+  if constexpr (MODE == kModeStrided) tma_load_3d_pair(dst, m, x, y, z, bar);
+  else tma_load_2d_pair(dst, m, x, y, bar);
+}
+template <int MODE>
+__device__ __forceinline__ void tstore(const CUtensorMap* m, int x, int y, int z, uint32_t src) {
+  if constexpr (MODE == kModeStrided) tma_store_3d(m, x, y, z, src);
+  else tma_store_2d(m, x, y, src);
 }
 
 // Position of one role in the cluster-launch-control answer ring.
@@ -174,11 +246,11 @@ __device__ __forceinline__ int next_tile(int t, int stride, const TileParams& p,
   return got ? (int)(first_x / CG) : p.num_tiles;
 }
 
-template <int CG, bool OUT_F32, int KIND>
+template <int CG, bool OUT_F32, int KIND, int MODE>
 __global__ void __launch_bounds__(kThreads, 1)
     gemm_tn_tiled_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
                          const __grid_constant__ CUtensorMap tmC, const __grid_constant__ CUtensorMap tmD,
-                         const TileParams p) {
+                         const TileParams p, const __grid_constant__ GroupArg<MODE> ga) {
   using C_ = Cfg<CG, OUT_F32>;
   constexpr bool kCluster = (CG == 2);
   constexpr int kBK = stage_k_elems<KIND>();
@@ -229,12 +301,15 @@ __global__ void __launch_bounds__(kThreads, 1)
     fence_proxy_async_smem();
   }
   if (warp == 0 && lane == 0) {
-    if (p.num_kb > 0) {
-      tma_prefetch_desc(&tmA);
-      tma_prefetch_desc(&tmB);
+    // the first tile's tensor maps (kernel parameters: valid before the
+    // previous kernel on the stream has finished)
+    const TileRef r0 = resolve<MODE>(cluster_id < p.num_tiles ? cluster_id : 0, p, ga, &tmA, &tmB, &tmC, &tmD);
+    if (r0.num_kb > 0) {
+      tma_prefetch_desc(r0.a);
+      tma_prefetch_desc(r0.b);
     }
-    if (p.has_c) tma_prefetch_desc(&tmC);
-    tma_prefetch_desc(&tmD);
+    if (p.has_c) tma_prefetch_desc(r0.c);
+    tma_prefetch_desc(r0.d);
   }
   if (warp == 1) tmem_alloc<CG>(smem_u32(tmem_slot), C_::TMEM_COLS);
   tc_fence_before();
@@ -244,7 +319,11 @@ __global__ void __launch_bounds__(kThreads, 1)
   const uint32_t tmem_base = *tmem_slot;
   // Inputs may come from the previous kernel on the stream: no global memory
   // access before this point (the set-up above overlaps that kernel's tail).
-  griddep_wait();
+  // Exception: a later launch of one grouped call.  It starts only after every
+  // CTA of the launch before it has passed this point, so the inputs are ready;
+  // its problems do not touch that launch's, so it runs alongside it and
+  // waits at its end instead, which keeps completion in stream order.
+  if (!p.defer_wait) griddep_wait();
   griddep_launch_dependents();
 
   if (warp == 0) {
@@ -272,11 +351,23 @@ __global__ void __launch_bounds__(kThreads, 1)
           }
           req.advance(C_::CLC_SLOTS);
         }
-        int tm, tn;
-        tile_coords(t, p, tm, tn);
-        const int a_row = tm * C_::TILE_M + (int)rank * 128;
-        const int b_row = tn * C_::BN + (int)rank * C_::B_ROWS;
-        for (int kb = 0; kb < p.num_kb; ++kb) {
+        const TileRef r = resolve<MODE>(t, p, ga, &tmA, &tmB, &tmC, &tmD);
+        if constexpr (MODE == kModeList) {
+          // a list's next tile is usually another problem: fetch its maps early
+          const int tn_next = t + num_clusters;
+          if (!p.clc && tn_next < p.num_tiles) {
+            const TileRef rn = resolve<MODE>(tn_next, p, ga, &tmA, &tmB, &tmC, &tmD);
+            if (rn.num_kb > 0) {
+              tma_prefetch_desc(rn.a);
+              tma_prefetch_desc(rn.b);
+            }
+            if (p.has_c) tma_prefetch_desc(rn.c);
+            tma_prefetch_desc(rn.d);
+          }
+        }
+        const int a_row = r.tm * C_::TILE_M + (int)rank * 128;
+        const int b_row = r.tn * C_::BN + (int)rank * C_::B_ROWS;
+        for (int kb = 0; kb < r.num_kb; ++kb) {
           if (!wait_bar<kCluster>(empty_bar(stage), phase ^ 1, ab)) {
             ok = false;
             break;
@@ -286,12 +377,12 @@ __global__ void __launch_bounds__(kThreads, 1)
           if (skip_once) {
             skip_once = false;  // test-only: leave this stage's bytes missing
           } else if constexpr (CG == 1) {
-            tma_load_2d(sA + stage * C_::A_BYTES, &tmA, kb * kBK, a_row, fb);
-            tma_load_2d(sB + stage * C_::B_BYTES, &tmB, kb * kBK, b_row, fb);
+            tload<MODE>(sA + stage * C_::A_BYTES, r.a, kb * kBK, a_row, r.z, fb);
+            tload<MODE>(sB + stage * C_::B_BYTES, r.b, kb * kBK, b_row, r.z, fb);
           } else {
             const uint32_t fb_leader = mapa_shared(fb, 0);
-            tma_load_2d_pair(sA + stage * C_::A_BYTES, &tmA, kb * kBK, a_row, fb_leader);
-            tma_load_2d_pair(sB + stage * C_::B_BYTES, &tmB, kb * kBK, b_row, fb_leader);
+            tload_pair<MODE>(sA + stage * C_::A_BYTES, r.a, kb * kBK, a_row, r.z, fb_leader);
+            tload_pair<MODE>(sB + stage * C_::B_BYTES, r.b, kb * kBK, b_row, r.z, fb_leader);
           }
           if (++stage == C_::STAGES) {
             stage = 0;
@@ -322,7 +413,8 @@ __global__ void __launch_bounds__(kThreads, 1)
         if (!wait_bar<kCluster>(acce_bar(acc), acc_phase ^ 1, ab)) break;
         tc_fence_after();
         const uint32_t d_tmem = tmem_base + (uint32_t)(acc * C_::BN);
-        for (int kb = 0; kb < p.num_kb; ++kb) {
+        const int num_kb = resolve<MODE>(t, p, ga, &tmA, &tmB, &tmC, &tmD).num_kb;
+        for (int kb = 0; kb < num_kb; ++kb) {
           if (!wait_bar<kCluster>(full_bar(stage), phase, ab)) {
             ok = false;
             break;
@@ -370,16 +462,15 @@ __global__ void __launch_bounds__(kThreads, 1)
     const uint32_t clce_leader = kCluster ? mapa_shared(clce0, 0) : clce0;
     int t = cluster_id;
     while (t < p.num_tiles) {
-      int tm, tn;
-      tile_coords(t, p, tm, tn);
-      const int row0 = tm * C_::TILE_M + (int)rank * 128 + q * 32;
+      const TileRef tr = resolve<MODE>(t, p, ga, &tmA, &tmB, &tmC, &tmD);
+      const int row0 = tr.tm * C_::TILE_M + (int)rank * 128 + q * 32;
       if (!wait_bar<kCluster>(accf_bar(acc), acc_phase, ab)) break;
       tc_fence_after();
 #pragma unroll 1
       for (int c = 0; c < C_::BN / C_::EPI_COLS; ++c) {
-        const int col0 = tn * C_::BN + c * C_::EPI_COLS;
+        const int col0 = tr.tn * C_::BN + c * C_::EPI_COLS;
         uint32_t r[32];
-        if (p.num_kb > 0) {
+        if (tr.num_kb > 0) {
           tmem_ld_32x32b_x32(tmem_base + ((uint32_t)(q * 32) << 16) + (uint32_t)(acc * C_::BN + c * 32), r);
           tmem_wait_ld();
         } else {
@@ -395,7 +486,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             else mbar_arrive(acce_bar(acc));
           }
         }
-        if (row0 >= p.M || col0 >= p.N) continue;  // box entirely outside D
+        if (row0 >= tr.M || col0 >= tr.N) continue;  // box entirely outside D
         const uint32_t sbuf = sE + (uint32_t)((ew * 2 + buf) * C_::EPI_BYTES);
         if (lane == 0) bulk_wait_read<1>();       // buffer's previous store has read it
         __syncwarp();
@@ -406,7 +497,7 @@ __global__ void __launch_bounds__(kThreads, 1)
           const uint32_t cb = c_bar(ew, buf);
           if (lane == 0) {
             mbar_arrive_expect_tx(cb, C_::EPI_BYTES);
-            tma_load_2d(sbuf, &tmC, col0, row0, cb);
+            tload<MODE>(sbuf, tr.c, col0, row0, tr.z, cb);
           }
           const uint32_t par = buf ? cphase1 : cphase0;
           if (!wait_bar<false>(cb, par, ab)) break;
@@ -464,7 +555,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         fence_proxy_async_smem();
         __syncwarp();
         if (lane == 0) {
-          tma_store_2d(&tmD, col0, row0, sbuf);
+          tstore<MODE>(tr.d, col0, row0, tr.z, sbuf);
           bulk_commit();
         }
         buf ^= 1;
@@ -485,14 +576,17 @@ __global__ void __launch_bounds__(kThreads, 1)
     tc_fence_after();
     tmem_dealloc<CG>(tmem_base, C_::TMEM_COLS);
   }
+  if (p.defer_wait) griddep_wait();
 }
 
-template <int CG, bool OUT_F32, int KIND>
+template <int CG, bool OUT_F32, int KIND, int MODE>
 cudaError_t launch_impl(const CUtensorMap& tmA, const CUtensorMap& tmB, const CUtensorMap& tmC,
-                        const CUtensorMap& tmD, const TileParams& p, int grid_override, bool pdl,
-                        cudaStream_t stream, LaunchInfo* info) {
+                        const CUtensorMap& tmD, const TileParams& p, const GroupArg<MODE>& ga, int grid_override,
+                        bool pdl, cudaStream_t stream, LaunchInfo* info) {
   using C_ = Cfg<CG, OUT_F32>;
-  auto kern = gemm_tn_tiled_kernel<CG, OUT_F32, KIND>;
+  static_assert(sizeof(GroupArg<MODE>) + 4 * sizeof(CUtensorMap) + sizeof(TileParams) < 32000,
+                "kernel parameters must stay within 32 KB");
+  auto kern = gemm_tn_tiled_kernel<CG, OUT_F32, KIND, MODE>;
   static bool configured[64] = {};
   int dev = 0;
   cudaError_t e = cudaGetDevice(&dev);
@@ -568,9 +662,15 @@ cudaError_t launch_impl(const CUtensorMap& tmA, const CUtensorMap& tmB, const CU
          {"gemm_tn_tiled_kernel<2,bf16>", "gemm_tn_tiled_kernel<2,f32>"}},
         {{"gemm_tn_tiled_kernel<1,bf16,fp8 in>", "gemm_tn_tiled_kernel<1,f32,fp8 in>"},
          {"gemm_tn_tiled_kernel<2,bf16,fp8 in>", "gemm_tn_tiled_kernel<2,f32,fp8 in>"}}};
-    info->kernel = names[KIND][CG - 1][OUT_F32 ? 1 : 0];
+    static const char* group_names[2][2][2] = {
+        {{"gemm_tn_tiled_kernel<1,bf16,list>", "gemm_tn_tiled_kernel<1,f32,list>"},
+         {"gemm_tn_tiled_kernel<2,bf16,list>", "gemm_tn_tiled_kernel<2,f32,list>"}},
+        {{"gemm_tn_tiled_kernel<1,bf16,strided>", "gemm_tn_tiled_kernel<1,f32,strided>"},
+         {"gemm_tn_tiled_kernel<2,bf16,strided>", "gemm_tn_tiled_kernel<2,f32,strided>"}}};
+    info->kernel = MODE == kModeSingle ? names[KIND][CG - 1][OUT_F32 ? 1 : 0]
+                                       : group_names[MODE == kModeStrided][CG - 1][OUT_F32 ? 1 : 0];
   }
-  return cudaLaunchKernelEx(&cfg, kern, tmA, tmB, tmC, tmD, p);
+  return cudaLaunchKernelEx(&cfg, kern, tmA, tmB, tmC, tmD, p, ga);
 }
 
 }  // namespace
@@ -588,13 +688,33 @@ void tiled_shape(int cta_group, int out_f32, int* tile_m, int* tile_n, int* b_ro
 cudaError_t launch_tiled(int cta_group, int out_f32, int kind, const CUtensorMap& tmA, const CUtensorMap& tmB,
                          const CUtensorMap& tmC, const CUtensorMap& tmD, TileParams p, int grid_override,
                          bool pdl, cudaStream_t stream, LaunchInfo* info) {
-#define GTN_LAUNCH(CGV, OF, KV) launch_impl<CGV, OF, KV>(tmA, tmB, tmC, tmD, p, grid_override, pdl, stream, info)
+  const NoGroup none{0};
+#define GTN_LAUNCH(CGV, OF, KV) \
+  launch_impl<CGV, OF, KV, kModeSingle>(tmA, tmB, tmC, tmD, p, none, grid_override, pdl, stream, info)
   if (kind == kKindF8F6F4) {
     if (cta_group == 2) return out_f32 ? GTN_LAUNCH(2, true, kKindF8F6F4) : GTN_LAUNCH(2, false, kKindF8F6F4);
     return out_f32 ? GTN_LAUNCH(1, true, kKindF8F6F4) : GTN_LAUNCH(1, false, kKindF8F6F4);
   }
   if (cta_group == 2) return out_f32 ? GTN_LAUNCH(2, true, kKindF16) : GTN_LAUNCH(2, false, kKindF16);
   return out_f32 ? GTN_LAUNCH(1, true, kKindF16) : GTN_LAUNCH(1, false, kKindF16);
+#undef GTN_LAUNCH
+}
+
+cudaError_t launch_tiled_group(int cta_group, int out_f32, int mode, const CUtensorMap& tmA, const CUtensorMap& tmB,
+                               const CUtensorMap& tmC, const CUtensorMap& tmD, const GroupList* list, TileParams p,
+                               bool pdl, cudaStream_t stream, LaunchInfo* info) {
+  if (mode == kModeList) {
+#define GTN_LAUNCH(CGV, OF) \
+  launch_impl<CGV, OF, kKindF16, kModeList>(tmA, tmB, tmC, tmD, p, *list, 0, pdl, stream, info)
+    if (cta_group == 2) return out_f32 ? GTN_LAUNCH(2, true) : GTN_LAUNCH(2, false);
+    return out_f32 ? GTN_LAUNCH(1, true) : GTN_LAUNCH(1, false);
+#undef GTN_LAUNCH
+  }
+  const NoGroup none{0};
+#define GTN_LAUNCH(CGV, OF) \
+  launch_impl<CGV, OF, kKindF16, kModeStrided>(tmA, tmB, tmC, tmD, p, none, 0, pdl, stream, info)
+  if (cta_group == 2) return out_f32 ? GTN_LAUNCH(2, true) : GTN_LAUNCH(2, false);
+  return out_f32 ? GTN_LAUNCH(1, true) : GTN_LAUNCH(1, false);
 #undef GTN_LAUNCH
 }
 

@@ -31,6 +31,30 @@ struct Epilogue {
   int act;             // kAct*
 };
 
+// Problem sources of the tiled kernel: one GEMM; a list of up to kMaxGroup
+// GEMMs of any shapes, each with its own tensor maps (kernel parameters); or
+// a strided batch of equal GEMMs read through 3D tensor maps (the third
+// coordinate is the batch index).
+constexpr int kModeSingle = 0, kModeList = 1, kModeStrided = 2;
+constexpr int kMaxGroup = 56;   // per launch: 56 x 4 tensor maps fill most of the 32 KB of kernel parameters
+
+struct GroupProblem {
+  int M, N, num_kb;
+  int tiles_m, tiles_n, raster_group;
+  int tile_begin;      // first tile of this problem in the launch's tile order
+  int pad;
+};
+
+struct GroupList {
+  CUtensorMap a[kMaxGroup], b[kMaxGroup], c[kMaxGroup], d[kMaxGroup];
+  GroupProblem prob[kMaxGroup];
+  int count;
+};
+
+struct NoGroup {
+  int unused;
+};
+
 struct TileParams {
   int M, N, K;
   int num_kb;          // ceil(K / 64)
@@ -40,6 +64,9 @@ struct TileParams {
   int has_c;           // beta != 0
   int a_fmt, b_fmt;    // fp8 inputs: kind::f8f6f4 format codes (0 = e4m3, 1 = e5m2)
   int clc;             // 1 = one CTA (pair) launched per tile, work taken over by cluster launch control
+  int batch;           // strided batch: number of problems (tiles = batch * tiles_m * tiles_n)
+  int defer_wait;      // 1 = later launch of one grouped call: wait for the previous launch at the end, not
+                       // the start (the launches' problems are independent; see the kernel)
   Epilogue epi;
   int fault;           // kFault* bits (tests only)
   uint64_t timeout_ns;
@@ -88,6 +115,13 @@ struct LaunchInfo {
 cudaError_t launch_tiled(int cta_group, int out_f32, int kind, const CUtensorMap& tmA, const CUtensorMap& tmB,
                          const CUtensorMap& tmC, const CUtensorMap& tmD, TileParams p, int grid_override,
                          bool pdl, cudaStream_t stream, LaunchInfo* info);
+
+// The same kernels over a list of problems (bf16 inputs; `list` holds the
+// per-problem tensor maps and sizes, p.num_tiles their total tile count) or
+// over a strided batch (3D tensor maps in tmA..tmD, p.batch problems).
+cudaError_t launch_tiled_group(int cta_group, int out_f32, int mode, const CUtensorMap& tmA,
+                               const CUtensorMap& tmB, const CUtensorMap& tmC, const CUtensorMap& tmD,
+                               const GroupList* list, TileParams p, bool pdl, cudaStream_t stream, LaunchInfo* info);
 
 // Tile shape of the tiled kernels for a CTA group size (for host set-up).
 void tiled_shape(int cta_group, int out_f32, int* tile_m, int* tile_n, int* b_rows_per_cta,

@@ -93,9 +93,49 @@ def test_unknown_scheduler_rejected(lib):
 def _struct_fields(name):
     text = re.sub(r"/\*.*?\*/", "", open(HEADER).read(), flags=re.S)
     body = re.search(r"typedef struct " + name + r" \{(.*?)\}", text, flags=re.S).group(1)
-    return [re.findall(r"(\w+)\s*;", line)[0] for line in body.split("\n") if ";" in line]
+    names = []
+    for decl in body.split(";"):
+        parts = [q for q in decl.split(",") if q.strip()]
+        names += [re.findall(r"\w+", q)[-1] for q in parts]
+    return names
 
 
-@pytest.mark.parametrize("name,cls", [("gemm_tn_config", g.GemmConfig), ("gemm_launch_info", g.LaunchInfo)])
+@pytest.mark.parametrize("name,cls", [("gemm_tn_config", g.GemmConfig), ("gemm_launch_info", g.LaunchInfo),
+                                      ("gemm_problem", g.GemmProblem)])
 def test_ctypes_structs_follow_the_header(name, cls):
     assert _struct_fields(name) == [f for f, _ in cls._fields_]
+
+
+def _problem(**kw):
+    q = dict(M=64, N=64, K=64, A=0x1000, lda=64, B=0x2000, ldb=64, C=0, ldc=0, D=0x3000, ldd=64)
+    q.update(kw)
+    return q
+
+
+@pytest.mark.parametrize("problems,out_dtype,code,text", [
+    ([_problem()], 2, g.GEMM_ERR_INVALID_VALUE, "out_dtype"),
+    ([_problem(), _problem(M=-1)], 0, g.GEMM_ERR_INVALID_VALUE, "problem 1"),
+    ([_problem(), _problem(), _problem(A=0x1008)], 0, g.GEMM_ERR_MISALIGNED, "problem 2"),
+    ([_problem(ldd=8)], 0, g.GEMM_ERR_INVALID_VALUE, "problem 0"),
+    ([_problem(M=0), _problem(N=0)], 0, g.GEMM_OK, ""),
+    ([], 0, g.GEMM_OK, ""),
+])
+def test_grouped_validation_before_any_device_call(lib, problems, out_dtype, code, text):
+    assert g.gemm_bf16_tn_grouped(problems, 1.0, 0.0, out_dtype, 0) == code
+    assert text in g.last_error()
+
+
+@pytest.mark.parametrize("kw,code", [
+    (dict(batch=-1), g.GEMM_ERR_INVALID_VALUE),
+    (dict(batch=0), g.GEMM_OK),
+    (dict(stride_a=64 * 64 - 8), g.GEMM_ERR_INVALID_VALUE),     # problems would overlap
+    (dict(stride_d=64 * 64 - 8), g.GEMM_ERR_INVALID_VALUE),
+    (dict(stride_b=64 * 64 + 4), g.GEMM_ERR_MISALIGNED),        # 8-byte step
+    (dict(lda=68), g.GEMM_ERR_MISALIGNED),
+    (dict(beta=1.0), g.GEMM_ERR_INVALID_VALUE),                 # C is NULL
+])
+def test_batched_validation_before_any_device_call(lib, kw, code):
+    a = dict(batch=3, M=64, N=64, K=64, A=0x1000, lda=64, stride_a=64 * 64, B=0x2000, ldb=64, stride_b=64 * 64,
+             C=0, ldc=0, stride_c=0, D=0x3000, ldd=64, stride_d=64 * 64, alpha=1.0, beta=0.0, out_dtype=0, stream=0)
+    a.update(kw)
+    assert g.gemm_bf16_tn_batched(*a.values()) == code
