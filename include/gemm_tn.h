@@ -112,6 +112,7 @@ typedef struct gemm_tn_config {
   int skinny_skew_kb;       /* skinny path, equal-split mode: k-blocks (of 64) moved to the part that
                                finishes each tile; 0 = default (K/4096), < 0 = none */
   int scheduler;            /* tiled paths: GEMM_SCHED_* (0 = the default) */
+  int skinny_bm;            /* skinny path: rows of B per tile (MMA M), 64 or 128; 0 = auto (128) */
 } gemm_tn_config;
 
 /* Tile schedulers of the tiled paths.

@@ -240,6 +240,9 @@ int run(int64_t M, int64_t N, int64_t K, const void* A, int64_t lda, const void*
   const int sched = cfg ? cfg->scheduler : GEMM_SCHED_DEFAULT;
   if (sched != GEMM_SCHED_DEFAULT && sched != GEMM_SCHED_STATIC && sched != GEMM_SCHED_CLC)
     return fail(GEMM_ERR_INVALID_VALUE, "unknown scheduler %d", sched);
+  const int bm_req = cfg ? cfg->skinny_bm : 0;
+  if (bm_req != 0 && bm_req != 64 && bm_req != 128)
+    return fail(GEMM_ERR_INVALID_VALUE, "skinny_bm must be 0, 64 or 128, got %d", bm_req);
   if (M == 0 || N == 0) return GEMM_OK;
   const bool has_c = (beta != 0.0f);
   const int esize = out_dtype == GEMM_OUT_F32 ? 4 : 2;
@@ -275,25 +278,27 @@ int run(int64_t M, int64_t N, int64_t K, const void* A, int64_t lda, const void*
     SkinnyParams p = {};
     p.M = (int)M; p.N = (int)N; p.K = (int)K; p.np = np;
     p.num_kb = (int)((K + kbe - 1) / kbe);
-    p.n_tiles = (int)((N + 127) / 128);
+    const int max_grid = skinny_max_grid(np, st->sms);
+    p.bm = bm_req ? bm_req : skinny_tile_rows(N, max_grid);
+    p.n_tiles = (int)((N + p.bm - 1) / p.bm);
     p.kind = in_kind;
     p.a_fmt = fp8_format;
     p.b_fmt = fp8_format;
     p.units = (long long)p.n_tiles * p.num_kb;
-    skinny_partition(&p, skinny_max_grid(np, st->sms), cfg ? cfg->skinny_grid : 0, cfg ? cfg->skinny_skew_kb : 0);
+    skinny_partition(&p, max_grid, cfg ? cfg->skinny_grid : 0, cfg ? cfg->skinny_skew_kb : 0);
     const int grid = p.grid;
     p.alpha = alpha; p.beta = beta; p.has_c = has_c; p.epi = epi;
     p.C = C; p.ldc = ldc; p.D = D; p.ldd = ldd; p.out_f32 = out_dtype == GEMM_OUT_F32;
     p.fault = fault; p.timeout_ns = tmo; p.status = st->status;
     Workspace* w = nullptr;
-    rc = get_workspace(dev, stream, (size_t)grid * 2 * 128 * np, (size_t)p.n_tiles * 4, &w);
+    rc = get_workspace(dev, stream, (size_t)grid * 2 * p.bm * np, (size_t)p.n_tiles * 4, &w);
     if (rc != GEMM_OK) return rc;
     p.partials = w->partials;
     p.counters = w->counters;
     CUtensorMap tA, tB;
     if ((rc = encode_2d(&tA, in_dt, in_bytes, A, K, M, lda, kbe, np, CU_TENSOR_MAP_SWIZZLE_128B, "A")))
       return rc;
-    if ((rc = encode_2d(&tB, in_dt, in_bytes, B, K, N, ldb, kbe, 128, CU_TENSOR_MAP_SWIZZLE_128B, "B")))
+    if ((rc = encode_2d(&tB, in_dt, in_bytes, B, K, N, ldb, kbe, p.bm, CU_TENSOR_MAP_SWIZZLE_128B, "B")))
       return rc;
     e = launch_skinny(tA, tB, p, pdl, stream, &li);
   } else {

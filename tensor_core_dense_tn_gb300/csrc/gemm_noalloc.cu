@@ -141,10 +141,13 @@ extern "C" int gemm_bf16_tn_skinny_noalloc(int64_t M, int64_t N, int64_t K, cons
   p.K = (int)K;
   p.np = (int)((M + 15) / 16) * 16;
   p.num_kb = (int)((K + 63) / 64);
-  p.n_tiles = (int)((N + 127) / 128);
-  p.units = (long long)p.n_tiles * p.num_kb;
   int sms = skinny_max_grid(p.np, d->sms);
   if (sms > kNaMaxGrid) sms = kNaMaxGrid;
+  // 64-row tiles only when they fit one wave (at most sms <= kNaMaxGrid tiles),
+  // so the counters never exceed the 128-row tile count the scratch is sized for
+  p.bm = skinny_tile_rows(N, sms);
+  p.n_tiles = (int)((N + p.bm - 1) / p.bm);
+  p.units = (long long)p.n_tiles * p.num_kb;
   skinny_partition(&p, sms, 0, 0);
   p.alpha = alpha;
   p.beta = beta;
@@ -165,7 +168,7 @@ extern "C" int gemm_bf16_tn_skinny_noalloc(int64_t M, int64_t N, int64_t K, cons
   if (cudaMemsetAsync(p.counters, 0, (size_t)p.n_tiles * 4 * sizeof(int), stream) != cudaSuccess)
     return na_fail(GEMM_ERR_CUDA, "clearing the counters failed");
   CUtensorMap tA, tB;
-  if (na_encode(&tA, A, K, M, lda, p.np) != GEMM_OK || na_encode(&tB, B, K, N, ldb, 128) != GEMM_OK)
+  if (na_encode(&tA, A, K, M, lda, p.np) != GEMM_OK || na_encode(&tB, B, K, N, ldb, (uint32_t)p.bm) != GEMM_OK)
     return na_fail(GEMM_ERR_LAUNCH, "tensor map encoding failed");
   LaunchInfo li = {};
   if (launch_skinny(tA, tB, p, false, stream, &li) != cudaSuccess) {

@@ -8,8 +8,12 @@
 // Blackwell, SemiAnalysis Blackwell page, section "TMA") from the first
 // cycle to the last.
 //
-// Swap-AB: the tensor core computes D^T = B * A^T, so the 128 rows of a B
-// tile fill the MMA's M = 128 and the (padded) M tokens become MMA N = np.
+// Swap-AB: the tensor core computes D^T = B * A^T, so the BM rows of a B
+// tile fill the MMA's M and the (padded) M tokens become MMA N = np.  BM is
+// 128, or 64 when 64-row tiles fill the GPU in one wave without splitting a
+// tile (16 x 8192 x 8192: 128 tiles, one per CTA, no partial sums at all).
+// With M = 64 the accumulator's row r sits in TMEM lane (r / 16) * 32 +
+// r % 16: each epilogue warp finds its 16 rows in lanes 0..15 of its quarter.
 //
 // Work is the list of (n-tile, k-block) units, split into `grid` contiguous
 // ranges, one per CTA (stream-K), so every SM streams the same number of
@@ -44,23 +48,23 @@ constexpr int kStageK = 128;      // bytes of K per operand row per stage
 constexpr int kMmaPerStage = 4;   // tcgen05.mma per stage, 32 bytes of K each
 constexpr int kEpiWarps = 4;
 constexpr int kThreads = 64 + 32 * kEpiWarps;
-constexpr int kMaxStages = 16;
+constexpr int kMaxStages = 24;
 constexpr int kNumAcc = 4;                   // TMEM accumulators (64 columns each)
-constexpr int kBTileBytes = 128 * kStageK;   // 16 KiB
 constexpr int kTmemCols = 64 * kNumAcc;
 constexpr int kErrTimeout = -5;
 constexpr int kSmemBudget = 216 * 1024;
 constexpr int kNumBars = 2 * kMaxStages + 2 * kNumAcc + 1;
 
-__host__ __device__ inline int stage_bytes(int np) { return kBTileBytes + np * kStageK; }
+// A stage: BM rows of B and np rows of A, 128 bytes of K each.
+__host__ __device__ inline int stage_bytes(int np, int bm) { return (bm + np) * kStageK; }
 
-__host__ __device__ inline int stages_for(int np) {
-  int s = kSmemBudget / stage_bytes(np);
+__host__ __device__ inline int stages_for(int np, int bm) {
+  int s = kSmemBudget / stage_bytes(np, bm);
   return s > kMaxStages ? kMaxStages : s;
 }
 
-__host__ __device__ inline int smem_for(int np) {
-  return 1024 + stages_for(np) * stage_bytes(np) + kNumBars * 8 + 16;
+__host__ __device__ inline int smem_for(int np, int bm) {
+  return 1024 + stages_for(np, bm) * stage_bytes(np, bm) + kNumBars * 8 + 16;
 }
 
 // First unit owned by CTA c when U units are split into G contiguous ranges.
@@ -147,17 +151,19 @@ __device__ __forceinline__ void store_d(const SkinnyParams& p, int m, int n, flo
 
 // Partial of CTA c's segment of a tile: slot 0 = the CTA's first tile,
 // slot 1 = its last (only the first and last segment of a range can be
-// partial).  Layout [cta][slot][row][np] so a thread's np values are
-// contiguous (16-byte vectors).
+// partial).  Layout [cta][slot][row][np] (BM rows) so a thread's np values
+// are contiguous (16-byte vectors).
+template <int BM>
 __device__ __forceinline__ float* partial_ptr(const SkinnyParams& p, long long c, int slot, int row) {
-  return p.partials + ((c * 2 + slot) * 128 + row) * (long long)p.np;
+  return p.partials + ((c * 2 + slot) * BM + row) * (long long)p.np;
 }
 
-template <int KIND>
+template <int KIND, int BM>
 __global__ void __launch_bounds__(kThreads, 1)
     gemm_tn_skinny_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
                           const SkinnyParams p) {
   constexpr int kBK = KIND == kKindF16 ? 64 : 128;  // K elements per stage
+  constexpr int kBTileBytes = BM * kStageK;          // 16 or 8 KiB of B per stage
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
   const int S = p.stages;
@@ -195,7 +201,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     if (skip_once) {
       skip_once = false;  // test-only: leave this stage's bytes missing
     } else {
-      tma_load_2d(sB + stage * kBTileBytes, &tmB, kb * kBK, n * 128, fb);
+      tma_load_2d(sB + stage * kBTileBytes, &tmB, kb * kBK, n * BM, fb);
       tma_load_2d(sA + stage * a_bytes, &tmA, kb * kBK, 0, fb);
     }
   };
@@ -253,8 +259,8 @@ __global__ void __launch_bounds__(kThreads, 1)
   } else if (warp == 1) {
     if (lane == 0) {
       // -------------------------------------------------------- MMA
-      const uint32_t idesc = KIND == kKindF16 ? instr_desc_bf16_f32(128, (uint32_t)p.np)
-                                              : instr_desc_f32acc(128, (uint32_t)p.np, p.b_fmt, p.a_fmt);
+      const uint32_t idesc = KIND == kKindF16 ? instr_desc_bf16_f32(BM, (uint32_t)p.np)
+                                              : instr_desc_f32acc(BM, (uint32_t)p.np, p.b_fmt, p.a_fmt);
       bool ok = true;
       int stage = 0, acc = 0;
       uint32_t phase = 0, acc_phase = 0;
@@ -295,12 +301,14 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
   } else {
     // ---------------------------------------------------------- epilogue
-    // Each warp owns 32 of the tile's 128 rows of D^T (TMEM lane quarter q)
-    // and finishes them on its own: split tiles keep one arrival counter per
-    // (tile, warp), so no barrier is shared between epilogue warps and no
-    // warp ever waits for another CTA.
+    // Each warp owns BM/4 of the tile's rows of D^T (TMEM lane quarter q;
+    // for BM = 64 only lanes 0..15 of the quarter hold rows) and finishes
+    // them on its own: split tiles keep one arrival counter per (tile,
+    // warp), so no barrier is shared between epilogue warps and no warp ever
+    // waits for another CTA.
     const int q = warp & 3;
-    const int n_local = q * 32 + lane;
+    const int n_local = BM == 128 ? q * 32 + lane : q * 16 + lane;
+    const bool row_lane = BM == 128 || lane < 16;  // this lane holds a row of the tile
     int acc = 0;
     uint32_t acc_phase = 0;
     long long u = u_begin;
@@ -333,7 +341,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         acc_phase ^= 1;
       }
 
-      const int ng = (int)(n * 128) + n_local;
+      const int ng = (int)(n * BM) + n_local;
       bool finish = whole;
       if (!whole) {
         // A split tile's parts.  Part 0 (the tile's first k-blocks) is
@@ -347,10 +355,10 @@ __global__ void __launch_bounds__(kThreads, 1)
           // Partial laid out so each thread writes 16-byte vectors.  The warp
           // barrier orders every lane's partial before lane 0's release.
           const int slot = (n == first_tile) ? 0 : 1;
-          float4* mine = reinterpret_cast<float4*>(partial_ptr(p, c, slot, n_local));
+          float4* mine = reinterpret_cast<float4*>(partial_ptr<BM>(p, c, slot, n_local));
 #pragma unroll
           for (int g4 = 0; g4 < 16; ++g4)
-            if (g4 * 4 < p.np)
+            if (row_lane && g4 * 4 < p.np)
               mine[g4] = make_float4(vals[4 * g4], vals[4 * g4 + 1], vals[4 * g4 + 2], vals[4 * g4 + 3]);
           __syncwarp();
           if (lane == 0) red_add_release_gpu(arrivals, 1);
@@ -398,9 +406,9 @@ __global__ void __launch_bounds__(kThreads, 1)
 #pragma unroll
               for (int b = 0; b < kBatch; ++b) {
                 const long long cc = j0 + b < nseg ? tile_part_cta(p, n, j0 + b) : -1;
-                if (cc >= 0 && cc != c) {
+                if (row_lane && cc >= 0 && cc != c) {
                   const int sl = (n == cta_begin(p, cc) / KB) ? 0 : 1;
-                  const float4* part = reinterpret_cast<const float4*>(partial_ptr(p, cc, sl, n_local) + g16 * 16);
+                  const float4* part = reinterpret_cast<const float4*>(partial_ptr<BM>(p, cc, sl, n_local) + g16 * 16);
 #pragma unroll
                   for (int v = 0; v < 4; ++v) buf[b][v] = __ldcg(part + v);
                 }
@@ -431,7 +439,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       // The fused bias/activation gets a loop of its own: with the test
       // inside the unrolled plain loop the activation code is scheduled
       // into it and the plain decode GEMM ran 1.7x slower (measured).
-      if (finish && ng < p.N && !(p.epi.bias || p.epi.act)) {
+      if (finish && row_lane && ng < p.N && !(p.epi.bias || p.epi.act)) {
 #pragma unroll
         for (int m = 0; m < 64; ++m) {
           if (m < p.M) {
@@ -440,7 +448,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             store_d(p, m, ng, v);
           }
         }
-      } else if (finish && ng < p.N) {
+      } else if (finish && row_lane && ng < p.N) {
         const float bias_n = p.epi.bias ? load_bias(p.epi, ng) : 0.0f;
 #pragma unroll
         for (int m = 0; m < 64; ++m) {
@@ -464,7 +472,16 @@ __global__ void __launch_bounds__(kThreads, 1)
 
 }  // namespace
 
-int skinny_stages(int np) { return stages_for(np); }
+int skinny_stages(int np, int bm) { return stages_for(np, bm); }
+
+int skinny_tile_rows(long long n, int max_grid) {
+  // 64-row tiles would avoid splitting a tile where they fill one wave, but
+  // measured they stream B slower (16 x 8192 x 8192: 41 us against 27 us with
+  // 128-row tiles split in two), so the automatic choice is 128 rows.
+  (void)n;
+  (void)max_grid;
+  return 128;
+}
 
 int skinny_max_grid(int np, int num_sms) {
   (void)np;
@@ -481,13 +498,14 @@ void skinny_partition(SkinnyParams* p, int num_sms, int grid_override, int skew_
   }
   // Splitting every tile into the same number s of k-ranges (one CTA each)
   // leaves every CTA with one segment; it wins over a full-GPU stream-K split
-  // as long as it keeps at least 80% of the SMs streaming.  Part j of tile n
-  // goes to CTA n + j * n_tiles, so the parts of a tile sit on SMs spread
-  // across the grid.  Part 0's CTA finishes the tile after the other parts
-  // land, so it gets a few more k-blocks.
-  if (p->n_tiles < num_sms) {
+  // as long as it keeps at least 80% of the SMs streaming.  s = 1 is a whole
+  // tile per CTA, with no partial sums.  Part j of tile n goes to CTA
+  // n + j * n_tiles, so the parts of a tile sit on SMs spread across the
+  // grid.  Part 0's CTA finishes the tile after the other parts land, so it
+  // gets a few more k-blocks.
+  if (p->n_tiles <= num_sms) {
     const int s = num_sms / p->n_tiles;
-    if (s >= 2 && s <= p->num_kb && 5 * p->n_tiles * s >= 4 * num_sms) {
+    if (s >= 1 && s <= p->num_kb && 5 * p->n_tiles * s >= 4 * num_sms) {
       p->grid = p->n_tiles * s;
       p->split = s;
       int skew = skew_kb > 0 ? skew_kb : (skew_kb < 0 ? 0 : p->num_kb / 64);
@@ -508,21 +526,27 @@ cudaError_t launch_skinny(const CUtensorMap& tmA, const CUtensorMap& tmB, Skinny
   if (e != cudaSuccess) return e;
   if (dev < 64 && !configured[dev]) {
     int worst = 0;
-    for (int np = 16; np <= 64; np += 16) worst = smem_for(np) > worst ? smem_for(np) : worst;
-    e = cudaFuncSetAttribute(gemm_tn_skinny_kernel<kKindF16>, cudaFuncAttributeMaxDynamicSharedMemorySize, worst);
-    if (e != cudaSuccess) return e;
-    e = cudaFuncSetAttribute(gemm_tn_skinny_kernel<kKindF8F6F4>, cudaFuncAttributeMaxDynamicSharedMemorySize, worst);
-    if (e != cudaSuccess) return e;
+    for (int np = 16; np <= 64; np += 16)
+      for (int bm = 64; bm <= 128; bm += 64) worst = smem_for(np, bm) > worst ? smem_for(np, bm) : worst;
+    const void* kernels[4] = {(const void*)gemm_tn_skinny_kernel<kKindF16, 128>,
+                              (const void*)gemm_tn_skinny_kernel<kKindF16, 64>,
+                              (const void*)gemm_tn_skinny_kernel<kKindF8F6F4, 128>,
+                              (const void*)gemm_tn_skinny_kernel<kKindF8F6F4, 64>};
+    for (const void* k : kernels) {
+      e = cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, worst);
+      if (e != cudaSuccess) return e;
+    }
     configured[dev] = true;
   }
-  p.stages = stages_for(p.np);
-  const int smem = smem_for(p.np);
+  if (p.bm != 64 && p.bm != 128) return cudaErrorInvalidValue;
+  p.stages = stages_for(p.np, p.bm);
+  const int smem = smem_for(p.np, p.bm);
   if (info) {
     info->path = 3;
     info->grid = p.grid;
     info->cluster = 1;
     info->block = kThreads;
-    info->tile_m = 128;
+    info->tile_m = p.bm;
     info->tile_n = p.np;
     info->stages = p.stages;
     info->smem_bytes = smem;
@@ -540,8 +564,11 @@ cudaError_t launch_skinny(const CUtensorMap& tmA, const CUtensorMap& tmB, Skinny
     cfg.attrs = attr;
     cfg.numAttrs = 1;
   }
-  return p.kind == kKindF8F6F4 ? cudaLaunchKernelEx(&cfg, gemm_tn_skinny_kernel<kKindF8F6F4>, tmA, tmB, p)
-                               : cudaLaunchKernelEx(&cfg, gemm_tn_skinny_kernel<kKindF16>, tmA, tmB, p);
+  if (p.kind == kKindF8F6F4)
+    return p.bm == 64 ? cudaLaunchKernelEx(&cfg, gemm_tn_skinny_kernel<kKindF8F6F4, 64>, tmA, tmB, p)
+                      : cudaLaunchKernelEx(&cfg, gemm_tn_skinny_kernel<kKindF8F6F4, 128>, tmA, tmB, p);
+  return p.bm == 64 ? cudaLaunchKernelEx(&cfg, gemm_tn_skinny_kernel<kKindF16, 64>, tmA, tmB, p)
+                    : cudaLaunchKernelEx(&cfg, gemm_tn_skinny_kernel<kKindF16, 128>, tmA, tmB, p);
 }
 
 }  // namespace gtn

@@ -89,6 +89,7 @@ struct SkinnyParams {
   const void* C; long long ldc;
   void* D; long long ldd;
   int out_f32;
+  int bm;              // rows of B per tile (MMA M): 128, or 64
   int kind;            // kKindF16 (bf16 inputs) or kKindF8F6F4 (fp8 inputs)
   int a_fmt, b_fmt;    // fp8 format codes
   Epilogue epi;
@@ -142,6 +143,8 @@ int skinny_max_grid(int np, int num_sms);
 // from p->n_tiles and p->num_kb.  grid_override > 0 forces a stream-K grid;
 // skew_kb: 0 = default, > 0 = that many k-blocks, < 0 = none.
 void skinny_partition(SkinnyParams* p, int num_sms, int grid_override, int skew_kb);
-int skinny_stages(int np);
+int skinny_stages(int np, int bm);
+// Rows of B per skinny tile chosen automatically for n columns of D.
+int skinny_tile_rows(long long n, int max_grid);
 
 }  // namespace gtn

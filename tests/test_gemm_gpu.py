@@ -36,7 +36,7 @@ def up8(x):
 
 
 def run_int(M, N, K, path, out_dtype, seed, lda=None, ldb=None, grid=0, skinny_grid=0, alpha=1.0,
-            disable_pdl=0, scheduler=0):
+            disable_pdl=0, scheduler=0, skinny_bm=0):
     lda = up8(K) if lda is None else lda
     ldb = up8(K) if ldb is None else ldb
     A = gi.draw_bf16(M, K, gi.Dist("int", -4, 4), seed, ld=lda)
@@ -45,7 +45,8 @@ def run_int(M, N, K, path, out_dtype, seed, lda=None, ldb=None, grid=0, skinny_g
     dA, dB = to_dev_bf16(A), to_dev_bf16(B)
     dD, ldd = empty_out(M, N, out_dtype, ld=up8(N))
     rc, st = call(M, N, K, dA, lda, dB, ldb, None, 0, dD, ldd, alpha, 0.0, out_dtype, path=path,
-                  grid=grid, skinny_grid=skinny_grid, disable_pdl=disable_pdl, scheduler=scheduler)
+                  grid=grid, skinny_grid=skinny_grid, disable_pdl=disable_pdl, scheduler=scheduler,
+                  skinny_bm=skinny_bm)
     assert rc == 0, g.last_error()
     assert st == 0, g.last_error()
     return from_dev(dD, out_dtype)[:, :N], expect_exact(ref, out_dtype)
@@ -97,6 +98,37 @@ def test_integer_ragged_skinny(shape, out_dtype):
     M, N, K = shape
     got, exp = run_int(M, N, K, PS, out_dtype, seed=200 + M + 7 * N + 13 * K)
     assert_same(got, exp)
+
+
+@pytest.mark.parametrize("shape", SKINNY_SHAPES)
+@pytest.mark.parametrize("bm", [64, 128])
+def test_integer_ragged_skinny_tile_rows(shape, bm):
+    """Both B-tile heights (MMA M = 64 or 128) on every skinny shape."""
+    M, N, K = shape
+    got, exp = run_int(M, N, K, PS, gi.OUT_F32, seed=250 + M + 7 * N + 13 * K, skinny_bm=bm)
+    assert_same(got, exp)
+
+
+@pytest.mark.parametrize("skinny_grid", [0, 1, 7, 33, 100, 151])
+@pytest.mark.parametrize("K", [64, 1344, 4160])
+def test_skinny_bm64_partitions(skinny_grid, K):
+    """64-row tiles split between CTAs (stream-K ranges): only lanes 0..15 of
+    each epilogue warp hold rows, in partials and fix-ups alike."""
+    got, exp = run_int(16, 1000, K, PS, gi.OUT_BF16, seed=700 + skinny_grid + K, skinny_grid=skinny_grid,
+                       skinny_bm=64)
+    assert_same(got, exp)
+
+
+def test_decode_shape_launch():
+    M, N, K = 16, 8192, 512
+    got, exp = run_int(M, N, K, 0, gi.OUT_BF16, seed=777)
+    assert_same(got, exp)
+    info = g.last_launch_info()
+    assert info["path"] == PS and info["tile_m"] == 128 and info["grid"] == 128
+    got, exp = run_int(M, N, K, 0, gi.OUT_BF16, seed=777, skinny_bm=64)
+    assert_same(got, exp)
+    info = g.last_launch_info()
+    assert info["tile_m"] == 64 and info["grid"] == 128      # 128 whole 64-row tiles, one per CTA
 
 
 @pytest.mark.parametrize("skinny_grid", [1, 3, 7, 64, 100, 151, 1000])

@@ -139,3 +139,10 @@ def test_batched_validation_before_any_device_call(lib, kw, code):
              C=0, ldc=0, stride_c=0, D=0x3000, ldd=64, stride_d=64 * 64, alpha=1.0, beta=0.0, out_dtype=0, stream=0)
     a.update(kw)
     assert g.gemm_bf16_tn_batched(*a.values()) == code
+
+
+@pytest.mark.parametrize("bm", [32, 96, -64, 256])
+def test_unknown_skinny_tile_rows_rejected(lib, bm):
+    a = (16, 64, 64, 0x1000, 64, 0x2000, 64, 0, 0, 0x3000, 64, 1.0, 0.0, 0, 0)
+    assert g.gemm_bf16_tn_ex(*a, config=g.GemmConfig(skinny_bm=bm)) == g.GEMM_ERR_INVALID_VALUE
+    assert "skinny_bm" in g.last_error()
