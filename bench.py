@@ -417,10 +417,38 @@ def run_e2e(args, g, torch, device, w, A, B, out_t, flops, dist):
     if st != 0:
         raise RuntimeError(f"device status {st}: {g.last_error()}")
     per = ms / 1e3 / n
+
+    # The transfer bound: the same copies per step on the same streams, with
+    # nothing computed (a reference measurement beside the e2e number).
+    def copies_only(steps):
+        for i in range(steps):
+            b = i % 2
+            with torch.cuda.stream(s_in):
+                dA[b].copy_(hA, non_blocking=True)
+                dB[b].copy_(hB, non_blocking=True)
+            with torch.cuda.stream(s_out):
+                hD.copy_(dD[b], non_blocking=True)
+
+    copies_only(2)
+    torch.cuda.synchronize()
+    c0, c1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    c0.record(s_in)
+    s_out.wait_event(c0)
+    copies_only(n)
+    done = torch.cuda.Event()
+    done.record(s_out)
+    s_in.wait_event(done)
+    c1.record(s_in)
+    torch.cuda.synchronize()
+    copy_ms = dist.max(c0.elapsed_time(c1)) / n
+    moved = hA.numel() * 2 + hB.numel() * 2 + hD.numel() * hD.element_size()
     return {"value": round(dist.world * flops / per / 1e12, 2), "unit": "TFLOP/s",
             "h2d_bytes_per_step": hA.numel() * 2 + hB.numel() * 2,
             "d2h_bytes_per_step": hD.numel() * hD.element_size(),
             "ms_per_step": round(ms / n, 3), "steps": n,
+            "copies_only_ms_per_step": round(copy_ms, 3),
+            "host_link_gbs": round(moved / (copy_ms / 1e3) / 1e9, 1),
+            "of_transfer_bound": round(copy_ms / (ms / n), 4),
             "api": "gemm_bf16_tn_ex (C ABI); pinned host A, B in and D out every step, "
                    "copies on their own streams, two device buffers"}
 
