@@ -226,7 +226,8 @@ typedef struct gemm_problem {
  * parameters); larger groups take several launches on `stream`, which may
  * run at the same time, so the problems must be independent: no problem's D
  * may overlap another problem's A, B, C or D.  Pair tiles
- * (256 x 256) are used if any problem has M > 128, else 128 x 256 tiles; M <=
+ * (256 x 256) are used if some problem has M > 128 and the problems need
+ * more 128 x 256 tiles than the GPU has SMs, else 128 x 256 tiles; M <=
  * 64 problems run on the tiled kernels too.  Errors: the codes of
  * gemm_bf16_tn, with the failing problem's index in gemm_last_error_string;
  * nothing is launched if any problem is invalid. */

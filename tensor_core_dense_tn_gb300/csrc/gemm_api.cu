@@ -197,6 +197,14 @@ int check_operands(int64_t M, int64_t N, int64_t K, const void* A, int64_t lda, 
   return GEMM_OK;
 }
 
+// A GEMM of at most this many 128 x 256 tiles runs on 1-SM tiles even when
+// M > 128: with so few tiles the pair kernel's cluster launch costs more than
+// its shared operand traffic saves (measured 0.5-0.8 us per call from 256^3
+// to 1024 x 2048 x 2048; with 120 tiles the pair kernel was faster).
+constexpr long long kSmallTileCount = 64;
+
+long long one_sm_tiles(int64_t M, int64_t N) { return ((M + 127) / 128) * ((N + 255) / 256); }
+
 // Tiles along M per raster strip: keep the strip's A rows within ~32 MiB of
 // L2, so that the strip is re-read from L2 for every tile column it meets.
 int raster_group_for(int tile_m, int64_t K, int in_bytes, int tiles_m) {
@@ -259,7 +267,7 @@ int run(int64_t M, int64_t N, int64_t K, const void* A, int64_t lda, const void*
   if (path == GEMM_PATH_AUTO) {
     if (K == 0) path = GEMM_PATH_1SM;
     else if (M <= 64) path = GEMM_PATH_SKINNY;
-    else if (M <= 128) path = GEMM_PATH_1SM;
+    else if (M <= 128 || one_sm_tiles(M, N) <= kSmallTileCount) path = GEMM_PATH_1SM;
     else path = GEMM_PATH_2SM;
   }
   if (path == GEMM_PATH_SKINNY && (M > 64 || K == 0))
@@ -395,9 +403,13 @@ int run_grouped(int count, const gemm_problem* probs, float alpha, float beta, i
   int rc = init_device(&dev, &st);
   if (rc != GEMM_OK) return rc;
 
-  // One tile shape for the whole list: pair tiles if any problem is taller
-  // than 128 rows, else 1-SM tiles.
-  const int cg = any_tall ? 2 : 1;
+  // One tile shape for the whole list: pair tiles if some problem is taller
+  // than 128 rows and the list needs more than one wave of 1-SM tiles, else
+  // 1-SM tiles.
+  long long small_tiles = 0;
+  for (int j = 0; j < count; ++j)
+    if (probs[j].M > 0 && probs[j].N > 0) small_tiles += one_sm_tiles(probs[j].M, probs[j].N);
+  const int cg = (any_tall && small_tiles > st->sms) ? 2 : 1;
   int tile_m, tile_n, b_rows, epi_r, epi_c;
   tiled_shape(cg, out_dtype == GEMM_OUT_F32, &tile_m, &tile_n, &b_rows, &epi_r, &epi_c);
   const CUtensorMapDataType out_dt = out_dtype == GEMM_OUT_F32 ? CU_TENSOR_MAP_DATA_TYPE_FLOAT32
@@ -497,7 +509,7 @@ int run_batched(int64_t batch, int64_t M, int64_t N, int64_t K, const void* A, i
   DeviceState* st = nullptr;
   if ((rc = init_device(&dev, &st)) != GEMM_OK) return rc;
 
-  const int cg = M > 128 ? 2 : 1;
+  const int cg = (M > 128 && one_sm_tiles(M, N) * batch > st->sms) ? 2 : 1;
   int tile_m, tile_n, b_rows, epi_r, epi_c;
   tiled_shape(cg, out_dtype == GEMM_OUT_F32, &tile_m, &tile_n, &b_rows, &epi_r, &epi_c);
   TileParams p = {};

@@ -17,8 +17,19 @@ pytestmark = pytest.mark.gpu
 g = pytest.importorskip("tensor_core_dense_tn_gb300")
 from gpu_util import empty_out, from_dev, to_dev_bf16, to_dev_f32  # noqa: E402
 
-# M picks the kernel path: 48 -> skinny, 100 -> 1-SM tiled, 300 -> 2-SM tiled
-PATH_M = {"skinny": 48, "1sm": 100, "2sm": 300}
+# M picks the kernel path: 48 -> skinny, 100 -> 1-SM tiled, 2200 -> 2-SM tiled
+# (with N at least 1040: more than 64 tiles of 128 x 256, so pair tiles)
+PATH_M = {"skinny": 48, "1sm": 100, "2sm": 2200}
+PATH_CODE = {"skinny": 3, "1sm": 1, "2sm": 2}
+
+
+def shape_n(path, n):
+    """N for a test on `path`: the 2-SM case needs enough tiles to use pair tiles."""
+    return max(n, 1040) if path == "2sm" else n
+
+
+def check_path(path):
+    assert g.last_launch_info()["path"] == PATH_CODE[path], g.last_launch_info()
 
 
 def _run(M, N, K, A, B, bias, bias_dtype, act, out_dtype, C=None, beta=0.0):
@@ -45,7 +56,7 @@ def _run(M, N, K, A, B, bias, bias_dtype, act, out_dtype, C=None, beta=0.0):
 @pytest.mark.parametrize("act", [0, 1])
 @pytest.mark.parametrize("bias_dtype", [0, 1])
 def test_integer_bias_exact(path, act, bias_dtype):
-    M, N, K = PATH_M[path], 520, 192
+    M, N, K = PATH_M[path], shape_n(path, 520), 192
     A = gi.draw_bf16(M, K, gi.Dist("int", -4, 4), 4000)
     B = gi.draw_bf16(N, K, gi.Dist("int", -4, 4), 4001)
     bias = gi.draw_bf16(N, 1, gi.Dist("int", -50, 50), 4002).reshape(N)
@@ -54,6 +65,7 @@ def test_integer_bias_exact(path, act, bias_dtype):
     ref, _ = oracle.gemm_ref(A, B)
     want = oracle.epilogue(ref, bias, act)
     got = _run(M, N, K, A, B, bias, bias_dtype, act, gi.OUT_F32)
+    check_path(path)
     assert np.array_equal(got, oracle.exact_f32(want))
 
 
@@ -61,7 +73,7 @@ def test_integer_bias_exact(path, act, bias_dtype):
 @pytest.mark.parametrize("act", [1, 2, 3, 4])
 @pytest.mark.parametrize("out_dtype", [gi.OUT_BF16, gi.OUT_F32])
 def test_activations_within_bound(path, act, out_dtype):
-    M, N, K = PATH_M[path], 776, 512
+    M, N, K = PATH_M[path], shape_n(path, 776), 512
     A = gi.draw_bf16(M, K, gi.Dist("normal", 1.0), 4100 + act)
     B = gi.draw_bf16(N, K, gi.Dist("normal", 4.0 / K), 4200 + act)       # z ~ N(0, 4)
     bias = gi.draw_bf16(N, 1, gi.Dist("normal", 1.0), 4300).reshape(N)
@@ -69,6 +81,7 @@ def test_activations_within_bound(path, act, out_dtype):
     z = oracle.epilogue(ref, bias, 0)
     fz = oracle.epilogue(ref, bias, act)
     got = oracle.decode_out(_run(M, N, K, A, B, bias, 0, act, out_dtype), out_dtype)
+    check_path(path)
     bnd = oracle.bound_act(z, fz, absdot, out_dtype, act)
     err = np.abs(got - fz)
     assert np.all(err <= bnd), float(np.max(err / bnd))
@@ -76,7 +89,7 @@ def test_activations_within_bound(path, act, out_dtype):
 
 @pytest.mark.parametrize("path", list(PATH_M))
 def test_gelu_with_c_and_fp32_bias(path):
-    M, N, K = PATH_M[path], 264, 320
+    M, N, K = PATH_M[path], shape_n(path, 264), 320
     A = gi.draw_bf16(M, K, gi.Dist("normal", 1.0), 4400)
     B = gi.draw_bf16(N, K, gi.Dist("normal", 1.0 / K), 4401)
     C = gi.draw_bf16(M, N, gi.Dist("normal", 1.0), 4402)
@@ -85,6 +98,7 @@ def test_gelu_with_c_and_fp32_bias(path):
     z = oracle.epilogue(ref, bias, 0)
     fz = oracle.epilogue(ref, bias, 2)
     got = oracle.decode_out(_run(M, N, K, A, B, bias, 1, 2, gi.OUT_BF16, C=C, beta=0.5), 0)
+    check_path(path)
     bnd = oracle.bound_act(z, fz, absdot, 0, 2, 0.5, gi.bf16_bits_to_f32(C))
     assert np.all(np.abs(got - fz) <= bnd)
 

@@ -19,8 +19,19 @@ pytestmark = pytest.mark.gpu
 g = pytest.importorskip("tensor_core_dense_tn_gb300")
 from gpu_util import empty_out, from_dev, sample_positions, to_dev_bf16, to_dev_f32  # noqa: E402
 
-# M picks the kernel path: 48 -> skinny, 100 -> 1-SM tiled, 300 -> 2-SM tiled
-PATH_M = {"skinny": 48, "1sm": 100, "2sm": 300}
+# M picks the kernel path: 48 -> skinny, 100 -> 1-SM tiled, 2200 -> 2-SM tiled
+# (with N at least 1040: more than 64 tiles of 128 x 256, so pair tiles)
+PATH_M = {"skinny": 48, "1sm": 100, "2sm": 2200}
+PATH_CODE = {"skinny": 3, "1sm": 1, "2sm": 2}
+
+
+def shape_n(path, n):
+    """N for a test on `path`: the 2-SM case needs enough tiles to use pair tiles."""
+    return max(n, 1040) if path == "2sm" else n
+
+
+def check_path(path):
+    assert g.last_launch_info()["path"] == PATH_CODE[path], g.last_launch_info()
 FMTS = [gi.FP8_E4M3, gi.FP8_E5M2]
 
 
@@ -52,23 +63,25 @@ def _run(M, N, K, A, B, fmt, out_dtype, scale_a=1.0, scale_b=1.0, alpha=1.0, bet
 @pytest.mark.parametrize("fmt", FMTS)
 @pytest.mark.parametrize("N,K", [(520, 320), (264, 1040)])
 def test_integer_exact(path, fmt, N, K):
-    M = PATH_M[path]
+    M, N = PATH_M[path], shape_n(path, N)
     A = gi.draw_fp8(M, K, gi.Dist("int", -4, 4), 5000 + fmt, fmt)
     B = gi.draw_fp8(N, K, gi.Dist("int", -4, 4), 5010 + fmt, fmt)
     ref, _ = oracle.gemm_ref_fp8(A, B, fmt)
     got = _run(M, N, K, A, B, fmt, gi.OUT_F32)
+    check_path(path)
     assert np.array_equal(got, oracle.exact_f32(ref))
 
 
 @pytest.mark.parametrize("path", list(PATH_M))
 def test_integer_exact_scales_and_padding(path):
     # power-of-two scales keep the result exact; padded rows (ld > K) hold NaN codes
-    M, N, K, ld = PATH_M[path] + 3, 392, 208, 256
+    M, N, K, ld = PATH_M[path] + 3, shape_n(path, 392), 208, 256
     fmt = gi.FP8_E4M3
     A = gi.draw_fp8(M, K, gi.Dist("int", -4, 4), 5100, fmt, ld=ld)
     B = gi.draw_fp8(N, K, gi.Dist("int", -4, 4), 5101, fmt, ld=ld)
     ref, _ = oracle.gemm_ref_fp8(A, B, fmt, M=M, N=N, K=K, lda=ld, ldb=ld, alpha=0.5 * 0.25 * 8.0)
     got = _run(M, N, K, A, B, fmt, gi.OUT_F32, scale_a=0.25, scale_b=8.0, alpha=0.5, lda=ld, ldb=ld)
+    check_path(path)
     assert np.array_equal(got, oracle.exact_f32(ref))
 
 
@@ -76,7 +89,7 @@ def test_integer_exact_scales_and_padding(path):
 @pytest.mark.parametrize("fmt", FMTS)
 @pytest.mark.parametrize("out_dtype", [gi.OUT_BF16, gi.OUT_F32])
 def test_normal_within_bound(path, fmt, out_dtype):
-    M, N, K = PATH_M[path], 776, 1536
+    M, N, K = PATH_M[path], shape_n(path, 776), 1536
     A = gi.draw_fp8(M, K, gi.Dist("normal", 4.0), 5200 + fmt, fmt)
     B = gi.draw_fp8(N, K, gi.Dist("normal", 4.0), 5210 + fmt, fmt)
     C = (gi.draw_bf16(M, N, gi.Dist("normal", 1.0), 5220) if out_dtype == gi.OUT_BF16
@@ -86,6 +99,7 @@ def test_normal_within_bound(path, fmt, out_dtype):
     ref, absdot = oracle.gemm_ref_fp8(A, B, fmt, C=C, alpha=alpha * np.float32(sa) * np.float32(sb),
                                       beta=beta)
     got = _run(M, N, K, A, B, fmt, out_dtype, scale_a=sa, scale_b=sb, alpha=alpha, beta=beta, C=C)
+    check_path(path)
     ok, worst, idx = oracle.check(got, ref, absdot, out_dtype, beta, c64)
     assert ok, (worst, idx)
 

@@ -67,7 +67,7 @@ def test_grouped_integer_exact(out_dtype, beta):
     rc = g.gemm_bf16_tn_grouped(arg, 1.0, beta, out_dtype, _stream())
     assert rc == 0, g.last_error()
     assert g.gemm_get_status(_stream()) == 0
-    assert g.last_launch_info()["cluster"] == 2          # some problem has M > 128
+    assert g.last_launch_info()["cluster"] == 1          # 30 tiles of 128 x 256: one wave
     for q, (_, _, _, dD) in zip(probs, dev):
         if q["M"] == 0:
             continue
@@ -75,6 +75,26 @@ def test_grouped_integer_exact(out_dtype, beta):
         ref, _ = oracle.gemm_ref(q["A"], q["B"], C, 1.0, beta, M=q["M"], N=q["N"], K=q["K"],
                                  lda=q["lda"], ldb=q["ldb"])
         _check_exact(from_dev(dD, out_dtype)[:, :q["N"]], ref, out_dtype)
+
+
+def test_grouped_pair_tiles():
+    """Problems taller than 128 rows needing more than one wave of 1-SM tiles run
+    on pair tiles: three 1024 x 2048 problems (64 tiles of 128 x 256 each)."""
+    probs, dev = [], []
+    for i in range(3):
+        q = _int_problem(1024 - 3 * i, 2048, 192, 1500 + 5 * i, gi.OUT_F32, False)
+        dA, dB = to_dev_bf16(q["A"]), to_dev_bf16(q["B"])
+        dD, _ = empty_out(q["M"], q["N"], gi.OUT_F32, ld=q["ldd"])
+        probs.append(q)
+        dev.append((dA, dB, dD))
+    arg = [dict(M=q["M"], N=q["N"], K=q["K"], A=dA.data_ptr(), lda=q["lda"], B=dB.data_ptr(), ldb=q["ldb"],
+                C=0, ldc=0, D=dD.data_ptr(), ldd=q["ldd"]) for q, (dA, dB, dD) in zip(probs, dev)]
+    assert g.gemm_bf16_tn_grouped(arg, 1.0, 0.0, gi.OUT_F32, _stream()) == 0, g.last_error()
+    assert g.gemm_get_status(_stream()) == 0
+    assert g.last_launch_info()["cluster"] == 2
+    for q, (_, _, dD) in zip(probs, dev):
+        ref, _ = oracle.gemm_ref(q["A"], q["B"], M=q["M"], N=q["N"], K=q["K"], lda=q["lda"], ldb=q["ldb"])
+        _check_exact(from_dev(dD, gi.OUT_F32)[:, :q["N"]], ref, gi.OUT_F32)
 
 
 def test_grouped_many_problems_several_launches():
