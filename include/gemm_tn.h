@@ -34,7 +34,7 @@
  * Degenerate shapes: M == 0 or N == 0 returns GEMM_OK with no launch;
  * K == 0 gives D = beta * C (or zeros).
  *
- * Library-owned memory: the skinny path (M <= 64) uses an fp32 partial-sum
+ * Library-owned memory: the skinny path (M <= 256) uses an fp32 partial-sum
  * workspace and arrival counters, allocated on the first such call for a
  * (device, stream) pair and kept until gemm_shutdown().  That first call
  * must not happen during stream capture.  Calls on different streams use
@@ -95,7 +95,9 @@ typedef enum {
   GEMM_PATH_AUTO = 0,   /* choose by shape */
   GEMM_PATH_1SM = 1,    /* persistent tiled kernel, 128x256 tile, one CTA per SM */
   GEMM_PATH_2SM = 2,    /* persistent tiled kernel, 256x256 tile per CTA pair */
-  GEMM_PATH_SKINNY = 3  /* M <= 64: swap-AB stream-K HBM streaming of B */
+  GEMM_PATH_SKINNY = 3  /* M <= 256: swap-AB stream-K HBM streaming of B (the tokens are MMA N);
+                           automatic for M <= 64, and for 64 < M <= 192 when K >= 2048 and the
+                           tiled paths would fill at most half of the SMs */
 } gemm_path;
 
 /* Overrides for gemm_bf16_tn_ex (benchmarks, ablations, tests).
@@ -153,7 +155,7 @@ int gemm_bf16_tn(int64_t M, int64_t N, int64_t K,
 
 /* Same operation with explicit overrides; cfg may be NULL (= gemm_bf16_tn).
  * A forced path that cannot run the shape returns GEMM_ERR_NOT_IMPLEMENTED
- * (GEMM_PATH_SKINNY needs M <= 64). */
+ * (GEMM_PATH_SKINNY needs 1 <= M <= 256 and K > 0). */
 int gemm_bf16_tn_ex(int64_t M, int64_t N, int64_t K,
                     const void *A, int64_t lda,
                     const void *B, int64_t ldb,

@@ -205,6 +205,16 @@ constexpr long long kSmallTileCount = 64;
 
 long long one_sm_tiles(int64_t M, int64_t N) { return ((M + 127) / 128) * ((N + 255) / 256); }
 
+// 65..192 tokens stream B with the swap-AB kernel (tokens as MMA N) instead
+// of the tiled kernels when K is long and the tiled kernels would fill at
+// most half of the SMs: 128 x 8192 x 8192 has 32 tiles of 128 x 256, so the
+// tiled path streamed B from 32 SMs (56.6 us; streaming: 41.0 us).  Every
+// stage also reloads the CTA's token rows, so the bytes entering each SM
+// grow with M; at 256 tokens the tiled path was faster again (56.9 against
+// 62.3 us), hence the cap.
+constexpr int64_t kStreamMinK = 2048;
+constexpr int64_t kStreamMaxM = 192;
+
 // Tiles along M per raster strip: keep the strip's A rows within ~32 MiB of
 // L2, so that the strip is re-read from L2 for every tile column it meets.
 int raster_group_for(int tile_m, int64_t K, int in_bytes, int tiles_m) {
@@ -267,11 +277,12 @@ int run(int64_t M, int64_t N, int64_t K, const void* A, int64_t lda, const void*
   if (path == GEMM_PATH_AUTO) {
     if (K == 0) path = GEMM_PATH_1SM;
     else if (M <= 64) path = GEMM_PATH_SKINNY;
+    else if (M <= kStreamMaxM && K >= kStreamMinK && 2 * one_sm_tiles(M, N) <= st->sms) path = GEMM_PATH_SKINNY;
     else if (M <= 128 || one_sm_tiles(M, N) <= kSmallTileCount) path = GEMM_PATH_1SM;
     else path = GEMM_PATH_2SM;
   }
-  if (path == GEMM_PATH_SKINNY && (M > 64 || K == 0))
-    return fail(GEMM_ERR_NOT_IMPLEMENTED, "skinny path needs 1 <= M <= 64 and K > 0");
+  if (path == GEMM_PATH_SKINNY && (M > 256 || K == 0))
+    return fail(GEMM_ERR_NOT_IMPLEMENTED, "skinny path needs 1 <= M <= 256 and K > 0");
 
   const CUtensorMapDataType out_dt = out_dtype == GEMM_OUT_F32 ? CU_TENSOR_MAP_DATA_TYPE_FLOAT32
                                                                 : CU_TENSOR_MAP_DATA_TYPE_BFLOAT16;

@@ -49,8 +49,8 @@ constexpr int kMmaPerStage = 4;   // tcgen05.mma per stage, 32 bytes of K each
 constexpr int kEpiWarps = 4;
 constexpr int kThreads = 64 + 32 * kEpiWarps;
 constexpr int kMaxStages = 24;
-constexpr int kNumAcc = 4;                   // TMEM accumulators (64 columns each)
-constexpr int kTmemCols = 64 * kNumAcc;
+constexpr int kNumAcc = 4;                   // TMEM accumulators: 4 of 64 columns (np <= 64), or
+                                             // 2 of 256 columns in the wide form (64 < np <= 256)
 constexpr int kErrTimeout = -5;
 constexpr int kSmemBudget = 216 * 1024;
 constexpr int kNumBars = 2 * kMaxStages + 2 * kNumAcc + 1;
@@ -158,12 +158,17 @@ __device__ __forceinline__ float* partial_ptr(const SkinnyParams& p, long long c
   return p.partials + ((c * 2 + slot) * BM + row) * (long long)p.np;
 }
 
-template <int KIND, int BM>
+template <int KIND, int BM, bool WIDE>
 __global__ void __launch_bounds__(kThreads, 1)
     gemm_tn_skinny_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
                           const SkinnyParams p) {
   constexpr int kBK = KIND == kKindF16 ? 64 : 128;  // K elements per stage
   constexpr int kBTileBytes = BM * kStageK;          // 16 or 8 KiB of B per stage
+  // Accumulators: 4 x 64 columns for up to 64 tokens; 2 x 256 columns in the
+  // wide form (65..256 tokens), whose epilogue walks them 16 columns at a time.
+  constexpr int kAccs = WIDE ? 2 : kNumAcc;
+  constexpr int kAccCols = WIDE ? 256 : 64;
+  constexpr int kTmemCols = WIDE ? 512 : 256;
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
   const int S = p.stages;
@@ -270,7 +275,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         const long long seg_end = min(u_end, (n + 1) * KB);
         if (!wait_bar(acce_bar(acc), acc_phase ^ 1, abort_flag, p.timeout_ns, p.status, kRoleMma)) break;
         tc_fence_after();
-        const uint32_t d_tmem = tmem_base + (uint32_t)(acc * 64);
+        const uint32_t d_tmem = tmem_base + (uint32_t)(acc * kAccCols);
         for (long long v = u; v < seg_end; ++v) {
           if (!wait_bar(full_bar(stage), phase, abort_flag, p.timeout_ns, p.status, kRoleMma)) {
             ok = false;
@@ -290,7 +295,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
         if (!ok) break;
         mma_commit(accf_bar(acc));
-        if (++acc == kNumAcc) {
+        if (++acc == kAccs) {
           acc = 0;
           acc_phase ^= 1;
         }
@@ -301,6 +306,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
   } else {
     // ---------------------------------------------------------- epilogue
+    if constexpr (!WIDE) {
     // Each warp owns BM/4 of the tile's rows of D^T (TMEM lane quarter q;
     // for BM = 64 only lanes 0..15 of the quarter hold rows) and finishes
     // them on its own: split tiles keep one arrival counter per (tile,
@@ -461,6 +467,140 @@ __global__ void __launch_bounds__(kThreads, 1)
       }
       u = seg_end;
     }
+    } else {
+      // -------------------------------------------------------- wide epilogue
+      // 65..256 tokens: the accumulator is read 16 columns at a time and each
+      // chunk is finished (stored, published as a partial, or added to the
+      // other parts) before the next is read, so a thread never holds more
+      // than 16 of its np values.  Same split-tile protocol as above.
+      const int q = warp & 3;
+      const int n_local = BM == 128 ? q * 32 + lane : q * 16 + lane;
+      const bool row_lane = BM == 128 || lane < 16;
+      int acc = 0;
+      uint32_t acc_phase = 0;
+      long long u = u_begin;
+      const long long first_tile = u_begin / KB;
+      const int nchunks = p.np / 16;
+      const bool plain = !(p.epi.bias || p.epi.act);
+      while (u < u_end) {
+        const long long n = u / KB;
+        const long long seg_end = min(u_end, (n + 1) * KB);
+        const bool whole = (u == n * KB) && (seg_end == (n + 1) * KB);
+        if (!wait_bar(accf_bar(acc), acc_phase, abort_flag, p.timeout_ns, p.status, kRoleEpilogue)) break;
+        tc_fence_after();
+        const uint32_t tcol = tmem_base + ((uint32_t)(q * 32) << 16) + (uint32_t)(acc * kAccCols);
+        const int ng = (int)(n * BM) + n_local;
+        const long long c_first = whole ? c : tile_part_cta(p, n, 0);
+        const int nseg = whole ? 1 : tile_parts(p, n);
+        int* arrivals = p.counters + n * 4 + q;
+        const bool publish = !whole && c != c_first;
+        const int slot = (n == first_tile) ? 0 : 1;
+        int ok = 1;
+        if (!whole && !publish) {
+          // finisher: wait (bounded) for the other nseg-1 parts
+          if (lane == 0) {
+            if (ld_acquire_gpu(arrivals) != nseg - 1) {
+              const uint64_t t0 = globaltimer();
+              while (ld_acquire_gpu(arrivals) != nseg - 1) {
+                if (*abort_flag || globaltimer() - t0 > p.timeout_ns) {
+                  if (!*abort_flag) {
+                    *abort_flag = 1;
+                    if (atomicCAS(p.status, 0, kErrTimeout) == 0)
+                      atomicExch(p.status + 1, (kRoleFixup << 24) | (int)blockIdx.x);
+                  }
+                  ok = 0;
+                  break;
+                }
+                __nanosleep(32);
+              }
+            }
+            if (ok) *arrivals = 0;  // every part is in: ready for the next call
+          }
+          ok = __shfl_sync(0xffffffffu, ok, 0);
+          __syncwarp();
+        }
+        if (ok) {
+          const float bias_n = (!publish && !plain && p.epi.bias && row_lane && ng < p.N) ? load_bias(p.epi, ng) : 0.0f;
+#pragma unroll 1
+          for (int g = 0; g < nchunks; ++g) {
+            uint32_t r[16];
+            tmem_ld_32x32b_x16(tcol + (uint32_t)(g * 16), r);
+            tmem_wait_ld();
+            float v[16];
+#pragma unroll
+            for (int t = 0; t < 16; ++t) v[t] = __uint_as_float(r[t]);
+            if (publish) {
+              if (row_lane) {
+                float4* mine = reinterpret_cast<float4*>(partial_ptr<BM>(p, c, slot, n_local) + g * 16);
+#pragma unroll
+                for (int v4 = 0; v4 < 4; ++v4)
+                  mine[v4] = make_float4(v[4 * v4], v[4 * v4 + 1], v[4 * v4 + 2], v[4 * v4 + 3]);
+              }
+              continue;
+            }
+            if (!whole) {
+              // the tile's parts in k order: this CTA's own part 0, then 1..nseg-1
+#pragma unroll
+              for (int t = 0; t < 16; ++t) v[t] = 0.0f + v[t];
+#pragma unroll 1
+              for (int j = 1; j < nseg; ++j) {
+                if (!row_lane) continue;
+                const long long cc = tile_part_cta(p, n, j);
+                const int sl = (n == cta_begin(p, cc) / KB) ? 0 : 1;
+                const float4* part = reinterpret_cast<const float4*>(partial_ptr<BM>(p, cc, sl, n_local) + g * 16);
+#pragma unroll
+                for (int v4 = 0; v4 < 4; ++v4) {
+                  const float4 x = __ldcg(part + v4);
+                  v[4 * v4 + 0] += x.x;
+                  v[4 * v4 + 1] += x.y;
+                  v[4 * v4 + 2] += x.z;
+                  v[4 * v4 + 3] += x.w;
+                }
+              }
+            }
+            if (row_lane && ng < p.N) {
+              if (plain) {
+#pragma unroll
+                for (int t = 0; t < 16; ++t) {
+                  const int m = g * 16 + t;
+                  if (m < p.M) {
+                    float x = p.alpha * v[t];
+                    if (p.has_c) x = fmaf(p.beta, load_c(p, m, ng), x);
+                    store_d(p, m, ng, x);
+                  }
+                }
+              } else {
+#pragma unroll
+                for (int t = 0; t < 16; ++t) {
+                  const int m = g * 16 + t;
+                  if (m < p.M) {
+                    float x = p.alpha * v[t];
+                    if (p.has_c) x = fmaf(p.beta, load_c(p, m, ng), x);
+                    store_d(p, m, ng, activate(x + bias_n, p.epi.act));
+                  }
+                }
+              }
+            }
+          }
+          if (publish) {
+            // every lane's partial before lane 0's release
+            __syncwarp();
+            if (lane == 0) red_add_release_gpu(arrivals, 1);
+          }
+        }
+        // the accumulator is read: hand it back to the MMA warp
+        tc_fence_before();
+        __syncwarp();
+        if (lane == 0) mbar_arrive(acce_bar(acc));
+        if (++acc == kAccs) {
+          acc = 0;
+          acc_phase ^= 1;
+        }
+        if (!ok) break;
+        u = seg_end;
+      }
+    }
+
   }
 
   __syncthreads();
@@ -526,19 +666,23 @@ cudaError_t launch_skinny(const CUtensorMap& tmA, const CUtensorMap& tmB, Skinny
   if (e != cudaSuccess) return e;
   if (dev < 64 && !configured[dev]) {
     int worst = 0;
-    for (int np = 16; np <= 64; np += 16)
+    for (int np = 16; np <= 256; np += 16)
       for (int bm = 64; bm <= 128; bm += 64) worst = smem_for(np, bm) > worst ? smem_for(np, bm) : worst;
-    const void* kernels[4] = {(const void*)gemm_tn_skinny_kernel<kKindF16, 128>,
-                              (const void*)gemm_tn_skinny_kernel<kKindF16, 64>,
-                              (const void*)gemm_tn_skinny_kernel<kKindF8F6F4, 128>,
-                              (const void*)gemm_tn_skinny_kernel<kKindF8F6F4, 64>};
+    const void* kernels[8] = {(const void*)gemm_tn_skinny_kernel<kKindF16, 128, false>,
+                              (const void*)gemm_tn_skinny_kernel<kKindF16, 64, false>,
+                              (const void*)gemm_tn_skinny_kernel<kKindF8F6F4, 128, false>,
+                              (const void*)gemm_tn_skinny_kernel<kKindF8F6F4, 64, false>,
+                              (const void*)gemm_tn_skinny_kernel<kKindF16, 128, true>,
+                              (const void*)gemm_tn_skinny_kernel<kKindF16, 64, true>,
+                              (const void*)gemm_tn_skinny_kernel<kKindF8F6F4, 128, true>,
+                              (const void*)gemm_tn_skinny_kernel<kKindF8F6F4, 64, true>};
     for (const void* k : kernels) {
       e = cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, worst);
       if (e != cudaSuccess) return e;
     }
     configured[dev] = true;
   }
-  if (p.bm != 64 && p.bm != 128) return cudaErrorInvalidValue;
+  if ((p.bm != 64 && p.bm != 128) || p.np < 16 || p.np > 256 || p.np % 16) return cudaErrorInvalidValue;
   p.stages = stages_for(p.np, p.bm);
   const int smem = smem_for(p.np, p.bm);
   if (info) {
@@ -550,7 +694,8 @@ cudaError_t launch_skinny(const CUtensorMap& tmA, const CUtensorMap& tmB, Skinny
     info->tile_n = p.np;
     info->stages = p.stages;
     info->smem_bytes = smem;
-    info->kernel = p.kind == kKindF8F6F4 ? "gemm_tn_skinny_kernel<fp8 in>" : "gemm_tn_skinny_kernel";
+    info->kernel = p.kind == kKindF8F6F4 ? (p.np > 64 ? "gemm_tn_skinny_kernel<fp8 in,wide>" : "gemm_tn_skinny_kernel<fp8 in>")
+                                         : (p.np > 64 ? "gemm_tn_skinny_kernel<wide>" : "gemm_tn_skinny_kernel");
   }
   cudaLaunchConfig_t cfg = {};
   cudaLaunchAttribute attr[1];
@@ -564,11 +709,13 @@ cudaError_t launch_skinny(const CUtensorMap& tmA, const CUtensorMap& tmB, Skinny
     cfg.attrs = attr;
     cfg.numAttrs = 1;
   }
-  if (p.kind == kKindF8F6F4)
-    return p.bm == 64 ? cudaLaunchKernelEx(&cfg, gemm_tn_skinny_kernel<kKindF8F6F4, 64>, tmA, tmB, p)
-                      : cudaLaunchKernelEx(&cfg, gemm_tn_skinny_kernel<kKindF8F6F4, 128>, tmA, tmB, p);
-  return p.bm == 64 ? cudaLaunchKernelEx(&cfg, gemm_tn_skinny_kernel<kKindF16, 64>, tmA, tmB, p)
-                    : cudaLaunchKernelEx(&cfg, gemm_tn_skinny_kernel<kKindF16, 128>, tmA, tmB, p);
+  const bool wide = p.np > 64;
+#define GTN_SKINNY(KV, BMV) \
+  (wide ? cudaLaunchKernelEx(&cfg, gemm_tn_skinny_kernel<KV, BMV, true>, tmA, tmB, p) \
+        : cudaLaunchKernelEx(&cfg, gemm_tn_skinny_kernel<KV, BMV, false>, tmA, tmB, p))
+  if (p.kind == kKindF8F6F4) return p.bm == 64 ? GTN_SKINNY(kKindF8F6F4, 64) : GTN_SKINNY(kKindF8F6F4, 128);
+  return p.bm == 64 ? GTN_SKINNY(kKindF16, 64) : GTN_SKINNY(kKindF16, 128);
+#undef GTN_SKINNY
 }
 
 }  // namespace gtn

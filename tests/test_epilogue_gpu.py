@@ -123,3 +123,22 @@ def test_bias_act_argument_errors():
     assert g.gemm_bf16_tn_bias_act(*a, 0x4000, 0, 7, 0) == g.GEMM_ERR_INVALID_VALUE
     assert g.gemm_bf16_tn_bias_act(*a, 0x4000, 5, 1, 0) == g.GEMM_ERR_INVALID_VALUE
     assert g.gemm_bf16_tn_bias_act(*a, 0x4002, 1, 1, 0) == g.GEMM_ERR_MISALIGNED
+
+
+@pytest.mark.parametrize("act", [0, 1, 3])
+def test_wide_streaming_epilogue(act):
+    """176 tokens, K = 2048: the auto path is the streaming kernel's wide form."""
+    M, N, K = 176, 1040, 2048
+    A = gi.draw_bf16(M, K, gi.Dist("int", -4, 4), 4600 + act)
+    B = gi.draw_bf16(N, K, gi.Dist("int", -4, 4), 4610 + act)
+    bias = gi.draw_bf16(N, 1, gi.Dist("int", -50, 50), 4620).reshape(N)
+    ref, absdot = oracle.gemm_ref(A, B)
+    got = _run(M, N, K, A, B, bias, 0, act, gi.OUT_F32)
+    assert g.last_launch_info()["path"] == 3
+    if act in (0, 1):
+        assert np.array_equal(got, oracle.exact_f32(oracle.epilogue(ref, bias, act)))
+    else:
+        z = oracle.epilogue(ref, bias, 0)
+        fz = oracle.epilogue(ref, bias, act)
+        bnd = oracle.bound_act(z, fz, absdot, gi.OUT_F32, act)
+        assert np.all(np.abs(got.astype(np.float64) - fz) <= bnd)

@@ -147,3 +147,15 @@ def test_fp8_argument_errors():
     # lda must be a multiple of 16 one-byte elements
     assert g.gemm_fp8_tn(64, 64, 64, 0x1000, 72, 0x2000, 64, 0, *tail) == g.GEMM_ERR_MISALIGNED
     assert g.gemm_fp8_tn(64, 64, 64, 0x1008, 64, 0x2000, 64, 0, *tail) == g.GEMM_ERR_MISALIGNED
+
+
+@pytest.mark.parametrize("fmt", FMTS)
+def test_wide_streaming_integer_exact(fmt):
+    """144 tokens, K = 2048: the streaming kernel's wide form on fp8 inputs."""
+    M, N, K = 144, 648, 2048
+    A = gi.draw_fp8(M, K, gi.Dist("int", -4, 4), 5500 + fmt, fmt)
+    B = gi.draw_fp8(N, K, gi.Dist("int", -4, 4), 5510 + fmt, fmt)
+    ref, _ = oracle.gemm_ref_fp8(A, B, fmt)
+    got = _run(M, N, K, A, B, fmt, gi.OUT_F32)
+    assert g.last_launch_info()["path"] == 3
+    assert np.array_equal(got, oracle.exact_f32(ref))

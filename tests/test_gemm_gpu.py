@@ -131,6 +131,44 @@ def test_decode_shape_launch():
     assert info["tile_m"] == 64 and info["grid"] == 128      # 128 whole 64-row tiles, one per CTA
 
 
+WIDE_SHAPES = [(65, 300, 256), (80, 1000, 640), (128, 520, 2048), (200, 130, 1000), (256, 384, 300),
+               (97, 8192, 128)]
+
+
+@pytest.mark.parametrize("shape", WIDE_SHAPES)
+@pytest.mark.parametrize("out_dtype", [gi.OUT_F32, gi.OUT_BF16])
+def test_integer_ragged_skinny_wide(shape, out_dtype):
+    """65..256 tokens on the streaming kernel (tokens as MMA N up to 256, chunked epilogue)."""
+    M, N, K = shape
+    got, exp = run_int(M, N, K, PS, out_dtype, seed=260 + M + 7 * N + 13 * K)
+    assert_same(got, exp)
+    assert g.last_launch_info()["tile_n"] == -(-M // 16) * 16
+
+
+@pytest.mark.parametrize("skinny_grid", [1, 7, 33, 100, 151])
+@pytest.mark.parametrize("bm", [64, 128])
+def test_skinny_wide_partitions(skinny_grid, bm):
+    """Wide accumulators split between CTAs: partials published and added chunk by chunk."""
+    for rep in range(2):
+        got, exp = run_int(144, 700, 1344, PS, gi.OUT_BF16, seed=310 + rep + bm, skinny_grid=skinny_grid,
+                           skinny_bm=bm)
+        assert_same(got, exp)
+
+
+def test_mid_batch_decode_streams():
+    """128 tokens against an 8192 x 4096 weight: auto path is the streaming kernel."""
+    M, N, K = 128, 8192, 4096
+    A = gi.draw_bf16(M, K, gi.Dist("normal", 1.0), 320)
+    B = gi.draw_bf16(N, K, gi.Dist("normal", 1.0 / K), 321)
+    dD, ldd = empty_out(M, N, gi.OUT_BF16)
+    rc, st = call(M, N, K, to_dev_bf16(A), K, to_dev_bf16(B), K, None, 0, dD, ldd, 1.0, 0.0, gi.OUT_BF16)
+    assert rc == 0 and st == 0, g.last_error()
+    assert g.last_launch_info()["path"] == PS
+    ref, absdot = oracle.gemm_ref(A, B)
+    ok, worst, where = oracle.check(from_dev(dD, gi.OUT_BF16), ref, absdot, gi.OUT_BF16)
+    assert ok, (worst, where)
+
+
 @pytest.mark.parametrize("skinny_grid", [1, 3, 7, 64, 100, 151, 1000])
 @pytest.mark.parametrize("K", [64, 1344, 4160])
 def test_skinny_stream_k_partitions(skinny_grid, K):
@@ -298,7 +336,7 @@ def test_argument_errors():
     assert rc(out_dtype=2) == g.GEMM_ERR_INVALID_VALUE
     assert rc(M=0) == g.GEMM_OK
     cfg = g.GemmConfig(path=g.PATH_SKINNY)
-    a = dict(base, M=65)
+    a = dict(base, M=257)
     assert g.gemm_bf16_tn_ex(*a.values(), cfg) == g.GEMM_ERR_NOT_IMPLEMENTED
     torch.cuda.synchronize()
     assert g.gemm_get_status(s) == 0
