@@ -96,8 +96,11 @@ typedef enum {
   GEMM_PATH_1SM = 1,    /* persistent tiled kernel, 128x256 tile, one CTA per SM */
   GEMM_PATH_2SM = 2,    /* persistent tiled kernel, 256x256 tile per CTA pair */
   GEMM_PATH_SKINNY = 3  /* M <= 256: swap-AB stream-K HBM streaming of B (the tokens are MMA N);
-                           automatic for M <= 64, and for 64 < M <= 192 when K >= 2048 and the
-                           tiled paths would fill at most half of the SMs */
+                           automatic for M <= 32, and for 32 < M <= 128 when B (N x K) is at
+                           least 32 MiB and each tile is split into at most two k-parts.
+                           AUTO otherwise takes pair tiles (2SM) when B is at least 32 MiB and
+                           M > 128 or the 1-SM tiles would fill at most half of the SMs, or
+                           when M > 128 with more than 64 tiles of 128x256; else 1SM */
 } gemm_path;
 
 /* Overrides for gemm_bf16_tn_ex (benchmarks, ablations, tests).
@@ -114,7 +117,13 @@ typedef struct gemm_tn_config {
   int skinny_skew_kb;       /* skinny path, equal-split mode: k-blocks (of 64) moved to the part that
                                finishes each tile; 0 = default (K/4096), < 0 = none */
   int scheduler;            /* tiled paths: GEMM_SCHED_* (0 = the default) */
-  int skinny_bm;            /* skinny path: rows of B per tile (MMA M), 64 or 128; 0 = auto (128) */
+  int skinny_bm;            /* skinny path: rows of B per tile (MMA M), 64 or 128; 0 = auto: 64 where
+                               64-row tiles fit one wave and M > 32 (or M > 16 and 128-row tiles would
+                               be split into 4 or more k-parts), else 128 */
+  int skinny_kgroup;        /* skinny path: k-blocks per ring stage, loaded as one TMA box per operand:
+                               1, 2 or 4; 0 = auto (32 KiB boxes of B while 4 stages fit).  Values
+                               above 1 apply only when K is a whole number of k-blocks (64 bf16 or
+                               128 fp8 elements); otherwise the path uses 1 */
 } gemm_tn_config;
 
 /* Tile schedulers of the tiled paths.
@@ -136,7 +145,7 @@ typedef struct gemm_launch_info {
   int grid;          /* CTAs launched */
   int cluster;       /* CTAs per cluster */
   int block;         /* threads per CTA */
-  int tile_m;        /* output rows per tile (pair tile for the 2-SM path; 128 for skinny) */
+  int tile_m;        /* output rows per tile (pair tile for the 2-SM path; skinny: rows of B, 64 or 128) */
   int tile_n;        /* output columns per tile (skinny: padded M) */
   int stages;        /* shared-memory ring depth */
   int smem_bytes;    /* dynamic shared memory per CTA */

@@ -56,7 +56,8 @@ class GemmConfig(ctypes.Structure):
     _fields_ = [("path", ctypes.c_int), ("grid", ctypes.c_int), ("raster_group", ctypes.c_int),
                 ("skinny_grid", ctypes.c_int), ("wait_timeout_ns", ctypes.c_uint64),
                 ("test_fault", ctypes.c_int), ("disable_pdl", ctypes.c_int),
-                ("skinny_skew_kb", ctypes.c_int), ("scheduler", ctypes.c_int), ("skinny_bm", ctypes.c_int)]
+                ("skinny_skew_kb", ctypes.c_int), ("scheduler", ctypes.c_int), ("skinny_bm", ctypes.c_int),
+                ("skinny_kgroup", ctypes.c_int)]
 
 
 class GemmProblem(ctypes.Structure):

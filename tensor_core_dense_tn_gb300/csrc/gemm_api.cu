@@ -118,6 +118,22 @@ int encode_2d(CUtensorMap* m, CUtensorMapDataType dt, int esize, const void* bas
   return GEMM_OK;
 }
 
+// 3D view of a row-major matrix for loads of kg consecutive k-blocks in one
+// box: dims {k in block, row, k-block}, the k-block stride being the block's
+// 128 bytes.  K must be a whole number of k-blocks (the view has no zero fill
+// inside a row); k-blocks past K and rows past `outer` are zero-filled.
+int encode_kgroups(CUtensorMap* m, CUtensorMapDataType dt, int esize, const void* base, uint64_t K, uint64_t outer,
+                   uint64_t ld_elems, uint32_t kbe, uint32_t box_outer, uint32_t kg, const char* what) {
+  cuuint64_t dims[3] = {kbe, outer, K / kbe};
+  cuuint64_t strides[2] = {ld_elems * (uint64_t)esize, (uint64_t)kbe * esize};
+  cuuint32_t box[3] = {kbe, box_outer, kg};
+  cuuint32_t estr[3] = {1, 1, 1};
+  CUresult r = g_encode(m, dt, 3, const_cast<void*>(base), dims, strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
+                        CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  if (r != CUDA_SUCCESS) return fail(GEMM_ERR_LAUNCH, "cuTensorMapEncodeTiled(%s, k-groups) failed with %d", what, (int)r);
+  return GEMM_OK;
+}
+
 bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
 
 uint64_t timeout_ns(const gemm_tn_config* cfg) {
@@ -197,23 +213,32 @@ int check_operands(int64_t M, int64_t N, int64_t K, const void* A, int64_t lda, 
   return GEMM_OK;
 }
 
-// A GEMM of at most this many 128 x 256 tiles runs on 1-SM tiles even when
-// M > 128: with so few tiles the pair kernel's cluster launch costs more than
-// its shared operand traffic saves (measured 0.5-0.8 us per call from 256^3
-// to 1024 x 2048 x 2048; with 120 tiles the pair kernel was faster).
+// A GEMM of at most this many 128 x 256 tiles whose B stays in L2 runs on
+// 1-SM tiles even when M > 128: with so few tiles the pair kernel's cluster
+// launch costs more than its shared operand traffic saves (measured 0.5-0.8
+// us per call from 256^3 to 1024 x 2048 x 2048; with 120 tiles the pair
+// kernel was faster).
 constexpr long long kSmallTileCount = 64;
 
 long long one_sm_tiles(int64_t M, int64_t N) { return ((M + 127) / 128) * ((N + 255) / 256); }
 
-// 65..192 tokens stream B with the swap-AB kernel (tokens as MMA N) instead
-// of the tiled kernels when K is long and the tiled kernels would fill at
-// most half of the SMs: 128 x 8192 x 8192 has 32 tiles of 128 x 256, so the
-// tiled path streamed B from 32 SMs (56.6 us; streaming: 41.0 us).  Every
-// stage also reloads the CTA's token rows, so the bytes entering each SM
-// grow with M; at 256 tokens the tiled path was faster again (56.9 against
-// 62.3 us), hence the cap.
-constexpr int64_t kStreamMinK = 2048;
-constexpr int64_t kStreamMaxM = 192;
+// Automatic path.  The numbers are GB300 measurements (graph-replayed calls,
+// B rotated over copies so that it streams from HBM where it is large).
+// - Up to 32 tokens: the streaming kernel (swap-AB, tokens as MMA N) is the
+//   fastest at every measured shape, 256 <= N <= 57344, 256 <= K <= 8192.
+// - 33..128 tokens: streaming where B is too large to stay in L2 between
+//   calls (>= 32 MiB) and the streaming kernel splits each tile into at most
+//   two k-parts.  128 x 8192 x 8192: 38.5 us against 43.6 (2-SM) and 56.6
+//   (1-SM).  Where tiles would be split into more parts (64 x 1024 x 4096:
+//   31.8 against 21.9 us) or fall to stream-K (64 x 28672 x 4096: 49.9
+//   against 44.5 us), or B is small (64 x 4096 x 1024: 13.1 against 9.3 us),
+//   the tiled kernels win.
+// - When B streams from HBM and the tiles are few, pair tiles win over 1-SM
+//   tiles even for M <= 128: each SM of a pair loads half of the B tile, and
+//   twice the SMs stream (96 x 16384 x 8192: 53.5 against 61.6 us).  For
+//   129..256 tokens this holds at any tile count (224 x 8192 x 8192: 44.0
+//   against 56.6 us); with B in L2 the 1-SM kernel's lighter launch wins.
+constexpr int64_t kStreamedBytes = 32ll << 20;
 
 // Tiles along M per raster strip: keep the strip's A rows within ~32 MiB of
 // L2, so that the strip is re-read from L2 for every tile column it meets.
@@ -261,6 +286,9 @@ int run(int64_t M, int64_t N, int64_t K, const void* A, int64_t lda, const void*
   const int bm_req = cfg ? cfg->skinny_bm : 0;
   if (bm_req != 0 && bm_req != 64 && bm_req != 128)
     return fail(GEMM_ERR_INVALID_VALUE, "skinny_bm must be 0, 64 or 128, got %d", bm_req);
+  const int kg_req = cfg ? cfg->skinny_kgroup : 0;
+  if (kg_req != 0 && kg_req != 1 && kg_req != 2 && kg_req != 4)
+    return fail(GEMM_ERR_INVALID_VALUE, "skinny_kgroup must be 0, 1, 2 or 4, got %d", kg_req);
   if (M == 0 || N == 0) return GEMM_OK;
   const bool has_c = (beta != 0.0f);
   const int esize = out_dtype == GEMM_OUT_F32 ? 4 : 2;
@@ -276,10 +304,17 @@ int run(int64_t M, int64_t N, int64_t K, const void* A, int64_t lda, const void*
   int path = path_req;
   if (path == GEMM_PATH_AUTO) {
     if (K == 0) path = GEMM_PATH_1SM;
-    else if (M <= 64) path = GEMM_PATH_SKINNY;
-    else if (M <= kStreamMaxM && K >= kStreamMinK && 2 * one_sm_tiles(M, N) <= st->sms) path = GEMM_PATH_SKINNY;
-    else if (M <= 128 || one_sm_tiles(M, N) <= kSmallTileCount) path = GEMM_PATH_1SM;
-    else path = GEMM_PATH_2SM;
+    else {
+      const bool streamed = N * K * in_bytes >= kStreamedBytes;
+      const int np = (int)((M + 15) / 16) * 16;
+      const int parts = skinny_parts(N, np, skinny_max_grid(np, st->sms));
+      const long long tiles = one_sm_tiles(M, N);
+      if (M <= 32) path = GEMM_PATH_SKINNY;
+      else if (M <= 128 && streamed && parts >= 1 && parts <= 2) path = GEMM_PATH_SKINNY;
+      else if (M > 128 && (streamed || tiles > kSmallTileCount)) path = GEMM_PATH_2SM;
+      else if (M <= 128 && streamed && 2 * tiles <= st->sms) path = GEMM_PATH_2SM;
+      else path = GEMM_PATH_1SM;
+    }
   }
   if (path == GEMM_PATH_SKINNY && (M > 256 || K == 0))
     return fail(GEMM_ERR_NOT_IMPLEMENTED, "skinny path needs 1 <= M <= 256 and K > 0");
@@ -296,9 +331,13 @@ int run(int64_t M, int64_t N, int64_t K, const void* A, int64_t lda, const void*
     const int np = (int)((M + 15) / 16) * 16;
     SkinnyParams p = {};
     p.M = (int)M; p.N = (int)N; p.K = (int)K; p.np = np;
-    p.num_kb = (int)((K + kbe - 1) / kbe);
     const int max_grid = skinny_max_grid(np, st->sms);
-    p.bm = bm_req ? bm_req : skinny_tile_rows(N, max_grid);
+    p.bm = bm_req ? bm_req : skinny_tile_rows(N, np, max_grid);
+    p.kg = skinny_kgroup(np, p.bm, K, kbe, kg_req);
+    if (skinny_stages(np, p.bm, p.kg) < 2)
+      return fail(GEMM_ERR_INVALID_VALUE, "skinny_kgroup %d leaves fewer than 2 ring stages at M = %lld", p.kg,
+                  (long long)M);
+    p.num_kb = (int)(((K + kbe - 1) / kbe + p.kg - 1) / p.kg);
     p.n_tiles = (int)((N + p.bm - 1) / p.bm);
     p.kind = in_kind;
     p.a_fmt = fp8_format;
@@ -315,10 +354,15 @@ int run(int64_t M, int64_t N, int64_t K, const void* A, int64_t lda, const void*
     p.partials = w->partials;
     p.counters = w->counters;
     CUtensorMap tA, tB;
-    if ((rc = encode_2d(&tA, in_dt, in_bytes, A, K, M, lda, kbe, np, CU_TENSOR_MAP_SWIZZLE_128B, "A")))
-      return rc;
-    if ((rc = encode_2d(&tB, in_dt, in_bytes, B, K, N, ldb, kbe, p.bm, CU_TENSOR_MAP_SWIZZLE_128B, "B")))
-      return rc;
+    if (p.kg == 1) {
+      if ((rc = encode_2d(&tA, in_dt, in_bytes, A, K, M, lda, kbe, np, CU_TENSOR_MAP_SWIZZLE_128B, "A")))
+        return rc;
+      if ((rc = encode_2d(&tB, in_dt, in_bytes, B, K, N, ldb, kbe, p.bm, CU_TENSOR_MAP_SWIZZLE_128B, "B")))
+        return rc;
+    } else {
+      if ((rc = encode_kgroups(&tA, in_dt, in_bytes, A, K, M, lda, kbe, np, p.kg, "A"))) return rc;
+      if ((rc = encode_kgroups(&tB, in_dt, in_bytes, B, K, N, ldb, kbe, p.bm, p.kg, "B"))) return rc;
+    }
     e = launch_skinny(tA, tB, p, pdl, stream, &li);
   } else {
     const int cg = path == GEMM_PATH_2SM ? 2 : 1;

@@ -88,14 +88,27 @@ int na_setup(int dev, NaDevice** out) {
   return GEMM_OK;
 }
 
-int na_encode(CUtensorMap* m, const void* base, uint64_t inner, uint64_t outer, uint64_t ld, uint32_t box_outer) {
-  cuuint64_t dims[2] = {inner, outer};
-  cuuint64_t strides[1] = {ld * 2};
-  cuuint32_t box[2] = {64, box_outer};
-  cuuint32_t estr[2] = {1, 1};
-  CUresult r = g_na_encode(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void*>(base), dims, strides, box, estr,
-                           CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
-                           CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+// bf16 operand map with 64-element k-blocks: 2D (kg = 1), or the 3D view
+// {k in block, row, k-block} that loads kg k-blocks per box (K a multiple of 64).
+int na_encode(CUtensorMap* m, const void* base, uint64_t K, uint64_t outer, uint64_t ld, uint32_t box_outer, int kg) {
+  CUresult r;
+  if (kg == 1) {
+    cuuint64_t dims[2] = {K, outer};
+    cuuint64_t strides[1] = {ld * 2};
+    cuuint32_t box[2] = {64, box_outer};
+    cuuint32_t estr[2] = {1, 1};
+    r = g_na_encode(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void*>(base), dims, strides, box, estr,
+                    CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                    CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  } else {
+    cuuint64_t dims[3] = {64, outer, K / 64};
+    cuuint64_t strides[2] = {ld * 2, 128};
+    cuuint32_t box[3] = {64, box_outer, (cuuint32_t)kg};
+    cuuint32_t estr[3] = {1, 1, 1};
+    r = g_na_encode(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void*>(base), dims, strides, box, estr,
+                    CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                    CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  }
   return r == CUDA_SUCCESS ? GEMM_OK : GEMM_ERR_LAUNCH;
 }
 
@@ -140,13 +153,14 @@ extern "C" int gemm_bf16_tn_skinny_noalloc(int64_t M, int64_t N, int64_t K, cons
   p.N = (int)N;
   p.K = (int)K;
   p.np = (int)((M + 15) / 16) * 16;
-  p.num_kb = (int)((K + 63) / 64);
   int sms = skinny_max_grid(p.np, d->sms);
   if (sms > kNaMaxGrid) sms = kNaMaxGrid;
   // 64-row tiles only when they fit one wave (at most sms <= kNaMaxGrid tiles),
   // so the counters never exceed the 128-row tile count the scratch is sized for
-  p.bm = skinny_tile_rows(N, sms);
+  p.bm = skinny_tile_rows(N, p.np, sms);
   p.n_tiles = (int)((N + p.bm - 1) / p.bm);
+  p.kg = skinny_kgroup(p.np, p.bm, K, 64, 0);
+  p.num_kb = (int)(((K + 63) / 64 + p.kg - 1) / p.kg);
   p.units = (long long)p.n_tiles * p.num_kb;
   skinny_partition(&p, sms, 0, 0);
   p.alpha = alpha;
@@ -168,7 +182,7 @@ extern "C" int gemm_bf16_tn_skinny_noalloc(int64_t M, int64_t N, int64_t K, cons
   if (cudaMemsetAsync(p.counters, 0, (size_t)p.n_tiles * 4 * sizeof(int), stream) != cudaSuccess)
     return na_fail(GEMM_ERR_CUDA, "clearing the counters failed");
   CUtensorMap tA, tB;
-  if (na_encode(&tA, A, K, M, lda, p.np) != GEMM_OK || na_encode(&tB, B, K, N, ldb, (uint32_t)p.bm) != GEMM_OK)
+  if (na_encode(&tA, A, K, M, lda, p.np, p.kg) != GEMM_OK || na_encode(&tB, B, K, N, ldb, (uint32_t)p.bm, p.kg) != GEMM_OK)
     return na_fail(GEMM_ERR_LAUNCH, "tensor map encoding failed");
   LaunchInfo li = {};
   if (launch_skinny(tA, tB, p, false, stream, &li) != cudaSuccess) {

@@ -55,16 +55,20 @@ constexpr int kErrTimeout = -5;
 constexpr int kSmemBudget = 216 * 1024;
 constexpr int kNumBars = 2 * kMaxStages + 2 * kNumAcc + 1;
 
-// A stage: BM rows of B and np rows of A, 128 bytes of K each.
-__host__ __device__ inline int stage_bytes(int np, int bm) { return (bm + np) * kStageK; }
+// A stage: kg k-blocks, each BM rows of B and np rows of A of 128 bytes of
+// K.  With kg > 1 each operand's kg k-blocks arrive as one TMA box: the TMA
+// unit sustains only a few million boxes per second per SM, so 8 KiB boxes
+// stream at about half the rate of 16-64 KiB ones (measured on GB300: 24 GB/s
+// per SM at 8 KiB, 42 at 16 KiB, 46 at 32-64 KiB, at equal bytes in flight).
+__host__ __device__ inline int stage_bytes(int np, int bm, int kg) { return kg * (bm + np) * kStageK; }
 
-__host__ __device__ inline int stages_for(int np, int bm) {
-  int s = kSmemBudget / stage_bytes(np, bm);
+__host__ __device__ inline int stages_for(int np, int bm, int kg) {
+  int s = kSmemBudget / stage_bytes(np, bm, kg);
   return s > kMaxStages ? kMaxStages : s;
 }
 
-__host__ __device__ inline int smem_for(int np, int bm) {
-  return 1024 + stages_for(np, bm) * stage_bytes(np, bm) + kNumBars * 8 + 16;
+__host__ __device__ inline int smem_for(int np, int bm, int kg) {
+  return 1024 + stages_for(np, bm, kg) * stage_bytes(np, bm, kg) + kNumBars * 8 + 16;
 }
 
 // First unit owned by CTA c when U units are split into G contiguous ranges.
@@ -158,12 +162,41 @@ __device__ __forceinline__ float* partial_ptr(const SkinnyParams& p, long long c
   return p.partials + ((c * 2 + slot) * BM + row) * (long long)p.np;
 }
 
+// Warp-wide bounded wait until `expected` parts have been counted at
+// `arrivals` (lane 0 polls with acquire; the warp barrier passes the acquire
+// on to the other lanes), then clears the counter for the next call.  False
+// if this CTA is aborting or the limit expired (status recorded).
+__device__ __noinline__ bool wait_parts(int* arrivals, int expected, volatile uint32_t* abort_flag,
+                                        uint64_t timeout_ns, int* status) {
+  int ok = 1;
+  if ((threadIdx.x & 31) == 0) {
+    if (ld_acquire_gpu(arrivals) != expected) {
+      const uint64_t t0 = globaltimer();
+      while (ld_acquire_gpu(arrivals) != expected) {
+        if (*abort_flag || globaltimer() - t0 > timeout_ns) {
+          if (!*abort_flag) {
+            *abort_flag = 1;
+            if (atomicCAS(status, 0, kErrTimeout) == 0) atomicExch(status + 1, (kRoleFixup << 24) | (int)blockIdx.x);
+          }
+          ok = 0;
+          break;
+        }
+        __nanosleep(32);
+      }
+    }
+    if (ok) *arrivals = 0;  // every part is in: ready for the next call
+  }
+  ok = __shfl_sync(0xffffffffu, ok, 0);
+  __syncwarp();
+  return ok != 0;
+}
+
 template <int KIND, int BM, bool WIDE>
 __global__ void __launch_bounds__(kThreads, 1)
     gemm_tn_skinny_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
                           const SkinnyParams p) {
   constexpr int kBK = KIND == kKindF16 ? 64 : 128;  // K elements per stage
-  constexpr int kBTileBytes = BM * kStageK;          // 16 or 8 KiB of B per stage
+  constexpr int kBTileBytes = BM * kStageK;          // 16 or 8 KiB of B per k-block
   // Accumulators: 4 x 64 columns for up to 64 tokens; 2 x 256 columns in the
   // wide form (65..256 tokens), whose epilogue walks them 16 columns at a time.
   constexpr int kAccs = WIDE ? 2 : kNumAcc;
@@ -172,10 +205,12 @@ __global__ void __launch_bounds__(kThreads, 1)
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
   const int S = p.stages;
-  const int a_bytes = p.np * kStageK;
+  const int KG = p.kg;                     // k-blocks per stage
+  const int a_bytes = p.np * kStageK;      // A bytes per k-block
+  const int b_stage = KG * kBTileBytes, a_stage = KG * a_bytes;
   const uint32_t sB = smem_u32(smem);
-  const uint32_t sA = sB + S * kBTileBytes;
-  uint64_t* bars = reinterpret_cast<uint64_t*>(smem + S * (kBTileBytes + a_bytes));
+  const uint32_t sA = sB + S * b_stage;
+  uint64_t* bars = reinterpret_cast<uint64_t*>(smem + S * (b_stage + a_stage));
   const uint32_t bar0 = smem_u32(bars);
   auto full_bar = [&](int s) { return bar0 + 8u * s; };
   auto empty_bar = [&](int s) { return bar0 + 8u * (kMaxStages + s); };
@@ -194,20 +229,25 @@ __global__ void __launch_bounds__(kThreads, 1)
   // ---- producer state (thread 0).  The first ring's worth of loads is
   // issued right after the barriers exist, before the block-wide sync, so
   // that it overlaps TMEM allocation and the other warps' start-up.
-  const uint32_t tx = (uint32_t)(kBTileBytes + a_bytes);
+  const uint32_t tx = (uint32_t)(b_stage + a_stage);
   bool skip_once = (p.fault & kFaultSkipTmaOnce) && blockIdx.x == 0;
   int p_stage = 0;
   uint32_t p_phase = 0;
   long long p_u = u_begin;
   auto issue = [&](long long u, int stage) {
-    const int n = (int)(u / KB), kb = (int)(u % KB);
+    const int n = (int)(u / KB), g = (int)(u % KB);
     const uint32_t fb = full_bar(stage);
     mbar_arrive_expect_tx(fb, tx);
     if (skip_once) {
       skip_once = false;  // test-only: leave this stage's bytes missing
+    } else if (KG == 1) {
+      tma_load_2d(sB + stage * b_stage, &tmB, g * kBK, n * BM, fb);
+      tma_load_2d(sA + stage * a_stage, &tmA, g * kBK, 0, fb);
     } else {
-      tma_load_2d(sB + stage * kBTileBytes, &tmB, kb * kBK, n * BM, fb);
-      tma_load_2d(sA + stage * a_bytes, &tmA, kb * kBK, 0, fb);
+      // 3D views {k in block, row, k-block}: k-blocks g*KG .. g*KG+KG-1,
+      // those past K zero-filled
+      tma_load_3d(sB + stage * b_stage, &tmB, 0, n * BM, g * KG, fb);
+      tma_load_3d(sA + stage * a_stage, &tmA, 0, 0, g * KG, fb);
     }
   };
 
@@ -282,11 +322,13 @@ __global__ void __launch_bounds__(kThreads, 1)
             break;
           }
           tc_fence_after();
-          const uint64_t a0 = smem_desc_sw128(sB + stage * kBTileBytes);
-          const uint64_t b0 = smem_desc_sw128(sA + stage * a_bytes);
+          for (int j = 0; j < KG; ++j) {
+            const uint64_t a0 = smem_desc_sw128(sB + stage * b_stage + j * kBTileBytes);
+            const uint64_t b0 = smem_desc_sw128(sA + stage * a_stage + j * a_bytes);
 #pragma unroll
-          for (int k = 0; k < kMmaPerStage; ++k)
-            mma_issue<1, KIND>(d_tmem, a0 + 2 * k, b0 + 2 * k, idesc, (v != u || k != 0) ? 1u : 0u);
+            for (int k = 0; k < kMmaPerStage; ++k)
+              mma_issue<1, KIND>(d_tmem, a0 + 2 * k, b0 + 2 * k, idesc, (v != u || j != 0 || k != 0) ? 1u : 0u);
+          }
           mma_commit(empty_bar(stage));
           if (++stage == S) {
             stage = 0;
@@ -323,6 +365,29 @@ __global__ void __launch_bounds__(kThreads, 1)
       const long long n = u / KB;
       const long long seg_end = min(u_end, (n + 1) * KB);
       const bool whole = (u == n * KB) && (seg_end == (n + 1) * KB);
+      // Finisher of a tile in two parts with up to 32 tokens: the other
+      // part's partial is fetched into registers before this part's own
+      // accumulator is waited for.  The other part has fewer k-blocks (the
+      // skew) and usually lands first, so its hand-off (an acquire and a
+      // load from L2) leaves the tail of the kernel.
+      const bool early = !whole && p.np <= 32 && tile_parts(p, n) == 2 && c == tile_part_cta(p, n, 0);
+      float pre[32];
+      if (early) {
+        int* arrivals = p.counters + n * 4 + q;
+        if (!wait_parts(arrivals, 1, abort_flag, p.timeout_ns, p.status)) break;
+        const long long cc = tile_part_cta(p, n, 1);
+        const int sl = (n == cta_begin(p, cc) / KB) ? 0 : 1;
+        const float4* part = reinterpret_cast<const float4*>(partial_ptr<BM>(p, cc, sl, n_local));
+#pragma unroll
+        for (int v = 0; v < 8; ++v) {
+          float4 x = make_float4(0.0f, 0.0f, 0.0f, 0.0f);
+          if (row_lane && v * 4 < p.np) x = __ldcg(part + v);
+          pre[4 * v] = x.x;
+          pre[4 * v + 1] = x.y;
+          pre[4 * v + 2] = x.z;
+          pre[4 * v + 3] = x.w;
+        }
+      }
       if (!wait_bar(accf_bar(acc), acc_phase, abort_flag, p.timeout_ns, p.status, kRoleEpilogue)) break;
       tc_fence_after();
       float vals[64];
@@ -349,7 +414,12 @@ __global__ void __launch_bounds__(kThreads, 1)
 
       const int ng = (int)(n * BM) + n_local;
       bool finish = whole;
-      if (!whole) {
+      if (early) {
+        // parts in k order, as below: (0 + part 0) + part 1
+#pragma unroll
+        for (int t = 0; t < 32; ++t) vals[t] = (0.0f + vals[t]) + pre[t];
+        finish = true;
+      } else if (!whole) {
         // A split tile's parts.  Part 0 (the tile's first k-blocks) is
         // always the last segment of its CTA's range; every other part is the
         // only segment of its CTA or that CTA's first segment.  Part 0's CTA
@@ -371,29 +441,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         } else {
           // Wait (bounded) for the other nseg-1 parts.  They are segments no
           // CTA waits in front of, so this wait never chains into another.
-          int ok = 1;
-          if (lane == 0) {
-            if (ld_acquire_gpu(arrivals) != nseg - 1) {
-              const uint64_t t0 = globaltimer();
-              while (ld_acquire_gpu(arrivals) != nseg - 1) {
-                if (*abort_flag || globaltimer() - t0 > p.timeout_ns) {
-                  if (!*abort_flag) {
-                    *abort_flag = 1;
-                    if (atomicCAS(p.status, 0, kErrTimeout) == 0)
-                      atomicExch(p.status + 1, (kRoleFixup << 24) | (int)blockIdx.x);
-                  }
-                  ok = 0;
-                  break;
-                }
-                __nanosleep(32);
-              }
-            }
-            if (ok) *arrivals = 0;  // every part is in: ready for the next call
-          }
-          ok = __shfl_sync(0xffffffffu, ok, 0);
-          // lane 0's acquire is passed to the other lanes by the warp barrier
-          __syncwarp();
-          if (!ok) break;
+          if (!wait_parts(arrivals, nseg - 1, abort_flag, p.timeout_ns, p.status)) break;
           finish = true;
         }
         if (finish) {
@@ -496,29 +544,8 @@ __global__ void __launch_bounds__(kThreads, 1)
         const bool publish = !whole && c != c_first;
         const int slot = (n == first_tile) ? 0 : 1;
         int ok = 1;
-        if (!whole && !publish) {
-          // finisher: wait (bounded) for the other nseg-1 parts
-          if (lane == 0) {
-            if (ld_acquire_gpu(arrivals) != nseg - 1) {
-              const uint64_t t0 = globaltimer();
-              while (ld_acquire_gpu(arrivals) != nseg - 1) {
-                if (*abort_flag || globaltimer() - t0 > p.timeout_ns) {
-                  if (!*abort_flag) {
-                    *abort_flag = 1;
-                    if (atomicCAS(p.status, 0, kErrTimeout) == 0)
-                      atomicExch(p.status + 1, (kRoleFixup << 24) | (int)blockIdx.x);
-                  }
-                  ok = 0;
-                  break;
-                }
-                __nanosleep(32);
-              }
-            }
-            if (ok) *arrivals = 0;  // every part is in: ready for the next call
-          }
-          ok = __shfl_sync(0xffffffffu, ok, 0);
-          __syncwarp();
-        }
+        // finisher: wait (bounded) for the other nseg-1 parts
+        if (!whole && !publish) ok = wait_parts(arrivals, nseg - 1, abort_flag, p.timeout_ns, p.status);
         if (ok) {
           const float bias_n = (!publish && !plain && p.epi.bias && row_lane && ng < p.N) ? load_bias(p.epi, ng) : 0.0f;
 #pragma unroll 1
@@ -612,14 +639,46 @@ __global__ void __launch_bounds__(kThreads, 1)
 
 }  // namespace
 
-int skinny_stages(int np, int bm) { return stages_for(np, bm); }
+int skinny_stages(int np, int bm, int kg) { return stages_for(np, bm, kg); }
 
-int skinny_tile_rows(long long n, int max_grid) {
-  // 64-row tiles would avoid splitting a tile where they fill one wave, but
-  // measured they stream B slower (16 x 8192 x 8192: 41 us against 27 us with
-  // 128-row tiles split in two), so the automatic choice is 128 rows.
-  (void)n;
-  (void)max_grid;
+int skinny_kgroup(int np, int bm, long long K, int kbe, int kg_req) {
+  if (K % kbe) return 1;  // a partial last k-block needs the 2D map's zero fill at K
+  if (kg_req) return kg_req;
+  // Largest group that leaves 3 stages in the ring (measured on GB300,
+  // N = 4096..28672, K = 8192: within 1% of the best forced choice except
+  // for 128-row tiles in the wide form, where one k-block per stage is as
+  // fast or faster).
+  if (np > 64 && bm == 128) return 1;
+  int kg = 4;
+  while (kg > 1 && (stages_for(np, bm, kg) < 3 || kg > K / kbe)) kg /= 2;
+  return kg;
+}
+
+// Parts per tile of the equal-split mode for n columns of D in bm-row
+// tiles, or 0 where that mode does not apply (stream-K over the grid).
+static int equal_split(long long n, int bm, int sms) {
+  const long long tiles = (n + bm - 1) / bm;
+  if (tiles > sms) return 0;
+  const int s = sms / (int)tiles;
+  return 5 * tiles * s >= 4LL * sms ? s : 0;
+}
+
+int skinny_parts(long long n, int np, int max_grid) {
+  return equal_split(n, skinny_tile_rows(n, np, max_grid), max_grid);
+}
+
+int skinny_tile_rows(long long n, int np, int max_grid) {
+  // 64-row tiles stream B at the same rate as 128-row ones once their boxes
+  // hold several k-blocks, but carry twice the token bytes per weight byte;
+  // they pay where they cut the number of parts a tile is split into (each
+  // part adds a partial to write, wait for and add).  Measured on GB300 with
+  // K = 8192 (graph-replayed): at N = 8192, 64 tokens take 31.4 us on
+  // 128 whole 64-row tiles against 34.9 us on 64 tiles in two parts; at N =
+  // 4096, 24 tokens 19.5 against 21.9 us (two parts against four), while 8
+  // tokens stay faster on 128 rows (18.0 against 19.1 us).
+  const int s64 = equal_split(n, 64, max_grid), s128 = equal_split(n, 128, max_grid);
+  if (s64 >= 1 && np >= 48) return 64;
+  if (s64 >= 1 && np >= 32 && s128 >= 4) return 64;
   return 128;
 }
 
@@ -648,8 +707,11 @@ void skinny_partition(SkinnyParams* p, int num_sms, int grid_override, int skew_
     if (s >= 1 && s <= p->num_kb && 5 * p->n_tiles * s >= 4 * num_sms) {
       p->grid = p->n_tiles * s;
       p->split = s;
-      int skew = skew_kb > 0 ? skew_kb : (skew_kb < 0 ? 0 : p->num_kb / 64);
-      const int room = p->num_kb / s - 1;  // every part keeps at least one k-block
+      // skew in k-blocks (default K / 4096), rounded up to whole stages' k-groups
+      const int kg = p->kg > 0 ? p->kg : 1;
+      const int skew_blocks = skew_kb > 0 ? skew_kb : (skew_kb < 0 ? 0 : p->num_kb * kg / 64);
+      int skew = (skew_blocks + kg - 1) / kg;
+      const int room = p->num_kb / s - 1;  // every part keeps at least one k-group
       p->skew = skew < room ? skew : (room > 0 ? room : 0);
       return;
     }
@@ -667,7 +729,8 @@ cudaError_t launch_skinny(const CUtensorMap& tmA, const CUtensorMap& tmB, Skinny
   if (dev < 64 && !configured[dev]) {
     int worst = 0;
     for (int np = 16; np <= 256; np += 16)
-      for (int bm = 64; bm <= 128; bm += 64) worst = smem_for(np, bm) > worst ? smem_for(np, bm) : worst;
+      for (int bm = 64; bm <= 128; bm += 64)
+        for (int kg = 1; kg <= 4; kg *= 2) worst = smem_for(np, bm, kg) > worst ? smem_for(np, bm, kg) : worst;
     const void* kernels[8] = {(const void*)gemm_tn_skinny_kernel<kKindF16, 128, false>,
                               (const void*)gemm_tn_skinny_kernel<kKindF16, 64, false>,
                               (const void*)gemm_tn_skinny_kernel<kKindF8F6F4, 128, false>,
@@ -683,8 +746,9 @@ cudaError_t launch_skinny(const CUtensorMap& tmA, const CUtensorMap& tmB, Skinny
     configured[dev] = true;
   }
   if ((p.bm != 64 && p.bm != 128) || p.np < 16 || p.np > 256 || p.np % 16) return cudaErrorInvalidValue;
-  p.stages = stages_for(p.np, p.bm);
-  const int smem = smem_for(p.np, p.bm);
+  if ((p.kg != 1 && p.kg != 2 && p.kg != 4) || stages_for(p.np, p.bm, p.kg) < 2) return cudaErrorInvalidValue;
+  p.stages = stages_for(p.np, p.bm, p.kg);
+  const int smem = smem_for(p.np, p.bm, p.kg);
   if (info) {
     info->path = 3;
     info->grid = p.grid;

@@ -76,13 +76,15 @@ struct TileParams {
 struct SkinnyParams {
   int M, N, K;
   int np;              // M rounded up to 16 (MMA N), 16..64
-  int num_kb;          // ceil(K / 64)
-  int n_tiles;         // ceil(N / 128)
-  long long units;     // n_tiles * num_kb
+  int num_kb;          // k-groups per tile: ceil(ceil(K / k-block) / kg)
+  int kg;              // k-blocks per ring stage (1, 2 or 4); > 1 loads through 3D tensor maps
+                       //    {k in block, row, k-block} with one box of kg k-blocks per operand
+  int n_tiles;         // ceil(N / bm)
+  long long units;     // n_tiles * num_kb (one unit = one k-group of one tile)
   int grid;            // CTAs; each owns a contiguous range of units
   int split;           // 0: stream-K ranges over the grid; s >= 2: every tile in s parts,
                        //    CTA c holds part c / n_tiles of tile c % n_tiles
-  int skew;            // split mode: k-blocks moved from the last part to part 0
+  int skew;            // split mode: k-groups moved from the last part to part 0
   int stages;
   float alpha, beta;
   int has_c;
@@ -143,8 +145,16 @@ int skinny_max_grid(int np, int num_sms);
 // from p->n_tiles and p->num_kb.  grid_override > 0 forces a stream-K grid;
 // skew_kb: 0 = default, > 0 = that many k-blocks, < 0 = none.
 void skinny_partition(SkinnyParams* p, int num_sms, int grid_override, int skew_kb);
-int skinny_stages(int np, int bm);
-// Rows of B per skinny tile chosen automatically for n columns of D.
-int skinny_tile_rows(long long n, int max_grid);
+int skinny_stages(int np, int bm, int kg);
+// k-blocks per skinny ring stage for K (kbe elements per k-block): kg_req if
+// non-zero, else the largest of 4, 2, 1 that leaves 3 stages in the ring; 1
+// whenever K is not a whole number of k-blocks.
+int skinny_kgroup(int np, int bm, long long K, int kbe, int kg_req);
+// Rows of B per skinny tile chosen automatically for n columns of D and np
+// padded tokens.
+int skinny_tile_rows(long long n, int np, int max_grid);
+// k-parts per tile of the skinny kernel's automatic partition for n columns
+// of D (tiles of skinny_tile_rows rows), or 0 where it is stream-K.
+int skinny_parts(long long n, int np, int max_grid);
 
 }  // namespace gtn

@@ -19,7 +19,7 @@ from gpu_util import empty_out, from_dev, to_dev_bf16, to_dev_f32  # noqa: E402
 
 # M picks the kernel path: 48 -> skinny, 100 -> 1-SM tiled, 2200 -> 2-SM tiled
 # (with N at least 1040: more than 64 tiles of 128 x 256, so pair tiles)
-PATH_M = {"skinny": 48, "1sm": 100, "2sm": 2200}
+PATH_M = {"skinny": 24, "1sm": 100, "2sm": 2200}
 PATH_CODE = {"skinny": 3, "1sm": 1, "2sm": 2}
 
 
@@ -127,18 +127,26 @@ def test_bias_act_argument_errors():
 
 @pytest.mark.parametrize("act", [0, 1, 3])
 def test_wide_streaming_epilogue(act):
-    """176 tokens, K = 2048: the auto path is the streaming kernel's wide form."""
-    M, N, K = 176, 1040, 2048
+    """96 tokens against a 4096 x 4096 weight (32 MiB): the auto path is the
+    streaming kernel's wide form (64-row tiles, two k-parts each).  Checked on
+    every row at sampled columns, tile edges included."""
+    M, N, K = 96, 4096, 4096
     A = gi.draw_bf16(M, K, gi.Dist("int", -4, 4), 4600 + act)
     B = gi.draw_bf16(N, K, gi.Dist("int", -4, 4), 4610 + act)
     bias = gi.draw_bf16(N, 1, gi.Dist("int", -50, 50), 4620).reshape(N)
-    ref, absdot = oracle.gemm_ref(A, B)
     got = _run(M, N, K, A, B, bias, 0, act, gi.OUT_F32)
-    assert g.last_launch_info()["path"] == 3
+    assert g.last_launch_info()["path"] == 3 and g.last_launch_info()["tile_m"] == 64
+    cols_1 = sorted(set(np.random.default_rng(4630).integers(0, N, 200).tolist())
+                    | {0, 63, 64, 127, 128, N - 65, N - 64, N - 1})
+    rows = np.repeat(np.arange(M), len(cols_1))
+    cols = np.tile(np.array(cols_1), M)
+    ref, absdot = oracle.gemm_ref_sampled(A, B, rows, cols)
+    g_s = got[rows, cols]
     if act in (0, 1):
-        assert np.array_equal(got, oracle.exact_f32(oracle.epilogue(ref, bias, act)))
+        exp = oracle.exact_f32(oracle.epilogue(ref[None, :], bias[cols], act))[0]
+        assert np.array_equal(g_s, exp)
     else:
-        z = oracle.epilogue(ref, bias, 0)
-        fz = oracle.epilogue(ref, bias, act)
+        z = oracle.epilogue(ref[None, :], bias[cols], 0)[0]
+        fz = oracle.epilogue(ref[None, :], bias[cols], act)[0]
         bnd = oracle.bound_act(z, fz, absdot, gi.OUT_F32, act)
-        assert np.all(np.abs(got.astype(np.float64) - fz) <= bnd)
+        assert np.all(np.abs(g_s.astype(np.float64) - fz) <= bnd)

@@ -21,7 +21,7 @@ from gpu_util import empty_out, from_dev, sample_positions, to_dev_bf16, to_dev_
 
 # M picks the kernel path: 48 -> skinny, 100 -> 1-SM tiled, 2200 -> 2-SM tiled
 # (with N at least 1040: more than 64 tiles of 128 x 256, so pair tiles)
-PATH_M = {"skinny": 48, "1sm": 100, "2sm": 2200}
+PATH_M = {"skinny": 24, "1sm": 100, "2sm": 2200}
 PATH_CODE = {"skinny": 3, "1sm": 1, "2sm": 2}
 
 
@@ -61,7 +61,7 @@ def _run(M, N, K, A, B, fmt, out_dtype, scale_a=1.0, scale_b=1.0, alpha=1.0, bet
 
 @pytest.mark.parametrize("path", list(PATH_M))
 @pytest.mark.parametrize("fmt", FMTS)
-@pytest.mark.parametrize("N,K", [(520, 320), (264, 1040)])
+@pytest.mark.parametrize("N,K", [(520, 320), (264, 1040), (300, 1152)])
 def test_integer_exact(path, fmt, N, K):
     M, N = PATH_M[path], shape_n(path, N)
     A = gi.draw_fp8(M, K, gi.Dist("int", -4, 4), 5000 + fmt, fmt)
@@ -151,11 +151,17 @@ def test_fp8_argument_errors():
 
 @pytest.mark.parametrize("fmt", FMTS)
 def test_wide_streaming_integer_exact(fmt):
-    """144 tokens, K = 2048: the streaming kernel's wide form on fp8 inputs."""
-    M, N, K = 144, 648, 2048
+    """96 tokens against an 8192 x 4096 fp8 weight (32 MiB): the auto path is the
+    streaming kernel's wide form (128 whole 64-row tiles).  Every row at
+    sampled columns, tile edges included."""
+    M, N, K = 96, 8192, 4096
     A = gi.draw_fp8(M, K, gi.Dist("int", -4, 4), 5500 + fmt, fmt)
     B = gi.draw_fp8(N, K, gi.Dist("int", -4, 4), 5510 + fmt, fmt)
-    ref, _ = oracle.gemm_ref_fp8(A, B, fmt)
     got = _run(M, N, K, A, B, fmt, gi.OUT_F32)
-    assert g.last_launch_info()["path"] == 3
-    assert np.array_equal(got, oracle.exact_f32(ref))
+    assert g.last_launch_info()["path"] == 3 and g.last_launch_info()["tile_m"] == 64
+    cols_1 = sorted(set(np.random.default_rng(5520 + fmt).integers(0, N, 200).tolist())
+                    | {0, 63, 64, 127, 128, N - 65, N - 64, N - 1})
+    rows = np.repeat(np.arange(M), len(cols_1))
+    cols = np.tile(np.array(cols_1), M)
+    ref, _ = oracle.gemm_ref_fp8_sampled(A, B, fmt, rows, cols)
+    assert np.array_equal(got[rows, cols], oracle.exact_f32(ref))

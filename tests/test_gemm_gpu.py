@@ -36,7 +36,7 @@ def up8(x):
 
 
 def run_int(M, N, K, path, out_dtype, seed, lda=None, ldb=None, grid=0, skinny_grid=0, alpha=1.0,
-            disable_pdl=0, scheduler=0, skinny_bm=0):
+            disable_pdl=0, scheduler=0, skinny_bm=0, skinny_kgroup=0):
     lda = up8(K) if lda is None else lda
     ldb = up8(K) if ldb is None else ldb
     A = gi.draw_bf16(M, K, gi.Dist("int", -4, 4), seed, ld=lda)
@@ -46,7 +46,7 @@ def run_int(M, N, K, path, out_dtype, seed, lda=None, ldb=None, grid=0, skinny_g
     dD, ldd = empty_out(M, N, out_dtype, ld=up8(N))
     rc, st = call(M, N, K, dA, lda, dB, ldb, None, 0, dD, ldd, alpha, 0.0, out_dtype, path=path,
                   grid=grid, skinny_grid=skinny_grid, disable_pdl=disable_pdl, scheduler=scheduler,
-                  skinny_bm=skinny_bm)
+                  skinny_bm=skinny_bm, skinny_kgroup=skinny_kgroup)
     assert rc == 0, g.last_error()
     assert st == 0, g.last_error()
     return from_dev(dD, out_dtype)[:, :N], expect_exact(ref, out_dtype)
@@ -129,6 +129,71 @@ def test_decode_shape_launch():
     assert_same(got, exp)
     info = g.last_launch_info()
     assert info["tile_m"] == 64 and info["grid"] == 128      # 128 whole 64-row tiles, one per CTA
+
+
+KGROUP_SHAPES = [(16, 1000, 640), (1, 300, 1344), (64, 260, 4160), (33, 8192, 256), (16, 129, 64),
+                 (7, 520, 1000)]
+
+
+@pytest.mark.parametrize("shape", KGROUP_SHAPES)
+@pytest.mark.parametrize("bm", [64, 128])
+@pytest.mark.parametrize("kg", [1, 2, 4])
+def test_skinny_kgroups(shape, bm, kg):
+    """kg k-blocks per ring stage, loaded as one 3D box per operand.  K = 640,
+    1344 and 4160 leave the last group short (its missing k-blocks are
+    zero-filled); K = 1000 is not a whole number of k-blocks, so the path
+    falls back to one k-block per stage."""
+    M, N, K = shape
+    got, exp = run_int(M, N, K, PS, gi.OUT_BF16, seed=330 + M + 7 * N + K + bm + kg, skinny_bm=bm,
+                       skinny_kgroup=kg)
+    assert_same(got, exp)
+
+
+@pytest.mark.parametrize("kg", [2, 4])
+@pytest.mark.parametrize("bm", [64, 128])
+def test_skinny_kgroups_padded_leading_dims(kg, bm):
+    got, exp = run_int(40, 270, 640, PS, gi.OUT_F32, seed=340 + kg + bm, lda=704, ldb=768, skinny_bm=bm,
+                       skinny_kgroup=kg)
+    assert_same(got, exp)
+
+
+@pytest.mark.parametrize("bm", [64, 128])
+def test_skinny_kgroups_wide(bm):
+    """144 tokens with two k-blocks per stage (forced; automatic keeps one here)."""
+    got, exp = run_int(144, 700, 1344, PS, gi.OUT_BF16, seed=350 + bm, skinny_bm=bm, skinny_kgroup=2)
+    assert_same(got, exp)
+
+
+def test_skinny_kgroups_too_large_for_the_ring():
+    M, N, K = 144, 256, 1024
+    dA, dB = to_dev_bf16(np.zeros((M, K), np.uint16)), to_dev_bf16(np.zeros((N, K), np.uint16))
+    dD, ldd = empty_out(M, N, gi.OUT_BF16)
+    rc, _ = call(M, N, K, dA, K, dB, K, None, 0, dD, ldd, 1.0, 0.0, gi.OUT_BF16, path=PS, skinny_bm=128,
+                 skinny_kgroup=4)
+    assert rc == g.GEMM_ERR_INVALID_VALUE and "ring stages" in g.last_error()
+
+
+@pytest.mark.parametrize("M", [1, 17, 32])
+@pytest.mark.parametrize("out_dtype", [gi.OUT_F32, gi.OUT_BF16])
+def test_skinny_two_part_tiles(M, out_dtype):
+    """N = 8192 splits each 128-row tile in two k-parts (128 CTAs); with up to
+    32 tokens the finisher fetches the other part's partial before its own
+    accumulator is ready."""
+    got, exp = run_int(M, 8192, 1088, PS, out_dtype, seed=360 + M)
+    assert_same(got, exp)
+    info = g.last_launch_info()
+    assert info["grid"] == 128 and info["tile_m"] == 128
+
+
+@pytest.mark.parametrize("M,N,tile_m,grid", [(64, 8192, 64, 128), (48, 8192, 64, 128), (32, 8192, 128, 128),
+                                             (24, 4096, 64, 128), (8, 4096, 128, 128), (64, 16384, 128, 128),
+                                             (128, 4096, 64, 128)])
+def test_skinny_automatic_tile_rows(M, N, tile_m, grid):
+    """64-row tiles where they fit one wave and cut the parts per tile, else 128 rows."""
+    got, exp = run_int(M, N, 2048, PS, gi.OUT_BF16, seed=370 + M + N)
+    assert_same(got, exp)
+    info = g.last_launch_info()
+    assert (info["tile_m"], info["grid"]) == (tile_m, grid), info
 
 
 WIDE_SHAPES = [(65, 300, 256), (80, 1000, 640), (128, 520, 2048), (200, 130, 1000), (256, 384, 300),
