@@ -114,8 +114,9 @@ typedef struct gemm_tn_config {
   int test_fault;           /* tests only: 1 = the producer of CTA 0 drops one stage's loads,
                                so the consumer's bounded wait must expire (GEMM_ERR_TIMEOUT) */
   int disable_pdl;          /* 1 = launch without programmatic dependent launch (see below) */
-  int skinny_skew_kb;       /* skinny path, equal-split mode: k-blocks (of 64) moved to the part that
-                               finishes each tile; 0 = default (K/4096), < 0 = none */
+  int skinny_skew_kb;       /* skinny path, equal-split mode: k-blocks (of 64 bf16 or 128 fp8 elements)
+                               moved to the part that finishes each tile, rounded up to whole k-groups;
+                               0 = default (M rounded up to 16, divided by 4), < 0 = none */
   int scheduler;            /* tiled paths: GEMM_SCHED_* (0 = the default) */
   int skinny_bm;            /* skinny path: rows of B per tile (MMA M), 64 or 128; 0 = auto: 64 where
                                64-row tiles fit one wave and M > 32 (or M > 16 and 128-row tiles would
@@ -212,6 +213,18 @@ int gemm_fp8_tn(int64_t M, int64_t N, int64_t K,
                 const void *C, int64_t ldc,
                 void *D, int64_t ldd,
                 float alpha, float beta, int out_dtype, void *stream);
+
+/* gemm_fp8_tn with explicit overrides (gemm_tn_config, as for
+ * gemm_bf16_tn_ex); cfg may be NULL (= gemm_fp8_tn).  Skew and k-groups count
+ * k-blocks of 128 fp8 elements. */
+int gemm_fp8_tn_ex(int64_t M, int64_t N, int64_t K,
+                   const void *A, int64_t lda,
+                   const void *B, int64_t ldb,
+                   int fp8_format, float scale_a, float scale_b,
+                   const void *C, int64_t ldc,
+                   void *D, int64_t ldd,
+                   float alpha, float beta, int out_dtype, void *stream,
+                   const gemm_tn_config *cfg);
 
 /* One GEMM of a grouped call: D = alpha * A * B^T + beta * C with this
  * problem's own sizes, pointers and leading dimensions (the rules of

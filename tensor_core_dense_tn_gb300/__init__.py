@@ -37,8 +37,8 @@ GEMM_ERR_CUDA = -8
 
 EXPORTED = ["gemm_bf16_tn", "gemm_bf16_tn_ex", "gemm_get_status", "gemm_get_status_detail",
             "gemm_last_error_string", "gemm_last_launch_info", "gemm_shutdown", "gemm_version",
-            "gemm_bf16_tn_skinny_noalloc", "gemm_bf16_tn_bias_act", "gemm_fp8_tn", "gemm_bf16_tn_grouped",
-            "gemm_bf16_tn_batched"]
+            "gemm_bf16_tn_skinny_noalloc", "gemm_bf16_tn_bias_act", "gemm_fp8_tn", "gemm_fp8_tn_ex",
+            "gemm_bf16_tn_grouped", "gemm_bf16_tn_batched"]
 
 FP8_E4M3, FP8_E5M2 = 0, 1
 SCHED_DEFAULT, SCHED_STATIC, SCHED_CLC = 0, 1, 2
@@ -98,6 +98,8 @@ def load(path: str = LIB_PATH):
         lib.gemm_fp8_tn.argtypes = [i64, i64, i64, vp, i64, vp, i64, i32, f32, f32, vp, i64, vp, i64,
                                     f32, f32, i32, vp]
         lib.gemm_fp8_tn.restype = i32
+        lib.gemm_fp8_tn_ex.argtypes = lib.gemm_fp8_tn.argtypes + [ctypes.POINTER(GemmConfig)]
+        lib.gemm_fp8_tn_ex.restype = i32
         lib.gemm_bf16_tn_bias_act.argtypes = args[:-1] + [vp, i32, i32, vp]
         lib.gemm_bf16_tn_bias_act.restype = i32
         lib.gemm_bf16_tn_skinny_noalloc.argtypes = args
@@ -179,6 +181,14 @@ def gemm_fp8_tn(M, N, K, A, lda, B, ldb, fp8_format, scale_a, scale_b, C, ldc, D
     """Raw C-ABI call: D = alpha * scale_a * scale_b * A B^T + beta * C, fp8 A and B."""
     return load().gemm_fp8_tn(M, N, K, A, lda, B, ldb, fp8_format, scale_a, scale_b, C or None, ldc, D,
                               ldd, alpha, beta, out_dtype, stream or None)
+
+
+def gemm_fp8_tn_ex(M, N, K, A, lda, B, ldb, fp8_format, scale_a, scale_b, C, ldc, D, ldd, alpha, beta,
+                   out_dtype, stream, config=None) -> int:
+    """gemm_fp8_tn with a GemmConfig of overrides (None = library defaults)."""
+    cfg = ctypes.byref(config) if config is not None else None
+    return load().gemm_fp8_tn_ex(M, N, K, A, lda, B, ldb, fp8_format, scale_a, scale_b, C or None, ldc, D,
+                                 ldd, alpha, beta, out_dtype, stream or None, cfg)
 
 
 def gemm_get_status(stream=None) -> int:

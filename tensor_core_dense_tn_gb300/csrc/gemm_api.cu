@@ -665,14 +665,21 @@ int gemm_bf16_tn_bias_act(int64_t M, int64_t N, int64_t K, const void* A, int64_
   return run(M, N, K, A, lda, B, ldb, C, ldc, D, ldd, alpha, beta, out_dtype, stream, nullptr, epi);
 }
 
-int gemm_fp8_tn(int64_t M, int64_t N, int64_t K, const void* A, int64_t lda, const void* B, int64_t ldb,
-                int fp8_format, float scale_a, float scale_b, const void* C, int64_t ldc, void* D, int64_t ldd,
-                float alpha, float beta, int out_dtype, void* stream) {
+int gemm_fp8_tn_ex(int64_t M, int64_t N, int64_t K, const void* A, int64_t lda, const void* B, int64_t ldb,
+                   int fp8_format, float scale_a, float scale_b, const void* C, int64_t ldc, void* D, int64_t ldd,
+                   float alpha, float beta, int out_dtype, void* stream, const gemm_tn_config* cfg) {
   using namespace gtn;
   if (fp8_format != GEMM_FP8_E4M3 && fp8_format != GEMM_FP8_E5M2)
     return fail(GEMM_ERR_INVALID_VALUE, "fp8_format must be 0 (e4m3) or 1 (e5m2), got %d", fp8_format);
-  return run(M, N, K, A, lda, B, ldb, C, ldc, D, ldd, alpha * scale_a * scale_b, beta, out_dtype, stream, nullptr,
+  return run(M, N, K, A, lda, B, ldb, C, ldc, D, ldd, alpha * scale_a * scale_b, beta, out_dtype, stream, cfg,
              Epilogue{nullptr, 0, kActNone}, kInFp8, fp8_format);
+}
+
+int gemm_fp8_tn(int64_t M, int64_t N, int64_t K, const void* A, int64_t lda, const void* B, int64_t ldb,
+                int fp8_format, float scale_a, float scale_b, const void* C, int64_t ldc, void* D, int64_t ldd,
+                float alpha, float beta, int out_dtype, void* stream) {
+  return gemm_fp8_tn_ex(M, N, K, A, lda, B, ldb, fp8_format, scale_a, scale_b, C, ldc, D, ldd, alpha, beta,
+                        out_dtype, stream, nullptr);
 }
 
 int gemm_get_status(void* stream) {

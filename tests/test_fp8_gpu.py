@@ -165,3 +165,26 @@ def test_wide_streaming_integer_exact(fmt):
     cols = np.tile(np.array(cols_1), M)
     ref, _ = oracle.gemm_ref_fp8_sampled(A, B, fmt, rows, cols)
     assert np.array_equal(got[rows, cols], oracle.exact_f32(ref))
+
+
+@pytest.mark.parametrize("path,bm,kg", [(1, 0, 0), (2, 0, 0), (3, 64, 1), (3, 64, 4), (3, 128, 2), (3, 128, 4)])
+@pytest.mark.parametrize("fmt", FMTS)
+def test_forced_path_and_kgroups(path, bm, kg, fmt):
+    """gemm_fp8_tn_ex: every path, tile height and k-group on one shape whose
+    K = 1408 is 11 k-blocks of 128 (the last group partly zero-filled)."""
+    import torch
+    M, N, K = 40, 648, 1408
+    A = gi.draw_fp8(M, K, gi.Dist("int", -4, 4), 5600 + fmt, fmt)
+    B = gi.draw_fp8(N, K, gi.Dist("int", -4, 4), 5610 + fmt, fmt)
+    ref, _ = oracle.gemm_ref_fp8(A, B, fmt)
+    dA, dB = to_dev_u8(A), to_dev_u8(B)
+    dD, ldd = empty_out(M, N, gi.OUT_F32)
+    s = torch.cuda.current_stream().cuda_stream
+    cfg = g.GemmConfig(path=path, skinny_bm=bm, skinny_kgroup=kg)
+    rc = g.gemm_fp8_tn_ex(M, N, K, dA.data_ptr(), K, dB.data_ptr(), K, fmt, 1.0, 1.0, 0, 0,
+                          dD.data_ptr(), ldd, 1.0, 0.0, gi.OUT_F32, s, cfg)
+    assert rc == 0, g.last_error()
+    assert g.gemm_get_status(s) == 0, g.last_error()
+    info = g.last_launch_info()
+    assert info["path"] == path and (bm == 0 or info["tile_m"] == bm)
+    assert np.array_equal(from_dev(dD, gi.OUT_F32), oracle.exact_f32(ref))
