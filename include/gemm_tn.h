@@ -214,6 +214,31 @@ int gemm_fp8_tn(int64_t M, int64_t N, int64_t K,
                 void *D, int64_t ldd,
                 float alpha, float beta, int out_dtype, void *stream);
 
+/* What a call would run, computed on the host without any device access:
+ * for capacity planning, and so that the automatic choices can be tested
+ * without a GPU.  The fields describe the path and, for the skinny path, its
+ * geometry and work split; gemm_last_launch_info reports the same values
+ * after a real launch. */
+typedef struct gemm_plan_info {
+  int path;           /* gemm_path the call would take (0 if M or N is 0: no launch) */
+  int tile_m;         /* skinny: rows of B per tile (64 or 128); tiled: 128 (1SM) or 256 (2SM pair) */
+  int tile_n;         /* skinny: M rounded up to 16 (MMA N); tiled: 256 */
+  int skinny_kgroup;  /* skinny: k-blocks per ring stage (one TMA box per operand); else 0 */
+  int skinny_stages;  /* skinny: ring stages; else 0 */
+  int skinny_grid;    /* skinny: CTAs; else 0 */
+  int skinny_parts;   /* skinny: k-parts per tile in the equal split; 0 = stream-K ranges or not skinny */
+  int skinny_skew;    /* skinny, equal split: k-groups moved to the part that finishes each tile */
+} gemm_plan_info;
+
+/* Plan D = A * B^T for M x N x K on a GPU with num_sms SMs (152 on a
+ * GB300), with bf16 (fp8_inputs = 0) or fp8 (fp8_inputs = 1) operands and
+ * the overrides in cfg (may be NULL).  Writes *out and returns GEMM_OK;
+ * GEMM_ERR_INVALID_VALUE for negative sizes, num_sms < 1, out == NULL or an
+ * invalid cfg; GEMM_ERR_NOT_IMPLEMENTED where the launch would refuse the
+ * forced path. */
+int gemm_plan(int64_t M, int64_t N, int64_t K, int fp8_inputs, int num_sms, const gemm_tn_config *cfg,
+              gemm_plan_info *out);
+
 /* gemm_fp8_tn with explicit overrides (gemm_tn_config, as for
  * gemm_bf16_tn_ex); cfg may be NULL (= gemm_fp8_tn).  Skew and k-groups count
  * k-blocks of 128 fp8 elements. */

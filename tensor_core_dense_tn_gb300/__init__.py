@@ -38,7 +38,7 @@ GEMM_ERR_CUDA = -8
 EXPORTED = ["gemm_bf16_tn", "gemm_bf16_tn_ex", "gemm_get_status", "gemm_get_status_detail",
             "gemm_last_error_string", "gemm_last_launch_info", "gemm_shutdown", "gemm_version",
             "gemm_bf16_tn_skinny_noalloc", "gemm_bf16_tn_bias_act", "gemm_fp8_tn", "gemm_fp8_tn_ex",
-            "gemm_bf16_tn_grouped", "gemm_bf16_tn_batched"]
+            "gemm_bf16_tn_grouped", "gemm_bf16_tn_batched", "gemm_plan"]
 
 FP8_E4M3, FP8_E5M2 = 0, 1
 SCHED_DEFAULT, SCHED_STATIC, SCHED_CLC = 0, 1, 2
@@ -58,6 +58,15 @@ class GemmConfig(ctypes.Structure):
                 ("test_fault", ctypes.c_int), ("disable_pdl", ctypes.c_int),
                 ("skinny_skew_kb", ctypes.c_int), ("scheduler", ctypes.c_int), ("skinny_bm", ctypes.c_int),
                 ("skinny_kgroup", ctypes.c_int)]
+
+
+class GemmPlanInfo(ctypes.Structure):
+    _fields_ = [("path", ctypes.c_int), ("tile_m", ctypes.c_int), ("tile_n", ctypes.c_int),
+                ("skinny_kgroup", ctypes.c_int), ("skinny_stages", ctypes.c_int), ("skinny_grid", ctypes.c_int),
+                ("skinny_parts", ctypes.c_int), ("skinny_skew", ctypes.c_int)]
+
+    def as_dict(self):
+        return {f: getattr(self, f) for f, _ in self._fields_}
 
 
 class GemmProblem(ctypes.Structure):
@@ -100,6 +109,8 @@ def load(path: str = LIB_PATH):
         lib.gemm_fp8_tn.restype = i32
         lib.gemm_fp8_tn_ex.argtypes = lib.gemm_fp8_tn.argtypes + [ctypes.POINTER(GemmConfig)]
         lib.gemm_fp8_tn_ex.restype = i32
+        lib.gemm_plan.argtypes = [i64, i64, i64, i32, i32, ctypes.POINTER(GemmConfig), ctypes.POINTER(GemmPlanInfo)]
+        lib.gemm_plan.restype = i32
         lib.gemm_bf16_tn_bias_act.argtypes = args[:-1] + [vp, i32, i32, vp]
         lib.gemm_bf16_tn_bias_act.restype = i32
         lib.gemm_bf16_tn_skinny_noalloc.argtypes = args
@@ -189,6 +200,14 @@ def gemm_fp8_tn_ex(M, N, K, A, lda, B, ldb, fp8_format, scale_a, scale_b, C, ldc
     cfg = ctypes.byref(config) if config is not None else None
     return load().gemm_fp8_tn_ex(M, N, K, A, lda, B, ldb, fp8_format, scale_a, scale_b, C or None, ldc, D,
                                  ldd, alpha, beta, out_dtype, stream or None, cfg)
+
+
+def gemm_plan(M, N, K, fp8_inputs=0, num_sms=152, config=None):
+    """Host-only plan of a call: (status, dict of GemmPlanInfo fields)."""
+    out = GemmPlanInfo()
+    cfg = ctypes.byref(config) if config is not None else None
+    rc = load().gemm_plan(M, N, K, fp8_inputs, num_sms, cfg, ctypes.byref(out))
+    return rc, out.as_dict()
 
 
 def gemm_get_status(stream=None) -> int:

@@ -240,6 +240,57 @@ long long one_sm_tiles(int64_t M, int64_t N) { return ((M + 127) / 128) * ((N + 
 //   against 56.6 us); with B in L2 the 1-SM kernel's lighter launch wins.
 constexpr int64_t kStreamedBytes = 32ll << 20;
 
+// Values of a gemm_tn_config that select among fixed choices.
+int check_config(const gemm_tn_config* cfg) {
+  if (!cfg) return GEMM_OK;
+  if (cfg->path < GEMM_PATH_AUTO || cfg->path > GEMM_PATH_SKINNY)
+    return fail(GEMM_ERR_INVALID_VALUE, "unknown path %d", cfg->path);
+  const int sched = cfg->scheduler;
+  if (sched != GEMM_SCHED_DEFAULT && sched != GEMM_SCHED_STATIC && sched != GEMM_SCHED_CLC)
+    return fail(GEMM_ERR_INVALID_VALUE, "unknown scheduler %d", sched);
+  if (cfg->skinny_bm != 0 && cfg->skinny_bm != 64 && cfg->skinny_bm != 128)
+    return fail(GEMM_ERR_INVALID_VALUE, "skinny_bm must be 0, 64 or 128, got %d", cfg->skinny_bm);
+  const int kg = cfg->skinny_kgroup;
+  if (kg != 0 && kg != 1 && kg != 2 && kg != 4)
+    return fail(GEMM_ERR_INVALID_VALUE, "skinny_kgroup must be 0, 1, 2 or 4, got %d", kg);
+  return GEMM_OK;
+}
+
+// Automatic path for a shape on `sms` SMs (host only; rules above).
+int auto_path(int64_t M, int64_t N, int64_t K, int in_bytes, int sms) {
+  if (K == 0) return GEMM_PATH_1SM;
+  const bool streamed = N * K * in_bytes >= kStreamedBytes;
+  const int np = (int)((M + 15) / 16) * 16;
+  const int parts = M <= 256 ? skinny_parts(N, np, skinny_max_grid(np, sms)) : 0;
+  const long long tiles = one_sm_tiles(M, N);
+  if (M <= 32) return GEMM_PATH_SKINNY;
+  if (M <= 128 && streamed && parts >= 1 && parts <= 2) return GEMM_PATH_SKINNY;
+  if (M > 128 && (streamed || tiles > kSmallTileCount)) return GEMM_PATH_2SM;
+  if (M <= 128 && streamed && 2 * tiles <= sms) return GEMM_PATH_2SM;
+  return GEMM_PATH_1SM;
+}
+
+// Skinny-path geometry and work partition (host only): tile rows, k-group,
+// k-groups per tile, tiles, units, grid, split and skew.  Config overrides
+// were validated by the caller.
+int skinny_geometry(SkinnyParams* p, int64_t M, int64_t N, int64_t K, int kbe, int sms, const gemm_tn_config* cfg) {
+  const int np = (int)((M + 15) / 16) * 16;
+  p->M = (int)M; p->N = (int)N; p->K = (int)K; p->np = np;
+  const int max_grid = skinny_max_grid(np, sms);
+  const int bm_req = cfg ? cfg->skinny_bm : 0, kg_req = cfg ? cfg->skinny_kgroup : 0;
+  p->bm = bm_req ? bm_req : skinny_tile_rows(N, np, max_grid);
+  p->kg = skinny_kgroup(np, p->bm, K, kbe, kg_req);
+  if (skinny_stages(np, p->bm, p->kg) < 2)
+    return fail(GEMM_ERR_INVALID_VALUE, "skinny_kgroup %d leaves fewer than 2 ring stages at M = %lld", p->kg,
+                (long long)M);
+  p->stages = skinny_stages(np, p->bm, p->kg);
+  p->num_kb = (int)(((K + kbe - 1) / kbe + p->kg - 1) / p->kg);
+  p->n_tiles = (int)((N + p->bm - 1) / p->bm);
+  p->units = (long long)p->n_tiles * p->num_kb;
+  skinny_partition(p, max_grid, cfg ? cfg->skinny_grid : 0, cfg ? cfg->skinny_skew_kb : 0);
+  return GEMM_OK;
+}
+
 // Tiles along M per raster strip: keep the strip's A rows within ~32 MiB of
 // L2, so that the strip is re-read from L2 for every tile column it meets.
 int raster_group_for(int tile_m, int64_t K, int in_bytes, int tiles_m) {
@@ -277,22 +328,14 @@ int run(int64_t M, int64_t N, int64_t K, const void* A, int64_t lda, const void*
     return fail(GEMM_ERR_INVALID_VALUE, "out_dtype must be 0 (bf16) or 1 (fp32), got %d", out_dtype);
   if (M < 0 || N < 0 || K < 0) return fail(GEMM_ERR_INVALID_VALUE, "negative size M=%lld N=%lld K=%lld",
                                            (long long)M, (long long)N, (long long)K);
+  int rc = check_config(cfg);
+  if (rc != GEMM_OK) return rc;
   const int path_req = cfg ? cfg->path : GEMM_PATH_AUTO;
-  if (path_req < GEMM_PATH_AUTO || path_req > GEMM_PATH_SKINNY)
-    return fail(GEMM_ERR_INVALID_VALUE, "unknown path %d", path_req);
   const int sched = cfg ? cfg->scheduler : GEMM_SCHED_DEFAULT;
-  if (sched != GEMM_SCHED_DEFAULT && sched != GEMM_SCHED_STATIC && sched != GEMM_SCHED_CLC)
-    return fail(GEMM_ERR_INVALID_VALUE, "unknown scheduler %d", sched);
-  const int bm_req = cfg ? cfg->skinny_bm : 0;
-  if (bm_req != 0 && bm_req != 64 && bm_req != 128)
-    return fail(GEMM_ERR_INVALID_VALUE, "skinny_bm must be 0, 64 or 128, got %d", bm_req);
-  const int kg_req = cfg ? cfg->skinny_kgroup : 0;
-  if (kg_req != 0 && kg_req != 1 && kg_req != 2 && kg_req != 4)
-    return fail(GEMM_ERR_INVALID_VALUE, "skinny_kgroup must be 0, 1, 2 or 4, got %d", kg_req);
   if (M == 0 || N == 0) return GEMM_OK;
   const bool has_c = (beta != 0.0f);
   const int esize = out_dtype == GEMM_OUT_F32 ? 4 : 2;
-  int rc = check_operands(M, N, K, A, lda, B, ldb, C, ldc, D, ldd, has_c, esize, in_bytes);
+  rc = check_operands(M, N, K, A, lda, B, ldb, C, ldc, D, ldd, has_c, esize, in_bytes);
   if (rc != GEMM_OK) return rc;
 
   int dev = 0;
@@ -301,21 +344,7 @@ int run(int64_t M, int64_t N, int64_t K, const void* A, int64_t lda, const void*
   if (rc != GEMM_OK) return rc;
 
   // ---- path
-  int path = path_req;
-  if (path == GEMM_PATH_AUTO) {
-    if (K == 0) path = GEMM_PATH_1SM;
-    else {
-      const bool streamed = N * K * in_bytes >= kStreamedBytes;
-      const int np = (int)((M + 15) / 16) * 16;
-      const int parts = skinny_parts(N, np, skinny_max_grid(np, st->sms));
-      const long long tiles = one_sm_tiles(M, N);
-      if (M <= 32) path = GEMM_PATH_SKINNY;
-      else if (M <= 128 && streamed && parts >= 1 && parts <= 2) path = GEMM_PATH_SKINNY;
-      else if (M > 128 && (streamed || tiles > kSmallTileCount)) path = GEMM_PATH_2SM;
-      else if (M <= 128 && streamed && 2 * tiles <= st->sms) path = GEMM_PATH_2SM;
-      else path = GEMM_PATH_1SM;
-    }
-  }
+  const int path = path_req == GEMM_PATH_AUTO ? auto_path(M, N, K, in_bytes, st->sms) : path_req;
   if (path == GEMM_PATH_SKINNY && (M > 256 || K == 0))
     return fail(GEMM_ERR_NOT_IMPLEMENTED, "skinny path needs 1 <= M <= 256 and K > 0");
 
@@ -330,20 +359,10 @@ int run(int64_t M, int64_t N, int64_t K, const void* A, int64_t lda, const void*
   if (path == GEMM_PATH_SKINNY) {
     const int np = (int)((M + 15) / 16) * 16;
     SkinnyParams p = {};
-    p.M = (int)M; p.N = (int)N; p.K = (int)K; p.np = np;
-    const int max_grid = skinny_max_grid(np, st->sms);
-    p.bm = bm_req ? bm_req : skinny_tile_rows(N, np, max_grid);
-    p.kg = skinny_kgroup(np, p.bm, K, kbe, kg_req);
-    if (skinny_stages(np, p.bm, p.kg) < 2)
-      return fail(GEMM_ERR_INVALID_VALUE, "skinny_kgroup %d leaves fewer than 2 ring stages at M = %lld", p.kg,
-                  (long long)M);
-    p.num_kb = (int)(((K + kbe - 1) / kbe + p.kg - 1) / p.kg);
-    p.n_tiles = (int)((N + p.bm - 1) / p.bm);
+    if ((rc = skinny_geometry(&p, M, N, K, kbe, st->sms, cfg))) return rc;
     p.kind = in_kind;
     p.a_fmt = fp8_format;
     p.b_fmt = fp8_format;
-    p.units = (long long)p.n_tiles * p.num_kb;
-    skinny_partition(&p, max_grid, cfg ? cfg->skinny_grid : 0, cfg ? cfg->skinny_skew_kb : 0);
     const int grid = p.grid;
     p.alpha = alpha; p.beta = beta; p.has_c = has_c; p.epi = epi;
     p.C = C; p.ldc = ldc; p.D = D; p.ldd = ldd; p.out_f32 = out_dtype == GEMM_OUT_F32;
@@ -680,6 +699,43 @@ int gemm_fp8_tn(int64_t M, int64_t N, int64_t K, const void* A, int64_t lda, con
                 float alpha, float beta, int out_dtype, void* stream) {
   return gemm_fp8_tn_ex(M, N, K, A, lda, B, ldb, fp8_format, scale_a, scale_b, C, ldc, D, ldd, alpha, beta,
                         out_dtype, stream, nullptr);
+}
+
+int gemm_plan(int64_t M, int64_t N, int64_t K, int fp8_inputs, int num_sms, const gemm_tn_config* cfg,
+              gemm_plan_info* out) {
+  using namespace gtn;
+  t_error.clear();
+  if (!out) return fail(GEMM_ERR_INVALID_VALUE, "out is NULL");
+  *out = gemm_plan_info{};
+  if (M < 0 || N < 0 || K < 0) return fail(GEMM_ERR_INVALID_VALUE, "negative size");
+  if (num_sms < 1) return fail(GEMM_ERR_INVALID_VALUE, "num_sms must be at least 1, got %d", num_sms);
+  if (fp8_inputs != 0 && fp8_inputs != 1) return fail(GEMM_ERR_INVALID_VALUE, "fp8_inputs must be 0 or 1");
+  int rc = check_config(cfg);
+  if (rc != GEMM_OK) return rc;
+  if (M == 0 || N == 0) return GEMM_OK;
+  const int in_bytes = fp8_inputs ? 1 : 2;
+  const int path_req = cfg ? cfg->path : GEMM_PATH_AUTO;
+  const int path = path_req == GEMM_PATH_AUTO ? auto_path(M, N, K, in_bytes, num_sms) : path_req;
+  if (path == GEMM_PATH_SKINNY && (M > 256 || K == 0))
+    return fail(GEMM_ERR_NOT_IMPLEMENTED, "skinny path needs 1 <= M <= 256 and K > 0");
+  out->path = path;
+  if (path == GEMM_PATH_SKINNY) {
+    SkinnyParams p = {};
+    if ((rc = skinny_geometry(&p, M, N, K, 128 / in_bytes, num_sms, cfg))) return rc;
+    out->tile_m = p.bm;
+    out->tile_n = p.np;
+    out->skinny_kgroup = p.kg;
+    out->skinny_stages = p.stages;
+    out->skinny_grid = p.grid;
+    out->skinny_parts = p.split;
+    out->skinny_skew = p.skew;
+  } else {
+    int tm, tn, br, er, ec;
+    tiled_shape(path == GEMM_PATH_2SM ? 2 : 1, 0, &tm, &tn, &br, &er, &ec);
+    out->tile_m = tm;
+    out->tile_n = tn;
+  }
+  return GEMM_OK;
 }
 
 int gemm_get_status(void* stream) {

@@ -716,7 +716,7 @@ void skinny_partition(SkinnyParams* p, int num_sms, int grid_override, int skew_
       const int skew_blocks = skew_kb > 0 ? skew_kb : (skew_kb < 0 ? 0 : p->np / 4);
       int skew = (skew_blocks + kg - 1) / kg;
       const int room = p->num_kb / s - 1;  // every part keeps at least one k-group
-      p->skew = skew < room ? skew : (room > 0 ? room : 0);
+      p->skew = s < 2 ? 0 : (skew < room ? skew : (room > 0 ? room : 0));
       return;
     }
   }

@@ -487,3 +487,22 @@ def test_workload_decode_full():
     ref, absdot = oracle.gemm_ref(A, B, C, w.alpha, w.beta)
     ok, worst, where = oracle.check(D, ref, absdot, w.out_dtype)
     assert ok, (worst, where)
+
+
+@pytest.mark.parametrize("M,N,K", [(16, 8192, 1024), (64, 8192, 2048), (24, 4096, 4096), (7, 520, 1000),
+                                    (96, 1024, 2048), (300, 1100, 448), (224, 8192, 2048)])
+def test_plan_matches_the_launch(M, N, K):
+    """gemm_plan (host only) predicts the path and skinny geometry the call takes."""
+    import torch
+    sms = torch.cuda.get_device_properties(0).multi_processor_count
+    rc, plan = g.gemm_plan(M, N, K, 0, sms)
+    assert rc == 0
+    got, exp = run_int(M, N, K, 0, gi.OUT_BF16, seed=380 + M)
+    assert_same(got, exp)
+    info = g.last_launch_info()
+    assert info["path"] == plan["path"]
+    if plan["path"] == PS:
+        assert (info["tile_m"], info["tile_n"], info["grid"], info["stages"]) == \
+            (plan["tile_m"], plan["tile_n"], plan["skinny_grid"], plan["skinny_stages"])
+    else:
+        assert info["tile_m"] == plan["tile_m"]

@@ -101,7 +101,7 @@ def _struct_fields(name):
 
 
 @pytest.mark.parametrize("name,cls", [("gemm_tn_config", g.GemmConfig), ("gemm_launch_info", g.LaunchInfo),
-                                      ("gemm_problem", g.GemmProblem)])
+                                      ("gemm_problem", g.GemmProblem), ("gemm_plan_info", g.GemmPlanInfo)])
 def test_ctypes_structs_follow_the_header(name, cls):
     assert _struct_fields(name) == [f for f, _ in cls._fields_]
 

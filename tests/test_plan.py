@@ -1,0 +1,119 @@
+"""Host-only planning (gemm_plan): the automatic path and skinny geometry for
+shapes whose best choice was measured on GB300 (152 SMs), without a GPU.
+
+Each expected value is the choice the shape sweeps found fastest (or within
+a few percent of it); the comments give the measured times."""
+import pytest
+
+import tensor_core_dense_tn_gb300 as g
+from tensor_core_dense_tn_gb300 import build as gbuild
+
+P1, P2, S = 1, 2, 3
+
+
+@pytest.fixture(scope="module", autouse=True)
+def lib():
+    gbuild.build()
+    return g.load()
+
+
+def plan(M, N, K, fp8=0, sms=152, **cfg):
+    rc, info = g.gemm_plan(M, N, K, fp8, sms, g.GemmConfig(**cfg) if cfg else None)
+    assert rc == 0, g.last_error()
+    return info
+
+
+@pytest.mark.parametrize("M,N,K,fp8,path", [
+    (16, 8192, 8192, 0, S),      # decode: skinny 25.6 us
+    (16, 8192, 8192, 1, S),
+    (1, 256, 256, 0, S),         # skinny 3.9 us against 5.9 (1-SM)
+    (32, 1024, 1024, 0, S),
+    (64, 8192, 8192, 0, S),      # 64-row whole tiles 31.4 us; 2-SM 43.1
+    (64, 4096, 4096, 0, S),      # 18.8 us; 2-SM 23.4
+    (64, 1024, 4096, 0, P1),     # small B: 1-SM 21.9 us; skinny 31.8
+    (64, 4096, 1024, 0, P1),     # 8 MiB B: 1-SM 9.3 us; skinny 13.1
+    (64, 28672, 4096, 0, P1),    # stream-K skinny 49.9 us; 1-SM 44.5
+    (96, 1024, 2048, 0, P1),     # 1-SM 13.5 us; skinny 49.7
+    (96, 8192, 2048, 0, S),      # 32 MiB: skinny 14.7 us; 2-SM 15.5
+    (96, 8192, 4096, 1, S),      # fp8, 32 MiB
+    (96, 8192, 2048, 1, P1),     # fp8, 16 MiB stays in L2
+    (96, 16384, 8192, 0, S),     # skinny 53.0 us; 2-SM 53.5
+    (128, 8192, 8192, 0, S),     # skinny 38.5 us; 2-SM 43.6; 1-SM 56.6
+    (96, 28672, 8192, 0, P1),    # 1-SM 83.1 us; skinny 90.6
+    (160, 8192, 8192, 0, P2),    # 2-SM 43.8 us; skinny 46.9
+    (224, 8192, 8192, 0, P2),    # 2-SM 44.0 us; 1-SM 56.6
+    (256, 4096, 4096, 0, P2),    # 2-SM 23.7 us; 1-SM 29.9
+    (256, 4096, 2048, 0, P1),    # B in L2: 1-SM 13.9 us; 2-SM 14.5
+    (256, 256, 256, 0, P1),      # 6.0 us against 6.6
+    (384, 8192, 2048, 0, P2),    # 16.5 us against 18.3
+    (3000, 5000, 2000, 0, P2),
+    (4096, 4096, 4096, 0, P2),
+    (8192, 28672, 4096, 0, P2),  # the up-projection
+    (8192, 28672, 4096, 1, P2),
+    (300, 264, 0, 0, P1),        # K = 0: D = beta C on the 1-SM kernel
+])
+def test_automatic_path(M, N, K, fp8, path):
+    assert plan(M, N, K, fp8)["path"] == path
+
+
+@pytest.mark.parametrize("M,N,K,fp8,geometry", [
+    # tile rows, k-group, stages, grid, parts, skew (k-groups)
+    (16, 8192, 8192, 0, (128, 4, 3, 128, 2, 1)),
+    (16, 8192, 8192, 1, (128, 4, 3, 128, 2, 1)),
+    (1, 8192, 8192, 0, (128, 4, 3, 128, 2, 1)),
+    (32, 8192, 8192, 0, (128, 2, 5, 128, 2, 4)),  # 4 k-blocks would leave 2 stages; skew 8 k-blocks
+    (64, 8192, 8192, 0, (64, 4, 3, 128, 1, 0)),
+    (24, 4096, 4096, 0, (64, 4, 4, 128, 2, 2)),   # 64 rows: two parts instead of four
+    (8, 4096, 8192, 0, (128, 4, 3, 128, 4, 1)),
+    (128, 8192, 8192, 0, (64, 2, 4, 128, 1, 0)),  # wide form
+    (16, 8192, 1000, 0, (128, 1, 12, 128, 2, 4)), # K not a whole number of k-blocks: 2D maps
+])
+def test_skinny_geometry(M, N, K, fp8, geometry):
+    p = plan(M, N, K, fp8)
+    assert p["path"] == S
+    got = (p["tile_m"], p["skinny_kgroup"], p["skinny_stages"], p["skinny_grid"], p["skinny_parts"],
+           p["skinny_skew"])
+    assert got == geometry
+    assert p["tile_n"] == -(-M // 16) * 16
+
+
+def test_skinny_partition_follows_the_sm_count():
+    # 148 SMs: 64 tiles x 2 parts still keep >= 80% of the SMs busy
+    assert plan(16, 8192, 8192, sms=148)["skinny_grid"] == 128
+    # 100 SMs: 64 tiles x 1 part leave 36% idle: stream-K over all 100
+    p = plan(16, 8192, 8192, sms=100)
+    assert p["skinny_grid"] == 100 and p["skinny_parts"] == 0
+
+
+def test_overrides_reach_the_plan():
+    p = plan(16, 8192, 8192, path=S, skinny_bm=64, skinny_kgroup=2, skinny_skew_kb=-1)
+    assert (p["tile_m"], p["skinny_kgroup"], p["skinny_parts"], p["skinny_skew"]) == (64, 2, 1, 0)
+    p = plan(16, 8192, 8192, path=S, skinny_grid=37)
+    assert p["skinny_grid"] == 37 and p["skinny_parts"] == 0
+    assert plan(16, 8192, 8192, path=P2)["tile_m"] == 256
+    assert plan(8192, 8192, 8192, path=P1)["tile_m"] == 128
+
+
+def test_tiled_tile_shape():
+    p = plan(8192, 28672, 4096)
+    assert (p["tile_m"], p["tile_n"], p["skinny_grid"]) == (256, 256, 0)
+
+
+@pytest.mark.parametrize("args,cfg,code,text", [
+    ((257, 64, 64), dict(path=3), g.GEMM_ERR_NOT_IMPLEMENTED, "skinny"),
+    ((16, 64, 0), dict(path=3), g.GEMM_ERR_NOT_IMPLEMENTED, "skinny"),
+    ((144, 256, 1024), dict(path=3, skinny_bm=128, skinny_kgroup=4), g.GEMM_ERR_INVALID_VALUE, "ring stages"),
+    ((-1, 64, 64), {}, g.GEMM_ERR_INVALID_VALUE, "negative"),
+    ((16, 64, 64), dict(skinny_kgroup=3), g.GEMM_ERR_INVALID_VALUE, "skinny_kgroup"),
+    ((16, 64, 64), dict(path=9), g.GEMM_ERR_INVALID_VALUE, "path"),
+])
+def test_plan_errors(args, cfg, code, text):
+    rc, _ = g.gemm_plan(*args, 0, 152, g.GemmConfig(**cfg) if cfg else None)
+    assert rc == code and text in g.last_error()
+
+
+def test_plan_argument_errors():
+    assert g.gemm_plan(16, 64, 64, 0, 0)[0] == g.GEMM_ERR_INVALID_VALUE
+    assert g.gemm_plan(16, 64, 64, 2, 152)[0] == g.GEMM_ERR_INVALID_VALUE
+    rc, info = g.gemm_plan(0, 64, 64)
+    assert rc == 0 and info["path"] == 0
