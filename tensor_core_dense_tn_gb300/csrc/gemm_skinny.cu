@@ -656,12 +656,23 @@ int skinny_kgroup(int np, int bm, long long K, int kbe, int kg_req) {
 
 // Parts per tile of the equal-split mode for n columns of D in bm-row
 // tiles, or 0 where that mode does not apply (stream-K over the grid).
-static int equal_split(long long n, int bm, int sms) {
-  const long long tiles = (n + bm - 1) / bm;
-  if (tiles > sms) return 0;
+// Parts per tile of the equal split for `tiles` tiles on `sms` SMs, or 0
+// (stream-K).  Every tile is split into s = sms / tiles parts, at most
+// kMaxParts: the finisher adds one partial per extra part, and beyond four
+// parts that costs more than the extra streaming SMs gain (measured,
+// graph-replayed 16 x N x 8192: N = 2048 takes 15.2 us bf16 / 11.9 us e4m3
+// with 4 parts on 64 CTAs against 16.8 / 14.3 us with 9 parts on 144; N =
+// 1024 is flat from 4 to 8 parts and 10-40% slower at 12-19).  Below the cap
+// the split must keep at least 80% of the SMs streaming; else stream-K.
+constexpr int kMaxParts = 4;
+static int split_parts(long long tiles, int sms) {
+  if (tiles < 1 || tiles > sms) return 0;
   const int s = sms / (int)tiles;
+  if (s >= kMaxParts) return kMaxParts;
   return 5 * tiles * s >= 4LL * sms ? s : 0;
 }
+
+static int equal_split(long long n, int bm, int sms) { return split_parts((n + bm - 1) / bm, sms); }
 
 int skinny_parts(long long n, int np, int max_grid) {
   return equal_split(n, skinny_tile_rows(n, np, max_grid), max_grid);
@@ -697,14 +708,15 @@ void skinny_partition(SkinnyParams* p, int num_sms, int grid_override, int skew_
   }
   // Splitting every tile into the same number s of k-ranges (one CTA each)
   // leaves every CTA with one segment; it wins over a full-GPU stream-K split
-  // as long as it keeps at least 80% of the SMs streaming.  s = 1 is a whole
+  // as long as it keeps at least 80% of the SMs streaming, or reaches the
+  // cap of four parts (split_parts).  s = 1 is a whole
   // tile per CTA, with no partial sums.  Part j of tile n goes to CTA
   // n + j * n_tiles, so the parts of a tile sit on SMs spread across the
   // grid.  Part 0's CTA finishes the tile after the other parts land, so it
   // gets a few more k-blocks.
-  if (p->n_tiles <= num_sms) {
-    const int s = num_sms / p->n_tiles;
-    if (s >= 1 && s <= p->num_kb && 5 * p->n_tiles * s >= 4 * num_sms) {
+  {
+    const int s = split_parts(p->n_tiles, num_sms);
+    if (s >= 1 && s <= p->num_kb) {
       p->grid = p->n_tiles * s;
       p->split = s;
       // Skew in k-blocks, rounded up to whole k-groups.  The finisher's extra

@@ -246,8 +246,8 @@ def test_skinny_stream_k_partitions(skinny_grid, K):
 
 @pytest.mark.parametrize("skew", [-1, 1, 5, 1000])
 def test_skinny_equal_split_skew(skew):
-    # default grid on 16 x 1024 x 4096 is the equal-split mode (8 tiles x 19 parts on 152 SMs);
-    # every skew (clamped so each part keeps a k-block) gives the exact result
+    # default grid on 16 x 1024 x 4096 is the equal-split mode (8 tiles x 4 parts);
+    # every skew (clamped so each part keeps a k-group) gives the exact result
     import torch
     M, N, K = 16, 1024, 4096
     A = gi.draw_bf16(M, K, gi.Dist("int", -4, 4), 320)
