@@ -125,6 +125,11 @@ typedef struct gemm_tn_config {
                                1, 2 or 4; 0 = auto (32 KiB boxes of B while 4 stages fit).  Values
                                above 1 apply only when K is a whole number of k-blocks (64 bf16 or
                                128 fp8 elements); otherwise the path uses 1 */
+  int tiled_k_parts;        /* tiled paths, single problem, static scheduler: k-parts per tile, 0..4;
+                               0 = auto (2 when the tiles fill at most a quarter of the clusters and K
+                               holds at least 128 k-blocks, else 1), 1 = no split.  Capped at launch
+                               so that every part has a co-resident cluster and at K's k-blocks;
+                               ignored with CLC or a grid override */
 } gemm_tn_config;
 
 /* Tile schedulers of the tiled paths.
@@ -152,6 +157,8 @@ typedef struct gemm_launch_info {
   int smem_bytes;    /* dynamic shared memory per CTA */
   const char *kernel;/* kernel name (static string) */
   int scheduler;     /* tiled paths: GEMM_SCHED_STATIC or GEMM_SCHED_CLC; 0 otherwise */
+  int k_parts;       /* k-parts per tile: tiled split (1 = none) or skinny equal split; 0 = skinny
+                        stream-K ranges */
 } gemm_launch_info;
 
 /* D = alpha * A * B^T + beta * C (see the file comment for every argument).
@@ -226,7 +233,8 @@ typedef struct gemm_plan_info {
   int skinny_kgroup;  /* skinny: k-blocks per ring stage (one TMA box per operand); else 0 */
   int skinny_stages;  /* skinny: ring stages; else 0 */
   int skinny_grid;    /* skinny: CTAs; else 0 */
-  int skinny_parts;   /* skinny: k-parts per tile in the equal split; 0 = stream-K ranges or not skinny */
+  int k_parts;        /* k-parts per tile: tiled split (1 = none; capped at launch to co-resident
+                         clusters) or skinny equal split; 0 = skinny stream-K ranges */
   int skinny_skew;    /* skinny, equal split: k-groups moved to the part that finishes each tile */
 } gemm_plan_info;
 

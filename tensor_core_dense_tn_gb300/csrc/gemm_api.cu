@@ -156,7 +156,7 @@ int get_workspace(int dev, cudaStream_t stream, size_t partial_floats, size_t co
     cudaStreamCaptureStatus cs = cudaStreamCaptureStatusNone;
     cudaStreamIsCapturing(stream, &cs);
     if (cs != cudaStreamCaptureStatusNone)
-      return fail(GEMM_ERR_INVALID_VALUE, "skinny workspace must be created outside stream capture");
+      return fail(GEMM_ERR_INVALID_VALUE, "split-K workspace must be created outside stream capture");
     // Work already queued may still use the old buffers.
     cudaError_t e = cudaStreamSynchronize(stream);
     if (e != cudaSuccess) return fail(GEMM_ERR_CUDA, "cudaStreamSynchronize: %s", cudaGetErrorString(e));
@@ -170,7 +170,7 @@ int get_workspace(int dev, cudaStream_t stream, size_t partial_floats, size_t co
       if (w.partials) cudaFree(w.partials);
       w = Workspace{};
       cudaGetLastError();
-      return fail(GEMM_ERR_OUT_OF_MEMORY, "skinny workspace allocation failed");
+      return fail(GEMM_ERR_OUT_OF_MEMORY, "split-K workspace allocation failed");
     }
     e = cudaMemset(w.counters, 0, ci * sizeof(int));
     if (e != cudaSuccess) return fail(GEMM_ERR_CUDA, "cudaMemset: %s", cudaGetErrorString(e));
@@ -240,6 +240,28 @@ long long one_sm_tiles(int64_t M, int64_t N) { return ((M + 127) / 128) * ((N + 
 //   against 56.6 us); with B in L2 the 1-SM kernel's lighter launch wins.
 constexpr int64_t kStreamedBytes = 32ll << 20;
 
+// k-parts per tile for the tiled kernels (single problem, static schedule),
+// one cluster per (tile, part); part 0 adds the other parts' fp32 partials.
+// Measured on GB300 (graph-replayed, bf16), two parts against none: 256 x
+// 2048 x 8192 (8 pair tiles) 37.4 against 40.7 us, 256 x 4096 x 8192 (16)
+// 38.7 against 41.3; about even at 32 pair tiles (224 x 8192 x 8192: 44.6
+// against 44.0); but 192 x 4096 x 4096 29.5 against 23.8, 512 x 4096 x 4096
+// 30.3 against 23.9 and 1024 x 2048 x 2048 24.8 against 14.1, and four parts
+// were never the fastest.  The partial hand-off costs a few microseconds and
+// the operand stream into the SMs is already near its aggregate rate, so
+// only a long k-range on few tiles pays: two parts where the tiles fill at
+// most a quarter of the clusters and K holds at least 128 k-blocks.  Forced
+// values (tiled_k_parts) go up to four.
+constexpr int kMaxTiledParts = 4;
+constexpr int kSplitMinKb = 128;
+int tiled_parts(long long tiles, int num_kb, int sms, int cg, const gemm_tn_config* cfg) {
+  const int req = cfg ? cfg->tiled_k_parts : 0;
+  if (req > 0) return req < num_kb ? req : (num_kb > 1 ? num_kb : 1);
+  const long long clusters = sms / cg;
+  if (tiles < 1 || 4 * tiles > clusters || num_kb < kSplitMinKb) return 1;
+  return 2;
+}
+
 // Values of a gemm_tn_config that select among fixed choices.
 int check_config(const gemm_tn_config* cfg) {
   if (!cfg) return GEMM_OK;
@@ -253,6 +275,8 @@ int check_config(const gemm_tn_config* cfg) {
   const int kg = cfg->skinny_kgroup;
   if (kg != 0 && kg != 1 && kg != 2 && kg != 4)
     return fail(GEMM_ERR_INVALID_VALUE, "skinny_kgroup must be 0, 1, 2 or 4, got %d", kg);
+  if (cfg->tiled_k_parts < 0 || cfg->tiled_k_parts > kMaxTiledParts)
+    return fail(GEMM_ERR_INVALID_VALUE, "tiled_k_parts must be 0..%d, got %d", kMaxTiledParts, cfg->tiled_k_parts);
   return GEMM_OK;
 }
 
@@ -310,6 +334,7 @@ void record_launch(const LaunchInfo& li) {
   t_info.stages = li.stages;
   t_info.smem_bytes = li.smem_bytes;
   t_info.kernel = li.kernel;
+  t_info.k_parts = li.k_parts;
   t_info.scheduler = li.scheduler;
 }
 
@@ -404,6 +429,16 @@ int run(int64_t M, int64_t N, int64_t K, const void* A, int64_t lda, const void*
     p.alpha = alpha; p.beta = beta; p.has_c = has_c; p.epi = epi;
     p.fault = fault; p.timeout_ns = tmo; p.status = st->status;
     p.clc = sched == GEMM_SCHED_CLC ? 1 : 0;
+    p.ksplit = p.clc || (cfg && cfg->grid > 0) ? 1 : tiled_parts(p.num_tiles, p.num_kb, st->sms, cg, cfg);
+    if (p.ksplit > p.num_kb) p.ksplit = p.num_kb > 1 ? p.num_kb : 1;  // every part owns a k-block
+    if (p.ksplit > 1) {
+      Workspace* w = nullptr;
+      rc = get_workspace(dev, stream, (size_t)p.num_tiles * (p.ksplit - 1) * cg * 128 * 256,
+                         (size_t)p.num_tiles * cg * 4, &w);
+      if (rc != GEMM_OK) return rc;
+      p.partials = w->partials;
+      p.counters = w->counters;
+    }
     CUtensorMap tA, tB, tC, tD;
     memset(&tA, 0, sizeof tA);
     memset(&tB, 0, sizeof tB);
@@ -727,13 +762,18 @@ int gemm_plan(int64_t M, int64_t N, int64_t K, int fp8_inputs, int num_sms, cons
     out->skinny_kgroup = p.kg;
     out->skinny_stages = p.stages;
     out->skinny_grid = p.grid;
-    out->skinny_parts = p.split;
+    out->k_parts = p.split;
     out->skinny_skew = p.skew;
   } else {
     int tm, tn, br, er, ec;
     tiled_shape(path == GEMM_PATH_2SM ? 2 : 1, 0, &tm, &tn, &br, &er, &ec);
     out->tile_m = tm;
     out->tile_n = tn;
+    const long long tiles = ((M + tm - 1) / tm) * ((N + tn - 1) / tn);
+    const bool clc = cfg && cfg->scheduler == GEMM_SCHED_CLC;
+    out->k_parts = clc || (cfg && cfg->grid > 0) || K == 0
+                       ? 1 : tiled_parts(tiles, (int)((K + 128 / in_bytes - 1) / (128 / in_bytes)), num_sms,
+                                         path == GEMM_PATH_2SM ? 2 : 1, cfg);
   }
   return GEMM_OK;
 }

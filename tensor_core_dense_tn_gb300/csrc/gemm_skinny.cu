@@ -773,6 +773,7 @@ cudaError_t launch_skinny(const CUtensorMap& tmA, const CUtensorMap& tmB, Skinny
     info->tile_m = p.bm;
     info->tile_n = p.np;
     info->stages = p.stages;
+    info->k_parts = p.split;
     info->smem_bytes = smem;
     info->kernel = p.kind == kKindF8F6F4 ? (p.np > 64 ? "gemm_tn_skinny_kernel<fp8 in,wide>" : "gemm_tn_skinny_kernel<fp8 in>")
                                          : (p.np > 64 ? "gemm_tn_skinny_kernel<wide>" : "gemm_tn_skinny_kernel");

@@ -79,7 +79,12 @@ struct Cfg {
   // readers of each answer, all arriving on the leader CTA's CLC_EMPTY:
   // producer + 4 epilogue warps per CTA, and the leader's MMA thread
   static constexpr int CLC_READERS = CG * (1 + kEpiWarps) + 1;
-  static constexpr int NUM_BARS = 2 * STAGES + 4 + 2 * kEpiWarps + 1 + 2 * CLC_SLOTS;
+  // + two barriers per epilogue warp for the k-split partials (see the epilogue)
+  static constexpr int NUM_BARS = 2 * STAGES + 4 + 2 * kEpiWarps + 1 + 2 * CLC_SLOTS + 2 * kEpiWarps;
+  // k-split: each epilogue warp stages two chunks of up to three partials
+  // (4 KiB each) in the operand ring, which is idle by then
+  static constexpr int PART_SLOT = 32 * 32 * 4;
+  static_assert(kEpiWarps * 2 * 3 * PART_SLOT <= STAGES * (A_BYTES + B_BYTES), "partial staging fits the ring");
   static constexpr int RING_BYTES = STAGES * (A_BYTES + B_BYTES);
   static constexpr int EPI_TOTAL = kEpiWarps * 2 * EPI_BYTES;
   static constexpr int CLC_BYTES = CLC_SLOTS * 16;
@@ -130,6 +135,41 @@ __device__ __forceinline__ bool wait_bar(uint32_t bar, uint32_t parity, const Ab
 __device__ __noinline__ void settle(uint64_t ns) {
   const uint64_t t0 = globaltimer();
   while (globaltimer() - t0 < ns) __nanosleep(1000);
+}
+
+// Warp-wide bounded wait until `expected` parts of a split tile have been
+// counted at `arrivals` (lane 0 polls with acquire; the warp barrier passes
+// the acquire on to the other lanes), then clears the counter for the next
+// call.  False if the CTA is aborting or the limit expired (status recorded).
+__device__ __noinline__ bool wait_parts(int* arrivals, int expected, const Abort& ab) {
+  int ok = 1;
+  if ((threadIdx.x & 31) == 0) {
+    if (ld_acquire_gpu(arrivals) != expected) {
+      const uint64_t t0 = globaltimer();
+      while (ld_acquire_gpu(arrivals) != expected) {
+        if (*ab.flag || globaltimer() - t0 > ab.timeout_ns) {
+          if (!*ab.flag) {
+            *ab.flag = 1;
+            if (atomicCAS(ab.status, 0, kErrTimeout) == 0)
+              atomicExch(ab.status + 1, (kRoleFixup << 24) | (int)blockIdx.x);
+          }
+          ok = 0;
+          break;
+        }
+        __nanosleep(64);
+      }
+    }
+    if (ok) *arrivals = 0;
+  }
+  ok = __shfl_sync(0xffffffffu, ok, 0);
+  __syncwarp();
+  return ok != 0;
+}
+
+// k-blocks [kb0, kb1) of part `part` of a tile split into `parts`.
+__device__ __forceinline__ void part_range(int num_kb, int parts, int part, int& kb0, int& kb1) {
+  kb0 = (int)((long long)part * num_kb / parts);
+  kb1 = (int)((long long)(part + 1) * num_kb / parts);
 }
 
 __device__ __forceinline__ void tile_coords(int t, int raster_group, int tiles_m, int tiles_n, int& tm, int& tn) {
@@ -243,10 +283,10 @@ __device__ __forceinline__ int next_tile(int t, int stride, const TileParams& p,
     else mbar_arrive_relaxed(empty0_leader + 8u * cur.slot);
   }
   cur.advance(SLOTS);
-  return got ? (int)(first_x / CG) : p.num_tiles;
+  return got ? (int)(first_x / CG) : p.num_units;
 }
 
-template <int CG, bool OUT_F32, int KIND, int MODE>
+template <int CG, bool OUT_F32, int KIND, int MODE, bool SPLIT>
 __global__ void __launch_bounds__(kThreads, 1)
     gemm_tn_tiled_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
                          const __grid_constant__ CUtensorMap tmC, const __grid_constant__ CUtensorMap tmD,
@@ -270,6 +310,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   const uint32_t drain_bar = bar0 + 8u * (2 * C_::STAGES + 4 + 2 * kEpiWarps);
   const uint32_t clcf0 = drain_bar + 8u;                          // CLC_FULL[slot]
   const uint32_t clce0 = clcf0 + 8u * C_::CLC_SLOTS;              // CLC_EMPTY[slot] (used in the leader)
+  const uint32_t pbar0 = clce0 + 8u * C_::CLC_SLOTS;              // PART[epilogue warp][buffer]
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bars + C_::NUM_BARS);
   volatile uint32_t* abort_flag = tmem_slot + 1;
 
@@ -279,6 +320,12 @@ __global__ void __launch_bounds__(kThreads, 1)
   const bool leader = (rank == 0);
   const int cluster_id = blockIdx.x / CG;
   const int num_clusters = gridDim.x / CG;
+  // Unit u -> tile and k-part.  Only a split launch (SPLIT, one unit per
+  // cluster) has more units than tiles; the finishing part 0 takes the
+  // highest units, so every part it waits for has a lower cluster id.
+  const int ks = SPLIT ? p.ksplit : 1;
+  auto unit_tile = [&](int u) { return SPLIT ? u % p.num_tiles : u; };
+  auto unit_part = [&](int u) { return SPLIT ? ks - 1 - u / p.num_tiles : 0; };
 
   if (threadIdx.x == 0) {
     for (int s = 0; s < C_::STAGES; ++s) {
@@ -296,6 +343,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       mbar_init(clcf0 + 8u * s, 1);
       mbar_init(clce0 + 8u * s, C_::CLC_READERS);
     }
+    for (int b = 0; b < 2 * kEpiWarps; ++b) mbar_init(pbar0 + 8u * b, 1);
     *abort_flag = 0;
     fence_mbar_init();
     fence_proxy_async_smem();
@@ -303,7 +351,8 @@ __global__ void __launch_bounds__(kThreads, 1)
   if (warp == 0 && lane == 0) {
     // the first tile's tensor maps (kernel parameters: valid before the
     // previous kernel on the stream has finished)
-    const TileRef r0 = resolve<MODE>(cluster_id < p.num_tiles ? cluster_id : 0, p, ga, &tmA, &tmB, &tmC, &tmD);
+    const TileRef r0 = resolve<MODE>(cluster_id < p.num_units ? unit_tile(cluster_id) : 0, p, ga, &tmA, &tmB,
+                                     &tmC, &tmD);
     if (r0.num_kb > 0) {
       tma_prefetch_desc(r0.a);
       tma_prefetch_desc(r0.b);
@@ -337,7 +386,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       ClcCursor req, rd;  // slot of the next request, slot of the next answer to read
       const uint32_t clce_leader = kCluster ? mapa_shared(clce0, 0) : clce0;
       int t = cluster_id;
-      while (t < p.num_tiles && ok) {
+      while (t < p.num_units && ok) {
         if (p.clc) {
           // ask for the tile after this one now; the answer is read once this tile's loads are issued
           if (leader && !wait_bar<kCluster>(clce0 + 8u * req.slot, req.phase ^ 1, ab)) {
@@ -351,7 +400,9 @@ __global__ void __launch_bounds__(kThreads, 1)
           }
           req.advance(C_::CLC_SLOTS);
         }
-        const TileRef r = resolve<MODE>(t, p, ga, &tmA, &tmB, &tmC, &tmD);
+        const TileRef r = resolve<MODE>(unit_tile(t), p, ga, &tmA, &tmB, &tmC, &tmD);
+        int kb0, kb1;
+        part_range(r.num_kb, ks, unit_part(t), kb0, kb1);
         if constexpr (MODE == kModeList) {
           // a list's next tile is usually another problem: fetch its maps early
           const int tn_next = t + num_clusters;
@@ -367,7 +418,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
         const int a_row = r.tm * C_::TILE_M + (int)rank * 128;
         const int b_row = r.tn * C_::BN + (int)rank * C_::B_ROWS;
-        for (int kb = 0; kb < r.num_kb; ++kb) {
+        for (int kb = kb0; kb < kb1; ++kb) {
           if (!wait_bar<kCluster>(empty_bar(stage), phase ^ 1, ab)) {
             ok = false;
             break;
@@ -409,12 +460,13 @@ __global__ void __launch_bounds__(kThreads, 1)
       ClcCursor rd;
       const uint32_t clce_leader = kCluster ? mapa_shared(clce0, 0) : clce0;
       int t = cluster_id;
-      while (t < p.num_tiles && ok) {
+      while (t < p.num_units && ok) {
         if (!wait_bar<kCluster>(acce_bar(acc), acc_phase ^ 1, ab)) break;
         tc_fence_after();
         const uint32_t d_tmem = tmem_base + (uint32_t)(acc * C_::BN);
-        const int num_kb = resolve<MODE>(t, p, ga, &tmA, &tmB, &tmC, &tmD).num_kb;
-        for (int kb = 0; kb < num_kb; ++kb) {
+        int kb0, kb1;
+        part_range(resolve<MODE>(unit_tile(t), p, ga, &tmA, &tmB, &tmC, &tmD).num_kb, ks, unit_part(t), kb0, kb1);
+        for (int kb = kb0; kb < kb1; ++kb) {
           if (!wait_bar<kCluster>(full_bar(stage), phase, ab)) {
             ok = false;
             break;
@@ -425,7 +477,7 @@ __global__ void __launch_bounds__(kThreads, 1)
 #pragma unroll
           for (int k = 0; k < kMmaPerStage; ++k) {
             // +32 bytes along K inside the swizzle atom = +2 in the encoded address
-            mma_issue<CG, KIND>(d_tmem, a0 + 2 * k, b0 + 2 * k, idesc, (kb | k) != 0);
+            mma_issue<CG, KIND>(d_tmem, a0 + 2 * k, b0 + 2 * k, idesc, (kb != kb0 || k != 0) ? 1u : 0u);
           }
           if constexpr (CG == 1) mma_commit(empty_bar(stage));
           else mma_commit_pair(empty_bar(stage), 0x3);
@@ -461,11 +513,44 @@ __global__ void __launch_bounds__(kThreads, 1)
     ClcCursor rd;
     const uint32_t clce_leader = kCluster ? mapa_shared(clce0, 0) : clce0;
     int t = cluster_id;
-    while (t < p.num_tiles) {
-      const TileRef tr = resolve<MODE>(t, p, ga, &tmA, &tmB, &tmC, &tmD);
+    while (t < p.num_units) {
+      const int tile = unit_tile(t);
+      const int part = unit_part(t);
+      const TileRef tr = resolve<MODE>(tile, p, ga, &tmA, &tmB, &tmC, &tmD);
       const int row0 = tr.tm * C_::TILE_M + (int)rank * 128 + q * 32;
+      // Split tile: parts > 0 publish this warp's 32 rows x 256 columns of
+      // raw fp32 accumulators and count them; part 0 waits for the count and
+      // adds the parts in order before the epilogue proper.
+      int* arrivals = ks > 1 ? p.counters + ((long long)tile * CG + rank) * 4 + q : nullptr;
+      // this warp's 32 x 32 block of part pt, chunk c (4 KiB, contiguous)
+      auto partial_at = [&](int pt, int c) {
+        return p.partials + ((((long long)tile * (ks - 1) + (pt - 1)) * CG + rank) * (C_::BN / 32) + c) *
+                                (128 * 32) +
+               q * 32 * 32;
+      };
+      // Part 0 stages the other parts' chunks in the operand ring, two chunks
+      // ahead, with bulk copies: a split launch runs one unit per cluster, so
+      // once the accumulator is complete no MMA or load touches the ring.
+      const bool fix = SPLIT && ks > 1 && part == 0;
+      const uint32_t pstage = sA + (uint32_t)(ew * 2 * 3 * C_::PART_SLOT);
+      auto fetch = [&](int c) {
+        const uint32_t bar = pbar0 + 8u * (uint32_t)(ew * 2 + (c & 1));
+        mbar_arrive_expect_tx(bar, (uint32_t)((ks - 1) * C_::PART_SLOT));
+        for (int pt = 1; pt < ks; ++pt)
+          bulk_load_1d(pstage + (uint32_t)(((c & 1) * 3 + pt - 1) * C_::PART_SLOT), partial_at(pt, c),
+                       C_::PART_SLOT, bar);
+      };
       if (!wait_bar<kCluster>(accf_bar(acc), acc_phase, ab)) break;
       tc_fence_after();
+      if (fix) {
+        Abort abf{abort_flag, p.timeout_ns, p.status, kRoleFixup};
+        if (!wait_parts(arrivals, ks - 1, abf)) break;
+        if (lane == 0) {
+          fence_proxy_async_global();  // the acquired partials, then the bulk copies that read them
+          fetch(0);
+          fetch(1);
+        }
+      }
 #pragma unroll 1
       for (int c = 0; c < C_::BN / C_::EPI_COLS; ++c) {
         const int col0 = tr.tn * C_::BN + c * C_::EPI_COLS;
@@ -485,6 +570,39 @@ __global__ void __launch_bounds__(kThreads, 1)
             if constexpr (kCluster) mbar_arrive_cluster(acce_target + 8u * acc);
             else mbar_arrive(acce_bar(acc));
           }
+        }
+        if (part > 0) {
+          float4* dst = reinterpret_cast<float4*>(partial_at(part, c) + lane * 32);
+#pragma unroll
+          for (int j = 0; j < 8; ++j)
+            dst[j] = make_float4(__uint_as_float(r[4 * j]), __uint_as_float(r[4 * j + 1]),
+                                 __uint_as_float(r[4 * j + 2]), __uint_as_float(r[4 * j + 3]));
+          continue;
+        }
+        if (fix) {
+          // parts in order: (0 + part 0) + part 1 + ...; the chunk's barrier
+          // is consumed even for a box outside D, so the phases stay in step
+          const int b = c & 1;
+          if (!wait_bar<false>(pbar0 + 8u * (uint32_t)(ew * 2 + b), (uint32_t)((c >> 1) & 1), ab)) break;
+          float a[32];
+#pragma unroll
+          for (int j = 0; j < 32; ++j) a[j] = 0.0f + __uint_as_float(r[j]);
+          for (int pt = 1; pt < ks; ++pt) {
+            const uint32_t src = pstage + (uint32_t)((b * 3 + pt - 1) * C_::PART_SLOT) + (uint32_t)lane * 128u;
+#pragma unroll
+            for (int j = 0; j < 8; ++j) {
+              uint32_t x0, x1, x2, x3;
+              ld_shared_v4(src + 16u * j, x0, x1, x2, x3);
+              a[4 * j] += __uint_as_float(x0);
+              a[4 * j + 1] += __uint_as_float(x1);
+              a[4 * j + 2] += __uint_as_float(x2);
+              a[4 * j + 3] += __uint_as_float(x3);
+            }
+          }
+#pragma unroll
+          for (int j = 0; j < 32; ++j) r[j] = __float_as_uint(a[j]);
+          __syncwarp();  // every lane has read buffer b
+          if (lane == 0 && c + 2 < C_::BN / C_::EPI_COLS) fetch(c + 2);
         }
         if (row0 >= tr.M || col0 >= tr.N) continue;  // box entirely outside D
         const uint32_t sbuf = sE + (uint32_t)((ew * 2 + buf) * C_::EPI_BYTES);
@@ -560,6 +678,11 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
         buf ^= 1;
       }
+      if (part > 0) {
+        // every lane's partial is written before lane 0 counts it
+        __syncwarp();
+        if (lane == 0) red_add_release_gpu(arrivals, 1);
+      }
       if (*abort_flag) break;
       acc ^= 1;
       if (acc == 0) acc_phase ^= 1;
@@ -568,6 +691,8 @@ __global__ void __launch_bounds__(kThreads, 1)
       if (t < 0) break;
     }
     if (lane == 0) bulk_wait<0>();
+    // an aborted k-split fix-up may leave bulk copies of partials in flight
+    if (SPLIT && ks > 1 && *abort_flag && lane == 0) settle(1000000);
   }
 
   __syncthreads();
@@ -579,14 +704,16 @@ __global__ void __launch_bounds__(kThreads, 1)
   if (p.defer_wait) griddep_wait();
 }
 
-template <int CG, bool OUT_F32, int KIND, int MODE>
+template <int CG, bool OUT_F32, int KIND, int MODE, bool SPLIT>
 cudaError_t launch_impl(const CUtensorMap& tmA, const CUtensorMap& tmB, const CUtensorMap& tmC,
-                        const CUtensorMap& tmD, const TileParams& p, const GroupArg<MODE>& ga, int grid_override,
+                        const CUtensorMap& tmD, const TileParams& p_in, const GroupArg<MODE>& ga, int grid_override,
                         bool pdl, cudaStream_t stream, LaunchInfo* info) {
+  TileParams p = p_in;
+  if (!SPLIT || MODE != kModeSingle || p.clc || p.ksplit < 1 || !p.partials || !p.counters) p.ksplit = 1;
   using C_ = Cfg<CG, OUT_F32>;
   static_assert(sizeof(GroupArg<MODE>) + 4 * sizeof(CUtensorMap) + sizeof(TileParams) < 32000,
                 "kernel parameters must stay within 32 KB");
-  auto kern = gemm_tn_tiled_kernel<CG, OUT_F32, KIND, MODE>;
+  auto kern = gemm_tn_tiled_kernel<CG, OUT_F32, KIND, MODE, SPLIT>;
   static bool configured[64] = {};
   int dev = 0;
   cudaError_t e = cudaGetDevice(&dev);
@@ -640,8 +767,12 @@ cudaError_t launch_impl(const CUtensorMap& tmA, const CUtensorMap& tmB, const CU
     max_units = sms;
   }
   if (max_units < 1) return cudaErrorInvalidConfiguration;
-  int units = p.num_tiles < max_units ? p.num_tiles : max_units;
-  if (grid_override > 0) units = grid_override / CG;
+  // A split tile's part 0 waits for its other parts: every unit must have
+  // its own co-resident cluster, so the split shrinks to what fits.
+  while (p.ksplit > 1 && (long long)p.num_tiles * p.ksplit > max_units) --p.ksplit;
+  p.num_units = p.num_tiles * p.ksplit;
+  int units = p.num_units < max_units ? p.num_units : max_units;
+  if (grid_override > 0 && p.ksplit == 1) units = grid_override / CG;
   // cluster launch control: one cluster per tile; the ones that find their
   // tile already taken over are cancelled before they start
   if (p.clc) units = p.num_tiles;
@@ -650,6 +781,7 @@ cudaError_t launch_impl(const CUtensorMap& tmA, const CUtensorMap& tmB, const CU
   if (info) {
     info->path = CG;
     info->scheduler = p.clc ? 2 : 1;
+    info->k_parts = p.ksplit;
     info->grid = units * CG;
     info->cluster = CG;
     info->block = kThreads;
@@ -690,7 +822,10 @@ cudaError_t launch_tiled(int cta_group, int out_f32, int kind, const CUtensorMap
                          bool pdl, cudaStream_t stream, LaunchInfo* info) {
   const NoGroup none{0};
 #define GTN_LAUNCH(CGV, OF, KV) \
-  launch_impl<CGV, OF, KV, kModeSingle>(tmA, tmB, tmC, tmD, p, none, grid_override, pdl, stream, info)
+  (p.ksplit > 1 ? launch_impl<CGV, OF, KV, kModeSingle, true>(tmA, tmB, tmC, tmD, p, none, grid_override, pdl, stream, \
+                                                               info) \
+                : launch_impl<CGV, OF, KV, kModeSingle, false>(tmA, tmB, tmC, tmD, p, none, grid_override, pdl, stream, \
+                                                                info))
   if (kind == kKindF8F6F4) {
     if (cta_group == 2) return out_f32 ? GTN_LAUNCH(2, true, kKindF8F6F4) : GTN_LAUNCH(2, false, kKindF8F6F4);
     return out_f32 ? GTN_LAUNCH(1, true, kKindF8F6F4) : GTN_LAUNCH(1, false, kKindF8F6F4);
@@ -705,14 +840,14 @@ cudaError_t launch_tiled_group(int cta_group, int out_f32, int mode, const CUten
                                bool pdl, cudaStream_t stream, LaunchInfo* info) {
   if (mode == kModeList) {
 #define GTN_LAUNCH(CGV, OF) \
-  launch_impl<CGV, OF, kKindF16, kModeList>(tmA, tmB, tmC, tmD, p, *list, 0, pdl, stream, info)
+  launch_impl<CGV, OF, kKindF16, kModeList, false>(tmA, tmB, tmC, tmD, p, *list, 0, pdl, stream, info)
     if (cta_group == 2) return out_f32 ? GTN_LAUNCH(2, true) : GTN_LAUNCH(2, false);
     return out_f32 ? GTN_LAUNCH(1, true) : GTN_LAUNCH(1, false);
 #undef GTN_LAUNCH
   }
   const NoGroup none{0};
 #define GTN_LAUNCH(CGV, OF) \
-  launch_impl<CGV, OF, kKindF16, kModeStrided>(tmA, tmB, tmC, tmD, p, none, 0, pdl, stream, info)
+  launch_impl<CGV, OF, kKindF16, kModeStrided, false>(tmA, tmB, tmC, tmD, p, none, 0, pdl, stream, info)
   if (cta_group == 2) return out_f32 ? GTN_LAUNCH(2, true) : GTN_LAUNCH(2, false);
   return out_f32 ? GTN_LAUNCH(1, true) : GTN_LAUNCH(1, false);
 #undef GTN_LAUNCH

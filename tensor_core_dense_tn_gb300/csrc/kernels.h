@@ -71,6 +71,15 @@ struct TileParams {
   int fault;           // kFault* bits (tests only)
   uint64_t timeout_ns;
   int* status;
+  // k-split of single-problem launches (static schedule, one unit per
+  // cluster): unit u is tile u % num_tiles, part ksplit - 1 - u / num_tiles
+  // (so the part that finishes a tile has the highest cluster ids), k-blocks
+  // [part * num_kb / ksplit, (part + 1) * num_kb / ksplit).  Parts > 0 write
+  // fp32 partials; part 0 adds them in part order.
+  int ksplit;          // parts per tile (1 = no split)
+  int num_units;       // num_tiles * ksplit
+  float* partials;     // num_tiles * (ksplit - 1) * cta_group * 128 * 256 floats
+  int* counters;       // num_tiles * cta_group * 4, zero between calls
 };
 
 struct SkinnyParams {
@@ -109,6 +118,7 @@ struct LaunchInfo {
   int smem_bytes;
   const char* kernel;
   int scheduler;       // 1 = static persistent, 2 = cluster launch control (tiled paths)
+  int k_parts;         // k-parts per tile (tiled split; skinny equal split), 0 = skinny stream-K
 };
 
 // Tiled persistent kernels (1-SM or 2-SM).  Returns a cudaError_t.  `pdl`

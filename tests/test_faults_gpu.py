@@ -64,3 +64,27 @@ def test_dropped_load_in_two_part_decode_tile():
     rc, st = call(M, N, K, dA, K, dB, K, None, 0, dD2, ldd, 1.0, 0.0, gi.OUT_F32, path=3)
     assert rc == 0 and st == 0
     assert np.array_equal(from_dev(dD2, gi.OUT_F32), oracle.exact_f32(ref))
+
+
+@pytest.mark.parametrize("path", [1, 2])
+def test_dropped_load_in_split_tile(path):
+    """A split tile whose publishing part (CTA 0) loses a stage: that part
+    aborts without publishing, part 0 gives up its bounded wait for it, and
+    the next call (counters cleared by the status read) is exact."""
+    import torch
+    M, N, K = 300, 520, 1024
+    A = gi.draw_bf16(M, K, gi.Dist("int", -4, 4), 81)
+    B = gi.draw_bf16(N, K, gi.Dist("int", -4, 4), 82)
+    dA, dB = to_dev_bf16(A), to_dev_bf16(B)
+    dD, ldd = empty_out(M, N, gi.OUT_F32)
+    rc, st = call(M, N, K, dA, K, dB, K, None, 0, dD, ldd, 1.0, 0.0, gi.OUT_F32, path=path,
+                  timeout_ns=20_000_000, fault=1, tiled_k_parts=2)
+    assert rc == 0
+    assert st == g.GEMM_ERR_TIMEOUT, (st, g.last_error())
+    s = torch.cuda.current_stream().cuda_stream
+    assert g.gemm_get_status(s) == 0
+    ref, _ = oracle.gemm_ref(A, B)
+    dD2, _ = empty_out(M, N, gi.OUT_F32)
+    rc, st = call(M, N, K, dA, K, dB, K, None, 0, dD2, ldd, 1.0, 0.0, gi.OUT_F32, path=path, tiled_k_parts=2)
+    assert rc == 0 and st == 0
+    assert np.array_equal(from_dev(dD2, gi.OUT_F32), oracle.exact_f32(ref))

@@ -36,7 +36,7 @@ def up8(x):
 
 
 def run_int(M, N, K, path, out_dtype, seed, lda=None, ldb=None, grid=0, skinny_grid=0, alpha=1.0,
-            disable_pdl=0, scheduler=0, skinny_bm=0, skinny_kgroup=0):
+            disable_pdl=0, scheduler=0, skinny_bm=0, skinny_kgroup=0, tiled_k_parts=0):
     lda = up8(K) if lda is None else lda
     ldb = up8(K) if ldb is None else ldb
     A = gi.draw_bf16(M, K, gi.Dist("int", -4, 4), seed, ld=lda)
@@ -46,7 +46,7 @@ def run_int(M, N, K, path, out_dtype, seed, lda=None, ldb=None, grid=0, skinny_g
     dD, ldd = empty_out(M, N, out_dtype, ld=up8(N))
     rc, st = call(M, N, K, dA, lda, dB, ldb, None, 0, dD, ldd, alpha, 0.0, out_dtype, path=path,
                   grid=grid, skinny_grid=skinny_grid, disable_pdl=disable_pdl, scheduler=scheduler,
-                  skinny_bm=skinny_bm, skinny_kgroup=skinny_kgroup)
+                  skinny_bm=skinny_bm, skinny_kgroup=skinny_kgroup, tiled_k_parts=tiled_k_parts)
     assert rc == 0, g.last_error()
     assert st == 0, g.last_error()
     return from_dev(dD, out_dtype)[:, :N], expect_exact(ref, out_dtype)
@@ -506,3 +506,72 @@ def test_plan_matches_the_launch(M, N, K):
             (plan["tile_m"], plan["tile_n"], plan["skinny_grid"], plan["skinny_stages"])
     else:
         assert info["tile_m"] == plan["tile_m"]
+
+
+# ----------------------------------------------------------------------------- tiled k-split
+
+SPLIT_SHAPES = [(129, 257, 1000), (300, 520, 640), (40, 300, 2048), (257, 1100, 96), (7, 9, 17), (128, 256, 512)]
+
+
+@pytest.mark.parametrize("shape", SPLIT_SHAPES)
+@pytest.mark.parametrize("path", [P1, P2])
+@pytest.mark.parametrize("parts", [2, 3, 4])
+def test_tiled_k_split_exact(shape, path, parts):
+    """Tiles split into k-parts: parts > 0 publish fp32 partials, part 0 adds
+    them in part order (exact on integers; K = 17 and 96 leave parts of one
+    or two k-blocks, K = 17 with 4 parts is capped at its single k-block)."""
+    M, N, K = shape
+    got, exp = run_int(M, N, K, path, gi.OUT_F32, seed=390 + M + N + K + parts, tiled_k_parts=parts)
+    assert_same(got, exp)
+    info = g.last_launch_info()
+    assert info["k_parts"] == min(parts, -(-K // 64))
+
+
+@pytest.mark.parametrize("path", [P1, P2])
+@pytest.mark.parametrize("out_dtype", [gi.OUT_F32, gi.OUT_BF16])
+def test_tiled_k_split_with_c_and_epilogue(path, out_dtype):
+    """beta C and the fused bias + ReLU on a split tile (part 0's epilogue only)."""
+    import torch
+    M, N, K = 300, 520, 1024
+    A = gi.draw_bf16(M, K, gi.Dist("int", -4, 4), 395)
+    B = gi.draw_bf16(N, K, gi.Dist("int", -4, 4), 396)
+    Cb = gi.draw_bf16(M, N, gi.Dist("int", -8, 8), 397)
+    bias = gi.draw_bf16(N, 1, gi.Dist("int", -50, 50), 398).reshape(N)
+    ref, _ = oracle.gemm_ref(A, B, Cb, 1.0, 0.5)
+    Cf = gi.bf16_bits_to_f32(Cb)
+    dC = to_dev_bf16(Cb) if out_dtype == gi.OUT_BF16 else to_dev_f32(Cf)
+    dD, ldd = empty_out(M, N, out_dtype)
+    s = torch.cuda.current_stream().cuda_stream
+    cfg = g.GemmConfig(path=path, tiled_k_parts=3)
+    rc = g.gemm_bf16_tn_ex(M, N, K, to_dev_bf16(A).data_ptr(), K, to_dev_bf16(B).data_ptr(), K, dC.data_ptr(), N,
+                           dD.data_ptr(), ldd, 1.0, 0.5, out_dtype, s, cfg)
+    assert rc == 0 and g.gemm_get_status(s) == 0, g.last_error()
+    assert g.last_launch_info()["k_parts"] == 3
+    assert_same(from_dev(dD, out_dtype), expect_exact(ref, out_dtype))
+
+
+def test_tiled_k_split_automatic():
+    """Few tiles and a long K split automatically (300 x 1100 x 8192: 15 tiles
+    of 128 x 256 on 152 SMs, 128 k-blocks -> 2 parts), deterministically."""
+    outs = []
+    for _ in range(3):
+        got, exp = run_int(300, 1100, 8192, 0, gi.OUT_F32, seed=399)
+        assert_same(got, exp)
+        outs.append(got.view(np.uint32))
+        info = g.last_launch_info()
+        assert info["path"] == P1 and info["k_parts"] == 2 and info["grid"] == 30
+    assert np.array_equal(outs[0], outs[1]) and np.array_equal(outs[0], outs[2])
+
+
+def test_tiled_k_split_normal_inputs_within_bound():
+    M, N, K = 224, 2048, 8192
+    A = gi.draw_bf16(M, K, gi.Dist("normal", 1.0), 400)
+    B = gi.draw_bf16(N, K, gi.Dist("normal", 1.0 / K), 401)
+    dD, ldd = empty_out(M, N, gi.OUT_BF16)
+    rc, st = call(M, N, K, to_dev_bf16(A), K, to_dev_bf16(B), K, None, 0, dD, ldd, 1.0, 0.0, gi.OUT_BF16)
+    assert rc == 0 and st == 0, g.last_error()
+    info = g.last_launch_info()
+    assert info["path"] == P2 and info["k_parts"] == 2
+    ref, absdot = oracle.gemm_ref(A, B)
+    ok, worst, where = oracle.check(from_dev(dD, gi.OUT_BF16), ref, absdot, gi.OUT_BF16)
+    assert ok, (worst, where)

@@ -73,7 +73,7 @@ def test_automatic_path(M, N, K, fp8, path):
 def test_skinny_geometry(M, N, K, fp8, geometry):
     p = plan(M, N, K, fp8)
     assert p["path"] == S
-    got = (p["tile_m"], p["skinny_kgroup"], p["skinny_stages"], p["skinny_grid"], p["skinny_parts"],
+    got = (p["tile_m"], p["skinny_kgroup"], p["skinny_stages"], p["skinny_grid"], p["k_parts"],
            p["skinny_skew"])
     assert got == geometry
     assert p["tile_n"] == -(-M // 16) * 16
@@ -84,21 +84,36 @@ def test_skinny_partition_follows_the_sm_count():
     assert plan(16, 8192, 8192, sms=148)["skinny_grid"] == 128
     # 100 SMs: 64 tiles x 1 part leave 36% idle: stream-K over all 100
     p = plan(16, 8192, 8192, sms=100)
-    assert p["skinny_grid"] == 100 and p["skinny_parts"] == 0
+    assert p["skinny_grid"] == 100 and p["k_parts"] == 0
 
 
 def test_overrides_reach_the_plan():
     p = plan(16, 8192, 8192, path=S, skinny_bm=64, skinny_kgroup=2, skinny_skew_kb=-1)
-    assert (p["tile_m"], p["skinny_kgroup"], p["skinny_parts"], p["skinny_skew"]) == (64, 2, 1, 0)
+    assert (p["tile_m"], p["skinny_kgroup"], p["k_parts"], p["skinny_skew"]) == (64, 2, 1, 0)
     p = plan(16, 8192, 8192, path=S, skinny_grid=37)
-    assert p["skinny_grid"] == 37 and p["skinny_parts"] == 0
+    assert p["skinny_grid"] == 37 and p["k_parts"] == 0
     assert plan(16, 8192, 8192, path=P2)["tile_m"] == 256
     assert plan(8192, 8192, 8192, path=P1)["tile_m"] == 128
 
 
 def test_tiled_tile_shape():
     p = plan(8192, 28672, 4096)
-    assert (p["tile_m"], p["tile_n"], p["skinny_grid"]) == (256, 256, 0)
+    assert (p["tile_m"], p["tile_n"], p["skinny_grid"], p["k_parts"]) == (256, 256, 0, 1)
+
+
+@pytest.mark.parametrize("M,N,K,path,parts", [
+    (256, 2048, 8192, P2, 2),     # 37.4 us against 42.5 unsplit
+    (224, 8192, 8192, P2, 1),     # 32 pair tiles: even (44.6 against 44.0)
+    (300, 1100, 8192, P1, 2),
+    (192, 4096, 4096, P2, 1),     # split 29.2 against 25.1: K too short
+    (1024, 2048, 2048, P1, 1),
+    (96, 28672, 8192, P1, 1),     # 112 tiles: more than half of the SMs
+])
+def test_tiled_k_split_choice(M, N, K, path, parts):
+    p = plan(M, N, K)
+    assert (p["path"], p["k_parts"]) == (path, parts)
+    # forced parts are capped at K's k-blocks
+    assert plan(M, N, 128, path=path, tiled_k_parts=4)["k_parts"] == 2
 
 
 @pytest.mark.parametrize("args,cfg,code,text", [
