@@ -96,8 +96,11 @@ typedef enum {
   GEMM_PATH_1SM = 1,    /* persistent tiled kernel, 128x256 tile, one CTA per SM */
   GEMM_PATH_2SM = 2,    /* persistent tiled kernel, 256x256 tile per CTA pair */
   GEMM_PATH_SKINNY = 3  /* M <= 256: swap-AB stream-K HBM streaming of B (the tokens are MMA N);
-                           automatic for M <= 32, and for 32 < M <= 128 when B (N x K) is at
-                           least 32 MiB and each tile is split into at most two k-parts.
+                           automatic for M <= 32; for 32 < M <= 64 when each tile is split into
+                           at most two k-parts and B (N x K) is at least 32 MiB, or into at most
+                           four with K at least 64 k-blocks; for 64 < M <= 128 when B is at least
+                           32 MiB, N <= 8192, tiles are split at most in two, and N = 8192 or K
+                           holds at least 128 k-blocks (k-block: 64 bf16 or 128 fp8 elements).
                            AUTO otherwise takes pair tiles (2SM) when B is at least 32 MiB and
                            M > 128 or the 1-SM tiles would fill at most half of the SMs, or
                            when M > 128 with more than 64 tiles of 128x256; else 1SM */

@@ -229,10 +229,11 @@ long long one_sm_tiles(int64_t M, int64_t N) { return ((M + 127) / 128) * ((N + 
 // - 33..128 tokens: streaming where B is too large to stay in L2 between
 //   calls (>= 32 MiB) and the streaming kernel splits each tile into at most
 //   two k-parts.  128 x 8192 x 8192: 38.5 us against 43.6 (2-SM) and 56.6
-//   (1-SM).  Where tiles would be split into more parts (64 x 1024 x 4096:
-//   31.8 against 21.9 us) or fall to stream-K (64 x 28672 x 4096: 49.9
-//   against 44.5 us), or B is small (64 x 4096 x 1024: 13.1 against 9.3 us),
-//   the tiled kernels win.
+//   (1-SM).  Where tiles fall to stream-K (64 x 28672 x 4096: 49.9 against
+//   44.5 us) or B is small (64 x 4096 x 1024: 13.1 against 9.3 us), the
+//   tiled kernels win.  Refinements (see auto_path): up to 64 tokens, four
+//   parts with a long K also stream; above 64, only N <= 8192 with long
+//   rows streams.
 // - When B streams from HBM and the tiles are few, pair tiles win over 1-SM
 //   tiles even for M <= 128: each SM of a pair loads half of the B tile, and
 //   twice the SMs stream (96 x 16384 x 8192: 53.5 against 61.6 us).  For
@@ -287,8 +288,17 @@ int auto_path(int64_t M, int64_t N, int64_t K, int in_bytes, int sms) {
   const int np = (int)((M + 15) / 16) * 16;
   const int parts = M <= 256 ? skinny_parts(N, np, skinny_max_grid(np, sms)) : 0;
   const long long tiles = one_sm_tiles(M, N);
+  const long long num_kb = (K + 128 / in_bytes - 1) / (128 / in_bytes);
   if (M <= 32) return GEMM_PATH_SKINNY;
-  if (M <= 128 && streamed && parts >= 1 && parts <= 2) return GEMM_PATH_SKINNY;
+  // 33..64 tokens: also on a few tiles split four ways once K is long
+  // (64 x 1024 x 8192: 24.1 against 37.8 us on split 1-SM tiles)
+  if (M <= 64 && parts >= 1 && ((streamed && parts <= 2) || num_kb >= 64)) return GEMM_PATH_SKINNY;
+  // 65..128 tokens (wide form): only up to N = 8192 and with long rows of B
+  // (96 x 4096 x 4096: 25.9 against 23.5 us on pair tiles; 128 x 16384 x K:
+  // pair tiles 4-17% faster; 128 x 4096 x 8192 and 128 x 8192 x 4096: the
+  // streaming kernel is the fastest)
+  if (M > 64 && M <= 128 && streamed && parts >= 1 && parts <= 2 && N <= 8192 && (N >= 8192 || num_kb >= 128))
+    return GEMM_PATH_SKINNY;
   if (M > 128 && (streamed || tiles > kSmallTileCount)) return GEMM_PATH_2SM;
   if (M <= 128 && streamed && 2 * tiles <= sms) return GEMM_PATH_2SM;
   return GEMM_PATH_1SM;

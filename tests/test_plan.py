@@ -30,14 +30,19 @@ def plan(M, N, K, fp8=0, sms=152, **cfg):
     (32, 1024, 1024, 0, S),
     (64, 8192, 8192, 0, S),      # 64-row whole tiles 31.4 us; 2-SM 43.1
     (64, 4096, 4096, 0, S),      # 18.8 us; 2-SM 23.4
-    (64, 1024, 4096, 0, P1),     # small B: 1-SM 21.9 us; skinny 31.8
+    (64, 1024, 4096, 0, S),      # 4 parts: skinny 20.5 us; 1-SM 21.9
+    (64, 1024, 8192, 0, S),      # skinny 24.1 us; split 1-SM 37.8
+    (64, 1024, 2048, 0, P1),     # K short: 1-SM 13.4 us
     (64, 4096, 1024, 0, P1),     # 8 MiB B: 1-SM 9.3 us; skinny 13.1
     (64, 28672, 4096, 0, P1),    # stream-K skinny 49.9 us; 1-SM 44.5
     (96, 1024, 2048, 0, P1),     # 1-SM 13.5 us; skinny 49.7
     (96, 8192, 2048, 0, S),      # 32 MiB: skinny 14.7 us; 2-SM 15.5
     (96, 8192, 4096, 1, S),      # fp8, 32 MiB
     (96, 8192, 2048, 1, P1),     # fp8, 16 MiB stays in L2
-    (96, 16384, 8192, 0, S),     # skinny 53.0 us; 2-SM 53.5
+    (96, 16384, 8192, 0, P2),    # N > 8192: 2-SM 53.0 us, skinny 53.0
+    (128, 16384, 2048, 0, P2),   # 2-SM 18.0 us; skinny 19.9
+    (128, 4096, 4096, 0, P2),    # 2-SM 23.7 us; skinny 29.5
+    (128, 4096, 8192, 0, S),     # skinny 37.6 us
     (128, 8192, 8192, 0, S),     # skinny 38.5 us; 2-SM 43.6; 1-SM 56.6
     (96, 28672, 8192, 0, P1),    # 1-SM 83.1 us; skinny 90.6
     (160, 8192, 8192, 0, P2),    # 2-SM 43.8 us; skinny 46.9
