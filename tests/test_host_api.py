@@ -153,3 +153,10 @@ def test_unknown_skinny_kgroup_rejected(lib, kg):
     a = (16, 64, 64, 0x1000, 64, 0x2000, 64, 0, 0, 0x3000, 64, 1.0, 0.0, 0, 0)
     assert g.gemm_bf16_tn_ex(*a, config=g.GemmConfig(skinny_kgroup=kg)) == g.GEMM_ERR_INVALID_VALUE
     assert "skinny_kgroup" in g.last_error()
+
+
+@pytest.mark.parametrize("parts", [5, -1])
+def test_unknown_tiled_k_parts_rejected(lib, parts):
+    a = (300, 64, 64, 0x1000, 64, 0x2000, 64, 0, 0, 0x3000, 64, 1.0, 0.0, 0, 0)
+    assert g.gemm_bf16_tn_ex(*a, config=g.GemmConfig(tiled_k_parts=parts)) == g.GEMM_ERR_INVALID_VALUE
+    assert "tiled_k_parts" in g.last_error()
