@@ -119,7 +119,8 @@ typedef struct gemm_tn_config {
   int disable_pdl;          /* 1 = launch without programmatic dependent launch (see below) */
   int skinny_skew_kb;       /* skinny path, equal-split mode: k-blocks (of 64 bf16 or 128 fp8 elements)
                                moved to the part that finishes each tile, rounded up to whole k-groups;
-                               0 = default (M rounded up to 16, divided by 4), < 0 = none */
+                               0 = default (8, or M rounded up to 16 divided by 4 when
+                               that is larger), < 0 = none */
   int scheduler;            /* tiled paths: GEMM_SCHED_* (0 = the default) */
   int skinny_bm;            /* skinny path: rows of B per tile (MMA M), 64 or 128; 0 = auto: 64 where
                                64-row tiles fit one wave and M > 32 (or M > 16 and 128-row tiles would

@@ -20,11 +20,13 @@
 // bytes.  A CTA that covers a whole n-tile writes D directly.  In a tile
 // split between CTAs, the CTA holding the tile's first k-blocks finishes it:
 // that part is always the last segment of its range, so by the time it gets
-// there the other parts (first segments, or whole ranges, of later CTAs) are
-// done or nearly so.  Those write fp32 partials to a workspace and count
-// them without waiting; the finisher waits (bounded) for the count and adds
-// the parts in k order, so the result does not depend on timing.  No CTA
-// waits in front of a part another CTA needs, so waits never chain.
+// there the other parts (first segments, or whole ranges, of the ranges
+// after it) are done or nearly so.  Those write fp32 partials to a workspace
+// and count them without waiting; the finisher waits (bounded) for the count
+// and adds the parts in k order, so the result does not depend on timing.  No
+// CTA waits in front of a part another CTA needs, so waits never chain, and
+// ranges go to CTAs in reverse order so that a finisher never waits for a CTA
+// with a higher index (one that may not be resident yet).
 //
 // Roles: warp 0 lane 0 issues TMA loads into a deep ring (its first loads go
 // out before the block-wide start-up sync); warp 1 lane 0 issues tcgen05.mma
@@ -87,14 +89,21 @@ __device__ __forceinline__ long long split_bound(const SkinnyParams& p, long lon
   return j * p.num_kb / p.split + p.skew;
 }
 
+// CTAs take the ranges in reverse order: range r belongs to CTA grid-1-r
+// (stream-K), part j of tile n to CTA n + (split-1-j) * n_tiles (equal
+// split).  A tile is finished by the CTA holding its first k-blocks, which
+// so has the highest index of the tile's CTAs: every part it waits for
+// belongs to a CTA launched before it, even when other work holds SMs and
+// not all CTAs are resident at once.
+
 // First and one-past-last unit of CTA c's range.
 __device__ __forceinline__ long long cta_begin(const SkinnyParams& p, long long c) {
-  if (p.split == 0) return range_start(c, p.units, p.grid);
-  return (c % p.n_tiles) * p.num_kb + split_bound(p, c / p.n_tiles);
+  if (p.split == 0) return range_start(p.grid - 1 - c, p.units, p.grid);
+  return (c % p.n_tiles) * p.num_kb + split_bound(p, p.split - 1 - c / p.n_tiles);
 }
 __device__ __forceinline__ long long cta_end(const SkinnyParams& p, long long c) {
-  if (p.split == 0) return range_start(c + 1, p.units, p.grid);
-  return (c % p.n_tiles) * p.num_kb + split_bound(p, c / p.n_tiles + 1);
+  if (p.split == 0) return range_start(p.grid - c, p.units, p.grid);
+  return (c % p.n_tiles) * p.num_kb + split_bound(p, p.split - c / p.n_tiles);
 }
 
 // Number of CTAs holding a part of tile n, and the CTA holding part j
@@ -105,8 +114,8 @@ __device__ __forceinline__ int tile_parts(const SkinnyParams& p, long long n) {
   return (int)(owner_of((n + 1) * KB - 1, p.units, p.grid) - owner_of(n * KB, p.units, p.grid) + 1);
 }
 __device__ __forceinline__ long long tile_part_cta(const SkinnyParams& p, long long n, int j) {
-  if (p.split) return n + (long long)j * p.n_tiles;
-  return owner_of(n * p.num_kb, p.units, p.grid) + j;
+  if (p.split) return n + (long long)(p.split - 1 - j) * p.n_tiles;
+  return p.grid - 1 - (owner_of(n * p.num_kb, p.units, p.grid) + j);
 }
 
 __device__ __noinline__ bool wait_bar_slow(uint32_t bar, uint32_t parity, volatile uint32_t* flag,
@@ -711,9 +720,10 @@ void skinny_partition(SkinnyParams* p, int num_sms, int grid_override, int skew_
   // as long as it keeps at least 80% of the SMs streaming, or reaches the
   // cap of four parts (split_parts).  s = 1 is a whole
   // tile per CTA, with no partial sums.  Part j of tile n goes to CTA
-  // n + j * n_tiles, so the parts of a tile sit on SMs spread across the
-  // grid.  Part 0's CTA finishes the tile after the other parts land, so it
-  // gets a few more k-blocks.
+  // n + (s - 1 - j) * n_tiles, so the parts of a tile sit on SMs spread
+  // across the grid and the finishing part 0 comes last.  Part 0's CTA
+  // finishes the tile after the other parts land, so it gets a few more
+  // k-blocks.
   {
     const int s = split_parts(p->n_tiles, num_sms);
     if (s >= 1 && s <= p->num_kb) {
@@ -721,11 +731,13 @@ void skinny_partition(SkinnyParams* p, int num_sms, int grid_override, int skew_
       p->split = s;
       // Skew in k-blocks, rounded up to whole k-groups.  The finisher's extra
       // work (its partial hand-off and the store) grows with the tokens, not
-      // with K, so the default is np / 4 k-blocks.  Measured on 8192 x 8192
-      // (graph-replayed): 32 tokens 28.0 -> 27.0 us bf16 and 17.7 -> 16.4 us
-      // e4m3 against K / 4096 k-blocks; 16 tokens are flat from 4 to 8.
+      // with K: the default is 8 k-blocks, or np / 4 for more than 32 tokens.
+      // Measured on 8192 x 8192 (graph-replayed), 8 against 4 k-blocks: 16
+      // tokens 15.15 against 15.68 us e4m3, 25.65 against 25.82 bf16; 32
+      // tokens 26.9 against 27.4 bf16 and 16.0 against 16.8 e4m3; 12 k-blocks
+      // slower again.
       const int kg = p->kg > 0 ? p->kg : 1;
-      const int skew_blocks = skew_kb > 0 ? skew_kb : (skew_kb < 0 ? 0 : p->np / 4);
+      const int skew_blocks = skew_kb > 0 ? skew_kb : (skew_kb < 0 ? 0 : (p->np / 4 > 8 ? p->np / 4 : 8));
       int skew = (skew_blocks + kg - 1) / kg;
       const int room = p->num_kb / s - 1;  // every part keeps at least one k-group
       p->skew = s < 2 ? 0 : (skew < room ? skew : (room > 0 ? room : 0));
