@@ -575,3 +575,17 @@ def test_tiled_k_split_normal_inputs_within_bound():
     ref, absdot = oracle.gemm_ref(A, B)
     ok, worst, where = oracle.check(from_dev(dD, gi.OUT_BF16), ref, absdot, gi.OUT_BF16)
     assert ok, (worst, where)
+
+
+@pytest.mark.parametrize("out_dtype", [gi.OUT_F32, gi.OUT_BF16])
+def test_skinny_whole_tiles_beyond_one_wave(out_dtype):
+    """More 128-row tiles than SMs (304 at N = 38912): each CTA takes whole
+    tiles, no partial sums; exact, and the grid is the one gemm_plan gives."""
+    import torch
+    M, N, K = 16, 38912, 256
+    sms = torch.cuda.get_device_properties(0).multi_processor_count
+    rc, plan = g.gemm_plan(M, N, K, 0, sms)
+    assert rc == 0
+    got, exp = run_int(M, N, K, PS, out_dtype, seed=410)
+    assert_same(got, exp)
+    assert g.last_launch_info()["grid"] == plan["skinny_grid"]

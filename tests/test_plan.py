@@ -84,6 +84,18 @@ def test_skinny_geometry(M, N, K, fp8, geometry):
     assert p["tile_n"] == -(-M // 16) * 16
 
 
+@pytest.mark.parametrize("N,K,fp8,grid", [
+    (32768, 8192, 0, 128),    # 256 tiles: 2 whole tiles per CTA (83.2 against 86.1 us stream-K)
+    (28672, 8192, 1, 112),    # 224 tiles: 2 per CTA
+    (57344, 4096, 1, 112),    # 448 tiles: 4 per CTA
+    (131072, 4096, 0, 128),   # 1024 tiles: 8 per CTA
+    (20480, 8192, 0, 152),    # 160 tiles: 80 CTAs would idle too many SMs: stream-K
+])
+def test_skinny_whole_tiles_when_tiles_exceed_sms(N, K, fp8, grid):
+    p = plan(16, N, K, fp8)
+    assert (p["path"], p["tile_m"], p["skinny_grid"], p["k_parts"]) == (S, 128, grid, 0)
+
+
 def test_skinny_partition_follows_the_sm_count():
     # 148 SMs: 64 tiles x 2 parts still keep >= 80% of the SMs busy
     assert plan(16, 8192, 8192, sms=148)["skinny_grid"] == 128
