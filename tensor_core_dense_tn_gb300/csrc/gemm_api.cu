@@ -149,14 +149,21 @@ uint64_t timeout_ns(const gemm_tn_config* cfg) {
   return env;
 }
 
-int get_workspace(int dev, cudaStream_t stream, size_t partial_floats, size_t counter_ints, Workspace** out) {
+// `optional`: the caller can do without (the tiled k-split): where the
+// workspace would have to grow during stream capture, return GEMM_OK with
+// *out = nullptr instead of an error.
+int get_workspace(int dev, cudaStream_t stream, size_t partial_floats, size_t counter_ints, Workspace** out,
+                  bool optional = false) {
   std::lock_guard<std::mutex> lk(g_mu);
+  *out = nullptr;
   Workspace& w = g_ws[{dev, reinterpret_cast<uintptr_t>(stream)}];
   if (w.partial_floats < partial_floats || w.counter_ints < counter_ints) {
     cudaStreamCaptureStatus cs = cudaStreamCaptureStatusNone;
     cudaStreamIsCapturing(stream, &cs);
-    if (cs != cudaStreamCaptureStatusNone)
+    if (cs != cudaStreamCaptureStatusNone) {
+      if (optional) return GEMM_OK;
       return fail(GEMM_ERR_INVALID_VALUE, "split-K workspace must be created outside stream capture");
+    }
     // Work already queued may still use the old buffers.
     cudaError_t e = cudaStreamSynchronize(stream);
     if (e != cudaSuccess) return fail(GEMM_ERR_CUDA, "cudaStreamSynchronize: %s", cudaGetErrorString(e));
@@ -442,12 +449,17 @@ int run(int64_t M, int64_t N, int64_t K, const void* A, int64_t lda, const void*
     p.ksplit = p.clc || (cfg && cfg->grid > 0) ? 1 : tiled_parts(p.num_tiles, p.num_kb, st->sms, cg, cfg);
     if (p.ksplit > p.num_kb) p.ksplit = p.num_kb > 1 ? p.num_kb : 1;  // every part owns a k-block
     if (p.ksplit > 1) {
+      // optional: during a capture that would need a larger workspace, run unsplit
       Workspace* w = nullptr;
       rc = get_workspace(dev, stream, (size_t)p.num_tiles * (p.ksplit - 1) * cg * 128 * 256,
-                         (size_t)p.num_tiles * cg * 4, &w);
+                         (size_t)p.num_tiles * cg * 4, &w, true);
       if (rc != GEMM_OK) return rc;
-      p.partials = w->partials;
-      p.counters = w->counters;
+      if (w) {
+        p.partials = w->partials;
+        p.counters = w->counters;
+      } else {
+        p.ksplit = 1;
+      }
     }
     CUtensorMap tA, tB, tC, tD;
     memset(&tA, 0, sizeof tA);

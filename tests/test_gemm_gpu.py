@@ -589,3 +589,31 @@ def test_skinny_whole_tiles_beyond_one_wave(out_dtype):
     got, exp = run_int(M, N, K, PS, out_dtype, seed=410)
     assert_same(got, exp)
     assert g.last_launch_info()["grid"] == plan["skinny_grid"]
+
+
+def test_tiled_split_first_used_inside_graph_capture():
+    """A split-eligible shape first called while a fresh stream is captured:
+    its workspace cannot grow then, so the call runs unsplit instead of
+    failing, and the replayed graph is exact."""
+    import torch
+    M, N, K = 300, 1104, 8192
+    A = gi.draw_bf16(M, K, gi.Dist("int", -4, 4), 420)
+    B = gi.draw_bf16(N, K, gi.Dist("int", -4, 4), 421)
+    ref, _ = oracle.gemm_ref(A, B)
+    dA, dB = to_dev_bf16(A), to_dev_bf16(B)
+    dD, ldd = empty_out(M, N, gi.OUT_F32)
+    stream = torch.cuda.Stream()
+    graph = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(graph, stream=stream):
+        rc = g.gemm_bf16_tn_ex(M, N, K, dA.data_ptr(), K, dB.data_ptr(), K, 0, 0, dD.data_ptr(), ldd, 1.0, 0.0,
+                               gi.OUT_F32, stream.cuda_stream, None)
+    assert rc == 0, g.last_error()
+    assert g.last_launch_info()["k_parts"] == 1
+    graph.replay()
+    torch.cuda.synchronize()
+    assert g.gemm_get_status(stream.cuda_stream) == 0
+    assert_same(from_dev(dD, gi.OUT_F32), oracle.exact_f32(ref))
+    # outside capture the same shape splits
+    got, exp = run_int(M, N, K, 0, gi.OUT_F32, seed=422)
+    assert_same(got, exp)
+    assert g.last_launch_info()["k_parts"] == 2
