@@ -133,7 +133,8 @@ typedef struct gemm_tn_config {
                                0 = auto (2 when the tiles fill at most a quarter of the clusters and K
                                holds at least 128 k-blocks, else 1), 1 = no split.  Capped at launch
                                so that every part has a co-resident cluster and at K's k-blocks;
-                               ignored with CLC or a grid override.  Inside a stream capture that
+                               ignored with CLC, a grid override or a fused epilogue
+                               (gemm_bf16_tn_bias_act).  Inside a stream capture that
                                would have to grow the stream's split workspace, the call runs
                                unsplit (the skinny path returns an error there instead) */
 } gemm_tn_config;

@@ -446,7 +446,10 @@ int run(int64_t M, int64_t N, int64_t K, const void* A, int64_t lda, const void*
     p.alpha = alpha; p.beta = beta; p.has_c = has_c; p.epi = epi;
     p.fault = fault; p.timeout_ns = tmo; p.status = st->status;
     p.clc = sched == GEMM_SCHED_CLC ? 1 : 0;
-    p.ksplit = p.clc || (cfg && cfg->grid > 0) ? 1 : tiled_parts(p.num_tiles, p.num_kb, st->sms, cg, cfg);
+    // no split with CLC, a grid override or a fused epilogue (bias and
+    // activation would sit on the unit's critical path, after the hand-off)
+    p.ksplit = p.clc || (cfg && cfg->grid > 0) || epi.bias || epi.act
+                   ? 1 : tiled_parts(p.num_tiles, p.num_kb, st->sms, cg, cfg);
     if (p.ksplit > p.num_kb) p.ksplit = p.num_kb > 1 ? p.num_kb : 1;  // every part owns a k-block
     if (p.ksplit > 1) {
       // optional: during a capture that would need a larger workspace, run unsplit

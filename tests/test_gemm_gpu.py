@@ -529,21 +529,21 @@ def test_tiled_k_split_exact(shape, path, parts):
 
 @pytest.mark.parametrize("path", [P1, P2])
 @pytest.mark.parametrize("out_dtype", [gi.OUT_F32, gi.OUT_BF16])
-def test_tiled_k_split_with_c_and_epilogue(path, out_dtype):
-    """beta C and the fused bias + ReLU on a split tile (part 0's epilogue only)."""
+def test_tiled_k_split_with_c(path, out_dtype):
+    """beta C on a split tile (part 0's epilogue only)."""
     import torch
     M, N, K = 300, 520, 1024
     A = gi.draw_bf16(M, K, gi.Dist("int", -4, 4), 395)
     B = gi.draw_bf16(N, K, gi.Dist("int", -4, 4), 396)
     Cb = gi.draw_bf16(M, N, gi.Dist("int", -8, 8), 397)
-    bias = gi.draw_bf16(N, 1, gi.Dist("int", -50, 50), 398).reshape(N)
     ref, _ = oracle.gemm_ref(A, B, Cb, 1.0, 0.5)
     Cf = gi.bf16_bits_to_f32(Cb)
     dC = to_dev_bf16(Cb) if out_dtype == gi.OUT_BF16 else to_dev_f32(Cf)
     dD, ldd = empty_out(M, N, out_dtype)
     s = torch.cuda.current_stream().cuda_stream
     cfg = g.GemmConfig(path=path, tiled_k_parts=3)
-    rc = g.gemm_bf16_tn_ex(M, N, K, to_dev_bf16(A).data_ptr(), K, to_dev_bf16(B).data_ptr(), K, dC.data_ptr(), N,
+    dA, dB = to_dev_bf16(A), to_dev_bf16(B)   # alive until the kernel has run
+    rc = g.gemm_bf16_tn_ex(M, N, K, dA.data_ptr(), K, dB.data_ptr(), K, dC.data_ptr(), N,
                            dD.data_ptr(), ldd, 1.0, 0.5, out_dtype, s, cfg)
     assert rc == 0 and g.gemm_get_status(s) == 0, g.last_error()
     assert g.last_launch_info()["k_parts"] == 3
@@ -617,3 +617,22 @@ def test_tiled_split_first_used_inside_graph_capture():
     got, exp = run_int(M, N, K, 0, gi.OUT_F32, seed=422)
     assert_same(got, exp)
     assert g.last_launch_info()["k_parts"] == 2
+
+
+def test_fused_epilogue_is_never_split():
+    """A shape the plain GEMM splits (300 x 1104 x 8192) runs unsplit with a
+    fused bias + ReLU, exactly."""
+    import torch
+    M, N, K = 300, 1104, 8192
+    A = gi.draw_bf16(M, K, gi.Dist("int", -4, 4), 430)
+    B = gi.draw_bf16(N, K, gi.Dist("int", -4, 4), 431)
+    bias = gi.draw_bf16(N, 1, gi.Dist("int", -50, 50), 432).reshape(N)
+    ref, _ = oracle.gemm_ref(A, B)
+    dD, ldd = empty_out(M, N, gi.OUT_F32)
+    dA, dB, dbias = to_dev_bf16(A), to_dev_bf16(B), to_dev_bf16(bias)   # alive until the kernel has run
+    s = torch.cuda.current_stream().cuda_stream
+    rc = g.gemm_bf16_tn_bias_act(M, N, K, dA.data_ptr(), K, dB.data_ptr(), K, 0, 0,
+                                 dD.data_ptr(), ldd, 1.0, 0.0, gi.OUT_F32, dbias.data_ptr(), 0, 1, s)
+    assert rc == 0 and g.gemm_get_status(s) == 0, g.last_error()
+    assert g.last_launch_info()["k_parts"] == 1
+    assert_same(from_dev(dD, gi.OUT_F32), oracle.exact_f32(oracle.epilogue(ref, bias, 1)))
