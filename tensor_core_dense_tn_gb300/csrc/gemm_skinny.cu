@@ -1,4 +1,5 @@
-// Skinny-M BF16 TN GEMM (M <= 64): HBM-bound streaming of B.
+// Skinny-M TN GEMM (M <= 64, a wide form up to 256; bf16 or fp8 inputs):
+// HBM-bound streaming of B.
 //
 // With M tokens this small the arithmetic intensity is ~M FLOP per byte of B
 // (the GEMV/decode bound of the Ampere-to-Hopper page, section on decode:
@@ -10,10 +11,10 @@
 //
 // Swap-AB: the tensor core computes D^T = B * A^T, so the BM rows of a B
 // tile fill the MMA's M and the (padded) M tokens become MMA N = np.  BM is
-// 128, or 64 when 64-row tiles fill the GPU in one wave without splitting a
-// tile (16 x 8192 x 8192: 128 tiles, one per CTA, no partial sums at all).
-// With M = 64 the accumulator's row r sits in TMEM lane (r / 16) * 32 +
-// r % 16: each epilogue warp finds its 16 rows in lanes 0..15 of its quarter.
+// 128, or 64 where 64-row tiles fit one wave and cut the k-parts a tile is
+// split into (skinny_tile_rows).  With M = 64 the accumulator's row r sits in
+// TMEM lane (r / 16) * 32 + r % 16: each epilogue warp finds its 16 rows in
+// lanes 0..15 of its quarter.
 //
 // Work is the list of (n-tile, k-block) units, split into `grid` contiguous
 // ranges, one per CTA (stream-K), so every SM streams the same number of
