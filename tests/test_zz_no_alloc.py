@@ -35,8 +35,11 @@ def test_noalloc_matches_regular_entry_point_twice_in_a_row():
 
     stream = torch.cuda.current_stream().cuda_stream
     cases = [  # (M, N, K, out, beta)
-        (16, 2112, 4096, gi.OUT_BF16, 0.0),
-        (40, 1000, 3000, gi.OUT_F32, -0.5),
+        (16, 2112, 4096, gi.OUT_BF16, 0.0),     # two k-parts per tile, 4 k-blocks per box
+        (40, 1000, 3000, gi.OUT_F32, -0.5),     # K not a whole number of k-blocks
+        (64, 8192, 1024, gi.OUT_BF16, 0.0),     # 128 whole 64-row tiles
+        (16, 38912, 256, gi.OUT_F32, 0.0),      # 304 tiles: whole tiles, two per CTA
+        (16, 1024, 2048, gi.OUT_BF16, 0.0),     # 8 tiles in four parts (the cap)
     ]
     for i, (M, N, K, out, beta) in enumerate(cases):
         A = gi.draw_bf16(M, K, gi.Dist("normal", 1.0), 5100 + 3 * i)
