@@ -304,7 +304,7 @@ def run_ours(args, dist):
                        grid=info.get("grid"), cluster=info.get("cluster"),
                        tile=[info.get("tile_m"), info.get("tile_n")], stages=info.get("stages"),
                        scheduler={1: "static", 2: "clc"}.get(info.get("scheduler"), None),
-                       l2="operands (288 MiB) larger than L2; no flush" if args.workload == MAIN
+                       l2="operands (288 MiB) larger than L2; no flush" if args.workload == MAIN and not args.shape
                        else "see workload", parallelism=f"replicas x{dist.world}"),
         "roofline": roof,
         "gpu_launches": args.steps,

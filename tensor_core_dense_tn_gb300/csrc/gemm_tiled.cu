@@ -802,8 +802,14 @@ cudaError_t launch_impl(const CUtensorMap& tmA, const CUtensorMap& tmB, const CU
          {"gemm_tn_tiled_kernel<2,bf16,list>", "gemm_tn_tiled_kernel<2,f32,list>"}},
         {{"gemm_tn_tiled_kernel<1,bf16,strided>", "gemm_tn_tiled_kernel<1,f32,strided>"},
          {"gemm_tn_tiled_kernel<2,bf16,strided>", "gemm_tn_tiled_kernel<2,f32,strided>"}}};
-    info->kernel = MODE == kModeSingle ? names[KIND][CG - 1][OUT_F32 ? 1 : 0]
-                                       : group_names[MODE == kModeStrided][CG - 1][OUT_F32 ? 1 : 0];
+    static const char* split_names[2][2][2] = {
+        {{"gemm_tn_tiled_kernel<1,bf16,split>", "gemm_tn_tiled_kernel<1,f32,split>"},
+         {"gemm_tn_tiled_kernel<2,bf16,split>", "gemm_tn_tiled_kernel<2,f32,split>"}},
+        {{"gemm_tn_tiled_kernel<1,bf16,fp8 in,split>", "gemm_tn_tiled_kernel<1,f32,fp8 in,split>"},
+         {"gemm_tn_tiled_kernel<2,bf16,fp8 in,split>", "gemm_tn_tiled_kernel<2,f32,fp8 in,split>"}}};
+    info->kernel = MODE != kModeSingle ? group_names[MODE == kModeStrided][CG - 1][OUT_F32 ? 1 : 0]
+                   : p.ksplit > 1  ? split_names[KIND][CG - 1][OUT_F32 ? 1 : 0]
+                                   : names[KIND][CG - 1][OUT_F32 ? 1 : 0];
   }
   return cudaLaunchKernelEx(&cfg, kern, tmA, tmB, tmC, tmD, p, ga);
 }
