@@ -97,3 +97,11 @@ def test_unknown_scheduler_rejected():
     dD, ldd = empty_out(256, 256, gi.OUT_F32)
     rc, _ = call(256, 256, 64, dA, 64, dA, 64, None, 0, dD, ldd, 1.0, 0.0, gi.OUT_F32, scheduler=7)
     assert rc == g.GEMM_ERR_INVALID_VALUE
+
+
+def test_clc_scheduler_never_splits():
+    """A k-split request under cluster launch control runs unsplit."""
+    got, exp = run_int(300, 520, 640, 2, gi.OUT_F32, seed=930, scheduler=2, tiled_k_parts=2)
+    assert_same(got, exp)
+    info = g.last_launch_info()
+    assert info["scheduler"] == 2 and info["k_parts"] == 1

@@ -188,3 +188,25 @@ def test_forced_path_and_kgroups(path, bm, kg, fmt):
     info = g.last_launch_info()
     assert info["path"] == path and (bm == 0 or info["tile_m"] == bm)
     assert np.array_equal(from_dev(dD, gi.OUT_F32), oracle.exact_f32(ref))
+
+
+@pytest.mark.parametrize("path", [1, 2])
+@pytest.mark.parametrize("parts", [2, 3])
+def test_fp8_tiled_k_split_exact(path, parts):
+    """fp8 inputs on split tiles (k-blocks of 128 elements: K = 1408 is 11)."""
+    import torch
+    fmt = gi.FP8_E4M3
+    M, N, K = 300, 520, 1408
+    A = gi.draw_fp8(M, K, gi.Dist("int", -4, 4), 5700 + parts, fmt)
+    B = gi.draw_fp8(N, K, gi.Dist("int", -4, 4), 5710 + parts, fmt)
+    ref, _ = oracle.gemm_ref_fp8(A, B, fmt)
+    dA, dB = to_dev_u8(A), to_dev_u8(B)
+    dD, ldd = empty_out(M, N, gi.OUT_F32)
+    s = torch.cuda.current_stream().cuda_stream
+    cfg = g.GemmConfig(path=path, tiled_k_parts=parts)
+    rc = g.gemm_fp8_tn_ex(M, N, K, dA.data_ptr(), K, dB.data_ptr(), K, fmt, 1.0, 1.0, 0, 0,
+                          dD.data_ptr(), ldd, 1.0, 0.0, gi.OUT_F32, s, cfg)
+    assert rc == 0 and g.gemm_get_status(s) == 0, g.last_error()
+    info = g.last_launch_info()
+    assert info["path"] == path and info["k_parts"] == parts and "split" in info["kernel"]
+    assert np.array_equal(from_dev(dD, gi.OUT_F32), oracle.exact_f32(ref))
