@@ -138,7 +138,7 @@ def test_tiled_k_split_choice(M, N, K, path, parts):
     ((16, 64, 0), dict(path=3), g.GEMM_ERR_NOT_IMPLEMENTED, "skinny"),
     ((144, 256, 1024), dict(path=3, skinny_bm=128, skinny_kgroup=4), g.GEMM_ERR_INVALID_VALUE, "ring stages"),
     ((-1, 64, 64), {}, g.GEMM_ERR_INVALID_VALUE, "negative"),
-    ((16, 64, 64), dict(skinny_kgroup=3), g.GEMM_ERR_INVALID_VALUE, "skinny_kgroup"),
+    ((16, 64, 64), dict(skinny_kgroup=5), g.GEMM_ERR_INVALID_VALUE, "skinny_kgroup"),
     ((16, 64, 64), dict(path=9), g.GEMM_ERR_INVALID_VALUE, "path"),
 ])
 def test_plan_errors(args, cfg, code, text):
