@@ -14,6 +14,11 @@ no flush is needed between steps.  Alongside it, in the same run:
   grouped calls;
 * ``fp8``: the e4m3 variant on both shapes (per-tensor scales folded into
   alpha), against twice the measured bf16 peak and the copy bandwidth;
+* ``stream_ceiling``: gemm_stream_read over each decode's weight matrix (the
+  same TMA boxes and ring, nothing else done): the read ceiling each decode
+  is compared with;
+* ``configs``: all five workloads, each timed and set against the roofline
+  min(P_tc, BW * F/Q), with the oracle's parity on its outputs;
 * ``e2e``: the same metric with host buffers — pinned host->device copies
   of A and B and the device->host copy of D inside every timed step;
 * ``cpu_baseline``: the FP64 CPU oracle timed on a bounded row sample of
@@ -239,7 +244,8 @@ def run_ours(args, dist):
         dC = dev_bf16(C, torch, device) if w.out_dtype == gi.OUT_BF16 else torch.from_numpy(C).to(device)
     dD = torch.empty((w.M, w.N), dtype=out_t, device=device)
     sched = {"default": 0, "static": 1, "clc": 2}[args.scheduler]
-    cfg = g.GemmConfig(path=args.path, scheduler=sched)
+    cfg = g.GemmConfig(path=args.path, scheduler=sched, l2_hints=args.l2_hints, raster_group=args.raster_group,
+                       cluster_pref=args.cluster_pref)
     c_ptr = dC.data_ptr() if dC is not None else 0
     ldc = w.N if dC is not None else 0
 
@@ -350,6 +356,8 @@ def run_ours(args, dist):
     if not args.no_secondary:
         result["secondary"] = run_decode(args, g, torch, device, peaks, dist)
         result["fp8"] = run_fp8(args, g, torch, device, peaks, dist)
+        result["stream_ceiling"] = run_stream_ceiling(args, g, torch, device, peaks, dist, result)
+        result["configs"] = run_configs(args, g, torch, device, peaks, dist, result, w, A, B, dD)
         result["scheduler_clc"] = run_scheduler_study(args, g, torch, device, w, dA, dB, dD, flops, peaks, dist)
         result["grouped"] = run_grouped_leg(args, g, torch, device, dist)
 
@@ -594,6 +602,164 @@ def run_fp8(args, g, torch, device, peaks, dist):
     return out
 
 
+def run_stream_ceiling(args, g, torch, device, peaks, dist, result):
+    """The read ceiling of each decode's weight stream: gemm_stream_read pulls
+    the decode's B matrix through the same TMA boxes (128 rows x 4 k-blocks)
+    into the same 216 KiB ring on the same number of CTAs, and does nothing
+    else.  B is rotated over the same number of copies as in the decode
+    legs, and the launches are timed the same way (graph-replayed and eager)."""
+    out = {"kernel": "gemm_stream_read (TMA boxes into a shared-memory ring, data discarded)"}
+    legs = [("bf16_128MiB", result.get("secondary"), 8192, 8192 * 2, 4),
+            ("e4m3_64MiB", (result.get("fp8") or {}).get("decode_e4m3"), 8192, 8192, 8)]
+    stream = torch.cuda.Stream(device)
+    sms = torch.cuda.get_device_properties(device).multi_processor_count
+    for name, dec, rows, row_bytes, copies in legs:
+        if not dec:
+            continue
+        grid = dec["config"].get("grid") or 128
+        bufs = [torch.empty(rows * row_bytes, dtype=torch.uint8, device=device).fill_(0x3C) for _ in range(copies)]
+        entry = {"bytes": rows * row_bytes, "box": "128 rows x 4 k-blocks of 128 B", "copies": copies}
+        for label, gsize in (("decode_grid", grid), ("all_sms", sms)):
+            def step(i, gsize=gsize):
+                rc = g.gemm_stream_read(bufs[i % copies].data_ptr(), rows, row_bytes, 128, 4, gsize,
+                                        stream.cuda_stream)
+                if rc != 0:
+                    raise RuntimeError(f"stream read failed: {rc} {g.last_error()}")
+            with torch.cuda.stream(stream):
+                for i in range(max(args.warmup, 3)):
+                    step(i)
+            torch.cuda.synchronize()
+            steps = max(args.steps, 50)
+            ms_eager, ms = time_eager_and_graph(torch, stream, step, steps, dist)
+            us, us_e = ms * 1e3 / steps, ms_eager * 1e3 / steps
+            gbs = rows * row_bytes / (us * 1e-6) / 1e9
+            entry[label] = {"grid": gsize, "us": round(us, 3), "gbs": round(gbs, 1),
+                            "frac_of_copy_peak": round(gbs / peaks["hbm_gbs"], 4),
+                            "eager_us": round(us_e, 3)}
+        if g.gemm_get_status(stream.cuda_stream) != 0:
+            raise RuntimeError(g.last_error())
+        dec_us = dec["ms_per_step"] * 1e3
+        entry["decode_us"] = round(dec_us, 3)
+        # the decode moves A and D as well; the ceiling streams B alone
+        entry["decode_frac_of_stream_ceiling"] = round(entry["decode_grid"]["us"] / dec_us, 4)
+        dec.setdefault("roofline", {})["frac_of_stream_ceiling"] = entry["decode_frac_of_stream_ceiling"]
+        out[name] = entry
+        del bufs
+    return out
+
+
+def run_configs(args, g, torch, device, peaks, dist, result, w_main, A_main, B_main, dD_main):
+    """All five workloads in one table: each timed in the launch configuration
+    the automatic path picks, against the roofline min(P_tc, BW * F/Q) (the
+    measured bf16 burst peak and copy bandwidth), with the oracle's parity on
+    a sample of its outputs (every output for the two small-output shapes).
+    Operand sets are rotated so that the bytes touched between two uses of
+    one set exceed L2.  The up-projection and the decode reuse the main and
+    secondary legs' timings."""
+    import oracle
+    l2 = torch.cuda.get_device_properties(device).L2_cache_size if hasattr(
+        torch.cuda.get_device_properties(device), "L2_cache_size") else 126 << 20
+    P, BW = peaks["bf16_tflops"], peaks["hbm_gbs"]
+    out = {"roofline": "min(measured bf16 burst peak, measured copy GB/s x F/Q)", "l2_bytes": l2}
+    stream = torch.cuda.Stream(device)
+    sh = stream.cuda_stream
+    for w in gi.WORKLOADS:
+        out_bytes = 4 if w.out_dtype == gi.OUT_F32 else 2
+        entry = {"workload": w.name, "M": w.M, "N": w.N, "K": w.K, "alpha": w.alpha, "beta": w.beta,
+                 "out": "f32" if w.out_dtype == gi.OUT_F32 else "bf16"}
+        if w.index == MAIN and args.workload == MAIN and not args.shape:
+            A, B, C = A_main, B_main, None
+            dD = dD_main
+            us = result["ms_per_step"] * 1e3
+            entry.update(us_per_call=round(us, 3), launch="eager (main leg)", steps=result["steps"])
+        elif w.index == DECODE:
+            A, B, C = gi.operands(w)
+            sec = result["secondary"]
+            us = sec["ms_per_step"] * 1e3
+            entry.update(us_per_call=round(us, 3), launch="CUDA graph (secondary leg)", steps=sec["steps"],
+                         eager_us_per_call=round(sec["eager"]["ms_per_step"] * 1e3, 3))
+            dD = None
+        else:
+            A, B, C = gi.operands(w)
+            set_bytes = rl.gemm_bytes(w.M, w.N, w.K, out_bytes, w.beta != 0)
+            copies = max(2, -(-int(1.5 * l2) // set_bytes))
+            dA = [dev_bf16(A, torch, device) for _ in range(copies)]
+            dB = [dev_bf16(B, torch, device) for _ in range(copies)]
+            dC = None
+            if C is not None:
+                dC = [dev_bf16(C, torch, device) if w.out_dtype == gi.OUT_BF16 else torch.from_numpy(C).to(device)
+                      for _ in range(copies)]
+            odt = torch.float32 if w.out_dtype == gi.OUT_F32 else torch.bfloat16
+            dDs = [torch.empty((w.M, w.N), dtype=odt, device=device) for _ in range(copies)]
+
+            def step(i, w=w, dA=dA, dB=dB, dC=dC, dDs=dDs, copies=copies):
+                j = i % copies
+                rc = g.gemm_bf16_tn(w.M, w.N, w.K, dA[j].data_ptr(), w.K, dB[j].data_ptr(), w.K,
+                                    dC[j].data_ptr() if dC is not None else 0, w.N if dC is not None else 0,
+                                    dDs[j].data_ptr(), w.N, w.alpha, w.beta, w.out_dtype, sh)
+                if rc != 0:
+                    raise RuntimeError(f"gemm failed: {rc} {g.last_error()}")
+
+            with torch.cuda.stream(stream):
+                for i in range(max(args.warmup, 3) + copies):
+                    step(i)
+            torch.cuda.synchronize()
+            info = g.last_launch_info()
+            steps = max(args.steps, 50) if w.index != 0 else max(args.steps, 400)
+            ms_eager, ms = time_eager_and_graph(torch, stream, step, steps, dist)
+            if g.gemm_get_status(sh) != 0:
+                raise RuntimeError(g.last_error())
+            us = ms * 1e3 / steps
+            entry.update(us_per_call=round(us, 3), launch="CUDA graph of the steps' launches", steps=steps,
+                         eager_us_per_call=round(ms_eager * 1e3 / steps, 3),
+                         path=PATH_NAMES.get(info.get("path")), grid=info.get("grid"),
+                         tile=[info.get("tile_m"), info.get("tile_n")],
+                         l2=f"{copies} operand sets rotated ({copies * set_bytes >> 20} MiB)")
+            dD = dDs[(steps - 1) % copies]
+        roof = rl.roofline_entry(w.M, w.N, w.K, us * 1e-6, P, BW, out_bytes, w.beta != 0)
+        entry["value"] = round(dist.world * roof["achieved_tflops"], 3)
+        entry["unit"] = "TFLOP/s"
+        entry["gbs"] = roof["achieved_gbs"]
+        entry["roofline"] = roof
+        if w.index == 0:
+            entry["note"] = "launch-bound: 0.5 MiB of operands, a few microseconds per call"
+        # parity: every output of the small-output shapes, sampled elsewhere
+        if dD is None:  # decode: recompute on its own buffers
+            dA1, dB1 = dev_bf16(A, torch, device), dev_bf16(B, torch, device)
+            dD = torch.empty((w.M, w.N), dtype=torch.bfloat16, device=device)
+            with torch.cuda.stream(stream):
+                if g.gemm_bf16_tn(w.M, w.N, w.K, dA1.data_ptr(), w.K, dB1.data_ptr(), w.K, 0, 0, dD.data_ptr(), w.N,
+                                  w.alpha, w.beta, w.out_dtype, sh) != 0:
+                    raise RuntimeError(g.last_error())
+            torch.cuda.synchronize()
+        got = (dD.view(torch.int16).cpu().numpy().view(np.uint16) if w.out_dtype == gi.OUT_BF16
+               else dD.cpu().numpy())
+        cvals = None if C is None else (gi.bf16_bits_to_f32(C) if w.out_dtype == gi.OUT_BF16 else C)
+        if w.M * w.N <= 1 << 18:
+            ref, absdot = oracle.gemm_ref(A, B, C, w.alpha, w.beta)
+            ok, worst, _ = oracle.check(got, ref, absdot, w.out_dtype, w.beta, cvals)
+            exact = bool(np.array_equal(got, oracle.exact_f32(ref))) if w.index == 0 else None
+            entry["parity"] = {"checked": "every output", "ok": bool(ok), "worst_err_over_bound": round(worst, 4)}
+            if exact is not None:
+                entry["parity"]["bit_exact"] = exact
+        else:
+            rng = np.random.default_rng(77 + w.index)
+            rows = rng.integers(0, w.M, 3000)
+            cols = rng.integers(0, w.N, 3000)
+            rows = np.concatenate([rows, [0, w.M - 1, w.M - 1, 0]])
+            cols = np.concatenate([cols, [0, w.N - 1, 0, w.N - 1]])
+            ref, absdot = oracle.gemm_ref_sampled(A, B, rows, cols, C, w.alpha, w.beta)
+            cs = None if cvals is None else cvals[rows, cols]
+            ok, worst, _ = oracle.check(got[rows, cols], ref, absdot, w.out_dtype, w.beta, cs)
+            entry["parity"] = {"checked": f"{rows.size} sampled outputs incl. corners", "ok": bool(ok),
+                               "worst_err_over_bound": round(worst, 4)}
+        out[str(w.index + 1)] = entry
+        if "l2" in entry:
+            del dA, dB, dC, dDs
+        torch.cuda.empty_cache()
+    return out
+
+
 def run_scheduler_study(args, g, torch, device, w, dA, dB, dD, flops, peaks, dist):
     """The cluster-launch-control tile scheduler against the static persistent
     grid: (1) the main GEMM under CLC on an idle GPU; (2) an 8192x8192x4096
@@ -757,10 +923,22 @@ def cpu_baseline(w, A, B, C, dD, out_t, torch, seconds):
     ok, worst, _ = oracle.check(got, ref, absdot, od, w.beta, cvals)
     if not ok:
         log(f"[bench] WARNING: GPU rows disagree with the oracle on the CPU sample (worst {worst:.3g} x bound)")
+    # one host thread on the two small workloads, in full: the 256^3 exact
+    # GEMM and the 16 x 8192 x 8192 decode
+    one_thread = {}
+    for wi in (0, DECODE):
+        ws = gi.WORKLOADS[wi]
+        As, Bs, Cs = gi.operands(ws)
+        t1 = time.time()
+        oracle.gemm_ref(As, Bs, Cs, ws.alpha, ws.beta, nthreads=1)
+        d1 = time.time() - t1
+        one_thread[ws.name] = {"seconds": round(d1, 3), "value": round(ws.flops / d1 / 1e12, 6),
+                               "unit": "TFLOP/s", "cores": 1, "sample": "every output"}
     return {"value": round(rows * per_row / dt / 1e12, 6), "unit": "TFLOP/s", "cores": threads,
             "kind": "oracle", "sample": f"rows {r0}..{r0 + rows - 1} of {w.M} ({rows} x {w.N} outputs, "
                                         f"K={w.K}) in {dt:.1f}s",
-            "parity_on_sample": {"ok": bool(ok), "worst_err_over_bound": round(worst, 4)}}
+            "parity_on_sample": {"ok": bool(ok), "worst_err_over_bound": round(worst, 4)},
+            "one_thread": one_thread}
 
 
 
@@ -814,6 +992,12 @@ def main():
     ap.add_argument("--path", type=int, default=0, help="0 auto, 1 1-SM, 2 2-SM, 3 skinny")
     ap.add_argument("--scheduler", choices=["default", "static", "clc"], default="default",
                     help="tile scheduler of the tiled paths (main step)")
+    ap.add_argument("--l2-hints", type=int, default=0,
+                    help="main step: L2 eviction hints of the tiled kernels (gemm_tn_config.l2_hints)")
+    ap.add_argument("--raster-group", type=int, default=0,
+                    help="main step: tiles along M per raster strip (0 = automatic)")
+    ap.add_argument("--cluster-pref", type=int, default=0, choices=[0, 4, 8],
+                    help="main step: preferred cluster size of the 2-SM path (gemm_tn_config.cluster_pref)")
     ap.add_argument("--in-dtype", choices=["bf16", "e4m3", "e5m2"], default="bf16",
                     help="input type of the main step (fp8 runs the main step alone)")
     ap.add_argument("--no-e2e", action="store_true")

@@ -137,6 +137,14 @@ typedef struct gemm_tn_config {
                                (gemm_bf16_tn_bias_act).  Inside a stream capture that
                                would have to grow the stream's split workspace, the call runs
                                unsplit (the skinny path returns an error there instead) */
+  int l2_hints;             /* tiled paths, single problem: L2 eviction priorities of the kernel's
+                               copies, a sum of 1 (A loads evict-last: A rows are re-read by every
+                               tile of their raster strip), 2 (B loads evict-first) and 4 (D stores
+                               evict-first); 0 = library default, -1 = none */
+  int cluster_pref;         /* 2-SM path, static scheduler, single problem: preferred cluster size,
+                               4 or 8 CTAs (two or four pairs), with pairs (2 CTAs) as the fallback
+                               where a cluster of SMs has no room for the larger size; 0 = pairs only.
+                               Applied only when it divides the grid */
 } gemm_tn_config;
 
 /* Tile schedulers of the tiled paths.
@@ -166,6 +174,8 @@ typedef struct gemm_launch_info {
   int scheduler;     /* tiled paths: GEMM_SCHED_STATIC or GEMM_SCHED_CLC; 0 otherwise */
   int k_parts;       /* k-parts per tile: tiled split (1 = none) or skinny equal split; 0 = skinny
                         stream-K ranges */
+  int cluster_pref;  /* preferred cluster size requested for the launch (gemm_tn_config.cluster_pref),
+                        0 = none */
 } gemm_launch_info;
 
 /* D = alpha * A * B^T + beta * C (see the file comment for every argument).
@@ -336,6 +346,26 @@ void gemm_shutdown(void);
 /* Library version, major * 10000 + minor * 100 + patch. */
 int gemm_version(void);
 
+/* Measurement kernel: the read ceiling of the skinny path's weight stream.
+ *
+ * Follows the Ampere-to-Hopper page, section "not reaching peak": a kernel
+ * is judged against ceilings measured on the same machine.  Reads the
+ * rows x row_bytes bytes at src (row-major, rows contiguous, device memory
+ * owned by the caller) through TMA boxes of box_rows rows x kgroup
+ * consecutive 128-byte chunks, as the skinny kernel loads its B operand,
+ * into a shared-memory ring of up to 216 KiB per CTA, and discards them.
+ * grid CTAs (0 = one per SM) each stream a contiguous range of boxes, in the
+ * skinny kernel's order (k-chunks fastest within a tile of box_rows rows).
+ * Nothing is written to global memory.
+ *
+ * box_rows is 32, 64, 128 or 256; kgroup 1, 2 or 4; rows a multiple of
+ * box_rows; row_bytes a multiple of 128 * kgroup; src 16-byte aligned.
+ * Otherwise GEMM_ERR_INVALID_VALUE or GEMM_ERR_MISALIGNED.  Asynchronous on
+ * stream, launched with programmatic stream serialisation like the GEMM
+ * kernels; device-side waits are bounded like theirs (gemm_get_status). */
+int gemm_stream_read(const void *src, int64_t rows, int64_t row_bytes, int box_rows, int kgroup, int grid,
+                     void *stream);
+
 /* The skinny path (1 <= M <= 64) without any allocation at call time.
  *
  * The pages have no counterpart to this entry point; it exists for callers
@@ -357,8 +387,9 @@ int gemm_version(void);
  * call before any stream capture.  Every call on a device shares the array:
  * each call clears the counters on its stream before its kernel, so calls
  * ordered in one stream are safe, but calls whose kernels overlap on the GPU
- * (unordered streams) race and give wrong results.  Device-side timeouts are
- * reported by gemm_get_status. */
+ * (unordered streams) race and give wrong results.  Device-side waits give
+ * up after GEMM_WAIT_TIMEOUT_NS nanoseconds (2 s when unset), as those of
+ * gemm_bf16_tn do; timeouts are reported by gemm_get_status. */
 int gemm_bf16_tn_skinny_noalloc(int64_t M, int64_t N, int64_t K,
                                 const void *A, int64_t lda,
                                 const void *B, int64_t ldb,

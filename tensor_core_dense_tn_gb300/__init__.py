@@ -38,7 +38,7 @@ GEMM_ERR_CUDA = -8
 EXPORTED = ["gemm_bf16_tn", "gemm_bf16_tn_ex", "gemm_get_status", "gemm_get_status_detail",
             "gemm_last_error_string", "gemm_last_launch_info", "gemm_shutdown", "gemm_version",
             "gemm_bf16_tn_skinny_noalloc", "gemm_bf16_tn_bias_act", "gemm_fp8_tn", "gemm_fp8_tn_ex",
-            "gemm_bf16_tn_grouped", "gemm_bf16_tn_batched", "gemm_plan"]
+            "gemm_bf16_tn_grouped", "gemm_bf16_tn_batched", "gemm_plan", "gemm_stream_read"]
 
 FP8_E4M3, FP8_E5M2 = 0, 1
 SCHED_DEFAULT, SCHED_STATIC, SCHED_CLC = 0, 1, 2
@@ -57,7 +57,8 @@ class GemmConfig(ctypes.Structure):
                 ("skinny_grid", ctypes.c_int), ("wait_timeout_ns", ctypes.c_uint64),
                 ("test_fault", ctypes.c_int), ("disable_pdl", ctypes.c_int),
                 ("skinny_skew_kb", ctypes.c_int), ("scheduler", ctypes.c_int), ("skinny_bm", ctypes.c_int),
-                ("skinny_kgroup", ctypes.c_int), ("tiled_k_parts", ctypes.c_int)]
+                ("skinny_kgroup", ctypes.c_int), ("tiled_k_parts", ctypes.c_int), ("l2_hints", ctypes.c_int),
+                ("cluster_pref", ctypes.c_int)]
 
 
 class GemmPlanInfo(ctypes.Structure):
@@ -80,7 +81,7 @@ class LaunchInfo(ctypes.Structure):
     _fields_ = [("path", ctypes.c_int), ("grid", ctypes.c_int), ("cluster", ctypes.c_int),
                 ("block", ctypes.c_int), ("tile_m", ctypes.c_int), ("tile_n", ctypes.c_int),
                 ("stages", ctypes.c_int), ("smem_bytes", ctypes.c_int), ("kernel", ctypes.c_char_p),
-                ("scheduler", ctypes.c_int), ("k_parts", ctypes.c_int)]
+                ("scheduler", ctypes.c_int), ("k_parts", ctypes.c_int), ("cluster_pref", ctypes.c_int)]
 
     def as_dict(self):
         return {f: (getattr(self, f).decode() if f == "kernel" and getattr(self, f) else getattr(self, f))
@@ -115,6 +116,8 @@ def load(path: str = LIB_PATH):
         lib.gemm_bf16_tn_bias_act.restype = i32
         lib.gemm_bf16_tn_skinny_noalloc.argtypes = args
         lib.gemm_bf16_tn_skinny_noalloc.restype = i32
+        lib.gemm_stream_read.argtypes = [vp, i64, i64, i32, i32, i32, vp]
+        lib.gemm_stream_read.restype = i32
         lib.gemm_bf16_tn_grouped.argtypes = [i32, ctypes.POINTER(GemmProblem), f32, f32, i32, vp]
         lib.gemm_bf16_tn_grouped.restype = i32
         lib.gemm_bf16_tn_batched.argtypes = [i64, i64, i64, i64, vp, i64, i64, vp, i64, i64, vp, i64, i64,
@@ -163,6 +166,12 @@ def gemm_bf16_tn_skinny_noalloc(M, N, K, A, lda, B, ldb, C, ldc, D, ldd, alpha, 
     """Raw C-ABI call of the allocation-free skinny entry point (1 <= M <= 64)."""
     return load().gemm_bf16_tn_skinny_noalloc(M, N, K, A, lda, B, ldb, C or None, ldc, D, ldd, alpha,
                                               beta, out_dtype, stream or None)
+
+
+def gemm_stream_read(src, rows, row_bytes, box_rows, kgroup, grid, stream) -> int:
+    """Raw C-ABI call of the TMA streaming-read ceiling kernel (reads rows x
+    row_bytes bytes at src in the skinny kernel's box shape, discards them)."""
+    return load().gemm_stream_read(src, rows, row_bytes, box_rows, kgroup, grid, stream or None)
 
 
 def gemm_bf16_tn_grouped(problems, alpha, beta, out_dtype, stream) -> int:

@@ -32,6 +32,8 @@ __device__ int g_status[kStatusWords];
 
 constexpr int kMaxDevices = 64;
 constexpr uint64_t kDefaultTimeoutNs = 2000000000ull;
+// L2 hints of single-problem tiled calls without a config (kL2Hint* bits).
+constexpr int kDefaultL2Hints = 0;
 
 thread_local std::string t_error;
 thread_local gemm_launch_info t_info = {};
@@ -283,6 +285,10 @@ int check_config(const gemm_tn_config* cfg) {
   const int kg = cfg->skinny_kgroup;
   if (kg != 0 && kg != 1 && kg != 2 && kg != 4)
     return fail(GEMM_ERR_INVALID_VALUE, "skinny_kgroup must be 0, 1, 2 or 4, got %d", kg);
+  if (cfg->cluster_pref != 0 && cfg->cluster_pref != 4 && cfg->cluster_pref != 8)
+    return fail(GEMM_ERR_INVALID_VALUE, "cluster_pref must be 0, 4 or 8, got %d", cfg->cluster_pref);
+  if (cfg->l2_hints < -1 || cfg->l2_hints > 7)
+    return fail(GEMM_ERR_INVALID_VALUE, "l2_hints must be -1..7, got %d", cfg->l2_hints);
   if (cfg->tiled_k_parts < 0 || cfg->tiled_k_parts > kMaxTiledParts)
     return fail(GEMM_ERR_INVALID_VALUE, "tiled_k_parts must be 0..%d, got %d", kMaxTiledParts, cfg->tiled_k_parts);
   return GEMM_OK;
@@ -353,6 +359,7 @@ void record_launch(const LaunchInfo& li) {
   t_info.kernel = li.kernel;
   t_info.k_parts = li.k_parts;
   t_info.scheduler = li.scheduler;
+  t_info.cluster_pref = li.cluster_pref;
 }
 
 int run(int64_t M, int64_t N, int64_t K, const void* A, int64_t lda, const void* B, int64_t ldb, const void* C,
@@ -446,6 +453,8 @@ int run(int64_t M, int64_t N, int64_t K, const void* A, int64_t lda, const void*
     p.alpha = alpha; p.beta = beta; p.has_c = has_c; p.epi = epi;
     p.fault = fault; p.timeout_ns = tmo; p.status = st->status;
     p.clc = sched == GEMM_SCHED_CLC ? 1 : 0;
+    p.l2_hints = cfg && cfg->l2_hints != 0 ? (cfg->l2_hints < 0 ? 0 : cfg->l2_hints) : kDefaultL2Hints;
+    p.cluster_pref = cfg ? cfg->cluster_pref : 0;
     // no split with CLC, a grid override or a fused epilogue (bias and
     // activation would sit on the unit's critical path, after the hand-off)
     p.ksplit = p.clc || (cfg && cfg->grid > 0) || epi.bias || epi.act
@@ -699,6 +708,16 @@ cudaError_t status_word_address(int** out) {
   cudaError_t e = cudaGetSymbolAddress(&p, g_status);
   if (e == cudaSuccess) *out = static_cast<int*>(p);
   return e;
+}
+
+// The wait limit of calls without a config (GEMM_WAIT_TIMEOUT_NS, else 2 s),
+// for entry points defined in other files.
+uint64_t default_wait_timeout_ns() { return timeout_ns(nullptr); }
+
+// The skinny path's automatic geometry and partition on `sms` SMs, as
+// gemm_bf16_tn computes it, for entry points defined in other files.
+int skinny_geometry_auto(SkinnyParams* p, int64_t M, int64_t N, int64_t K, int kbe, int sms) {
+  return skinny_geometry(p, M, N, K, kbe, sms, nullptr);
 }
 
 }  // namespace gtn

@@ -148,21 +148,16 @@ extern "C" int gemm_bf16_tn_skinny_noalloc(int64_t M, int64_t N, int64_t K, cons
   int rc = na_setup(dev, &d);
   if (rc != GEMM_OK) return na_fail(rc, "device set-up failed (needs sm_103)");
 
+  // The same geometry and partition as gemm_bf16_tn's skinny path, on at
+  // most kNaMaxGrid SMs; then every bound the fixed scratch rests on is
+  // checked before anything is launched.
   SkinnyParams p = {};
-  p.M = (int)M;
-  p.N = (int)N;
-  p.K = (int)K;
-  p.np = (int)((M + 15) / 16) * 16;
-  int sms = skinny_max_grid(p.np, d->sms);
-  if (sms > kNaMaxGrid) sms = kNaMaxGrid;
-  // 64-row tiles only when they fit one wave (at most sms <= kNaMaxGrid tiles),
-  // so the counters never exceed the 128-row tile count the scratch is sized for
-  p.bm = skinny_tile_rows(N, p.np, sms);
-  p.n_tiles = (int)((N + p.bm - 1) / p.bm);
-  p.kg = skinny_kgroup(p.np, p.bm, K, 64, 0);
-  p.num_kb = (int)(((K + 63) / 64 + p.kg - 1) / p.kg);
-  p.units = (long long)p.n_tiles * p.num_kb;
-  skinny_partition(&p, sms, 0, 0);
+  const int sms = d->sms < kNaMaxGrid ? d->sms : kNaMaxGrid;
+  rc = skinny_geometry_auto(&p, M, N, K, 64, sms);
+  if (rc != GEMM_OK) return rc;
+  if (p.grid < 1 || p.grid > kNaMaxGrid || (size_t)p.n_tiles * 4 > kNaCounterInts ||
+      (size_t)p.grid * 2 * p.bm * p.np > kNaPartialFloats)
+    return na_fail(GEMM_ERR_INVALID_VALUE, "shape needs more scratch than the no-alloc path holds");
   p.alpha = alpha;
   p.beta = beta;
   p.has_c = has_c;
@@ -174,7 +169,7 @@ extern "C" int gemm_bf16_tn_skinny_noalloc(int64_t M, int64_t N, int64_t K, cons
   p.partials = reinterpret_cast<float*>(d->scratch);
   p.counters = reinterpret_cast<int*>(d->scratch + kNaPartialFloats * 4);
   p.fault = 0;
-  p.timeout_ns = 2000000000ull;
+  p.timeout_ns = default_wait_timeout_ns();
   p.status = d->status;
 
   cudaStream_t stream = static_cast<cudaStream_t>(stream_v);

@@ -316,7 +316,14 @@ __global__ void __launch_bounds__(kThreads, 1)
 
   const int warp = threadIdx.x >> 5;
   const int lane = threadIdx.x & 31;
-  const uint32_t rank = kCluster ? cluster_ctarank() : 0;
+  // A pair is two CTAs whose cluster ranks differ in bit 0.  The launch may
+  // group pairs into larger clusters (a preferred cluster size): the pair's
+  // leader is then the CTA of rank pair_base, and its barriers are addressed
+  // and its commits multicast by that rank.
+  const uint32_t crank = kCluster ? cluster_ctarank() : 0;
+  const uint32_t rank = crank & 1u;
+  const uint32_t pair_base = crank & ~1u;
+  const uint16_t pair_mask = (uint16_t)(0x3u << pair_base);
   const bool leader = (rank == 0);
   const int cluster_id = blockIdx.x / CG;
   const int num_clusters = gridDim.x / CG;
@@ -384,7 +391,12 @@ __global__ void __launch_bounds__(kThreads, 1)
       int stage = 0;
       uint32_t phase = 0;
       ClcCursor req, rd;  // slot of the next request, slot of the next answer to read
-      const uint32_t clce_leader = kCluster ? mapa_shared(clce0, 0) : clce0;
+      const uint32_t clce_leader = kCluster ? mapa_shared(clce0, pair_base) : clce0;
+      // L2 priorities (single problems): A rows are re-read by every tile of
+      // their raster strip, B columns only by the strip's few concurrent tiles
+      const bool hint_a = MODE == kModeSingle && (p.l2_hints & kL2HintAEvictLast);
+      const bool hint_b = MODE == kModeSingle && (p.l2_hints & kL2HintBEvictFirst);
+      const uint64_t pol_a = l2_policy_evict_last(), pol_b = l2_policy_evict_first();
       int t = cluster_id;
       while (t < p.num_units && ok) {
         if (p.clc) {
@@ -428,12 +440,16 @@ __global__ void __launch_bounds__(kThreads, 1)
           if (skip_once) {
             skip_once = false;  // test-only: leave this stage's bytes missing
           } else if constexpr (CG == 1) {
-            tload<MODE>(sA + stage * C_::A_BYTES, r.a, kb * kBK, a_row, r.z, fb);
-            tload<MODE>(sB + stage * C_::B_BYTES, r.b, kb * kBK, b_row, r.z, fb);
+            if (hint_a) tma_load_2d_hint(sA + stage * C_::A_BYTES, r.a, kb * kBK, a_row, fb, pol_a);
+            else tload<MODE>(sA + stage * C_::A_BYTES, r.a, kb * kBK, a_row, r.z, fb);
+            if (hint_b) tma_load_2d_hint(sB + stage * C_::B_BYTES, r.b, kb * kBK, b_row, fb, pol_b);
+            else tload<MODE>(sB + stage * C_::B_BYTES, r.b, kb * kBK, b_row, r.z, fb);
           } else {
-            const uint32_t fb_leader = mapa_shared(fb, 0);
-            tload_pair<MODE>(sA + stage * C_::A_BYTES, r.a, kb * kBK, a_row, r.z, fb_leader);
-            tload_pair<MODE>(sB + stage * C_::B_BYTES, r.b, kb * kBK, b_row, r.z, fb_leader);
+            const uint32_t fb_leader = mapa_shared(fb, pair_base);
+            if (hint_a) tma_load_2d_pair_hint(sA + stage * C_::A_BYTES, r.a, kb * kBK, a_row, fb_leader, pol_a);
+            else tload_pair<MODE>(sA + stage * C_::A_BYTES, r.a, kb * kBK, a_row, r.z, fb_leader);
+            if (hint_b) tma_load_2d_pair_hint(sB + stage * C_::B_BYTES, r.b, kb * kBK, b_row, fb_leader, pol_b);
+            else tload_pair<MODE>(sB + stage * C_::B_BYTES, r.b, kb * kBK, b_row, r.z, fb_leader);
           }
           if (++stage == C_::STAGES) {
             stage = 0;
@@ -458,7 +474,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       int acc = 0;
       uint32_t acc_phase = 0;
       ClcCursor rd;
-      const uint32_t clce_leader = kCluster ? mapa_shared(clce0, 0) : clce0;
+      const uint32_t clce_leader = kCluster ? mapa_shared(clce0, pair_base) : clce0;
       int t = cluster_id;
       while (t < p.num_units && ok) {
         if (!wait_bar<kCluster>(acce_bar(acc), acc_phase ^ 1, ab)) break;
@@ -480,7 +496,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             mma_issue<CG, KIND>(d_tmem, a0 + 2 * k, b0 + 2 * k, idesc, (kb != kb0 || k != 0) ? 1u : 0u);
           }
           if constexpr (CG == 1) mma_commit(empty_bar(stage));
-          else mma_commit_pair(empty_bar(stage), 0x3);
+          else mma_commit_pair(empty_bar(stage), pair_mask);
           if (++stage == C_::STAGES) {
             stage = 0;
             phase ^= 1;
@@ -488,7 +504,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
         if (!ok) break;
         if constexpr (CG == 1) mma_commit(accf_bar(acc));
-        else mma_commit_pair(accf_bar(acc), 0x3);
+        else mma_commit_pair(accf_bar(acc), pair_mask);
         acc ^= 1;
         if (acc == 0) acc_phase ^= 1;
         t = next_tile<kCluster, CG, C_::CLC_SLOTS, false>(t, num_clusters, p, rd, clcf0, clce_leader, sClc, true, ab);
@@ -496,7 +512,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       }
       // All MMAs issued by this thread complete before TMEM is released.
       if constexpr (CG == 1) mma_commit(drain_bar);
-      else mma_commit_pair(drain_bar, 0x1);
+      else mma_commit_pair(drain_bar, (uint16_t)(0x1u << pair_base));
       Abort ab_drain{nullptr, p.timeout_ns, p.status, kRoleMma};
       wait_bar<kCluster>(drain_bar, 0, ab_drain);
     }
@@ -509,9 +525,9 @@ __global__ void __launch_bounds__(kThreads, 1)
     uint32_t acc_phase = 0;
     uint32_t cphase0 = 0, cphase1 = 0;
     int buf = 0;
-    const uint32_t acce_target = kCluster ? mapa_shared(acce_bar(0), 0) : acce_bar(0);
+    const uint32_t acce_target = kCluster ? mapa_shared(acce_bar(0), pair_base) : acce_bar(0);
     ClcCursor rd;
-    const uint32_t clce_leader = kCluster ? mapa_shared(clce0, 0) : clce0;
+    const uint32_t clce_leader = kCluster ? mapa_shared(clce0, pair_base) : clce0;
     int t = cluster_id;
     while (t < p.num_units) {
       const int tile = unit_tile(t);
@@ -676,7 +692,10 @@ __global__ void __launch_bounds__(kThreads, 1)
         fence_proxy_async_smem();
         __syncwarp();
         if (lane == 0) {
-          tstore<MODE>(tr.d, col0, row0, tr.z, sbuf);
+          // D is written once and not read again by this kernel
+          if (MODE == kModeSingle && (p.l2_hints & kL2HintDEvictFirst))
+            tma_store_2d_hint(tr.d, col0, row0, sbuf, l2_policy_evict_first());
+          else tstore<MODE>(tr.d, col0, row0, tr.z, sbuf);
           bulk_commit();
         }
         buf ^= 1;
@@ -731,7 +750,7 @@ cudaError_t launch_impl(const CUtensorMap& tmA, const CUtensorMap& tmB, const CU
     configured[dev] = true;
   }
   cudaLaunchConfig_t cfg = {};
-  cudaLaunchAttribute attr[2];
+  cudaLaunchAttribute attr[3];
   cfg.blockDim = dim3(kThreads, 1, 1);
   cfg.dynamicSmemBytes = C_::SMEM;
   cfg.stream = stream;
@@ -781,12 +800,27 @@ cudaError_t launch_impl(const CUtensorMap& tmA, const CUtensorMap& tmB, const CU
   if (p.clc) units = p.num_tiles;
   if (units < 1) units = 1;
   cfg.gridDim = dim3(units * CG, 1, 1);
+  // Preferred cluster size (pairs grouped into clusters of 4 or 8 CTAs where
+  // the GPU's clusters of SMs have room, single pairs elsewhere): a static
+  // single-problem pair launch whose grid it divides.
+  int pref = 0;
+  if (CG == 2 && MODE == kModeSingle && !p.clc && (p.cluster_pref == 4 || p.cluster_pref == 8) &&
+      (units * CG) % p.cluster_pref == 0) {
+    pref = p.cluster_pref;
+    attr[num_attrs].id = cudaLaunchAttributePreferredClusterDimension;
+    attr[num_attrs].val.preferredClusterDim.x = (unsigned)pref;
+    attr[num_attrs].val.preferredClusterDim.y = 1;
+    attr[num_attrs].val.preferredClusterDim.z = 1;
+    ++num_attrs;
+    cfg.numAttrs = num_attrs;
+  }
   if (info) {
     info->path = CG;
     info->scheduler = p.clc ? 2 : 1;
     info->k_parts = p.ksplit;
     info->grid = units * CG;
     info->cluster = CG;
+    info->cluster_pref = pref;
     info->block = kThreads;
     info->tile_m = C_::TILE_M;
     info->tile_n = C_::BN;

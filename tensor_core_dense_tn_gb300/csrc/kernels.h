@@ -18,6 +18,9 @@ constexpr int kStatusWords = 2;
 
 enum Role : int { kRoleProducer = 1, kRoleMma = 2, kRoleEpilogue = 3, kRoleFixup = 4 };
 
+// L2 eviction-priority hints of the tiled kernels' copies (TileParams.l2_hints).
+constexpr int kL2HintAEvictLast = 1, kL2HintBEvictFirst = 2, kL2HintDEvictFirst = 4;
+
 // Test-only fault injection bits.
 constexpr int kFaultSkipTmaOnce = 1;
 
@@ -68,6 +71,8 @@ struct TileParams {
   int defer_wait;      // 1 = later launch of one grouped call: wait for the previous launch at the end, not
                        // the start (the launches' problems are independent; see the kernel)
   Epilogue epi;
+  int l2_hints;        // kL2Hint* bits (single problems only)
+  int cluster_pref;    // host only: preferred cluster size (4 or 8 CTAs) of a static pair launch, 0 = none
   int fault;           // kFault* bits (tests only)
   uint64_t timeout_ns;
   int* status;
@@ -119,6 +124,7 @@ struct LaunchInfo {
   const char* kernel;
   int scheduler;       // 1 = static persistent, 2 = cluster launch control (tiled paths)
   int k_parts;         // k-parts per tile (tiled split; skinny equal split), 0 = skinny stream-K
+  int cluster_pref;    // preferred cluster size requested at launch (0 = none)
 };
 
 // Tiled persistent kernels (1-SM or 2-SM).  Returns a cudaError_t.  `pdl`
@@ -148,6 +154,12 @@ cudaError_t launch_skinny(const CUtensorMap& tmA, const CUtensorMap& tmB, Skinny
 cudaError_t status_word_address(int** out);
 // Text returned by gemm_last_error_string on this thread (gemm_api.cu).
 void set_error_text(const char* msg);
+// Wait limit of calls without a config: GEMM_WAIT_TIMEOUT_NS, else 2 s (gemm_api.cu).
+uint64_t default_wait_timeout_ns();
+// The skinny path's automatic geometry and partition (tile rows, k-group,
+// tiles, units, grid, split, skew, stages) for M x N x K with kbe elements per
+// k-block on `sms` SMs; GEMM_OK or a gemm_status code (gemm_api.cu).
+int skinny_geometry_auto(SkinnyParams* p, int64_t M, int64_t N, int64_t K, int kbe, int sms);
 
 // Largest co-resident grid for the skinny kernel at this np.
 int skinny_max_grid(int np, int num_sms);

@@ -43,6 +43,25 @@ def attainable_tflops(M, N, K, peak_tflops, hbm_gbs, out_bytes=2, beta_nonzero=F
     return min(peak_tflops, hbm_gbs * 1e9 * intensity(M, N, K, out_bytes, beta_nonzero) / 1e12)
 
 
+def roofline_entry(M, N, K, seconds, tensor_peak_tflops, hbm_gbs, out_bytes=2, beta_nonzero=False,
+                   in_bytes=2) -> dict:
+    """One launch of M x N x K taking `seconds` against the roofline
+    min(P_tc, BW * F/Q): achieved TFLOP/s and GB/s (algorithmic F and Q), the
+    attainable rate, which roof binds, and achieved / attainable."""
+    f = gemm_flops(M, N, K)
+    q = gemm_bytes(M, N, K, out_bytes, beta_nonzero, in_bytes)
+    ai = f / q
+    bw_roof = hbm_gbs * 1e9 * ai / 1e12
+    roof = min(tensor_peak_tflops, bw_roof)
+    tf = f / seconds / 1e12
+    gbs = q / seconds / 1e9
+    bound = "tensor" if tensor_peak_tflops <= bw_roof else "hbm"
+    return {"bound": bound, "achieved_tflops": round(tf, 3), "achieved_gbs": round(gbs, 1),
+            "algorithmic_flops": f, "algorithmic_bytes": q, "intensity_flop_per_byte": round(ai, 2),
+            "attainable_tflops": round(roof, 2), "tensor_peak_tflops": tensor_peak_tflops, "hbm_peak_gbs": hbm_gbs,
+            "frac": round(tf / roof, 4)}
+
+
 def load_peaks(path: str | None = None) -> dict:
     """Measured peaks (HBM GB/s, bf16 TFLOP/s burst and sustained) with their source."""
     if path is None:

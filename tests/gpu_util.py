@@ -76,3 +76,22 @@ def sample_positions(M, N, n_random=4096, seed=0, tile_m=256, tile_n=256):
             rows.append(int(r))
             cols.append(int(c))
     return np.array(rows, dtype=np.int64), np.array(cols, dtype=np.int64)
+
+
+def check_every_element(D, ref_rows, out_dtype, M, chunk_rows=512, beta=0.0, c_rows=None):
+    """Compare every element of the host result D (M rows) with the oracle, a
+    block of rows at a time so that the FP64 reference never needs more than
+    chunk_rows x N doubles at once.  ref_rows(r0, r1) returns the oracle's
+    (ref, absdot) for rows r0..r1-1; c_rows(r0, r1) the matching C values
+    (or None).  Returns (ok, worst |D - ref| / bound, (row, col) of the worst)."""
+    import oracle
+    worst, where = 0.0, None
+    for r0 in range(0, M, chunk_rows):
+        r1 = min(M, r0 + chunk_rows)
+        ref, absdot = ref_rows(r0, r1)
+        c = None if c_rows is None else c_rows(r0, r1)
+        ok, w, idx = oracle.check(D[r0:r1], ref, absdot, out_dtype, beta, c)
+        if w > worst or where is None:
+            worst, where = w, (r0 + int(idx[0]), int(idx[1])) if idx is not None else None
+        del ref, absdot
+    return worst <= 1.0, worst, where

@@ -17,7 +17,7 @@ import oracle
 pytestmark = pytest.mark.gpu
 
 g = pytest.importorskip("tensor_core_dense_tn_gb300")
-from gpu_util import empty_out, from_dev, sample_positions, to_dev_bf16, to_dev_f32  # noqa: E402
+from gpu_util import check_every_element, empty_out, from_dev, to_dev_bf16, to_dev_f32  # noqa: E402
 
 # M picks the kernel path: 48 -> skinny, 100 -> 1-SM tiled, 2200 -> 2-SM tiled
 # (with N at least 1040: more than 64 tiles of 128 x 256, so pair tiles)
@@ -104,18 +104,19 @@ def test_normal_within_bound(path, fmt, out_dtype):
     assert ok, (worst, idx)
 
 
-@pytest.mark.parametrize("M,N,K", [(16, 8192, 8192), (8192, 28672, 4096)])
-def test_full_size_sampled(M, N, K):
-    """The two FP8 bench shapes (decode and MLP up-projection), e4m3, sampled outputs."""
+@pytest.mark.parametrize("idx", [4, 3])
+def test_bench_shapes_every_element(idx):
+    """The two FP8 bench steps (the 16 x 8192 x 8192 decode and the
+    8192 x 28672 x 4096 up-projection, e4m3 codes with per-tensor scales, the
+    same operands the benchmark draws): every output against the oracle."""
+    w = gi.WORKLOADS[idx]
     fmt = gi.FP8_E4M3
-    A = gi.draw_fp8(M, K, gi.Dist("normal", 1.0), 5300, fmt)
-    B = gi.draw_fp8(N, K, gi.Dist("normal", 1.0), 5301, fmt)
-    sb = 1.0 / K
-    got = _run(M, N, K, A, B, fmt, gi.OUT_BF16, scale_b=sb)
-    rows, cols = sample_positions(M, N, n_random=2048, seed=53)
-    ref, absdot = oracle.gemm_ref_fp8_sampled(A, B, fmt, rows, cols, alpha=sb)
-    ok, worst, idx = oracle.check(got[rows, cols], ref, absdot, gi.OUT_BF16)
-    assert ok, (worst, idx)
+    A, B, sa, sb = gi.fp8_operands(w, fmt)
+    got = _run(w.M, w.N, w.K, A, B, fmt, gi.OUT_BF16, scale_a=sa, scale_b=sb)
+    alpha = float(np.float32(sa) * np.float32(sb))   # the scales fold into alpha in FP32
+    ok, worst, where = check_every_element(
+        got, lambda r0, r1: oracle.gemm_ref_fp8(A[r0:r1], B, fmt, alpha=alpha), gi.OUT_BF16, w.M)
+    assert ok, (worst, where)
 
 
 def test_fp8_matches_bf16_path_on_common_values():

@@ -160,3 +160,26 @@ def test_unknown_tiled_k_parts_rejected(lib, parts):
     a = (300, 64, 64, 0x1000, 64, 0x2000, 64, 0, 0, 0x3000, 64, 1.0, 0.0, 0, 0)
     assert g.gemm_bf16_tn_ex(*a, config=g.GemmConfig(tiled_k_parts=parts)) == g.GEMM_ERR_INVALID_VALUE
     assert "tiled_k_parts" in g.last_error()
+
+
+@pytest.mark.parametrize("args,code", [
+    ((0x1008, 128, 512, 128, 4, 0), g.GEMM_ERR_MISALIGNED),      # src not 16-byte aligned
+    ((0, 128, 512, 128, 4, 0), g.GEMM_ERR_MISALIGNED),           # NULL src
+    ((0x1000, 128, 512, 96, 4, 0), g.GEMM_ERR_INVALID_VALUE),    # box_rows not 32/64/128/256
+    ((0x1000, 128, 512, 128, 3, 0), g.GEMM_ERR_INVALID_VALUE),   # kgroup not 1/2/4
+    ((0x1000, 100, 512, 64, 4, 0), g.GEMM_ERR_INVALID_VALUE),    # rows not a multiple of box_rows
+    ((0x1000, 128, 640, 128, 4, 0), g.GEMM_ERR_INVALID_VALUE),   # row_bytes not a multiple of 512
+    ((0x1000, 128, 512, 128, 4, -1), g.GEMM_ERR_INVALID_VALUE),  # negative grid
+    ((0x1000, 256, 1024, 256, 4, 0), g.GEMM_ERR_INVALID_VALUE),  # 128 KiB box: no two-stage ring
+])
+def test_stream_read_argument_errors(lib, args, code):
+    assert g.gemm_stream_read(*args, 0) == code
+    assert g.last_error() != ""
+
+
+@pytest.mark.parametrize("field,value", [("l2_hints", 8), ("l2_hints", -2), ("cluster_pref", 2),
+                                         ("cluster_pref", 6), ("cluster_pref", 16)])
+def test_unknown_l2_hints_and_cluster_pref_rejected(lib, field, value):
+    a = (300, 64, 64, 0x1000, 64, 0x2000, 64, 0, 0, 0x3000, 64, 1.0, 0.0, 0, 0)
+    assert g.gemm_bf16_tn_ex(*a, config=g.GemmConfig(**{field: value})) == g.GEMM_ERR_INVALID_VALUE
+    assert field in g.last_error()

@@ -59,3 +59,17 @@ def test_peaks_fallback(tmp_path):
     f.write_text(json.dumps({"hbm_gbs": 1.0, "bf16_tflops": 2.0}))
     p = rl.load_peaks(str(f))
     assert p == {"hbm_gbs": 1.0, "bf16_tflops": 2.0, "bf16_tflops_sustained": 2.0, "source": "measured"}
+
+
+def test_roofline_entry_picks_the_binding_roof():
+    # 16 x 8192 x 8192 bf16: intensity ~15.9 FLOP/B, far left of the ridge -> HBM roof
+    e = rl.roofline_entry(16, 8192, 8192, 25e-6, 1922.1, 6668.5)
+    q = 2 * (16 * 8192 + 8192 * 8192) + 2 * 16 * 8192
+    assert e["bound"] == "hbm" and e["algorithmic_bytes"] == q
+    assert e["achieved_gbs"] == pytest.approx(q / 25e-6 / 1e9, rel=1e-3)
+    # on the HBM roof, achieved / attainable is the fraction of the bandwidth
+    assert e["frac"] == pytest.approx(q / 25e-6 / 1e9 / 6668.5, rel=1e-3)
+    # 4096^3 with beta: C is read as well; intensity 2*4096^3 / (4 * 32 MiB) = 1024
+    e = rl.roofline_entry(4096, 4096, 4096, 1e-4, 1922.1, 6668.5, beta_nonzero=True)
+    assert e["intensity_flop_per_byte"] == 1024.0 and e["bound"] == "tensor"
+    assert e["frac"] == pytest.approx(2 * 4096 ** 3 / 1e-4 / 1e12 / 1922.1, rel=1e-3)
