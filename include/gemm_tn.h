@@ -145,6 +145,12 @@ typedef struct gemm_tn_config {
                                4 or 8 CTAs (two or four pairs), with pairs (2 CTAs) as the fallback
                                where a cluster of SMs has no room for the larger size; 0 = pairs only.
                                Applied only when it divides the grid */
+  int b_static;             /* skinny path: 1 = the caller promises that no work still running on the
+                               GPU when this call starts writes B (B holds weights, written long
+                               before); the kernel then loads its first ring of B before it waits for
+                               the preceding kernel on the stream to finish, so that the weight
+                               stream starts during that kernel's tail.  A, C and D keep the
+                               stream order.  0 = B is loaded only after that wait */
 } gemm_tn_config;
 
 /* Tile schedulers of the tiled paths.

@@ -285,6 +285,8 @@ int check_config(const gemm_tn_config* cfg) {
   const int kg = cfg->skinny_kgroup;
   if (kg != 0 && kg != 1 && kg != 2 && kg != 4)
     return fail(GEMM_ERR_INVALID_VALUE, "skinny_kgroup must be 0, 1, 2 or 4, got %d", kg);
+  if (cfg->b_static != 0 && cfg->b_static != 1)
+    return fail(GEMM_ERR_INVALID_VALUE, "b_static must be 0 or 1, got %d", cfg->b_static);
   if (cfg->cluster_pref != 0 && cfg->cluster_pref != 4 && cfg->cluster_pref != 8)
     return fail(GEMM_ERR_INVALID_VALUE, "cluster_pref must be 0, 4 or 8, got %d", cfg->cluster_pref);
   if (cfg->l2_hints < -1 || cfg->l2_hints > 7)
@@ -416,6 +418,7 @@ int run(int64_t M, int64_t N, int64_t K, const void* A, int64_t lda, const void*
     p.alpha = alpha; p.beta = beta; p.has_c = has_c; p.epi = epi;
     p.C = C; p.ldc = ldc; p.D = D; p.ldd = ldd; p.out_f32 = out_dtype == GEMM_OUT_F32;
     p.fault = fault; p.timeout_ns = tmo; p.status = st->status;
+    p.b_early = cfg && cfg->b_static && pdl ? 1 : 0;
     Workspace* w = nullptr;
     rc = get_workspace(dev, stream, (size_t)grid * 2 * p.bm * np, (size_t)p.n_tiles * 4, &w);
     if (rc != GEMM_OK) return rc;

@@ -244,22 +244,26 @@ __global__ void __launch_bounds__(kThreads, 1)
   int p_stage = 0;
   uint32_t p_phase = 0;
   long long p_u = u_begin;
-  auto issue = [&](long long u, int stage) {
+  // One stage: arm its FULL barrier with both operands' bytes, then load B
+  // (the weights) and A (the tokens); `which` = 1 B only (arms), 2 A only
+  // (already armed), 3 both.
+  auto issue_part = [&](long long u, int stage, int which) {
     const int n = (int)(u / KB), g = (int)(u % KB);
     const uint32_t fb = full_bar(stage);
-    mbar_arrive_expect_tx(fb, tx);
+    if (which & 1) mbar_arrive_expect_tx(fb, tx);
     if (skip_once) {
-      skip_once = false;  // test-only: leave this stage's bytes missing
+      if (which & 2) skip_once = false;  // test-only: leave this stage's bytes missing
     } else if (KG == 1) {
-      tma_load_2d(sB + stage * b_stage, &tmB, g * kBK, n * BM, fb);
-      tma_load_2d(sA + stage * a_stage, &tmA, g * kBK, 0, fb);
+      if (which & 1) tma_load_2d(sB + stage * b_stage, &tmB, g * kBK, n * BM, fb);
+      if (which & 2) tma_load_2d(sA + stage * a_stage, &tmA, g * kBK, 0, fb);
     } else {
       // 3D views {k in block, row, k-block}: k-blocks g*KG .. g*KG+KG-1,
       // those past K zero-filled
-      tma_load_3d(sB + stage * b_stage, &tmB, 0, n * BM, g * KG, fb);
-      tma_load_3d(sA + stage * a_stage, &tmA, 0, 0, g * KG, fb);
+      if (which & 1) tma_load_3d(sB + stage * b_stage, &tmB, 0, n * BM, g * KG, fb);
+      if (which & 2) tma_load_3d(sA + stage * a_stage, &tmA, 0, 0, g * KG, fb);
     }
   };
+  auto issue = [&](long long u, int stage) { issue_part(u, stage, 3); };
 
   if (threadIdx.x == 0) {
     for (int s = 0; s < S; ++s) {
@@ -278,11 +282,17 @@ __global__ void __launch_bounds__(kThreads, 1)
     tma_prefetch_desc(&tmB);
   }
   // Inputs may come from the previous kernel on the stream: no global memory
-  // access before this point.
+  // access before this point.  Exception: with p.b_early the caller has
+  // promised that nothing still running writes B (weights), so the first
+  // ring's B boxes go out now, while the previous kernel finishes, and only
+  // the token loads wait.
+  if (p.b_early && threadIdx.x == 0) {
+    for (int s = 0; s < S && u_begin + s < u_end; ++s) issue_part(u_begin + s, s, 1);
+  }
   griddep_wait();
   griddep_launch_dependents();
   if (threadIdx.x == 0) {
-    while (p_u < u_end && p_stage < S) issue(p_u++, p_stage++);  // every stage starts empty
+    while (p_u < u_end && p_stage < S) issue_part(p_u++, p_stage++, p.b_early ? 2 : 3);  // every stage starts empty
     if (p_stage == S) {
       p_stage = 0;
       p_phase = 1;

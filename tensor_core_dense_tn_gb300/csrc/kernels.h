@@ -99,6 +99,8 @@ struct SkinnyParams {
   int split;           // 0: stream-K ranges over the grid; s >= 2: every tile in s parts,
                        //    CTA c holds part c / n_tiles of tile c % n_tiles
   int skew;            // split mode: k-groups moved from the last part to part 0
+  int b_early;         // 1 = B is not written by anything still running: its first ring is loaded
+                       //    before the dependency wait on the previous kernel
   int stages;
   float alpha, beta;
   int has_c;

@@ -35,7 +35,7 @@ def up8(x):
 
 
 def run_int(M, N, K, path, out_dtype, seed, lda=None, ldb=None, grid=0, skinny_grid=0, alpha=1.0,
-            disable_pdl=0, scheduler=0, skinny_bm=0, skinny_kgroup=0, tiled_k_parts=0):
+            disable_pdl=0, scheduler=0, skinny_bm=0, skinny_kgroup=0, tiled_k_parts=0, b_static=0):
     lda = up8(K) if lda is None else lda
     ldb = up8(K) if ldb is None else ldb
     A = gi.draw_bf16(M, K, gi.Dist("int", -4, 4), seed, ld=lda)
@@ -45,7 +45,8 @@ def run_int(M, N, K, path, out_dtype, seed, lda=None, ldb=None, grid=0, skinny_g
     dD, ldd = empty_out(M, N, out_dtype, ld=up8(N))
     rc, st = call(M, N, K, dA, lda, dB, ldb, None, 0, dD, ldd, alpha, 0.0, out_dtype, path=path,
                   grid=grid, skinny_grid=skinny_grid, disable_pdl=disable_pdl, scheduler=scheduler,
-                  skinny_bm=skinny_bm, skinny_kgroup=skinny_kgroup, tiled_k_parts=tiled_k_parts)
+                  skinny_bm=skinny_bm, skinny_kgroup=skinny_kgroup, tiled_k_parts=tiled_k_parts,
+                  b_static=b_static)
     assert rc == 0, g.last_error()
     assert st == 0, g.last_error()
     return from_dev(dD, out_dtype)[:, :N], expect_exact(ref, out_dtype)
@@ -680,3 +681,20 @@ def test_l2_hints_exact(hints, path):
                            1.0, 0.5, gi.OUT_F32, s, cfg)
     assert rc == 0 and g.gemm_get_status(s) == 0, g.last_error()
     assert_same(from_dev(dD, gi.OUT_F32), oracle.exact_f32(ref))
+
+
+@pytest.mark.parametrize("M,N,K,skinny_grid,kg", [
+    (16, 8192, 1024, 0, 0),      # two parts per tile, 4 k-blocks per box
+    (16, 2048, 4096, 0, 0),      # four parts
+    (16, 1000, 4160, 37, 0),     # stream-K ranges
+    (5, 300, 70, 0, 0),          # ragged, K below one k-block (2D maps)
+    (48, 4096, 2048, 0, 2),      # 64-row tiles, 2 k-blocks per box
+    (96, 8192, 4096, 0, 0),      # wide form
+])
+def test_skinny_b_static_exact(M, N, K, skinny_grid, kg):
+    """B loaded before the dependency wait (gemm_tn_config.b_static): the same
+    bits, with the previous call on the stream writing the D this one writes."""
+    for rep in range(2):
+        got, exp = run_int(M, N, K, PS, gi.OUT_F32, seed=1400 + M + N + K + rep, skinny_grid=skinny_grid,
+                           skinny_kgroup=kg, b_static=1)
+        assert_same(got, exp)

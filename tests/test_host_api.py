@@ -183,3 +183,10 @@ def test_unknown_l2_hints_and_cluster_pref_rejected(lib, field, value):
     a = (300, 64, 64, 0x1000, 64, 0x2000, 64, 0, 0, 0x3000, 64, 1.0, 0.0, 0, 0)
     assert g.gemm_bf16_tn_ex(*a, config=g.GemmConfig(**{field: value})) == g.GEMM_ERR_INVALID_VALUE
     assert field in g.last_error()
+
+
+@pytest.mark.parametrize("value", [-1, 2])
+def test_unknown_b_static_rejected(lib, value):
+    a = (16, 64, 64, 0x1000, 64, 0x2000, 64, 0, 0, 0x3000, 64, 1.0, 0.0, 0, 0)
+    assert g.gemm_bf16_tn_ex(*a, config=g.GemmConfig(b_static=value)) == g.GEMM_ERR_INVALID_VALUE
+    assert "b_static" in g.last_error()
