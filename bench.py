@@ -17,6 +17,8 @@ no flush is needed between steps.  Alongside it, in the same run:
 * ``stream_ceiling``: gemm_stream_read over each decode's weight matrix (the
   same TMA boxes and ring, nothing else done): the read ceiling each decode
   is compared with;
+* ``mma_rate``: gemm_mma_rate, the cost of one tcgen05.mma at the skinny
+  path's shapes (M = 128 per CTA or 256 per pair, N = 16..256);
 * ``configs``: all five workloads, each timed and set against the roofline
   min(P_tc, BW * F/Q), with the oracle's parity on its outputs;
 * ``e2e``: the same metric with host buffers — pinned host->device copies
@@ -245,7 +247,7 @@ def run_ours(args, dist):
     dD = torch.empty((w.M, w.N), dtype=out_t, device=device)
     sched = {"default": 0, "static": 1, "clc": 2}[args.scheduler]
     cfg = g.GemmConfig(path=args.path, scheduler=sched, l2_hints=args.l2_hints, raster_group=args.raster_group,
-                       cluster_pref=args.cluster_pref)
+                       cluster_pref=args.cluster_pref, tiled_k_parts=args.tiled_k_parts)
     c_ptr = dC.data_ptr() if dC is not None else 0
     ldc = w.N if dC is not None else 0
 
@@ -358,6 +360,7 @@ def run_ours(args, dist):
         result["decode_b_static"] = run_decode(args, g, torch, device, peaks, dist, b_static=1)
         result["fp8"] = run_fp8(args, g, torch, device, peaks, dist)
         result["stream_ceiling"] = run_stream_ceiling(args, g, torch, device, peaks, dist, result)
+        result["mma_rate"] = run_mma_rate(g, torch, device)
         result["configs"] = run_configs(args, g, torch, device, peaks, dist, result, w, A, B, dD)
         result["scheduler_clc"] = run_scheduler_study(args, g, torch, device, w, dA, dB, dD, flops, peaks, dist)
         result["grouped"] = run_grouped_leg(args, g, torch, device, dist)
@@ -676,6 +679,33 @@ def run_stream_ceiling(args, g, torch, device, peaks, dist, result):
         out[name] = entry
         del bufs
     return out
+
+
+def run_mma_rate(g, torch, device):
+    """gemm_mma_rate on every SM: nanoseconds per tcgen05.mma instruction at
+    M = 128 rows per CTA (one CTA or a pair) against N, and the weight bytes
+    each SM's tensor core consumes per nanosecond at that rate (each
+    instruction reads 128 rows x 32 bytes of K per CTA)."""
+    sms = torch.cuda.get_device_properties(device).multi_processor_count
+    out = torch.zeros(2, dtype=torch.int64, device=device)
+    stream = torch.cuda.current_stream(device).cuda_stream
+    reps = 4096
+    res = {"reps": reps, "mma_per_rep": 4, "grid": sms}
+    for fp8, kind in ((0, "bf16"), (1, "e4m3")):
+        for cg in (1, 2):
+            row = {}
+            for n in (16, 32, 64, 128, 256):
+                for _ in range(2):
+                    rc = g.gemm_mma_rate(n, cg, fp8, reps, sms - sms % cg, out.data_ptr(), stream)
+                    if rc != 0:
+                        raise RuntimeError(f"mma rate failed: {rc} {g.last_error()}")
+                torch.cuda.synchronize()
+                ns = float(out[0].item()) / (reps * 4)
+                row[str(n)] = {"ns_per_mma": round(ns, 2), "weight_bytes_per_ns_per_sm": round(128 * 32 / ns, 1)}
+            res[f"{kind}_cta_group{cg}"] = row
+    if g.gemm_get_status(stream) != 0:
+        raise RuntimeError(g.last_error())
+    return res
 
 
 def run_configs(args, g, torch, device, peaks, dist, result, w_main, A_main, B_main, dD_main):
@@ -1026,6 +1056,8 @@ def main():
                     help="main step: L2 eviction hints of the tiled kernels (gemm_tn_config.l2_hints)")
     ap.add_argument("--raster-group", type=int, default=0,
                     help="main step: tiles along M per raster strip (0 = automatic)")
+    ap.add_argument("--tiled-k-parts", type=int, default=0,
+                    help="main step: k-parts per tile of the tiled paths (gemm_tn_config.tiled_k_parts)")
     ap.add_argument("--cluster-pref", type=int, default=0, choices=[0, 4, 8],
                     help="main step: preferred cluster size of the 2-SM path (gemm_tn_config.cluster_pref)")
     ap.add_argument("--in-dtype", choices=["bf16", "e4m3", "e5m2"], default="bf16",

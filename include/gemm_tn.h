@@ -372,6 +372,26 @@ int gemm_version(void);
 int gemm_stream_read(const void *src, int64_t rows, int64_t row_bytes, int box_rows, int kgroup, int grid,
                      void *stream);
 
+/* Measurement kernel: the tcgen05.mma rate at the skinny path's shapes.
+ *
+ * grid CTAs (cta_group = 1) or grid / 2 CTA pairs (cta_group = 2) each issue
+ * reps groups of four tcgen05.mma instructions (kind::f16 with bf16 operands,
+ * or kind::f8f6f4 with e4m3 when fp8 != 0; K = one 128-byte atom per group)
+ * with M = 128 rows per CTA and N = n columns (the pair splits the n rows of
+ * its second operand between its CTAs), on zeroed shared-memory operands,
+ * accumulating in Tensor Memory; then they commit and wait.  out_ns (device
+ * memory, two unsigned 64-bit words, owned by the caller) receives from the
+ * first CTA: [0] the nanoseconds from the first issue to the completion of
+ * all MMAs, [1] those of the issue loop alone.  It is the per-instruction
+ * cost the skinny kernel pays for every stage it consumes (the SemiAnalysis
+ * Blackwell page, section "5th-generation tensor core MMA", measures the
+ * same instruction's throughput against its shape).
+ *
+ * n is a multiple of 16 in [16, 256], cta_group 1 or 2, 1 <= reps <= 2^24,
+ * grid a multiple of cta_group up to 1024; else GEMM_ERR_INVALID_VALUE.
+ * Asynchronous on stream; waits are bounded (gemm_get_status). */
+int gemm_mma_rate(int n, int cta_group, int fp8, int reps, int grid, unsigned long long *out_ns, void *stream);
+
 /* The skinny path (1 <= M <= 64) without any allocation at call time.
  *
  * The pages have no counterpart to this entry point; it exists for callers

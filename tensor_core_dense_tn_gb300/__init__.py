@@ -38,7 +38,8 @@ GEMM_ERR_CUDA = -8
 EXPORTED = ["gemm_bf16_tn", "gemm_bf16_tn_ex", "gemm_get_status", "gemm_get_status_detail",
             "gemm_last_error_string", "gemm_last_launch_info", "gemm_shutdown", "gemm_version",
             "gemm_bf16_tn_skinny_noalloc", "gemm_bf16_tn_bias_act", "gemm_fp8_tn", "gemm_fp8_tn_ex",
-            "gemm_bf16_tn_grouped", "gemm_bf16_tn_batched", "gemm_plan", "gemm_stream_read"]
+            "gemm_bf16_tn_grouped", "gemm_bf16_tn_batched", "gemm_plan", "gemm_stream_read",
+            "gemm_mma_rate"]
 
 FP8_E4M3, FP8_E5M2 = 0, 1
 SCHED_DEFAULT, SCHED_STATIC, SCHED_CLC = 0, 1, 2
@@ -118,6 +119,8 @@ def load(path: str = LIB_PATH):
         lib.gemm_bf16_tn_skinny_noalloc.restype = i32
         lib.gemm_stream_read.argtypes = [vp, i64, i64, i32, i32, i32, vp]
         lib.gemm_stream_read.restype = i32
+        lib.gemm_mma_rate.argtypes = [i32, i32, i32, i32, i32, vp, vp]
+        lib.gemm_mma_rate.restype = i32
         lib.gemm_bf16_tn_grouped.argtypes = [i32, ctypes.POINTER(GemmProblem), f32, f32, i32, vp]
         lib.gemm_bf16_tn_grouped.restype = i32
         lib.gemm_bf16_tn_batched.argtypes = [i64, i64, i64, i64, vp, i64, i64, vp, i64, i64, vp, i64, i64,
@@ -172,6 +175,11 @@ def gemm_stream_read(src, rows, row_bytes, box_rows, kgroup, grid, stream) -> in
     """Raw C-ABI call of the TMA streaming-read ceiling kernel (reads rows x
     row_bytes bytes at src in the skinny kernel's box shape, discards them)."""
     return load().gemm_stream_read(src, rows, row_bytes, box_rows, kgroup, grid, stream or None)
+
+
+def gemm_mma_rate(n, cta_group, fp8, reps, grid, out_ns, stream) -> int:
+    """Raw C-ABI call of the tcgen05.mma rate kernel (out_ns: device pointer to two uint64)."""
+    return load().gemm_mma_rate(n, cta_group, fp8, reps, grid, out_ns, stream or None)
 
 
 def gemm_bf16_tn_grouped(problems, alpha, beta, out_dtype, stream) -> int:

@@ -17,7 +17,7 @@ INCLUDE = os.path.join(os.path.dirname(PKG), "include")
 OUT_DIR = os.path.join(PKG, "_lib")
 BUILD_DIR = os.path.join(PKG, "_build")
 LIB = os.path.join(OUT_DIR, "libgemm_tn.so")
-SOURCES = ["gemm_api.cu", "gemm_tiled.cu", "gemm_skinny.cu", "gemm_noalloc.cu", "stream_read.cu"]
+SOURCES = ["gemm_api.cu", "gemm_tiled.cu", "gemm_skinny.cu", "gemm_noalloc.cu", "measure.cu"]
 HEADERS = ["ptx.cuh", "kernels.h", "epilogue.cuh"]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 

@@ -1,3 +1,7 @@
+// Measurement kernels: the read ceiling of the skinny kernel's operand
+// stream (gemm_stream_read) and the tcgen05.mma rate at the skinny path's
+// shapes (gemm_mma_rate).
+//
 // gemm_stream_read: the read ceiling of the skinny kernel's operand stream.
 //
 // The Ampere-to-Hopper page (section "not reaching peak") judges a kernel
@@ -79,6 +83,78 @@ __global__ void __launch_bounds__(32, 1) gemm_stream_read_kernel(const __grid_co
     // After a failure nothing new is issued; the loop still waits (bounded)
     // once for every copy already in flight so that none lands after exit.
     if (!failed && issued < e) issue(issued++, s);
+  }
+}
+
+// One CTA (CG = 1) or CTA pair (CG = 2) issues `reps` groups of four
+// tcgen05.mma (K = 16 bf16 or 32 fp8 each, walking one 128-byte K atom) on
+// zeroed shared-memory operands: MMA M = 128 per CTA, N = n (split between
+// the pair's CTAs for CG = 2), accumulating into TMEM, then commits and waits
+// (bounded).  out[0] = ns from the first issue to completion, out[1] = ns of
+// issue alone.  The operands' values do not matter for the timing.
+constexpr int kRateStages = 3;
+
+template <int CG, int KIND>
+__global__ void __launch_bounds__(64, 1) gemm_mma_rate_kernel(int n, int reps, uint64_t timeout_ns, int* status,
+                                                              unsigned long long* out) {
+  extern __shared__ uint8_t raw[];
+  uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(raw) + 1023) & ~uintptr_t(1023));
+  __shared__ uint64_t bar;
+  __shared__ uint32_t tslot;
+  const uint32_t rank = CG == 2 ? cluster_ctarank() : 0;
+  const int nb = n / CG;                                 // B rows held by this CTA
+  const uint32_t sA = smem_u32(smem);                    // stages x 128 rows x 128 B
+  const uint32_t sB = sA + kRateStages * 16384;          // stages x nb rows x 128 B
+  for (int i = threadIdx.x; i < kRateStages * (16384 + nb * 128) / 16; i += blockDim.x)
+    reinterpret_cast<uint4*>(smem)[i] = make_uint4(0, 0, 0, 0);
+  if (threadIdx.x == 0) {
+    mbar_init(smem_u32(&bar), 1);
+    fence_mbar_init();
+  }
+  if (threadIdx.x < 32) tmem_alloc<CG>(smem_u32(&tslot), 256);
+  fence_proxy_async_smem();
+  tc_fence_before();
+  __syncthreads();
+  if constexpr (CG == 2) cluster_sync();
+  tc_fence_after();
+  const uint32_t tmem = tslot;
+  if (threadIdx.x == 0) {
+    bool ok = true;
+    if (rank == 0) {
+      const uint32_t idesc = KIND == kKindF16 ? instr_desc_bf16_f32(128 * CG, (uint32_t)n)
+                                              : instr_desc_f32acc(128 * CG, (uint32_t)n, 0, 0);
+      const unsigned long long t0 = globaltimer();
+      for (int r = 0; r < reps; ++r) {
+        const int st = r % kRateStages;
+        const uint64_t a0 = smem_desc_sw128(sA + st * 16384), b0 = smem_desc_sw128(sB + st * nb * 128);
+#pragma unroll
+        for (int k = 0; k < 4; ++k) mma_issue<CG, KIND>(tmem, a0 + 2 * k, b0 + 2 * k, idesc, (r | k) ? 1u : 0u);
+      }
+      if constexpr (CG == 1) mma_commit(smem_u32(&bar));
+      else mma_commit_pair(smem_u32(&bar), 0x3);
+      const unsigned long long t1 = globaltimer();
+      ok = false;
+      while (globaltimer() - t1 < timeout_ns)
+        if (mbar_try_wait(smem_u32(&bar), 0)) { ok = true; break; }
+      const unsigned long long t2 = globaltimer();
+      if (blockIdx.x == 0) {
+        out[0] = t2 - t0;
+        out[1] = t1 - t0;
+      }
+    } else {
+      const unsigned long long t1 = globaltimer();
+      ok = false;
+      while (globaltimer() - t1 < timeout_ns)
+        if (mbar_try_wait_cluster(smem_u32(&bar), 0)) { ok = true; break; }
+    }
+    if (!ok && atomicCAS(status, 0, GEMM_ERR_TIMEOUT) == 0) atomicExch(status + 1, (kRoleMma << 24) | (int)blockIdx.x);
+  }
+  tc_fence_before();
+  __syncthreads();
+  if constexpr (CG == 2) cluster_sync();
+  if (threadIdx.x < 32) {
+    tc_fence_after();
+    tmem_dealloc<CG>(tmem, 256);
   }
 }
 
@@ -173,6 +249,53 @@ extern "C" int gemm_stream_read(const void* src, int64_t rows, int64_t row_bytes
   cfg.attrs = attr;
   cfg.numAttrs = 1;
   if (cudaLaunchKernelEx(&cfg, gemm_stream_read_kernel, tm, p) != cudaSuccess) {
+    cudaGetLastError();
+    return sr_fail(GEMM_ERR_LAUNCH, "kernel launch failed");
+  }
+  return GEMM_OK;
+}
+
+extern "C" int gemm_mma_rate(int n, int cta_group, int fp8, int reps, int grid, unsigned long long* out_ns,
+                             void* stream_v) {
+  using namespace gtn;
+  set_error_text("");
+  if (cta_group != 1 && cta_group != 2) return sr_fail(GEMM_ERR_INVALID_VALUE, "cta_group must be 1 or 2");
+  if (n < 16 || n > 256 || n % 16) return sr_fail(GEMM_ERR_INVALID_VALUE, "n must be a multiple of 16 in [16, 256]");
+  if (reps < 1 || reps > (1 << 24)) return sr_fail(GEMM_ERR_INVALID_VALUE, "reps must be in [1, 2^24]");
+  if (grid < 1 || grid > 1024 || grid % cta_group) return sr_fail(GEMM_ERR_INVALID_VALUE, "bad grid");
+  if (!out_ns || (reinterpret_cast<uintptr_t>(out_ns) & 7u)) return sr_fail(GEMM_ERR_MISALIGNED, "out_ns");
+  int dev = 0, major = 0, minor = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess ||
+      cudaDeviceGetAttribute(&major, cudaDevAttrComputeCapabilityMajor, dev) != cudaSuccess ||
+      cudaDeviceGetAttribute(&minor, cudaDevAttrComputeCapabilityMinor, dev) != cudaSuccess)
+    return sr_fail(GEMM_ERR_CUDA, "device query failed");
+  if (!(major == 10 && minor == 3)) return sr_fail(GEMM_ERR_UNSUPPORTED_DEVICE, "needs sm_103");
+  int* status = nullptr;
+  if (status_word_address(&status) != cudaSuccess) return sr_fail(GEMM_ERR_CUDA, "status word lookup failed");
+  const int smem = 1024 + kRateStages * (16384 + n / cta_group * 128);
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3((unsigned)grid);
+  cfg.blockDim = dim3(64);
+  cfg.dynamicSmemBytes = smem;
+  cfg.stream = static_cast<cudaStream_t>(stream_v);
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeClusterDimension;
+  attr[0].val.clusterDim.x = (unsigned)cta_group;
+  attr[0].val.clusterDim.y = 1;
+  attr[0].val.clusterDim.z = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  const uint64_t tmo = default_wait_timeout_ns();
+  cudaError_t e;
+#define GTN_RATE(CGV, KV)                                                                              \
+  ((e = cudaFuncSetAttribute(gemm_mma_rate_kernel<CGV, KV>, cudaFuncAttributeMaxDynamicSharedMemorySize, smem)) \
+       == cudaSuccess                                                                                  \
+       ? cudaLaunchKernelEx(&cfg, gemm_mma_rate_kernel<CGV, KV>, n, reps, tmo, status, out_ns)           \
+       : e)
+  if (cta_group == 1) e = fp8 ? GTN_RATE(1, kKindF8F6F4) : GTN_RATE(1, kKindF16);
+  else e = fp8 ? GTN_RATE(2, kKindF8F6F4) : GTN_RATE(2, kKindF16);
+#undef GTN_RATE
+  if (e != cudaSuccess) {
     cudaGetLastError();
     return sr_fail(GEMM_ERR_LAUNCH, "kernel launch failed");
   }

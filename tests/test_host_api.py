@@ -190,3 +190,17 @@ def test_unknown_b_static_rejected(lib, value):
     a = (16, 64, 64, 0x1000, 64, 0x2000, 64, 0, 0, 0x3000, 64, 1.0, 0.0, 0, 0)
     assert g.gemm_bf16_tn_ex(*a, config=g.GemmConfig(b_static=value)) == g.GEMM_ERR_INVALID_VALUE
     assert "b_static" in g.last_error()
+
+
+@pytest.mark.parametrize("args,code", [
+    ((8, 1, 0, 16, 1, 0x1000), g.GEMM_ERR_INVALID_VALUE),      # n below 16
+    ((24, 1, 0, 16, 1, 0x1000), g.GEMM_ERR_INVALID_VALUE),     # n not a multiple of 16
+    ((272, 1, 0, 16, 1, 0x1000), g.GEMM_ERR_INVALID_VALUE),    # n above 256
+    ((16, 3, 0, 16, 3, 0x1000), g.GEMM_ERR_INVALID_VALUE),     # cta_group
+    ((16, 2, 0, 16, 3, 0x1000), g.GEMM_ERR_INVALID_VALUE),     # grid not a multiple of the pair
+    ((16, 1, 0, 0, 1, 0x1000), g.GEMM_ERR_INVALID_VALUE),      # reps
+    ((16, 1, 0, 16, 1, 0x1004), g.GEMM_ERR_MISALIGNED),        # out_ns not 8-byte aligned
+])
+def test_mma_rate_argument_errors(lib, args, code):
+    assert g.gemm_mma_rate(*args, 0) == code
+    assert g.last_error() != ""
