@@ -151,6 +151,11 @@ typedef struct gemm_tn_config {
                                the preceding kernel on the stream to finish, so that the weight
                                stream starts during that kernel's tail.  A, C and D keep the
                                stream order.  0 = B is loaded only after that wait */
+  int skinny_pair;          /* skinny path: 2 = the pair form, clusters of two CTAs on tiles of 256 rows
+                               of B (cta_group::2 MMAs, M = 256) with the tokens split between the two
+                               CTAs, so that each MMA instruction consumes twice the weight rows and each
+                               CTA loads half the token bytes; 1 = one CTA per tile; 0 = library
+                               default (one CTA per tile) */
 } gemm_tn_config;
 
 /* Tile schedulers of the tiled paths.

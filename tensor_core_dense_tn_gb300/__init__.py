@@ -59,7 +59,7 @@ class GemmConfig(ctypes.Structure):
                 ("test_fault", ctypes.c_int), ("disable_pdl", ctypes.c_int),
                 ("skinny_skew_kb", ctypes.c_int), ("scheduler", ctypes.c_int), ("skinny_bm", ctypes.c_int),
                 ("skinny_kgroup", ctypes.c_int), ("tiled_k_parts", ctypes.c_int), ("l2_hints", ctypes.c_int),
-                ("cluster_pref", ctypes.c_int), ("b_static", ctypes.c_int)]
+                ("cluster_pref", ctypes.c_int), ("b_static", ctypes.c_int), ("skinny_pair", ctypes.c_int)]
 
 
 class GemmPlanInfo(ctypes.Structure):

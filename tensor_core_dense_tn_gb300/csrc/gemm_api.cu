@@ -287,6 +287,8 @@ int check_config(const gemm_tn_config* cfg) {
     return fail(GEMM_ERR_INVALID_VALUE, "skinny_kgroup must be 0, 1, 2 or 4, got %d", kg);
   if (cfg->b_static != 0 && cfg->b_static != 1)
     return fail(GEMM_ERR_INVALID_VALUE, "b_static must be 0 or 1, got %d", cfg->b_static);
+  if (cfg->skinny_pair < 0 || cfg->skinny_pair > 2)
+    return fail(GEMM_ERR_INVALID_VALUE, "skinny_pair must be 0, 1 or 2, got %d", cfg->skinny_pair);
   if (cfg->cluster_pref != 0 && cfg->cluster_pref != 4 && cfg->cluster_pref != 8)
     return fail(GEMM_ERR_INVALID_VALUE, "cluster_pref must be 0, 4 or 8, got %d", cfg->cluster_pref);
   if (cfg->l2_hints < -1 || cfg->l2_hints > 7)
@@ -325,16 +327,22 @@ int auto_path(int64_t M, int64_t N, int64_t K, int in_bytes, int sms) {
 int skinny_geometry(SkinnyParams* p, int64_t M, int64_t N, int64_t K, int kbe, int sms, const gemm_tn_config* cfg) {
   const int np = (int)((M + 15) / 16) * 16;
   p->M = (int)M; p->N = (int)N; p->K = (int)K; p->np = np;
-  const int max_grid = skinny_max_grid(np, sms);
+  // The pair form (clusters of two CTAs, 256-row tiles, cta_group::2 MMAs,
+  // half the tokens per CTA) only where asked for.
+  p->cg = cfg && cfg->skinny_pair == 2 ? 2 : 1;
+  const int npc = np / p->cg;  // token rows per CTA
+  const int max_grid = skinny_max_grid(np, sms) / p->cg;  // CTAs, or pairs
   const int bm_req = cfg ? cfg->skinny_bm : 0, kg_req = cfg ? cfg->skinny_kgroup : 0;
-  p->bm = bm_req ? bm_req : skinny_tile_rows(N, np, max_grid);
-  p->kg = skinny_kgroup(np, p->bm, K, kbe, kg_req);
-  if (skinny_stages(np, p->bm, p->kg) < 2)
+  if (p->cg == 2 && bm_req && bm_req != 128)
+    return fail(GEMM_ERR_INVALID_VALUE, "the pair form takes 128 rows of B per CTA (skinny_bm 0 or 128)");
+  p->bm = p->cg == 2 ? 128 : (bm_req ? bm_req : skinny_tile_rows(N, np, max_grid));
+  p->kg = skinny_kgroup(npc, p->bm, K, kbe, kg_req);
+  if (skinny_stages(npc, p->bm, p->kg) < 2)
     return fail(GEMM_ERR_INVALID_VALUE, "skinny_kgroup %d leaves fewer than 2 ring stages at M = %lld", p->kg,
                 (long long)M);
-  p->stages = skinny_stages(np, p->bm, p->kg);
+  p->stages = skinny_stages(npc, p->bm, p->kg);
   p->num_kb = (int)(((K + kbe - 1) / kbe + p->kg - 1) / p->kg);
-  p->n_tiles = (int)((N + p->bm - 1) / p->bm);
+  p->n_tiles = (int)((N + p->bm * p->cg - 1) / (p->bm * p->cg));
   p->units = (long long)p->n_tiles * p->num_kb;
   skinny_partition(p, max_grid, cfg ? cfg->skinny_grid : 0, cfg ? cfg->skinny_skew_kb : 0);
   return GEMM_OK;
@@ -420,18 +428,18 @@ int run(int64_t M, int64_t N, int64_t K, const void* A, int64_t lda, const void*
     p.fault = fault; p.timeout_ns = tmo; p.status = st->status;
     p.b_early = cfg && cfg->b_static && pdl ? 1 : 0;
     Workspace* w = nullptr;
-    rc = get_workspace(dev, stream, (size_t)grid * 2 * p.bm * np, (size_t)p.n_tiles * 4, &w);
+    rc = get_workspace(dev, stream, (size_t)grid * p.cg * 2 * p.bm * np, (size_t)p.n_tiles * p.cg * 4, &w);
     if (rc != GEMM_OK) return rc;
     p.partials = w->partials;
     p.counters = w->counters;
     CUtensorMap tA, tB;
     if (p.kg == 1) {
-      if ((rc = encode_2d(&tA, in_dt, in_bytes, A, K, M, lda, kbe, np, CU_TENSOR_MAP_SWIZZLE_128B, "A")))
+      if ((rc = encode_2d(&tA, in_dt, in_bytes, A, K, M, lda, kbe, np / p.cg, CU_TENSOR_MAP_SWIZZLE_128B, "A")))
         return rc;
       if ((rc = encode_2d(&tB, in_dt, in_bytes, B, K, N, ldb, kbe, p.bm, CU_TENSOR_MAP_SWIZZLE_128B, "B")))
         return rc;
     } else {
-      if ((rc = encode_kgroups(&tA, in_dt, in_bytes, A, K, M, lda, kbe, np, p.kg, "A"))) return rc;
+      if ((rc = encode_kgroups(&tA, in_dt, in_bytes, A, K, M, lda, kbe, np / p.cg, p.kg, "A"))) return rc;
       if ((rc = encode_kgroups(&tB, in_dt, in_bytes, B, K, N, ldb, kbe, p.bm, p.kg, "B"))) return rc;
     }
     e = launch_skinny(tA, tB, p, pdl, stream, &li);
@@ -804,11 +812,11 @@ int gemm_plan(int64_t M, int64_t N, int64_t K, int fp8_inputs, int num_sms, cons
   if (path == GEMM_PATH_SKINNY) {
     SkinnyParams p = {};
     if ((rc = skinny_geometry(&p, M, N, K, 128 / in_bytes, num_sms, cfg))) return rc;
-    out->tile_m = p.bm;
+    out->tile_m = p.bm * p.cg;
     out->tile_n = p.np;
     out->skinny_kgroup = p.kg;
     out->skinny_stages = p.stages;
-    out->skinny_grid = p.grid;
+    out->skinny_grid = p.grid * p.cg;
     out->k_parts = p.split;
     out->skinny_skew = p.skew;
   } else {

@@ -119,13 +119,23 @@ __device__ __forceinline__ long long tile_part_cta(const SkinnyParams& p, long l
   return p.grid - 1 - (owner_of(n * p.num_kb, p.units, p.grid) + j);
 }
 
+template <bool CLUSTER = false>
+__device__ __forceinline__ bool try_wait_scoped(uint32_t bar, uint32_t parity) {
+  if constexpr (CLUSTER) return mbar_try_wait_cluster(bar, parity);
+  else return mbar_try_wait(bar, parity);
+}
+
+// CLUSTER: the phase may be completed by the pair's other CTA (its TMA
+// bytes, its arrivals, or a multicast tcgen05.commit), so the wait acquires
+// at cluster scope.
+template <bool CLUSTER = false>
 __device__ __noinline__ bool wait_bar_slow(uint32_t bar, uint32_t parity, volatile uint32_t* flag,
                                            uint64_t timeout_ns, int* status, int role) {
   const uint64_t t0 = globaltimer();
   while (true) {
 #pragma unroll 1
     for (int i = 0; i < 32; ++i)
-      if (mbar_try_wait(bar, parity)) return true;
+      if (try_wait_scoped<CLUSTER>(bar, parity)) return true;
     if (flag && *flag) return false;
     if (globaltimer() - t0 > timeout_ns) {
       if (flag) *flag = 1;
@@ -137,10 +147,11 @@ __device__ __noinline__ bool wait_bar_slow(uint32_t bar, uint32_t parity, volati
 
 // Bounded wait on an mbarrier phase (inline fast path).  Returns false if
 // this CTA is aborting or the limit expired.
+template <bool CLUSTER = false>
 __device__ __forceinline__ bool wait_bar(uint32_t bar, uint32_t parity, volatile uint32_t* flag,
                                          uint64_t timeout_ns, int* status, int role) {
-  if (mbar_try_wait(bar, parity)) return true;
-  return wait_bar_slow(bar, parity, flag, timeout_ns, status, role);
+  if (try_wait_scoped<CLUSTER>(bar, parity)) return true;
+  return wait_bar_slow<CLUSTER>(bar, parity, flag, timeout_ns, status, role);
 }
 
 __device__ __noinline__ void settle(uint64_t ns) {
@@ -201,7 +212,7 @@ __device__ __noinline__ bool wait_parts(int* arrivals, int expected, volatile ui
   return ok != 0;
 }
 
-template <int KIND, int BM, bool WIDE>
+template <int KIND, int BM, bool WIDE, int CG>
 __global__ void __launch_bounds__(kThreads, 1)
     gemm_tn_skinny_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
                           const SkinnyParams p) {
@@ -214,9 +225,14 @@ __global__ void __launch_bounds__(kThreads, 1)
   constexpr int kTmemCols = WIDE ? 512 : 256;
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+  // CG = 2, the pair form: a cluster of two CTAs on one tile of 2 * BM rows
+  // of B.  Each CTA loads its own BM rows and half of the np token rows; the
+  // first CTA's MMA thread issues cta_group::2 MMAs (M = 2 * BM) for both,
+  // and each CTA's TMEM holds its own BM rows for all np tokens.
+  constexpr bool kPair = CG == 2;
   const int S = p.stages;
   const int KG = p.kg;                     // k-blocks per stage
-  const int a_bytes = p.np * kStageK;      // A bytes per k-block
+  const int a_bytes = p.np / CG * kStageK; // this CTA's A (token) bytes per k-block
   const int b_stage = KG * kBTileBytes, a_stage = KG * a_bytes;
   const uint32_t sB = smem_u32(smem);
   const uint32_t sA = sB + S * b_stage;
@@ -233,13 +249,16 @@ __global__ void __launch_bounds__(kThreads, 1)
   const int warp = threadIdx.x >> 5;
   const int lane = threadIdx.x & 31;
   const long long KB = p.num_kb;
-  const long long c = blockIdx.x;
+  const uint32_t rank = kPair ? cluster_ctarank() : 0;  // 0 = the pair's MMA issuer
+  const bool leader = rank == 0;
+  const long long c = blockIdx.x / CG;                   // owner of a unit range: a CTA or a pair
+  const long long cta_self = c * CG + rank;              // this CTA's partial-sum slots (= blockIdx.x)
   const long long u_begin = cta_begin(p, c), u_end = cta_end(p, c);
 
   // ---- producer state (thread 0).  The first ring's worth of loads is
   // issued right after the barriers exist, before the block-wide sync, so
   // that it overlaps TMEM allocation and the other warps' start-up.
-  const uint32_t tx = (uint32_t)(b_stage + a_stage);
+  const uint32_t tx = (uint32_t)(CG * (b_stage + a_stage));  // both CTAs' bytes on the first CTA's barrier
   bool skip_once = (p.fault & kFaultSkipTmaOnce) && blockIdx.x == 0;
   int p_stage = 0;
   uint32_t p_phase = 0;
@@ -250,17 +269,29 @@ __global__ void __launch_bounds__(kThreads, 1)
   auto issue_part = [&](long long u, int stage, int which) {
     const int n = (int)(u / KB), g = (int)(u % KB);
     const uint32_t fb = full_bar(stage);
-    if (which & 1) mbar_arrive_expect_tx(fb, tx);
+    const int b_row = n * BM * CG + (int)rank * BM;      // this CTA's rows of B
+    const int a_row = (int)rank * (p.np / CG);           // this CTA's token rows
+    if ((which & 1) && leader) mbar_arrive_expect_tx(fb, tx);
     if (skip_once) {
       if (which & 2) skip_once = false;  // test-only: leave this stage's bytes missing
+    } else if constexpr (kPair) {
+      // both CTAs' copies complete on the first CTA's barrier
+      const uint32_t fbl = mapa_shared(fb, 0);
+      if (KG == 1) {
+        if (which & 1) tma_load_2d_pair(sB + stage * b_stage, &tmB, g * kBK, b_row, fbl);
+        if (which & 2) tma_load_2d_pair(sA + stage * a_stage, &tmA, g * kBK, a_row, fbl);
+      } else {
+        if (which & 1) tma_load_3d_pair(sB + stage * b_stage, &tmB, 0, b_row, g * KG, fbl);
+        if (which & 2) tma_load_3d_pair(sA + stage * a_stage, &tmA, 0, a_row, g * KG, fbl);
+      }
     } else if (KG == 1) {
-      if (which & 1) tma_load_2d(sB + stage * b_stage, &tmB, g * kBK, n * BM, fb);
-      if (which & 2) tma_load_2d(sA + stage * a_stage, &tmA, g * kBK, 0, fb);
+      if (which & 1) tma_load_2d(sB + stage * b_stage, &tmB, g * kBK, b_row, fb);
+      if (which & 2) tma_load_2d(sA + stage * a_stage, &tmA, g * kBK, a_row, fb);
     } else {
       // 3D views {k in block, row, k-block}: k-blocks g*KG .. g*KG+KG-1,
       // those past K zero-filled
-      if (which & 1) tma_load_3d(sB + stage * b_stage, &tmB, 0, n * BM, g * KG, fb);
-      if (which & 2) tma_load_3d(sA + stage * a_stage, &tmA, 0, 0, g * KG, fb);
+      if (which & 1) tma_load_3d(sB + stage * b_stage, &tmB, 0, b_row, g * KG, fb);
+      if (which & 2) tma_load_3d(sA + stage * a_stage, &tmA, 0, a_row, g * KG, fb);
     }
   };
   auto issue = [&](long long u, int stage) { issue_part(u, stage, 3); };
@@ -272,7 +303,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
     for (int b = 0; b < kNumAcc; ++b) {
       mbar_init(accf_bar(b), 1);
-      mbar_init(acce_bar(b), kEpiWarps);
+      mbar_init(acce_bar(b), kEpiWarps * CG);  // the epilogue warps of both CTAs of a pair
     }
     mbar_init(drain_bar, 1);
     *abort_flag = 0;
@@ -281,6 +312,8 @@ __global__ void __launch_bounds__(kThreads, 1)
     tma_prefetch_desc(&tmA);
     tma_prefetch_desc(&tmB);
   }
+  // a pair's copies and arrivals target the other CTA's barriers: both exist first
+  if constexpr (kPair) cluster_sync();
   // Inputs may come from the previous kernel on the stream: no global memory
   // access before this point.  Exception: with p.b_early the caller has
   // promised that nothing still running writes B (weights), so the first
@@ -298,7 +331,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       p_phase = 1;
     }
   }
-  if (warp == 1) tmem_alloc<1>(smem_u32(tmem_slot), kTmemCols);
+  if (warp == 1) tmem_alloc<CG>(smem_u32(tmem_slot), kTmemCols);
   tc_fence_before();
   __syncthreads();
   tc_fence_after();
@@ -309,7 +342,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       // -------------------------------------------------------- producer
       bool ok = true;
       for (; p_u < u_end; ++p_u) {
-        if (!wait_bar(empty_bar(p_stage), p_phase ^ 1, abort_flag, p.timeout_ns, p.status, kRoleProducer)) {
+        if (!wait_bar<kPair>(empty_bar(p_stage), p_phase ^ 1, abort_flag, p.timeout_ns, p.status, kRoleProducer)) {
           ok = false;
           break;
         }
@@ -322,10 +355,10 @@ __global__ void __launch_bounds__(kThreads, 1)
       if (!ok) settle(2000000);
     }
   } else if (warp == 1) {
-    if (lane == 0) {
+    if (lane == 0 && leader) {
       // -------------------------------------------------------- MMA
-      const uint32_t idesc = KIND == kKindF16 ? instr_desc_bf16_f32(BM, (uint32_t)p.np)
-                                              : instr_desc_f32acc(BM, (uint32_t)p.np, p.b_fmt, p.a_fmt);
+      const uint32_t idesc = KIND == kKindF16 ? instr_desc_bf16_f32(BM * CG, (uint32_t)p.np)
+                                              : instr_desc_f32acc(BM * CG, (uint32_t)p.np, p.b_fmt, p.a_fmt);
       bool ok = true;
       int stage = 0, acc = 0;
       uint32_t phase = 0, acc_phase = 0;
@@ -333,11 +366,11 @@ __global__ void __launch_bounds__(kThreads, 1)
       while (u < u_end && ok) {
         const long long n = u / KB;
         const long long seg_end = min(u_end, (n + 1) * KB);
-        if (!wait_bar(acce_bar(acc), acc_phase ^ 1, abort_flag, p.timeout_ns, p.status, kRoleMma)) break;
+        if (!wait_bar<kPair>(acce_bar(acc), acc_phase ^ 1, abort_flag, p.timeout_ns, p.status, kRoleMma)) break;
         tc_fence_after();
         const uint32_t d_tmem = tmem_base + (uint32_t)(acc * kAccCols);
         for (long long v = u; v < seg_end; ++v) {
-          if (!wait_bar(full_bar(stage), phase, abort_flag, p.timeout_ns, p.status, kRoleMma)) {
+          if (!wait_bar<kPair>(full_bar(stage), phase, abort_flag, p.timeout_ns, p.status, kRoleMma)) {
             ok = false;
             break;
           }
@@ -347,24 +380,27 @@ __global__ void __launch_bounds__(kThreads, 1)
             const uint64_t b0 = smem_desc_sw128(sA + stage * a_stage + j * a_bytes);
 #pragma unroll
             for (int k = 0; k < kMmaPerStage; ++k)
-              mma_issue<1, KIND>(d_tmem, a0 + 2 * k, b0 + 2 * k, idesc, (v != u || j != 0 || k != 0) ? 1u : 0u);
+              mma_issue<CG, KIND>(d_tmem, a0 + 2 * k, b0 + 2 * k, idesc, (v != u || j != 0 || k != 0) ? 1u : 0u);
           }
-          mma_commit(empty_bar(stage));
+          if constexpr (kPair) mma_commit_pair(empty_bar(stage), 0x3);
+          else mma_commit(empty_bar(stage));
           if (++stage == S) {
             stage = 0;
             phase ^= 1;
           }
         }
         if (!ok) break;
-        mma_commit(accf_bar(acc));
+        if constexpr (kPair) mma_commit_pair(accf_bar(acc), 0x3);
+        else mma_commit(accf_bar(acc));
         if (++acc == kAccs) {
           acc = 0;
           acc_phase ^= 1;
         }
         u = seg_end;
       }
-      mma_commit(drain_bar);
-      wait_bar(drain_bar, 0, nullptr, p.timeout_ns, p.status, kRoleMma);
+      if constexpr (kPair) mma_commit_pair(drain_bar, 0x1);
+      else mma_commit(drain_bar);
+      wait_bar<kPair>(drain_bar, 0, nullptr, p.timeout_ns, p.status, kRoleMma);
     }
   } else {
     // ---------------------------------------------------------- epilogue
@@ -393,11 +429,11 @@ __global__ void __launch_bounds__(kThreads, 1)
       const bool early = !whole && p.np <= 32 && tile_parts(p, n) == 2 && c == tile_part_cta(p, n, 0);
       float pre[32];
       if (early) {
-        int* arrivals = p.counters + n * 4 + q;
+        int* arrivals = p.counters + (n * CG + rank) * 4 + q;
         if (!wait_parts(arrivals, 1, abort_flag, p.timeout_ns, p.status)) break;
         const long long cc = tile_part_cta(p, n, 1);
         const int sl = (n == cta_begin(p, cc) / KB) ? 0 : 1;
-        const float4* part = reinterpret_cast<const float4*>(partial_ptr<BM>(p, cc, sl, n_local));
+        const float4* part = reinterpret_cast<const float4*>(partial_ptr<BM>(p, cc * CG + rank, sl, n_local));
 #pragma unroll
         for (int v = 0; v < 8; ++v) {
           float4 x = make_float4(0.0f, 0.0f, 0.0f, 0.0f);
@@ -408,7 +444,7 @@ __global__ void __launch_bounds__(kThreads, 1)
           pre[4 * v + 3] = x.w;
         }
       }
-      if (!wait_bar(accf_bar(acc), acc_phase, abort_flag, p.timeout_ns, p.status, kRoleEpilogue)) break;
+      if (!wait_bar<kPair>(accf_bar(acc), acc_phase, abort_flag, p.timeout_ns, p.status, kRoleEpilogue)) break;
       tc_fence_after();
       float vals[64];
 #pragma unroll
@@ -426,13 +462,16 @@ __global__ void __launch_bounds__(kThreads, 1)
       }
       tc_fence_before();
       __syncwarp();
-      if (lane == 0) mbar_arrive(acce_bar(acc));
+      if (lane == 0) {
+        if constexpr (kPair) mbar_arrive_cluster(mapa_shared(acce_bar(acc), 0));
+        else mbar_arrive(acce_bar(acc));
+      }
       if (++acc == kNumAcc) {
         acc = 0;
         acc_phase ^= 1;
       }
 
-      const int ng = (int)(n * BM) + n_local;
+      const int ng = (int)(n * BM * CG) + (int)rank * BM + n_local;
       bool finish = whole;
       if (early) {
         // parts in k order, as below: (0 + part 0) + part 1
@@ -446,12 +485,12 @@ __global__ void __launch_bounds__(kThreads, 1)
         // finishes the tile; the others publish a partial and go on.
         const long long c_first = tile_part_cta(p, n, 0);
         const int nseg = tile_parts(p, n);
-        int* arrivals = p.counters + n * 4 + q;
+        int* arrivals = p.counters + (n * CG + rank) * 4 + q;
         if (c != c_first) {
           // Partial laid out so each thread writes 16-byte vectors.  The warp
           // barrier orders every lane's partial before lane 0's release.
           const int slot = (n == first_tile) ? 0 : 1;
-          float4* mine = reinterpret_cast<float4*>(partial_ptr<BM>(p, c, slot, n_local));
+          float4* mine = reinterpret_cast<float4*>(partial_ptr<BM>(p, cta_self, slot, n_local));
 #pragma unroll
           for (int g4 = 0; g4 < 16; ++g4)
             if (row_lane && g4 * 4 < p.np)
@@ -482,7 +521,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                 const long long cc = j0 + b < nseg ? tile_part_cta(p, n, j0 + b) : -1;
                 if (row_lane && cc >= 0 && cc != c) {
                   const int sl = (n == cta_begin(p, cc) / KB) ? 0 : 1;
-                  const float4* part = reinterpret_cast<const float4*>(partial_ptr<BM>(p, cc, sl, n_local) + g16 * 16);
+                  const float4* part = reinterpret_cast<const float4*>(partial_ptr<BM>(p, cc * CG + rank, sl, n_local) + g16 * 16);
 #pragma unroll
                   for (int v = 0; v < 4; ++v) buf[b][v] = __ldcg(part + v);
                 }
@@ -554,13 +593,13 @@ __global__ void __launch_bounds__(kThreads, 1)
         const long long n = u / KB;
         const long long seg_end = min(u_end, (n + 1) * KB);
         const bool whole = (u == n * KB) && (seg_end == (n + 1) * KB);
-        if (!wait_bar(accf_bar(acc), acc_phase, abort_flag, p.timeout_ns, p.status, kRoleEpilogue)) break;
+        if (!wait_bar<kPair>(accf_bar(acc), acc_phase, abort_flag, p.timeout_ns, p.status, kRoleEpilogue)) break;
         tc_fence_after();
         const uint32_t tcol = tmem_base + ((uint32_t)(q * 32) << 16) + (uint32_t)(acc * kAccCols);
-        const int ng = (int)(n * BM) + n_local;
+        const int ng = (int)(n * BM * CG) + (int)rank * BM + n_local;
         const long long c_first = whole ? c : tile_part_cta(p, n, 0);
         const int nseg = whole ? 1 : tile_parts(p, n);
-        int* arrivals = p.counters + n * 4 + q;
+        int* arrivals = p.counters + (n * CG + rank) * 4 + q;
         const bool publish = !whole && c != c_first;
         const int slot = (n == first_tile) ? 0 : 1;
         int ok = 1;
@@ -578,7 +617,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             for (int t = 0; t < 16; ++t) v[t] = __uint_as_float(r[t]);
             if (publish) {
               if (row_lane) {
-                float4* mine = reinterpret_cast<float4*>(partial_ptr<BM>(p, c, slot, n_local) + g * 16);
+                float4* mine = reinterpret_cast<float4*>(partial_ptr<BM>(p, cta_self, slot, n_local) + g * 16);
 #pragma unroll
                 for (int v4 = 0; v4 < 4; ++v4)
                   mine[v4] = make_float4(v[4 * v4], v[4 * v4 + 1], v[4 * v4 + 2], v[4 * v4 + 3]);
@@ -594,7 +633,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                 if (!row_lane) continue;
                 const long long cc = tile_part_cta(p, n, j);
                 const int sl = (n == cta_begin(p, cc) / KB) ? 0 : 1;
-                const float4* part = reinterpret_cast<const float4*>(partial_ptr<BM>(p, cc, sl, n_local) + g * 16);
+                const float4* part = reinterpret_cast<const float4*>(partial_ptr<BM>(p, cc * CG + rank, sl, n_local) + g * 16);
 #pragma unroll
                 for (int v4 = 0; v4 < 4; ++v4) {
                   const float4 x = __ldcg(part + v4);
@@ -638,7 +677,10 @@ __global__ void __launch_bounds__(kThreads, 1)
         // the accumulator is read: hand it back to the MMA warp
         tc_fence_before();
         __syncwarp();
-        if (lane == 0) mbar_arrive(acce_bar(acc));
+        if (lane == 0) {
+        if constexpr (kPair) mbar_arrive_cluster(mapa_shared(acce_bar(acc), 0));
+        else mbar_arrive(acce_bar(acc));
+      }
         if (++acc == kAccs) {
           acc = 0;
           acc_phase ^= 1;
@@ -651,9 +693,10 @@ __global__ void __launch_bounds__(kThreads, 1)
   }
 
   __syncthreads();
+  if constexpr (kPair) cluster_sync();  // every MMA of the pair is done with both CTAs' TMEM and shared memory
   if (warp == 1) {
     tc_fence_after();
-    tmem_dealloc<1>(tmem_base, kTmemCols);
+    tmem_dealloc<CG>(tmem_base, kTmemCols);
   }
 }
 
@@ -787,14 +830,18 @@ cudaError_t launch_skinny(const CUtensorMap& tmA, const CUtensorMap& tmB, Skinny
     for (int np = 16; np <= 256; np += 16)
       for (int bm = 64; bm <= 128; bm += 64)
         for (int kg = 1; kg <= 4; kg *= 2) worst = smem_for(np, bm, kg) > worst ? smem_for(np, bm, kg) : worst;
-    const void* kernels[8] = {(const void*)gemm_tn_skinny_kernel<kKindF16, 128, false>,
-                              (const void*)gemm_tn_skinny_kernel<kKindF16, 64, false>,
-                              (const void*)gemm_tn_skinny_kernel<kKindF8F6F4, 128, false>,
-                              (const void*)gemm_tn_skinny_kernel<kKindF8F6F4, 64, false>,
-                              (const void*)gemm_tn_skinny_kernel<kKindF16, 128, true>,
-                              (const void*)gemm_tn_skinny_kernel<kKindF16, 64, true>,
-                              (const void*)gemm_tn_skinny_kernel<kKindF8F6F4, 128, true>,
-                              (const void*)gemm_tn_skinny_kernel<kKindF8F6F4, 64, true>};
+    const void* kernels[12] = {(const void*)gemm_tn_skinny_kernel<kKindF16, 128, false, 1>,
+                               (const void*)gemm_tn_skinny_kernel<kKindF16, 64, false, 1>,
+                               (const void*)gemm_tn_skinny_kernel<kKindF8F6F4, 128, false, 1>,
+                               (const void*)gemm_tn_skinny_kernel<kKindF8F6F4, 64, false, 1>,
+                               (const void*)gemm_tn_skinny_kernel<kKindF16, 128, true, 1>,
+                               (const void*)gemm_tn_skinny_kernel<kKindF16, 64, true, 1>,
+                               (const void*)gemm_tn_skinny_kernel<kKindF8F6F4, 128, true, 1>,
+                               (const void*)gemm_tn_skinny_kernel<kKindF8F6F4, 64, true, 1>,
+                               (const void*)gemm_tn_skinny_kernel<kKindF16, 128, false, 2>,
+                               (const void*)gemm_tn_skinny_kernel<kKindF8F6F4, 128, false, 2>,
+                               (const void*)gemm_tn_skinny_kernel<kKindF16, 128, true, 2>,
+                               (const void*)gemm_tn_skinny_kernel<kKindF8F6F4, 128, true, 2>};
     for (const void* k : kernels) {
       e = cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, worst);
       if (e != cudaSuccess) return e;
@@ -802,40 +849,56 @@ cudaError_t launch_skinny(const CUtensorMap& tmA, const CUtensorMap& tmB, Skinny
     configured[dev] = true;
   }
   if ((p.bm != 64 && p.bm != 128) || p.np < 16 || p.np > 256 || p.np % 16) return cudaErrorInvalidValue;
-  if ((p.kg != 1 && p.kg != 2 && p.kg != 4) || stages_for(p.np, p.bm, p.kg) < 2) return cudaErrorInvalidValue;
-  p.stages = stages_for(p.np, p.bm, p.kg);
-  const int smem = smem_for(p.np, p.bm, p.kg);
+  if ((p.cg != 1 && p.cg != 2) || (p.cg == 2 && p.bm != 128)) return cudaErrorInvalidValue;
+  const int npc = p.np / p.cg;  // token rows held by each CTA
+  if ((p.kg != 1 && p.kg != 2 && p.kg != 4) || stages_for(npc, p.bm, p.kg) < 2) return cudaErrorInvalidValue;
+  p.stages = stages_for(npc, p.bm, p.kg);
+  const int smem = smem_for(npc, p.bm, p.kg);
   if (info) {
     info->path = 3;
-    info->grid = p.grid;
-    info->cluster = 1;
+    info->grid = p.grid * p.cg;
+    info->cluster = p.cg;
     info->block = kThreads;
-    info->tile_m = p.bm;
+    info->tile_m = p.bm * p.cg;
     info->tile_n = p.np;
     info->stages = p.stages;
     info->k_parts = p.split;
     info->smem_bytes = smem;
-    info->kernel = p.kind == kKindF8F6F4 ? (p.np > 64 ? "gemm_tn_skinny_kernel<fp8 in,wide>" : "gemm_tn_skinny_kernel<fp8 in>")
-                                         : (p.np > 64 ? "gemm_tn_skinny_kernel<wide>" : "gemm_tn_skinny_kernel");
+    static const char* names[2][2][2] = {
+        {{"gemm_tn_skinny_kernel", "gemm_tn_skinny_kernel<wide>"},
+         {"gemm_tn_skinny_kernel<fp8 in>", "gemm_tn_skinny_kernel<fp8 in,wide>"}},
+        {{"gemm_tn_skinny_kernel<pair>", "gemm_tn_skinny_kernel<pair,wide>"},
+         {"gemm_tn_skinny_kernel<pair,fp8 in>", "gemm_tn_skinny_kernel<pair,fp8 in,wide>"}}};
+    info->kernel = names[p.cg - 1][p.kind == kKindF8F6F4][p.np > 64];
   }
   cudaLaunchConfig_t cfg = {};
-  cudaLaunchAttribute attr[1];
-  cfg.gridDim = dim3(p.grid, 1, 1);
+  cudaLaunchAttribute attr[2];
+  cfg.gridDim = dim3(p.grid * p.cg, 1, 1);  // p.grid counts unit-range owners: CTAs, or pairs
   cfg.blockDim = dim3(kThreads, 1, 1);
   cfg.dynamicSmemBytes = smem;
   cfg.stream = stream;
+  int na = 0;
   if (pdl) {
-    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
-    attr[0].val.programmaticStreamSerializationAllowed = 1;
-    cfg.attrs = attr;
-    cfg.numAttrs = 1;
+    attr[na].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[na].val.programmaticStreamSerializationAllowed = 1;
+    ++na;
   }
+  if (p.cg == 2) {
+    attr[na].id = cudaLaunchAttributeClusterDimension;
+    attr[na].val.clusterDim.x = 2;
+    attr[na].val.clusterDim.y = 1;
+    attr[na].val.clusterDim.z = 1;
+    ++na;
+  }
+  cfg.attrs = attr;
+  cfg.numAttrs = na;
   const bool wide = p.np > 64;
-#define GTN_SKINNY(KV, BMV) \
-  (wide ? cudaLaunchKernelEx(&cfg, gemm_tn_skinny_kernel<KV, BMV, true>, tmA, tmB, p) \
-        : cudaLaunchKernelEx(&cfg, gemm_tn_skinny_kernel<KV, BMV, false>, tmA, tmB, p))
-  if (p.kind == kKindF8F6F4) return p.bm == 64 ? GTN_SKINNY(kKindF8F6F4, 64) : GTN_SKINNY(kKindF8F6F4, 128);
-  return p.bm == 64 ? GTN_SKINNY(kKindF16, 64) : GTN_SKINNY(kKindF16, 128);
+#define GTN_SKINNY(KV, BMV, CGV) \
+  (wide ? cudaLaunchKernelEx(&cfg, gemm_tn_skinny_kernel<KV, BMV, true, CGV>, tmA, tmB, p) \
+        : cudaLaunchKernelEx(&cfg, gemm_tn_skinny_kernel<KV, BMV, false, CGV>, tmA, tmB, p))
+  if (p.cg == 2) return p.kind == kKindF8F6F4 ? GTN_SKINNY(kKindF8F6F4, 128, 2) : GTN_SKINNY(kKindF16, 128, 2);
+  if (p.kind == kKindF8F6F4) return p.bm == 64 ? GTN_SKINNY(kKindF8F6F4, 64, 1) : GTN_SKINNY(kKindF8F6F4, 128, 1);
+  return p.bm == 64 ? GTN_SKINNY(kKindF16, 64, 1) : GTN_SKINNY(kKindF16, 128, 1);
 #undef GTN_SKINNY
 }
 

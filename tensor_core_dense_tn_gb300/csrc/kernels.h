@@ -107,7 +107,9 @@ struct SkinnyParams {
   const void* C; long long ldc;
   void* D; long long ldd;
   int out_f32;
-  int bm;              // rows of B per tile (MMA M): 128, or 64
+  int bm;              // rows of B per tile (MMA M): 128, or 64; per CTA in the pair form
+  int cg;              // 1, or 2 = pair form: clusters of two CTAs on tiles of 2 * bm rows (MMA M = 256),
+                       //    each CTA holding np / 2 token rows; grid, split and units count pairs
   int kind;            // kKindF16 (bf16 inputs) or kKindF8F6F4 (fp8 inputs)
   int a_fmt, b_fmt;    // fp8 format codes
   Epilogue epi;

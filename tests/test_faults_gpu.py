@@ -43,8 +43,8 @@ def test_dropped_load_times_out_then_recovers(path, scheduler):
     assert np.array_equal(from_dev(dD2, gi.OUT_F32), oracle.exact_f32(ref))
 
 
-@pytest.mark.parametrize("b_static", [0, 1])
-def test_dropped_load_in_two_part_decode_tile(b_static):
+@pytest.mark.parametrize("b_static,pair", [(0, 0), (1, 0), (0, 2), (1, 2)])
+def test_dropped_load_in_two_part_decode_tile(b_static, pair):
     """16 x 8192: CTA 0 finishes tile 0 and takes the other part's partial
     before its own accumulator; its dropped stage must still end in a timeout
     and leave the counters clean for the next call."""
@@ -55,14 +55,14 @@ def test_dropped_load_in_two_part_decode_tile(b_static):
     dA, dB = to_dev_bf16(A), to_dev_bf16(B)
     dD, ldd = empty_out(M, N, gi.OUT_F32)
     rc, st = call(M, N, K, dA, K, dB, K, None, 0, dD, ldd, 1.0, 0.0, gi.OUT_F32, path=3,
-                  timeout_ns=20_000_000, fault=1, b_static=b_static)
+                  timeout_ns=20_000_000, fault=1, b_static=b_static, skinny_pair=pair)
     assert rc == 0
     assert st == g.GEMM_ERR_TIMEOUT, (st, g.last_error())
     s = torch.cuda.current_stream().cuda_stream
     assert g.gemm_get_status(s) == 0
     ref, _ = oracle.gemm_ref(A, B)
     dD2, _ = empty_out(M, N, gi.OUT_F32)
-    rc, st = call(M, N, K, dA, K, dB, K, None, 0, dD2, ldd, 1.0, 0.0, gi.OUT_F32, path=3)
+    rc, st = call(M, N, K, dA, K, dB, K, None, 0, dD2, ldd, 1.0, 0.0, gi.OUT_F32, path=3, skinny_pair=pair)
     assert rc == 0 and st == 0
     assert np.array_equal(from_dev(dD2, gi.OUT_F32), oracle.exact_f32(ref))
 

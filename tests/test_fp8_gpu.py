@@ -211,3 +211,22 @@ def test_fp8_tiled_k_split_exact(path, parts):
     info = g.last_launch_info()
     assert info["path"] == path and info["k_parts"] == parts and "split" in info["kernel"]
     assert np.array_equal(from_dev(dD, gi.OUT_F32), oracle.exact_f32(ref))
+
+
+@pytest.mark.parametrize("M,N,K", [(16, 8192, 2048), (40, 648, 1408), (96, 2048, 1024)])
+@pytest.mark.parametrize("fmt", FMTS)
+def test_fp8_skinny_pair_exact(M, N, K, fmt):
+    """fp8 inputs through the pair form of the streaming kernel."""
+    import torch
+    A = gi.draw_fp8(M, K, gi.Dist("int", -4, 4), 5800 + fmt + M, fmt)
+    B = gi.draw_fp8(N, K, gi.Dist("int", -4, 4), 5810 + fmt + N, fmt)
+    ref, _ = oracle.gemm_ref_fp8(A, B, fmt)
+    dA, dB = to_dev_u8(A), to_dev_u8(B)
+    dD, ldd = empty_out(M, N, gi.OUT_F32)
+    s = torch.cuda.current_stream().cuda_stream
+    cfg = g.GemmConfig(path=3, skinny_pair=2)
+    rc = g.gemm_fp8_tn_ex(M, N, K, dA.data_ptr(), K, dB.data_ptr(), K, fmt, 1.0, 1.0, 0, 0,
+                          dD.data_ptr(), ldd, 1.0, 0.0, gi.OUT_F32, s, cfg)
+    assert rc == 0 and g.gemm_get_status(s) == 0, g.last_error()
+    assert g.last_launch_info()["cluster"] == 2
+    assert np.array_equal(from_dev(dD, gi.OUT_F32), oracle.exact_f32(ref))

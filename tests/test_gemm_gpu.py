@@ -35,7 +35,8 @@ def up8(x):
 
 
 def run_int(M, N, K, path, out_dtype, seed, lda=None, ldb=None, grid=0, skinny_grid=0, alpha=1.0,
-            disable_pdl=0, scheduler=0, skinny_bm=0, skinny_kgroup=0, tiled_k_parts=0, b_static=0):
+            disable_pdl=0, scheduler=0, skinny_bm=0, skinny_kgroup=0, tiled_k_parts=0, b_static=0,
+            skinny_pair=0):
     lda = up8(K) if lda is None else lda
     ldb = up8(K) if ldb is None else ldb
     A = gi.draw_bf16(M, K, gi.Dist("int", -4, 4), seed, ld=lda)
@@ -46,7 +47,7 @@ def run_int(M, N, K, path, out_dtype, seed, lda=None, ldb=None, grid=0, skinny_g
     rc, st = call(M, N, K, dA, lda, dB, ldb, None, 0, dD, ldd, alpha, 0.0, out_dtype, path=path,
                   grid=grid, skinny_grid=skinny_grid, disable_pdl=disable_pdl, scheduler=scheduler,
                   skinny_bm=skinny_bm, skinny_kgroup=skinny_kgroup, tiled_k_parts=tiled_k_parts,
-                  b_static=b_static)
+                  b_static=b_static, skinny_pair=skinny_pair)
     assert rc == 0, g.last_error()
     assert st == 0, g.last_error()
     return from_dev(dD, out_dtype)[:, :N], expect_exact(ref, out_dtype)
@@ -698,3 +699,64 @@ def test_skinny_b_static_exact(M, N, K, skinny_grid, kg):
         got, exp = run_int(M, N, K, PS, gi.OUT_F32, seed=1400 + M + N + K + rep, skinny_grid=skinny_grid,
                            skinny_kgroup=kg, b_static=1)
         assert_same(got, exp)
+
+
+PAIR_SHAPES = [
+    (16, 8192, 1024, 0, 0),     # 32 pair tiles in two parts (equal split)
+    (16, 2048, 4096, 0, 0),     # 8 pair tiles in four parts
+    (1, 300, 70, 0, 0),         # ragged: one token, K below one k-block (2D maps), last tile partial
+    (5, 1000, 4160, 23, 0),     # stream-K ranges over 23 pairs
+    (32, 1000, 640, 0, 2),      # 32 tokens (16 per CTA), 2 k-blocks per box
+    (48, 520, 1408, 7, 1),      # 48 tokens (24 per CTA), one k-block per box, stream-K
+    (64, 4096, 2048, 0, 0),     # 64 tokens (32 per CTA)
+    (80, 1100, 1000, 0, 0),     # wide form: 80 tokens (40 per CTA)
+    (128, 8192, 2048, 0, 0),    # wide form, 64 tokens per CTA
+    (224, 2048, 1024, 11, 0),   # wide form, 112 tokens per CTA, stream-K
+    (256, 600, 512, 0, 0),      # wide form, the largest token count
+]
+
+
+@pytest.mark.parametrize("M,N,K,grid,kg", PAIR_SHAPES)
+@pytest.mark.parametrize("out_dtype", [gi.OUT_F32, gi.OUT_BF16])
+def test_skinny_pair_exact(M, N, K, grid, kg, out_dtype):
+    """The pair form of the streaming kernel (gemm_tn_config.skinny_pair = 2):
+    clusters of two CTAs on 256-row tiles of B, cta_group::2 MMAs, the tokens
+    split between the CTAs; bit-exact on integers, twice in a row."""
+    for rep in range(2):
+        got, exp = run_int(M, N, K, PS, out_dtype, seed=1500 + M + N + K + rep, skinny_grid=grid, skinny_kgroup=kg,
+                           skinny_pair=2)
+        info = g.last_launch_info()
+        assert info["path"] == PS and info["cluster"] == 2 and info["tile_m"] == 256 and "pair" in info["kernel"]
+        assert_same(got, exp)
+
+
+def test_skinny_pair_with_c_and_b_static():
+    """beta * C read in the pair form's epilogue, with the early weight loads."""
+    import torch
+    M, N, K = 24, 3000, 2048
+    A = gi.draw_bf16(M, K, gi.Dist("int", -4, 4), 1601)
+    B = gi.draw_bf16(N, K, gi.Dist("int", -4, 4), 1602)
+    C = gi.draw_f32(M, N, gi.Dist("int", -4, 4), 1603)
+    ref, _ = oracle.gemm_ref(A, B, C, 1.0, 0.5)
+    dA, dB, dC = to_dev_bf16(A), to_dev_bf16(B), to_dev_f32(C)
+    dD, ldd = empty_out(M, N, gi.OUT_F32)
+    s = torch.cuda.current_stream().cuda_stream
+    cfg = g.GemmConfig(path=PS, skinny_pair=2, b_static=1)
+    rc = g.gemm_bf16_tn_ex(M, N, K, dA.data_ptr(), K, dB.data_ptr(), K, dC.data_ptr(), N, dD.data_ptr(), ldd,
+                           1.0, 0.5, gi.OUT_F32, s, cfg)
+    assert rc == 0 and g.gemm_get_status(s) == 0, g.last_error()
+    assert_same(from_dev(dD, gi.OUT_F32), oracle.exact_f32(ref))
+
+
+def test_skinny_pair_decode_normal_within_bound():
+    """The 16 x 8192 x 8192 decode's own operands through the pair form, every output."""
+    w = gi.WORKLOADS[4]
+    A, B, C = gi.operands(w)
+    dA, dB = to_dev_bf16(A), to_dev_bf16(B)
+    dD, ldd = empty_out(w.M, w.N, w.out_dtype)
+    rc, st = call(w.M, w.N, w.K, dA, w.K, dB, w.K, None, 0, dD, ldd, w.alpha, w.beta, w.out_dtype, path=PS,
+                  skinny_pair=2)
+    assert rc == 0 and st == 0, g.last_error()
+    ref, absdot = oracle.gemm_ref(A, B, C, w.alpha, w.beta)
+    ok, worst, where = oracle.check(from_dev(dD, w.out_dtype), ref, absdot, w.out_dtype)
+    assert ok, (worst, where)

@@ -204,3 +204,18 @@ def test_unknown_b_static_rejected(lib, value):
 def test_mma_rate_argument_errors(lib, args, code):
     assert g.gemm_mma_rate(*args, 0) == code
     assert g.last_error() != ""
+
+
+@pytest.mark.parametrize("kw", [dict(skinny_pair=3), dict(skinny_pair=-1)])
+def test_unknown_skinny_pair_rejected(lib, kw):
+    a = (16, 64, 64, 0x1000, 64, 0x2000, 64, 0, 0, 0x3000, 64, 1.0, 0.0, 0, 0)
+    assert g.gemm_bf16_tn_ex(*a, config=g.GemmConfig(**kw)) == g.GEMM_ERR_INVALID_VALUE
+    assert "skinny_pair" in g.last_error()
+
+
+def test_plan_reports_the_pair_form(lib):
+    rc, plan = g.gemm_plan(16, 8192, 8192, 0, 152, g.GemmConfig(path=3, skinny_pair=2))
+    assert rc == 0
+    assert plan["tile_m"] == 256 and plan["skinny_grid"] % 2 == 0
+    rc, _ = g.gemm_plan(16, 8192, 8192, 0, 152, g.GemmConfig(path=3, skinny_pair=2, skinny_bm=64))
+    assert rc == g.GEMM_ERR_INVALID_VALUE
