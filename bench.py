@@ -694,7 +694,7 @@ def run_mma_rate(g, torch, device):
     for fp8, kind in ((0, "bf16"), (1, "e4m3")):
         for cg in (1, 2):
             row = {}
-            for n in (16, 32, 64, 128, 256):
+            for n in (16, 32, 64, 128, 160, 192, 224, 256):
                 for _ in range(2):
                     rc = g.gemm_mma_rate(n, cg, fp8, reps, sms - sms % cg, out.data_ptr(), stream)
                     if rc != 0:
@@ -1002,6 +1002,92 @@ def cpu_baseline(w, A, B, C, dD, out_t, torch, seconds):
 
 
 
+# ----------------------------------------------------------------------------- automatic-path check
+
+
+def run_path_check(args):
+    """The automatic path against every forced choice (1-SM and 2-SM tiles,
+    each with and without the tiled k-split, and the streaming kernel) over a
+    grid of shapes: M 1..512 tokens, N 1024..28672, K 1024..8192, bf16,
+    graph-replayed, B rotated over copies so that large weights stream from
+    HBM.  Prints one JSON line: per shape the automatic choice's time and the
+    fastest forced choice's, and the mean and worst ratio."""
+    import torch
+    import tensor_core_dense_tn_gb300 as g
+    g.load()
+    dev = torch.device("cuda", 0)
+    torch.cuda.set_device(dev)
+    stream = torch.cuda.Stream(dev)
+    sh = stream.cuda_stream
+    opts = [dict(path=0), dict(path=1, tiled_k_parts=1), dict(path=1, tiled_k_parts=2),
+            dict(path=2, tiled_k_parts=1), dict(path=2, tiled_k_parts=2), dict(path=3)]
+    names = ["auto", "1sm", "1sm_split2", "2sm", "2sm_split2", "skinny"]
+
+    def timeit(M, N, K, Bs, A, D, opt):
+        cfg = g.GemmConfig(**opt)
+
+        def step(i):
+            rc = g.gemm_bf16_tn_ex(M, N, K, A.data_ptr(), K, Bs[i % len(Bs)].data_ptr(), K, 0, 0, D.data_ptr(), N,
+                                   1.0, 0.0, gi.OUT_BF16, sh, cfg)
+            if rc != 0:
+                raise ValueError(g.last_error())
+        with torch.cuda.stream(stream):
+            step(0)
+            torch.cuda.synchronize()
+            info = g.last_launch_info()
+            graph = torch.cuda.CUDAGraph()
+            with torch.cuda.graph(graph, stream=stream):
+                for i in range(30):
+                    step(i)
+            graph.replay()
+            torch.cuda.synchronize()
+            t = []
+            for _ in range(3):
+                e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+                e0.record(stream)
+                graph.replay()
+                e1.record(stream)
+                torch.cuda.synchronize()
+                t.append(e0.elapsed_time(e1) / 30 * 1e3)
+        if g.gemm_get_status(sh) != 0:
+            raise RuntimeError(g.last_error())
+        return sorted(t)[1], info
+
+    rows, ratios = [], []
+    Ms = [int(x) for x in args.path_check_m.split(",")]
+    Ns = [int(x) for x in args.path_check_n.split(",")]
+    Ks = [int(x) for x in args.path_check_k.split(",")]
+    for K in Ks:
+        for N in Ns:
+            copies = max(2, min(4, int(600 * 2 ** 20 // (N * K * 2))))
+            Bs = [torch.empty(N, K, device=dev, dtype=torch.bfloat16).normal_(0, 0.01) for _ in range(copies)]
+            for M in Ms:
+                A = torch.empty(M, K, device=dev, dtype=torch.bfloat16).normal_()
+                D = torch.empty(M, N, dtype=torch.bfloat16, device=dev)
+                res = {}
+                for name, opt in zip(names, opts):
+                    try:
+                        us, info = timeit(M, N, K, Bs, A, D, opt)
+                        res[name] = (round(us, 2), info["path"], info["k_parts"])
+                    except ValueError:
+                        pass  # a forced path that cannot run the shape
+                best_name = min((n for n in res if n != "auto"), key=lambda n: res[n][0])
+                ratio = res["auto"][0] / res[best_name][0]
+                ratios.append(ratio)
+                rows.append({"shape": [M, N, K], "auto_us": res["auto"][0],
+                             "auto_path": PATH_NAMES.get(res["auto"][1], res["auto"][1]),
+                             "auto_k_parts": res["auto"][2], "best": best_name, "best_us": res[best_name][0],
+                             "ratio": round(ratio, 4)})
+                log(f"[path-check] {M}x{N}x{K}: auto {res['auto'][0]} us, best {best_name} {res[best_name][0]} us")
+                del A, D
+            del Bs
+            torch.cuda.empty_cache()
+    return {"path_check": {"shapes": len(rows), "mean_ratio": round(statistics.mean(ratios), 4),
+                           "max_ratio": round(max(ratios), 4), "over_1.05": sum(r > 1.05 for r in ratios),
+                           "launch": "CUDA graph of 30 calls, median of 3 replays, B rotated over copies",
+                           "rows": rows}}
+
+
 # ----------------------------------------------------------------------------- reference arm
 
 
@@ -1062,6 +1148,11 @@ def main():
                     help="main step: preferred cluster size of the 2-SM path (gemm_tn_config.cluster_pref)")
     ap.add_argument("--in-dtype", choices=["bf16", "e4m3", "e5m2"], default="bf16",
                     help="input type of the main step (fp8 runs the main step alone)")
+    ap.add_argument("--path-check", action="store_true",
+                    help="time the automatic path against every forced choice over a grid of shapes and exit")
+    ap.add_argument("--path-check-m", default="1,16,32,64,96,128,192,256,512")
+    ap.add_argument("--path-check-n", default="1024,4096,8192,16384,28672")
+    ap.add_argument("--path-check-k", default="1024,2048,4096,8192")
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--no-secondary", action="store_true")
     ap.add_argument("--no-cpu-baseline", action="store_true")
@@ -1069,6 +1160,9 @@ def main():
     ap.add_argument("--reference-seconds", type=float, default=120.0)
     args = ap.parse_args()
     dist = Dist()
+    if args.path_check:
+        print(json.dumps(run_path_check(args)), flush=True)
+        return
     if args.impl == "reference":
         res = run_reference(args, dist)
     else:
