@@ -448,16 +448,21 @@ def run_e2e(args, g, torch, device, w, A, B, out_t, flops, dist):
 
     copies_only(2)
     torch.cuda.synchronize()
-    c0, c1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-    c0.record(s_in)
-    s_out.wait_event(c0)
-    copies_only(n)
-    done = torch.cuda.Event()
-    done.record(s_out)
-    s_in.wait_event(done)
-    c1.record(s_in)
-    torch.cuda.synchronize()
-    copy_ms = dist.max(c0.elapsed_time(c1)) / n
+    # three rounds, the fastest taken: the host link is shared with the
+    # machine's other GPUs, and the bound is what the link allows at best
+    copy_rounds = []
+    for _ in range(3):
+        c0, c1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        c0.record(s_in)
+        s_out.wait_event(c0)
+        copies_only(n)
+        done = torch.cuda.Event()
+        done.record(s_out)
+        s_in.wait_event(done)
+        c1.record(s_in)
+        torch.cuda.synchronize()
+        copy_rounds.append(dist.max(c0.elapsed_time(c1)) / n)
+    copy_ms = min(copy_rounds)
     moved = hA.numel() * 2 + hB.numel() * 2 + hD.numel() * hD.element_size()
     return {"value": round(dist.world * flops / per / 1e12, 2), "unit": "TFLOP/s",
             "h2d_bytes_per_step": hA.numel() * 2 + hB.numel() * 2,
@@ -465,6 +470,7 @@ def run_e2e(args, g, torch, device, w, A, B, out_t, flops, dist):
             "ms_per_step": round(ms / n, 3), "steps": n,
             "rounds_ms_per_step": [round(r / n, 3) for r in rounds],
             "copies_only_ms_per_step": round(copy_ms, 3),
+            "copies_only_rounds_ms_per_step": [round(r, 3) for r in copy_rounds],
             "host_link_gbs": round(moved / (copy_ms / 1e3) / 1e9, 1),
             "of_transfer_bound": round(copy_ms / (ms / n), 4),
             "api": "gemm_bf16_tn_ex (C ABI); pinned host A, B in and D out every step, "
