@@ -1094,6 +1094,55 @@ def run_path_check(args):
                            "rows": rows}}
 
 
+def run_box_rate(args):
+    """gemm_stream_read over four copies of a 128 MiB matrix (8192 rows of
+    16 KiB, as the decode's bf16 weights) on 128 CTAs, for each TMA box shape
+    (rows x k-blocks of 128 bytes): microseconds per 128 MiB and GB/s per SM.
+    The ring holds as many stages of the box as fit 216 KiB (at most 64)."""
+    import torch
+    import tensor_core_dense_tn_gb300 as g
+    g.load()
+    dev = torch.device("cuda", 0)
+    torch.cuda.set_device(dev)
+    stream = torch.cuda.Stream(dev)
+    rows, row_bytes, copies, grid = 8192, 16384, 4, 128
+    bufs = [torch.zeros(rows * row_bytes, dtype=torch.uint8, device=dev) for _ in range(copies)]
+    out = []
+    for box_rows, kgroup in ((32, 1), (64, 1), (128, 1), (64, 2), (128, 2), (128, 4), (256, 1), (64, 4)):
+        def step(i, box_rows=box_rows, kgroup=kgroup):
+            rc = g.gemm_stream_read(bufs[i % copies].data_ptr(), rows, row_bytes, box_rows, kgroup, grid,
+                                    stream.cuda_stream)
+            if rc != 0:
+                raise RuntimeError(g.last_error())
+        with torch.cuda.stream(stream):
+            for i in range(6):
+                step(i)
+            torch.cuda.synchronize()
+            graph = torch.cuda.CUDAGraph()
+            with torch.cuda.graph(graph, stream=stream):
+                for i in range(40):
+                    step(i)
+            graph.replay()
+            t = []
+            for _ in range(3):
+                e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+                e0.record(stream)
+                graph.replay()
+                e1.record(stream)
+                torch.cuda.synchronize()
+                t.append(e0.elapsed_time(e1) * 1e3 / 40)
+        us = statistics.median(t)
+        box = box_rows * 128 * kgroup
+        stages = min(64, 216 * 1024 // box)
+        out.append({"box_rows": box_rows, "k_blocks": kgroup, "box_kib": box // 1024, "stages": stages,
+                    "us": round(us, 2), "gbs": round(rows * row_bytes / us / 1e3, 1),
+                    "gbs_per_sm": round(rows * row_bytes / us / 1e3 / grid, 1)})
+    if g.gemm_get_status(stream.cuda_stream) != 0:
+        raise RuntimeError(g.last_error())
+    return {"box_rate": {"bytes": rows * row_bytes, "copies": copies, "grid": grid,
+                         "launch": "CUDA graph of 40 calls, median of 3 replays", "rows": out}}
+
+
 # ----------------------------------------------------------------------------- reference arm
 
 
@@ -1159,6 +1208,8 @@ def main():
     ap.add_argument("--path-check-m", default="1,16,32,64,96,128,192,256,512")
     ap.add_argument("--path-check-n", default="1024,4096,8192,16384,28672")
     ap.add_argument("--path-check-k", default="1024,2048,4096,8192")
+    ap.add_argument("--box-rate", action="store_true",
+                    help="time gemm_stream_read for each TMA box shape and exit")
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--no-secondary", action="store_true")
     ap.add_argument("--no-cpu-baseline", action="store_true")
@@ -1168,6 +1219,9 @@ def main():
     dist = Dist()
     if args.path_check:
         print(json.dumps(run_path_check(args)), flush=True)
+        return
+    if args.box_rate:
+        print(json.dumps(run_box_rate(args)), flush=True)
         return
     if args.impl == "reference":
         res = run_reference(args, dist)

@@ -364,7 +364,7 @@ int gemm_version(void);
  * rows x row_bytes bytes at src (row-major, rows contiguous, device memory
  * owned by the caller) through TMA boxes of box_rows rows x kgroup
  * consecutive 128-byte chunks, as the skinny kernel loads its B operand,
- * into a shared-memory ring of up to 216 KiB per CTA, and discards them.
+ * into a shared-memory ring of up to 216 KiB (at most 64 boxes) per CTA, and discards them.
  * grid CTAs (0 = one per SM) each stream a contiguous range of boxes, in the
  * skinny kernel's order (k-chunks fastest within a tile of box_rows rows).
  * Nothing is written to global memory.

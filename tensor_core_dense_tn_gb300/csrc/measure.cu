@@ -32,7 +32,7 @@ namespace gtn {
 namespace {
 
 constexpr int kSrRing = 216 * 1024;   // ring bytes per CTA (the skinny kernel's)
-constexpr int kSrMaxStages = 8;
+constexpr int kSrMaxStages = 64;
 
 struct StreamParams {
   long long units;      // tiles * groups
