@@ -631,6 +631,28 @@ def run_fp8(args, g, torch, device, peaks, dist):
                                        "peak_source": "2 x measured burst bf16 (the nominal fp8:bf16 "
                                                       "dense ratio, 4.5:2.25 PFLOP/s)"}})
             entry["config"]["l2"] = "operands 144 MiB + D 448 MiB per step, larger than L2; no flush"
+            # the same up-projection with bias + tanh-GELU fused into its epilogue
+            hb = gi.draw_bf16(w.N, 1, gi.Dist("normal", 1.0), w.seed(gi.TENSOR_C)).reshape(w.N)
+            dbias = dev_bf16(hb, torch, device)
+            dDf = torch.empty_like(dD)
+
+            def fused(_i, w=w, dA=dA, dBs=dBs, sa=sa, sb=sb):
+                rc = g.gemm_fp8_tn_bias_act(w.M, w.N, w.K, dA.data_ptr(), w.K, dBs[0].data_ptr(), w.K, fmt, sa, sb,
+                                            0, 0, dDf.data_ptr(), w.N, 1.0, 0.0, gi.OUT_BF16, dbias.data_ptr(), 0,
+                                            g.ACT_GELU_TANH, s_handle)
+                if rc != 0:
+                    raise RuntimeError(f"fp8 fused gemm failed: {rc} {g.last_error()}")
+            with torch.cuda.stream(stream):
+                for i in range(3):
+                    fused(i)
+            f_ms = dist.max(time_steps(torch, stream, fused, steps))
+            if g.gemm_get_status(s_handle) != 0:
+                raise RuntimeError(g.last_error())
+            entry["bias_gelu"] = {"value": round(dist.world * flops / (f_ms / 1e3 / steps) / 1e12, 2),
+                                  "unit": "TFLOP/s", "ms_per_step": round(f_ms / steps, 5), "steps": steps,
+                                  "op": "D = gelu_tanh(scale_a scale_b A B^T + bias) in the epilogue "
+                                        "(gemm_fp8_tn_bias_act)"}
+            del dDf
         out[name] = entry
         del dA, dBs, dD
     return out

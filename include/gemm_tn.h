@@ -249,6 +249,23 @@ int gemm_fp8_tn(int64_t M, int64_t N, int64_t K,
                 void *D, int64_t ldd,
                 float alpha, float beta, int out_dtype, void *stream);
 
+/* FP8 TN GEMM with the fused epilogue of gemm_bf16_tn_bias_act:
+ *
+ *     D = act(alpha * (scale_a * scale_b) * A * B^T + beta * C + bias[n])
+ *
+ * Operands and scales as gemm_fp8_tn; bias, bias_dtype and activation as
+ * gemm_bf16_tn_bias_act.  The fp8 MLP up-projection with its bias and
+ * activation in one pass (the FP8 variant of the Ampere-to-Hopper page and
+ * the epilogue fusion of the H100 Nsight Compute page, section 7). */
+int gemm_fp8_tn_bias_act(int64_t M, int64_t N, int64_t K,
+                         const void *A, int64_t lda,
+                         const void *B, int64_t ldb,
+                         int fp8_format, float scale_a, float scale_b,
+                         const void *C, int64_t ldc,
+                         void *D, int64_t ldd,
+                         float alpha, float beta, int out_dtype,
+                         const void *bias, int bias_dtype, int activation, void *stream);
+
 /* What a call would run, computed on the host without any device access:
  * for capacity planning, and so that the automatic choices can be tested
  * without a GPU.  The fields describe the path and, for the skinny path, its

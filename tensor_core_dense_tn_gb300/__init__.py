@@ -39,7 +39,7 @@ EXPORTED = ["gemm_bf16_tn", "gemm_bf16_tn_ex", "gemm_get_status", "gemm_get_stat
             "gemm_last_error_string", "gemm_last_launch_info", "gemm_shutdown", "gemm_version",
             "gemm_bf16_tn_skinny_noalloc", "gemm_bf16_tn_bias_act", "gemm_fp8_tn", "gemm_fp8_tn_ex",
             "gemm_bf16_tn_grouped", "gemm_bf16_tn_batched", "gemm_plan", "gemm_stream_read",
-            "gemm_mma_rate"]
+            "gemm_mma_rate", "gemm_fp8_tn_bias_act"]
 
 FP8_E4M3, FP8_E5M2 = 0, 1
 SCHED_DEFAULT, SCHED_STATIC, SCHED_CLC = 0, 1, 2
@@ -109,6 +109,8 @@ def load(path: str = LIB_PATH):
         lib.gemm_fp8_tn.argtypes = [i64, i64, i64, vp, i64, vp, i64, i32, f32, f32, vp, i64, vp, i64,
                                     f32, f32, i32, vp]
         lib.gemm_fp8_tn.restype = i32
+        lib.gemm_fp8_tn_bias_act.argtypes = lib.gemm_fp8_tn.argtypes[:-1] + [vp, i32, i32, vp]
+        lib.gemm_fp8_tn_bias_act.restype = i32
         lib.gemm_fp8_tn_ex.argtypes = lib.gemm_fp8_tn.argtypes + [ctypes.POINTER(GemmConfig)]
         lib.gemm_fp8_tn_ex.restype = i32
         lib.gemm_plan.argtypes = [i64, i64, i64, i32, i32, ctypes.POINTER(GemmConfig), ctypes.POINTER(GemmPlanInfo)]
@@ -202,6 +204,14 @@ def gemm_bf16_tn_bias_act(M, N, K, A, lda, B, ldb, C, ldc, D, ldd, alpha, beta, 
     """Raw C-ABI call: D = act(alpha * A B^T + beta * C + bias)."""
     return load().gemm_bf16_tn_bias_act(M, N, K, A, lda, B, ldb, C or None, ldc, D, ldd, alpha, beta,
                                         out_dtype, bias or None, bias_dtype, activation, stream or None)
+
+
+def gemm_fp8_tn_bias_act(M, N, K, A, lda, B, ldb, fp8_format, scale_a, scale_b, C, ldc, D, ldd, alpha, beta,
+                         out_dtype, bias, bias_dtype, activation, stream) -> int:
+    """Raw C-ABI call: D = act(alpha * scale_a * scale_b * A B^T + beta * C + bias), fp8 A and B."""
+    return load().gemm_fp8_tn_bias_act(M, N, K, A, lda, B, ldb, fp8_format, scale_a, scale_b, C or None, ldc, D,
+                                       ldd, alpha, beta, out_dtype, bias or None, bias_dtype, activation,
+                                       stream or None)
 
 
 def gemm_fp8_tn(M, N, K, A, lda, B, ldb, fp8_format, scale_a, scale_b, C, ldc, D, ldd, alpha, beta,

@@ -774,6 +774,24 @@ int gemm_bf16_tn_bias_act(int64_t M, int64_t N, int64_t K, const void* A, int64_
   return run(M, N, K, A, lda, B, ldb, C, ldc, D, ldd, alpha, beta, out_dtype, stream, nullptr, epi);
 }
 
+int gemm_fp8_tn_bias_act(int64_t M, int64_t N, int64_t K, const void* A, int64_t lda, const void* B, int64_t ldb,
+                         int fp8_format, float scale_a, float scale_b, const void* C, int64_t ldc, void* D,
+                         int64_t ldd, float alpha, float beta, int out_dtype, const void* bias, int bias_dtype,
+                         int activation, void* stream) {
+  using namespace gtn;
+  if (fp8_format != GEMM_FP8_E4M3 && fp8_format != GEMM_FP8_E5M2)
+    return fail(GEMM_ERR_INVALID_VALUE, "fp8_format must be 0 (e4m3) or 1 (e5m2), got %d", fp8_format);
+  if (activation < GEMM_ACT_NONE || activation > GEMM_ACT_SILU)
+    return fail(GEMM_ERR_INVALID_VALUE, "unknown activation %d", activation);
+  if (bias && bias_dtype != GEMM_OUT_BF16 && bias_dtype != GEMM_OUT_F32)
+    return fail(GEMM_ERR_INVALID_VALUE, "bias_dtype must be 0 (bf16) or 1 (fp32), got %d", bias_dtype);
+  if (bias && (reinterpret_cast<uintptr_t>(bias) & (bias_dtype == GEMM_OUT_F32 ? 3u : 1u)))
+    return fail(GEMM_ERR_MISALIGNED, "bias must be aligned to its element size");
+  const Epilogue epi{bias, bias_dtype == GEMM_OUT_F32 ? 1 : 0, activation};
+  return run(M, N, K, A, lda, B, ldb, C, ldc, D, ldd, alpha * scale_a * scale_b, beta, out_dtype, stream, nullptr,
+             epi, kInFp8, fp8_format);
+}
+
 int gemm_fp8_tn_ex(int64_t M, int64_t N, int64_t K, const void* A, int64_t lda, const void* B, int64_t ldb,
                    int fp8_format, float scale_a, float scale_b, const void* C, int64_t ldc, void* D, int64_t ldd,
                    float alpha, float beta, int out_dtype, void* stream, const gemm_tn_config* cfg) {

@@ -34,6 +34,15 @@
 // into TMEM accumulators; warps 2..5 read them back (tcgen05.ld) and finish
 // each segment.  Every wait is bounded as in the tiled kernel
 // (gemm_tiled.cu).
+//
+// Two options change the start and the tile shape.  With p.b_early the
+// caller has promised that nothing still running writes B, and the first
+// ring of B boxes goes out before the dependency wait on the previous
+// kernel.  With CG = 2 (the pair form) a cluster of two CTAs takes a tile of
+// 2 * BM rows of B: each loads its own BM rows and half of the tokens, both
+// CTAs' copies complete on the first CTA's barriers, and that CTA's MMA
+// thread issues cta_group::2 MMAs (M = 2 * BM) whose accumulator rows land
+// in each CTA's own TMEM.
 #include <cuda.h>
 #include <cuda_runtime.h>
 

@@ -230,3 +230,62 @@ def test_fp8_skinny_pair_exact(M, N, K, fmt):
     assert rc == 0 and g.gemm_get_status(s) == 0, g.last_error()
     assert g.last_launch_info()["cluster"] == 2
     assert np.array_equal(from_dev(dD, gi.OUT_F32), oracle.exact_f32(ref))
+
+
+def _run_fused(M, N, K, A, B, fmt, bias, bias_dtype, act, out_dtype, scale_a=1.0, scale_b=1.0):
+    import torch
+    dA, dB = to_dev_u8(A), to_dev_u8(B)
+    dbias = to_dev_bf16(bias) if bias_dtype == 0 else to_dev_f32(bias)
+    dD, ldd = empty_out(M, N, out_dtype)
+    s = torch.cuda.current_stream().cuda_stream
+    rc = g.gemm_fp8_tn_bias_act(M, N, K, dA.data_ptr(), K, dB.data_ptr(), K, fmt, scale_a, scale_b, 0, 0,
+                                dD.data_ptr(), ldd, 1.0, 0.0, out_dtype, dbias.data_ptr(), bias_dtype, act, s)
+    assert rc == 0, g.last_error()
+    assert g.gemm_get_status(s) == 0, g.last_error()
+    return from_dev(dD, out_dtype)
+
+
+@pytest.mark.parametrize("path", list(PATH_M))
+@pytest.mark.parametrize("fmt", FMTS)
+@pytest.mark.parametrize("act", [0, 1])
+def test_fp8_bias_act_integer_exact(path, fmt, act):
+    """gemm_fp8_tn_bias_act: integer codes and bias, no activation or ReLU, bit-exact on every path."""
+    M, N, K = PATH_M[path], shape_n(path, 520), 384
+    A = gi.draw_fp8(M, K, gi.Dist("int", -4, 4), 5900 + fmt, fmt)
+    B = gi.draw_fp8(N, K, gi.Dist("int", -4, 4), 5910 + fmt, fmt)
+    bias = gi.draw_bf16(N, 1, gi.Dist("int", -50, 50), 5920).reshape(N)
+    ref, _ = oracle.gemm_ref_fp8(A, B, fmt)
+    want = oracle.epilogue(ref, bias, act)
+    got = _run_fused(M, N, K, A, B, fmt, bias, 0, act, gi.OUT_F32)
+    check_path(path)
+    assert np.array_equal(got, oracle.exact_f32(want))
+
+
+@pytest.mark.parametrize("path", list(PATH_M))
+def test_fp8_bias_gelu_within_bound(path):
+    """e4m3 with real per-tensor scales, fp32 bias and tanh-GELU: within the
+    oracle's activation bound (the pre-activation bound times the slope plus
+    fp32 evaluation error and one bf16 ulp)."""
+    fmt = gi.FP8_E4M3
+    M, N, K = PATH_M[path], shape_n(path, 776), 1024
+    A = gi.draw_fp8(M, K, gi.Dist("normal", 1.0), 5930, fmt)
+    B = gi.draw_fp8(N, K, gi.Dist("normal", 1.0), 5931, fmt)
+    bias = gi.draw_f32(N, 1, gi.Dist("normal", 1.0), 5932).reshape(N)
+    sa, sb = 1.0, 1.0 / 32.0
+    alpha = float(np.float32(sa) * np.float32(sb))
+    ref, absdot = oracle.gemm_ref_fp8(A, B, fmt, alpha=alpha)
+    z = oracle.epilogue(ref, bias, 0)
+    fz = oracle.epilogue(ref, bias, 3)
+    got = oracle.decode_out(_run_fused(M, N, K, A, B, fmt, bias, 1, 3, gi.OUT_BF16, sa, sb), 0)
+    check_path(path)
+    bnd = oracle.bound_act(z, fz, absdot, 0, 3)
+    assert np.all(np.abs(got - fz) <= bnd), float(np.max(np.abs(got - fz) / bnd))
+
+
+def test_fp8_bias_act_argument_errors():
+    a = (64, 64, 64, 0x1000, 64, 0x2000, 64)
+    tail = (1.0, 1.0, 0, 0, 0x3000, 64, 1.0, 0.0, 0)
+    assert g.gemm_fp8_tn_bias_act(*a, 2, *tail, 0x4000, 0, 1, 0) == g.GEMM_ERR_INVALID_VALUE   # format
+    assert g.gemm_fp8_tn_bias_act(*a, 0, *tail, 0x4000, 0, 7, 0) == g.GEMM_ERR_INVALID_VALUE   # activation
+    assert g.gemm_fp8_tn_bias_act(*a, 0, *tail, 0x4000, 5, 1, 0) == g.GEMM_ERR_INVALID_VALUE   # bias dtype
+    assert g.gemm_fp8_tn_bias_act(*a, 0, *tail, 0x4002, 1, 1, 0) == g.GEMM_ERR_MISALIGNED      # fp32 bias at 2 B

@@ -219,3 +219,11 @@ def test_plan_reports_the_pair_form(lib):
     assert plan["tile_m"] == 256 and plan["skinny_grid"] % 2 == 0
     rc, _ = g.gemm_plan(16, 8192, 8192, 0, 152, g.GemmConfig(path=3, skinny_pair=2, skinny_bm=64))
     assert rc == g.GEMM_ERR_INVALID_VALUE
+
+
+def test_fp8_bias_act_rejects_before_any_device_call(lib):
+    a = (64, 64, 64, 0x1000, 64, 0x2000, 64)
+    tail = (1.0, 1.0, 0, 0, 0x3000, 64, 1.0, 0.0, 0)
+    assert g.gemm_fp8_tn_bias_act(*a, 2, *tail, 0x4000, 0, 1, 0) == g.GEMM_ERR_INVALID_VALUE
+    assert g.gemm_fp8_tn_bias_act(*a, 0, *tail, 0x4000, 0, 9, 0) == g.GEMM_ERR_INVALID_VALUE
+    assert g.gemm_fp8_tn_bias_act(*a, 0, *tail, 0x4002, 1, 1, 0) == g.GEMM_ERR_MISALIGNED
