@@ -665,14 +665,12 @@ __global__ void __launch_bounds__(kThreads, 1)
         if (!SPLIT && (p.epi.bias || p.epi.act)) {
           // bias is per column: lane l fetches column col0 + l, every lane
           // then takes the 32 values by shuffle
-          float bl = 0.0f;
-          if (p.epi.bias && col0 + lane < p.N) bl = load_bias(p.epi, col0 + lane);
+          if (p.epi.bias) {
+            const float bl = col0 + lane < p.N ? load_bias(p.epi, col0 + lane) : 0.0f;
 #pragma unroll
-          for (int j = 0; j < 32; ++j) {
-            float x = v[j];
-            if (p.epi.bias) x += __shfl_sync(0xffffffffu, bl, j);
-            v[j] = activate(x, p.epi.act);
+            for (int j = 0; j < 32; ++j) v[j] += __shfl_sync(0xffffffffu, bl, j);
           }
+          activate_chunk(v, p.epi.act);
         }
         if constexpr (OUT_F32) {
           // 128-byte rows, 128-byte swizzle: 16-byte chunk j sits at j ^ (row % 8)

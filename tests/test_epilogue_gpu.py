@@ -88,6 +88,28 @@ def test_activations_within_bound(path, act, out_dtype):
 
 
 @pytest.mark.parametrize("path", list(PATH_M))
+@pytest.mark.parametrize("act", [3, 4])
+def test_logistic_activations_in_the_tails(path, act):
+    """Pre-activations spread over [-130, 130] by an fp32 bias: the saturated
+    tails of tanh-GELU and SiLU, and below -80 (SiLU) or about -9.7
+    (tanh-GELU), where the kernel caps the exponent of its logistic form."""
+    M, N, K = PATH_M[path], shape_n(path, 520), 128
+    A = gi.draw_bf16(M, K, gi.Dist("normal", 1.0), 4700 + act)
+    B = gi.draw_bf16(N, K, gi.Dist("normal", 1.0 / K), 4710 + act)
+    bias = gi.draw_f32(N, 1, gi.Dist("uniform", -130.0, 130.0), 4720 + act).reshape(N)
+    ref, absdot = oracle.gemm_ref(A, B)
+    z = oracle.epilogue(ref, bias, 0)
+    fz = oracle.epilogue(ref, bias, act)
+    assert np.any(z < -90.0) and np.any(z > 90.0)
+    for out_dtype in (gi.OUT_F32, gi.OUT_BF16):
+        got = oracle.decode_out(_run(M, N, K, A, B, bias, 1, act, out_dtype), out_dtype)
+        check_path(path)
+        bnd = oracle.bound_act(z, fz, absdot, out_dtype, act)
+        err = np.abs(got - fz)
+        assert np.all(err <= bnd), float(np.max(err / bnd))
+
+
+@pytest.mark.parametrize("path", list(PATH_M))
 def test_gelu_with_c_and_fp32_bias(path):
     M, N, K = PATH_M[path], shape_n(path, 264), 320
     A = gi.draw_bf16(M, K, gi.Dist("normal", 1.0), 4400)
