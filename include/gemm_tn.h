@@ -156,6 +156,14 @@ typedef struct gemm_tn_config {
                                CTAs, so that each MMA instruction consumes twice the weight rows and each
                                CTA loads half the token bytes; 1 = one CTA per tile; 0 = library
                                default (one CTA per tile) */
+  int tail_slices;          /* tiled paths, single problem, static scheduler, no k-split: the tiles of
+                               the last, partial round of the persistent grid (all tiles when they
+                               fill less than one round) are each computed as 2 or 4 slices of
+                               128 or 64 columns, one cluster per slice, so that the round uses
+                               more of the GPU; 0 = auto (when the tiles fill less than one
+                               round: the most slices, up to 4, that still fit it), 1 = none,
+                               2 or 4 = that many where the round's tiles times the count fit one
+                               round, at any number of rounds, else none */
 } gemm_tn_config;
 
 /* Tile schedulers of the tiled paths.
@@ -187,6 +195,7 @@ typedef struct gemm_launch_info {
                         stream-K ranges */
   int cluster_pref;  /* preferred cluster size requested for the launch (gemm_tn_config.cluster_pref),
                         0 = none */
+  int tail_slices;   /* tiled paths: slices per tile of the last round (1 = none) */
 } gemm_launch_info;
 
 /* D = alpha * A * B^T + beta * C (see the file comment for every argument).
@@ -281,6 +290,7 @@ typedef struct gemm_plan_info {
   int k_parts;        /* k-parts per tile: tiled split (1 = none; capped at launch to co-resident
                          clusters) or skinny equal split; 0 = skinny stream-K ranges */
   int skinny_skew;    /* skinny, equal split: k-groups moved to the part that finishes each tile */
+  int tail_slices;    /* tiled: slices per tile of the last round (gemm_tn_config.tail_slices; 1 = none) */
 } gemm_plan_info;
 
 /* Plan D = A * B^T for M x N x K on a GPU with num_sms SMs (152 on a

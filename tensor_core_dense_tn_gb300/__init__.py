@@ -59,13 +59,14 @@ class GemmConfig(ctypes.Structure):
                 ("test_fault", ctypes.c_int), ("disable_pdl", ctypes.c_int),
                 ("skinny_skew_kb", ctypes.c_int), ("scheduler", ctypes.c_int), ("skinny_bm", ctypes.c_int),
                 ("skinny_kgroup", ctypes.c_int), ("tiled_k_parts", ctypes.c_int), ("l2_hints", ctypes.c_int),
-                ("cluster_pref", ctypes.c_int), ("b_static", ctypes.c_int), ("skinny_pair", ctypes.c_int)]
+                ("cluster_pref", ctypes.c_int), ("b_static", ctypes.c_int), ("skinny_pair", ctypes.c_int),
+                ("tail_slices", ctypes.c_int)]
 
 
 class GemmPlanInfo(ctypes.Structure):
     _fields_ = [("path", ctypes.c_int), ("tile_m", ctypes.c_int), ("tile_n", ctypes.c_int),
                 ("skinny_kgroup", ctypes.c_int), ("skinny_stages", ctypes.c_int), ("skinny_grid", ctypes.c_int),
-                ("k_parts", ctypes.c_int), ("skinny_skew", ctypes.c_int)]
+                ("k_parts", ctypes.c_int), ("skinny_skew", ctypes.c_int), ("tail_slices", ctypes.c_int)]
 
     def as_dict(self):
         return {f: getattr(self, f) for f, _ in self._fields_}
@@ -82,7 +83,8 @@ class LaunchInfo(ctypes.Structure):
     _fields_ = [("path", ctypes.c_int), ("grid", ctypes.c_int), ("cluster", ctypes.c_int),
                 ("block", ctypes.c_int), ("tile_m", ctypes.c_int), ("tile_n", ctypes.c_int),
                 ("stages", ctypes.c_int), ("smem_bytes", ctypes.c_int), ("kernel", ctypes.c_char_p),
-                ("scheduler", ctypes.c_int), ("k_parts", ctypes.c_int), ("cluster_pref", ctypes.c_int)]
+                ("scheduler", ctypes.c_int), ("k_parts", ctypes.c_int), ("cluster_pref", ctypes.c_int),
+                ("tail_slices", ctypes.c_int)]
 
     def as_dict(self):
         return {f: (getattr(self, f).decode() if f == "kernel" and getattr(self, f) else getattr(self, f))

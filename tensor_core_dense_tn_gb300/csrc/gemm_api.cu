@@ -272,6 +272,36 @@ int tiled_parts(long long tiles, int num_kb, int sms, int cg, const gemm_tn_conf
   return 2;
 }
 
+// Slices of the last round of a static tiled launch over `clusters`
+// clusters: the tiles past the last whole round (all of them when they fill
+// less than one round) are cut into 2^shift slices each, the most (up to 4,
+// or the count cfg asks for) that still fit one round.  begin = first tile
+// cut; shift = 0 when none is.  Automatic only when the tiles fill less
+// than one round (small GEMMs: 256^3 6.1 -> 3.8 us, 512 x 3072 x 4096
+// 32.1 -> 26.4 us).  Over several rounds the gain was small and the code
+// that slices cost more than it: with slices in the kernel everything else
+// ran 1-4% slower, and the launches with slices now take a kernel of their
+// own.  At 8192 x 28672 x 4096 quarters of the last round's 12 tiles were
+// 0.4-0.8% slower; 4096^3 and 3000 x 5000 x 2000 (3.4 and 3.2 rounds)
+// gained 1.4% and 2.8% against that kernel without slices (interleaved runs).
+void tail_slices_plan(long long tiles, int clusters, const gemm_tn_config* cfg, int* begin, int* shift) {
+  *begin = (int)tiles;
+  *shift = 0;
+  const int req = cfg ? cfg->tail_slices : 0;
+  if (req == 1 || tiles < 1 || clusters < 2) return;
+  if (req == 0 && tiles >= clusters) return;
+  const long long r = tiles % clusters;   // tiles of the last round (all of them if < clusters)
+  if (r == 0) return;
+  for (int sh = 2; sh >= 1; --sh) {
+    if (req != 0 && req != (1 << sh)) continue;
+    if ((r << sh) <= clusters) {
+      *begin = (int)(tiles - r);
+      *shift = sh;
+      return;
+    }
+  }
+}
+
 // Values of a gemm_tn_config that select among fixed choices.
 int check_config(const gemm_tn_config* cfg) {
   if (!cfg) return GEMM_OK;
@@ -291,6 +321,8 @@ int check_config(const gemm_tn_config* cfg) {
     return fail(GEMM_ERR_INVALID_VALUE, "skinny_pair must be 0, 1 or 2, got %d", cfg->skinny_pair);
   if (cfg->cluster_pref != 0 && cfg->cluster_pref != 4 && cfg->cluster_pref != 8)
     return fail(GEMM_ERR_INVALID_VALUE, "cluster_pref must be 0, 4 or 8, got %d", cfg->cluster_pref);
+  if (cfg->tail_slices != 0 && cfg->tail_slices != 1 && cfg->tail_slices != 2 && cfg->tail_slices != 4)
+    return fail(GEMM_ERR_INVALID_VALUE, "tail_slices must be 0, 1, 2 or 4, got %d", cfg->tail_slices);
   if (cfg->l2_hints < -1 || cfg->l2_hints > 7)
     return fail(GEMM_ERR_INVALID_VALUE, "l2_hints must be -1..7, got %d", cfg->l2_hints);
   if (cfg->tiled_k_parts < 0 || cfg->tiled_k_parts > kMaxTiledParts)
@@ -370,6 +402,7 @@ void record_launch(const LaunchInfo& li) {
   t_info.k_parts = li.k_parts;
   t_info.scheduler = li.scheduler;
   t_info.cluster_pref = li.cluster_pref;
+  t_info.tail_slices = li.tail_slices > 0 ? li.tail_slices : 1;
 }
 
 int run(int64_t M, int64_t N, int64_t K, const void* A, int64_t lda, const void* B, int64_t ldb, const void* C,
@@ -484,7 +517,12 @@ int run(int64_t M, int64_t N, int64_t K, const void* A, int64_t lda, const void*
         p.ksplit = 1;
       }
     }
-    CUtensorMap tA, tB, tC, tD;
+    // slices of the last round (static single launches without a split)
+    if (p.ksplit == 1 && !p.clc && !(cfg && cfg->grid > 0) && K > 0)
+      tail_slices_plan(p.num_tiles, st->sms / cg, cfg, &p.sub_begin, &p.sub_shift);
+    else
+      p.sub_begin = p.num_tiles;
+    CUtensorMap tA, tB, tC, tD, tBs;
     memset(&tA, 0, sizeof tA);
     memset(&tB, 0, sizeof tB);
     memset(&tC, 0, sizeof tC);
@@ -496,9 +534,14 @@ int run(int64_t M, int64_t N, int64_t K, const void* A, int64_t lda, const void*
                           "B")))
         return rc;
     }
+    tBs = tB;
+    if (p.sub_shift > 0 && (rc = encode_2d(&tBs, in_dt, in_bytes, B, K, N, ldb, kbe, b_rows >> p.sub_shift,
+                                           CU_TENSOR_MAP_SWIZZLE_128B, "B slices")))
+      return rc;
     if (has_c && (rc = encode_2d(&tC, out_dt, esize, C, N, M, ldc, epi_c, epi_r, out_sw, "C"))) return rc;
     if ((rc = encode_2d(&tD, out_dt, esize, D, N, M, ldd, epi_c, epi_r, out_sw, "D"))) return rc;
-    e = launch_tiled(cg, out_dtype == GEMM_OUT_F32, in_kind, tA, tB, tC, tD, p, cfg ? cfg->grid : 0, pdl, stream, &li);
+    e = launch_tiled(cg, out_dtype == GEMM_OUT_F32, in_kind, tA, tB, tC, tD, tBs, p, cfg ? cfg->grid : 0, pdl, stream,
+                     &li);
   }
   if (e != cudaSuccess) {
     cudaGetLastError();
@@ -844,9 +887,15 @@ int gemm_plan(int64_t M, int64_t N, int64_t K, int fp8_inputs, int num_sms, cons
     out->tile_n = tn;
     const long long tiles = ((M + tm - 1) / tm) * ((N + tn - 1) / tn);
     const bool clc = cfg && cfg->scheduler == GEMM_SCHED_CLC;
+    const int cg = path == GEMM_PATH_2SM ? 2 : 1;
     out->k_parts = clc || (cfg && cfg->grid > 0) || K == 0
-                       ? 1 : tiled_parts(tiles, (int)((K + 128 / in_bytes - 1) / (128 / in_bytes)), num_sms,
-                                         path == GEMM_PATH_2SM ? 2 : 1, cfg);
+                       ? 1 : tiled_parts(tiles, (int)((K + 128 / in_bytes - 1) / (128 / in_bytes)), num_sms, cg, cfg);
+    out->tail_slices = 1;
+    if (out->k_parts == 1 && !clc && !(cfg && cfg->grid > 0) && K > 0) {
+      int begin = 0, shift = 0;
+      tail_slices_plan(tiles, num_sms / cg, cfg, &begin, &shift);
+      out->tail_slices = 1 << shift;
+    }
   }
   return GEMM_OK;
 }

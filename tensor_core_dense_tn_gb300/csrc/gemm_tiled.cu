@@ -185,6 +185,15 @@ __device__ __forceinline__ void tile_coords(int t, int raster_group, int tiles_m
 template <int MODE>
 using GroupArg = typename std::conditional<MODE == kModeList, GroupList, NoGroup>::type;
 
+// B with boxes of a slice's rows, for a launch whose last round is cut into slices.
+struct SliceArg {
+  CUtensorMap b;
+};
+
+// The kernel's last parameter: the problem list, the slice map, or nothing.
+template <int MODE, bool SLICE>
+using KernelArg = typename std::conditional<SLICE, SliceArg, GroupArg<MODE>>::type;
+
 // Everything a role needs to know about tile t: its position, the sizes of
 // its problem and that problem's tensor maps (z = batch index for a strided
 // batch, else 0).
@@ -286,11 +295,16 @@ __device__ __forceinline__ int next_tile(int t, int stride, const TileParams& p,
   return got ? (int)(first_x / CG) : p.num_units;
 }
 
-template <int CG, bool OUT_F32, int KIND, int MODE, bool SPLIT>
+// SLICE: the launch's last round is cut into column slices (single problems,
+// static schedule, no split); a separate instantiation, so that the code of
+// every other launch stays as it is.
+template <int CG, bool OUT_F32, int KIND, int MODE, bool SPLIT, bool SLICE>
 __global__ void __launch_bounds__(kThreads, 1)
     gemm_tn_tiled_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
                          const __grid_constant__ CUtensorMap tmC, const __grid_constant__ CUtensorMap tmD,
-                         const TileParams p, const __grid_constant__ GroupArg<MODE> ga) {
+                         const TileParams p, const __grid_constant__ KernelArg<MODE, SLICE> karg) {
+  static_assert(!SLICE || (MODE == kModeSingle && !SPLIT), "slices: single problems without a split");
+  const GroupArg<MODE>& ga = *reinterpret_cast<const GroupArg<MODE>*>(&karg);
   using C_ = Cfg<CG, OUT_F32>;
   constexpr bool kCluster = (CG == 2);
   constexpr int kBK = stage_k_elems<KIND>();
@@ -331,8 +345,18 @@ __global__ void __launch_bounds__(kThreads, 1)
   // cluster) has more units than tiles; the finishing part 0 takes the
   // highest units, so every part it waits for has a lower cluster id.
   const int ks = SPLIT ? p.ksplit : 1;
-  auto unit_tile = [&](int u) { return SPLIT ? u % p.num_tiles : u; };
+  auto unit_tile = [&](int u) {
+    if (SPLIT) return u % p.num_tiles;
+    if (SLICE && u >= p.sub_begin) return p.sub_begin + ((u - p.sub_begin) >> p.sub_shift);
+    return u;
+  };
   auto unit_part = [&](int u) { return SPLIT ? ks - 1 - u / p.num_tiles : 0; };
+  // Slice of a unit of the last round (-1: the whole tile).  A slice is
+  // BN >> sub_shift columns of its tile, with an MMA of that width.
+  auto unit_slice = [&](int u) {
+    if (!SLICE || u < p.sub_begin) return -1;
+    return (u - p.sub_begin) & ((1 << p.sub_shift) - 1);
+  };
 
   if (threadIdx.x == 0) {
     for (int s = 0; s < C_::STAGES; ++s) {
@@ -363,6 +387,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     if (r0.num_kb > 0) {
       tma_prefetch_desc(r0.a);
       tma_prefetch_desc(r0.b);
+      if constexpr (SLICE) tma_prefetch_desc(&karg.b);
     }
     if (p.has_c) tma_prefetch_desc(r0.c);
     tma_prefetch_desc(r0.d);
@@ -429,27 +454,39 @@ __global__ void __launch_bounds__(kThreads, 1)
           }
         }
         const int a_row = r.tm * C_::TILE_M + (int)rank * 128;
-        const int b_row = r.tn * C_::BN + (int)rank * C_::B_ROWS;
+        const CUtensorMap* bmap = r.b;
+        int b_row = r.tn * C_::BN + (int)rank * C_::B_ROWS;
+        uint32_t stage_tx = C_::STAGE_TX;
+        if constexpr (SLICE) {
+          const int slice = unit_slice(t);
+          if (slice >= 0) {
+            // this CTA's rows of the slice, through the map with slice-high boxes
+            const int cols = C_::BN >> p.sub_shift;
+            bmap = &karg.b;
+            b_row = r.tn * C_::BN + slice * cols + (int)rank * (cols / CG);
+            stage_tx = (uint32_t)((C_::A_BYTES + (C_::B_BYTES >> p.sub_shift)) * CG);
+          }
+        }
         for (int kb = kb0; kb < kb1; ++kb) {
           if (!wait_bar<kCluster>(empty_bar(stage), phase ^ 1, ab)) {
             ok = false;
             break;
           }
           const uint32_t fb = full_bar(stage);
-          if (leader) mbar_arrive_expect_tx(fb, C_::STAGE_TX);
+          if (leader) mbar_arrive_expect_tx(fb, stage_tx);
           if (skip_once) {
             skip_once = false;  // test-only: leave this stage's bytes missing
           } else if constexpr (CG == 1) {
             if (hint_a) tma_load_2d_hint(sA + stage * C_::A_BYTES, r.a, kb * kBK, a_row, fb, pol_a);
             else tload<MODE>(sA + stage * C_::A_BYTES, r.a, kb * kBK, a_row, r.z, fb);
-            if (hint_b) tma_load_2d_hint(sB + stage * C_::B_BYTES, r.b, kb * kBK, b_row, fb, pol_b);
-            else tload<MODE>(sB + stage * C_::B_BYTES, r.b, kb * kBK, b_row, r.z, fb);
+            if (hint_b) tma_load_2d_hint(sB + stage * C_::B_BYTES, bmap, kb * kBK, b_row, fb, pol_b);
+            else tload<MODE>(sB + stage * C_::B_BYTES, bmap, kb * kBK, b_row, r.z, fb);
           } else {
             const uint32_t fb_leader = mapa_shared(fb, pair_base);
             if (hint_a) tma_load_2d_pair_hint(sA + stage * C_::A_BYTES, r.a, kb * kBK, a_row, fb_leader, pol_a);
             else tload_pair<MODE>(sA + stage * C_::A_BYTES, r.a, kb * kBK, a_row, r.z, fb_leader);
-            if (hint_b) tma_load_2d_pair_hint(sB + stage * C_::B_BYTES, r.b, kb * kBK, b_row, fb_leader, pol_b);
-            else tload_pair<MODE>(sB + stage * C_::B_BYTES, r.b, kb * kBK, b_row, r.z, fb_leader);
+            if (hint_b) tma_load_2d_pair_hint(sB + stage * C_::B_BYTES, bmap, kb * kBK, b_row, fb_leader, pol_b);
+            else tload_pair<MODE>(sB + stage * C_::B_BYTES, bmap, kb * kBK, b_row, r.z, fb_leader);
           }
           if (++stage == C_::STAGES) {
             stage = 0;
@@ -468,6 +505,9 @@ __global__ void __launch_bounds__(kThreads, 1)
       Abort ab{abort_flag, p.timeout_ns, p.status, kRoleMma};
       const uint32_t idesc = KIND == kKindF16 ? instr_desc_bf16_f32(C_::TILE_M, C_::BN)
                                               : instr_desc_f32acc(C_::TILE_M, C_::BN, p.a_fmt, p.b_fmt);
+      const uint32_t slice_n = (uint32_t)(C_::BN >> p.sub_shift);
+      const uint32_t idesc_slice = KIND == kKindF16 ? instr_desc_bf16_f32(C_::TILE_M, slice_n)
+                                                    : instr_desc_f32acc(C_::TILE_M, slice_n, p.a_fmt, p.b_fmt);
       bool ok = true;
       int stage = 0;
       uint32_t phase = 0;
@@ -480,6 +520,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         if (!wait_bar<kCluster>(acce_bar(acc), acc_phase ^ 1, ab)) break;
         tc_fence_after();
         const uint32_t d_tmem = tmem_base + (uint32_t)(acc * C_::BN);
+        const uint32_t id = (SLICE && unit_slice(t) >= 0) ? idesc_slice : idesc;
         int kb0, kb1;
         part_range(resolve<MODE>(unit_tile(t), p, ga, &tmA, &tmB, &tmC, &tmD).num_kb, ks, unit_part(t), kb0, kb1);
         for (int kb = kb0; kb < kb1; ++kb) {
@@ -493,7 +534,7 @@ __global__ void __launch_bounds__(kThreads, 1)
 #pragma unroll
           for (int k = 0; k < kMmaPerStage; ++k) {
             // +32 bytes along K inside the swizzle atom = +2 in the encoded address
-            mma_issue<CG, KIND>(d_tmem, a0 + 2 * k, b0 + 2 * k, idesc, (kb != kb0 || k != 0) ? 1u : 0u);
+            mma_issue<CG, KIND>(d_tmem, a0 + 2 * k, b0 + 2 * k, id, (kb != kb0 || k != 0) ? 1u : 0u);
           }
           if constexpr (CG == 1) mma_commit(empty_bar(stage));
           else mma_commit_pair(empty_bar(stage), pair_mask);
@@ -533,6 +574,10 @@ __global__ void __launch_bounds__(kThreads, 1)
       const int tile = unit_tile(t);
       const int part = unit_part(t);
       const TileRef tr = resolve<MODE>(tile, p, ga, &tmA, &tmB, &tmC, &tmD);
+      const int slice = SLICE ? unit_slice(t) : -1;
+      const int cols = slice >= 0 ? (C_::BN >> p.sub_shift) : C_::BN;   // this unit's columns
+      const int col_base = tr.tn * C_::BN + (slice >= 0 ? slice * cols : 0);
+      const int chunks = cols / C_::EPI_COLS;
       const int row0 = tr.tm * C_::TILE_M + (int)rank * 128 + q * 32;
       // Split tile: parts > 0 publish this warp's 32 rows x 256 columns of
       // raw fp32 accumulators and count them; part 0 waits for the count and
@@ -568,8 +613,8 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
       }
 #pragma unroll 1
-      for (int c = 0; c < C_::BN / C_::EPI_COLS; ++c) {
-        const int col0 = tr.tn * C_::BN + c * C_::EPI_COLS;
+      for (int c = 0; c < chunks; ++c) {
+        const int col0 = col_base + c * C_::EPI_COLS;
         uint32_t r[32];
         if (tr.num_kb > 0) {
           tmem_ld_32x32b_x32(tmem_base + ((uint32_t)(q * 32) << 16) + (uint32_t)(acc * C_::BN + c * 32), r);
@@ -578,7 +623,7 @@ __global__ void __launch_bounds__(kThreads, 1)
 #pragma unroll
           for (int j = 0; j < 32; ++j) r[j] = 0;
         }
-        if (c == C_::BN / C_::EPI_COLS - 1) {
+        if (c == chunks - 1) {
           // accumulator fully read: hand it back to the MMA warp
           tc_fence_before();
           __syncwarp();
@@ -724,16 +769,16 @@ __global__ void __launch_bounds__(kThreads, 1)
   if (p.defer_wait) griddep_wait();
 }
 
-template <int CG, bool OUT_F32, int KIND, int MODE, bool SPLIT>
+template <int CG, bool OUT_F32, int KIND, int MODE, bool SPLIT, bool SLICE = false>
 cudaError_t launch_impl(const CUtensorMap& tmA, const CUtensorMap& tmB, const CUtensorMap& tmC,
-                        const CUtensorMap& tmD, const TileParams& p_in, const GroupArg<MODE>& ga, int grid_override,
-                        bool pdl, cudaStream_t stream, LaunchInfo* info) {
+                        const CUtensorMap& tmD, const TileParams& p_in, const KernelArg<MODE, SLICE>& ga,
+                        int grid_override, bool pdl, cudaStream_t stream, LaunchInfo* info) {
   TileParams p = p_in;
   if (!SPLIT || MODE != kModeSingle || p.clc || p.ksplit < 1 || !p.partials || !p.counters) p.ksplit = 1;
   using C_ = Cfg<CG, OUT_F32>;
-  static_assert(sizeof(GroupArg<MODE>) + 4 * sizeof(CUtensorMap) + sizeof(TileParams) < 32000,
+  static_assert(sizeof(KernelArg<MODE, SLICE>) + 4 * sizeof(CUtensorMap) + sizeof(TileParams) < 32000,
                 "kernel parameters must stay within 32 KB");
-  auto kern = gemm_tn_tiled_kernel<CG, OUT_F32, KIND, MODE, SPLIT>;
+  auto kern = gemm_tn_tiled_kernel<CG, OUT_F32, KIND, MODE, SPLIT, SLICE>;
   static bool configured[64] = {};
   int dev = 0;
   cudaError_t e = cudaGetDevice(&dev);
@@ -791,6 +836,14 @@ cudaError_t launch_impl(const CUtensorMap& tmA, const CUtensorMap& tmB, const CU
   // its own co-resident cluster, so the split shrinks to what fits.
   while (p.ksplit > 1 && (long long)p.num_tiles * p.ksplit > max_units) --p.ksplit;
   p.num_units = p.num_tiles * p.ksplit;
+  // slices of the last round: static single-problem launches without a split
+  if (SLICE && p.ksplit == 1 && !p.clc && grid_override <= 0 && p.sub_shift > 0 && p.sub_shift <= 2 &&
+      p.sub_begin >= 0 && p.sub_begin < p.num_tiles) {
+    p.num_units = p.sub_begin + ((p.num_tiles - p.sub_begin) << p.sub_shift);
+  } else {
+    p.sub_begin = p.num_units;
+    p.sub_shift = 0;
+  }
   int units = p.num_units < max_units ? p.num_units : max_units;
   if (grid_override > 0 && p.ksplit == 1) units = grid_override / CG;
   // cluster launch control: one cluster per tile; the ones that find their
@@ -819,6 +872,7 @@ cudaError_t launch_impl(const CUtensorMap& tmA, const CUtensorMap& tmB, const CU
     info->grid = units * CG;
     info->cluster = CG;
     info->cluster_pref = pref;
+    info->tail_slices = 1 << p.sub_shift;
     info->block = kThreads;
     info->tile_m = C_::TILE_M;
     info->tile_n = C_::BN;
@@ -839,8 +893,14 @@ cudaError_t launch_impl(const CUtensorMap& tmA, const CUtensorMap& tmB, const CU
          {"gemm_tn_tiled_kernel<2,bf16,split>", "gemm_tn_tiled_kernel<2,f32,split>"}},
         {{"gemm_tn_tiled_kernel<1,bf16,fp8 in,split>", "gemm_tn_tiled_kernel<1,f32,fp8 in,split>"},
          {"gemm_tn_tiled_kernel<2,bf16,fp8 in,split>", "gemm_tn_tiled_kernel<2,f32,fp8 in,split>"}}};
+    static const char* slice_names[2][2][2] = {
+        {{"gemm_tn_tiled_kernel<1,bf16,slices>", "gemm_tn_tiled_kernel<1,f32,slices>"},
+         {"gemm_tn_tiled_kernel<2,bf16,slices>", "gemm_tn_tiled_kernel<2,f32,slices>"}},
+        {{"gemm_tn_tiled_kernel<1,bf16,fp8 in,slices>", "gemm_tn_tiled_kernel<1,f32,fp8 in,slices>"},
+         {"gemm_tn_tiled_kernel<2,bf16,fp8 in,slices>", "gemm_tn_tiled_kernel<2,f32,fp8 in,slices>"}}};
     info->kernel = MODE != kModeSingle ? group_names[MODE == kModeStrided][CG - 1][OUT_F32 ? 1 : 0]
                    : p.ksplit > 1  ? split_names[KIND][CG - 1][OUT_F32 ? 1 : 0]
+                   : SLICE         ? slice_names[KIND][CG - 1][OUT_F32 ? 1 : 0]
                                    : names[KIND][CG - 1][OUT_F32 ? 1 : 0];
   }
   return cudaLaunchKernelEx(&cfg, kern, tmA, tmB, tmC, tmD, p, ga);
@@ -859,14 +919,19 @@ void tiled_shape(int cta_group, int out_f32, int* tile_m, int* tile_n, int* b_ro
 }
 
 cudaError_t launch_tiled(int cta_group, int out_f32, int kind, const CUtensorMap& tmA, const CUtensorMap& tmB,
-                         const CUtensorMap& tmC, const CUtensorMap& tmD, TileParams p, int grid_override,
-                         bool pdl, cudaStream_t stream, LaunchInfo* info) {
+                         const CUtensorMap& tmC, const CUtensorMap& tmD, const CUtensorMap& tmBs, TileParams p,
+                         int grid_override, bool pdl, cudaStream_t stream, LaunchInfo* info) {
   const NoGroup none{0};
-#define GTN_LAUNCH(CGV, OF, KV) \
-  (p.ksplit > 1 ? launch_impl<CGV, OF, KV, kModeSingle, true>(tmA, tmB, tmC, tmD, p, none, grid_override, pdl, stream, \
-                                                               info) \
-                : launch_impl<CGV, OF, KV, kModeSingle, false>(tmA, tmB, tmC, tmD, p, none, grid_override, pdl, stream, \
-                                                                info))
+  SliceArg sl;
+  sl.b = tmBs;
+  const bool slices = p.ksplit <= 1 && p.sub_shift > 0;
+#define GTN_LAUNCH(CGV, OF, KV)                                                                                    \
+  (p.ksplit > 1 ? launch_impl<CGV, OF, KV, kModeSingle, true>(tmA, tmB, tmC, tmD, p, none, grid_override, pdl,      \
+                                                               stream, info)                                      \
+   : slices     ? launch_impl<CGV, OF, KV, kModeSingle, false, true>(tmA, tmB, tmC, tmD, p, sl, grid_override, pdl, \
+                                                                      stream, info)                               \
+                : launch_impl<CGV, OF, KV, kModeSingle, false>(tmA, tmB, tmC, tmD, p, none, grid_override, pdl,     \
+                                                                stream, info))
   if (kind == kKindF8F6F4) {
     if (cta_group == 2) return out_f32 ? GTN_LAUNCH(2, true, kKindF8F6F4) : GTN_LAUNCH(2, false, kKindF8F6F4);
     return out_f32 ? GTN_LAUNCH(1, true, kKindF8F6F4) : GTN_LAUNCH(1, false, kKindF8F6F4);

@@ -82,7 +82,13 @@ struct TileParams {
   // [part * num_kb / ksplit, (part + 1) * num_kb / ksplit).  Parts > 0 write
   // fp32 partials; part 0 adds them in part order.
   int ksplit;          // parts per tile (1 = no split)
-  int num_units;       // num_tiles * ksplit
+  int num_units;       // num_tiles * ksplit, or with slices sub_begin + (num_tiles - sub_begin) << sub_shift
+  // Slices of the last, partial round (single problems, static schedule, no
+  // k-split): unit u >= sub_begin is slice (u - sub_begin) % 2^sub_shift, of
+  // width 256 >> sub_shift columns, of tile sub_begin + (u - sub_begin) >>
+  // sub_shift, so that the round's r tiles occupy r << sub_shift clusters.
+  int sub_begin;       // first slice unit (num_units when no tile is sliced)
+  int sub_shift;       // log2 of the slices per tile: 0, 1 or 2
   float* partials;     // num_tiles * (ksplit - 1) * cta_group * 128 * 256 floats
   int* counters;       // num_tiles * cta_group * 4, zero between calls
 };
@@ -129,15 +135,19 @@ struct LaunchInfo {
   int scheduler;       // 1 = static persistent, 2 = cluster launch control (tiled paths)
   int k_parts;         // k-parts per tile (tiled split; skinny equal split), 0 = skinny stream-K
   int cluster_pref;    // preferred cluster size requested at launch (0 = none)
+  int tail_slices;     // tiled: slices per tile of the last round (1 = none)
 };
 
 // Tiled persistent kernels (1-SM or 2-SM).  Returns a cudaError_t.  `pdl`
 // launches with programmatic stream serialisation: the kernel's set-up may
 // overlap the previous kernel on the stream; it waits for that kernel's
 // completion (griddepcontrol.wait) before touching global memory.
+// `tmBs` is B with boxes of b_rows_per_cta >> p.sub_shift rows, for the
+// slices of the last round (ignored when p.sub_begin >= p.num_units).
 cudaError_t launch_tiled(int cta_group, int out_f32, int kind, const CUtensorMap& tmA, const CUtensorMap& tmB,
-                         const CUtensorMap& tmC, const CUtensorMap& tmD, TileParams p, int grid_override,
-                         bool pdl, cudaStream_t stream, LaunchInfo* info);
+                         const CUtensorMap& tmC, const CUtensorMap& tmD, const CUtensorMap& tmBs, TileParams p,
+                         int grid_override, bool pdl, cudaStream_t stream, LaunchInfo* info);
+
 
 // The same kernels over a list of problems (bf16 inputs; `list` holds the
 // per-problem tensor maps and sizes, p.num_tiles their total tile count) or

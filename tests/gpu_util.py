@@ -45,14 +45,15 @@ def empty_out(M, N, out_dtype, ld=None, fill_bits=None):
 
 def call(M, N, K, dA, lda, dB, ldb, dC, ldc, dD, ldd, alpha, beta, out_dtype, path=0, grid=0,
          skinny_grid=0, timeout_ns=0, fault=0, stream=None, disable_pdl=0, scheduler=0, skinny_bm=0,
-         skinny_kgroup=0, tiled_k_parts=0, b_static=0, skinny_pair=0):
+         skinny_kgroup=0, tiled_k_parts=0, b_static=0, skinny_pair=0, tail_slices=0):
     """C-ABI call on device tensors; returns (rc, status)."""
     import torch
     import tensor_core_dense_tn_gb300 as g
     cfg = g.GemmConfig(path=path, grid=grid, raster_group=0, skinny_grid=skinny_grid,
                        wait_timeout_ns=timeout_ns, test_fault=fault, disable_pdl=disable_pdl,
                        scheduler=scheduler, skinny_bm=skinny_bm, skinny_kgroup=skinny_kgroup,
-                       tiled_k_parts=tiled_k_parts, b_static=b_static, skinny_pair=skinny_pair)
+                       tiled_k_parts=tiled_k_parts, b_static=b_static, skinny_pair=skinny_pair,
+                       tail_slices=tail_slices)
     s = torch.cuda.current_stream().cuda_stream if stream is None else stream
     rc = g.gemm_bf16_tn_ex(M, N, K, dA.data_ptr() if dA is not None else 0, lda,
                            dB.data_ptr() if dB is not None else 0, ldb,

@@ -663,6 +663,58 @@ def test_preferred_cluster_exact(pref, shape):
         assert_same(from_dev(dD, gi.OUT_F32), oracle.exact_f32(ref))
 
 
+# Shapes whose last round of tiles can be cut into slices: (M, N, K, path,
+# slices with tail_slices = 0, which slices only grids of less than one
+# round).  2-SM: 76 pair slots, 1-SM: 152 CTAs.
+SLICE_SHAPES = [
+    (2300, 2248, 320, P2, 1),    # 81 pair tiles: 76 whole + 5 in the last round, ragged M and N
+    (600, 696, 448, P2, 4),      # 9 pair tiles, less than one round
+    (4096, 4096, 256, P2, 1),    # 256 tiles: 28 in the last round
+    (1000, 5000, 192, P1, 1),    # 160 1-SM tiles: 8 in the last round
+    (130, 296, 72, P1, 4),       # 4 tiles, K not a whole k-block
+]
+
+
+def expected_slices(M, N, path, slices, auto):
+    """Slices a launch takes: the automatic count, or a forced one where the
+    last round's tiles times it still fit one round of clusters."""
+    import torch
+    if slices == 0:
+        return auto
+    clusters = torch.cuda.get_device_properties(0).multi_processor_count // path
+    tiles = -(-M // (128 * path)) * -(-N // 256)
+    r = tiles % clusters
+    return slices if r and r * slices <= clusters else 1
+
+
+@pytest.mark.parametrize("M,N,K,path,auto", SLICE_SHAPES)
+@pytest.mark.parametrize("slices", [0, 2, 4])
+def test_tail_slices_exact(M, N, K, path, auto, slices):
+    """The last round's tiles computed as 2 or 4 column slices, one cluster
+    each (narrower MMAs and B boxes), give the same bits as the oracle, with
+    beta * C through the epilogue, fp32 and bf16 outputs."""
+    import torch
+    A = gi.draw_bf16(M, K, gi.Dist("int", -4, 4), 1300 + M % 97)
+    B = gi.draw_bf16(N, K, gi.Dist("int", -4, 4), 1310 + N % 89)
+    C = gi.draw_f32(M, N, gi.Dist("int", -4, 4), 1320 + K % 83)
+    ref, _ = oracle.gemm_ref(A, B, C, 1.0, 0.5)
+    dA, dB, dC = to_dev_bf16(A), to_dev_bf16(B), to_dev_f32(C)
+    for out_dtype in (gi.OUT_F32, gi.OUT_BF16):
+        dD, ldd = empty_out(M, N, out_dtype)
+        dCo = dC if out_dtype == gi.OUT_F32 else to_dev_bf16(gi.f32_to_bf16_bits(C))
+        rc, st = call(M, N, K, dA, K, dB, K, dCo, N, dD, ldd, 1.0, 0.5, out_dtype, path=path,
+                      tail_slices=slices)
+        assert rc == 0 and st == 0, g.last_error()
+        info = g.last_launch_info()
+        assert info["tail_slices"] == expected_slices(M, N, path, slices, auto), info
+        assert_same(from_dev(dD, out_dtype)[:, :N], expect_exact(ref, out_dtype))
+    # and switched off
+    dD, ldd = empty_out(M, N, gi.OUT_F32)
+    rc, st = call(M, N, K, dA, K, dB, K, dC, N, dD, ldd, 1.0, 0.5, gi.OUT_F32, path=path, tail_slices=1)
+    assert rc == 0 and st == 0 and g.last_launch_info()["tail_slices"] == 1, g.last_error()
+    assert_same(from_dev(dD, gi.OUT_F32), oracle.exact_f32(ref))
+
+
 @pytest.mark.parametrize("hints", [1, 2, 4, 7])
 @pytest.mark.parametrize("path", [P1, P2])
 def test_l2_hints_exact(hints, path):

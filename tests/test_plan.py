@@ -133,6 +133,33 @@ def test_tiled_k_split_choice(M, N, K, path, parts):
     assert plan(M, N, 128, path=path, tiled_k_parts=4)["k_parts"] == 2
 
 
+@pytest.mark.parametrize("M,N,K,path,slices", [
+    (256, 256, 256, P1, 4),        # two 128 x 256 tiles: 6.1 -> 3.8 us
+    (512, 3072, 4096, P1, 2),      # 48 1-SM tiles: 96 halves fit one round (32.1 -> 26.4 us)
+    (600, 696, 448, P1, 4),        # 15 1-SM tiles: 60 quarters
+    (2048, 2048, 2048, P2, 1),     # 64 tiles: less than one round, but 128 halves would not fit it
+    (4096, 4096, 4096, P2, 1),     # 256 tiles: several rounds, no automatic slices
+    (3000, 5000, 2000, P2, 1),
+    (8192, 28672, 4096, P2, 1),
+    (256, 2048, 8192, P2, 1),      # k-split instead
+])
+def test_tail_slices_choice(M, N, K, path, slices):
+    p = plan(M, N, K)
+    assert (p["path"], p["tail_slices"]) == (path, slices)
+    assert p["tail_slices"] == 1 or p["k_parts"] == 1
+    assert plan(M, N, K, tail_slices=1)["tail_slices"] == 1
+    # a forced count applies, at any number of rounds, where the round's tiles
+    # times it still fit one round
+    if path == P2 and p["k_parts"] == 1:
+        r = (((M + 255) // 256) * ((N + 255) // 256)) % 76
+        for want in (2, 4):
+            got = plan(M, N, K, tail_slices=want)["tail_slices"]
+            assert got == (want if r and r * want <= 76 else 1)
+    # with the cluster-launch-control scheduler or a grid override there are none
+    assert plan(M, N, K, scheduler=2)["tail_slices"] == 1
+    assert plan(M, N, K, grid=64)["tail_slices"] == 1
+
+
 @pytest.mark.parametrize("args,cfg,code,text", [
     ((257, 64, 64), dict(path=3), g.GEMM_ERR_NOT_IMPLEMENTED, "skinny"),
     ((16, 64, 0), dict(path=3), g.GEMM_ERR_NOT_IMPLEMENTED, "skinny"),
@@ -140,6 +167,7 @@ def test_tiled_k_split_choice(M, N, K, path, parts):
     ((-1, 64, 64), {}, g.GEMM_ERR_INVALID_VALUE, "negative"),
     ((16, 64, 64), dict(skinny_kgroup=5), g.GEMM_ERR_INVALID_VALUE, "skinny_kgroup"),
     ((16, 64, 64), dict(path=9), g.GEMM_ERR_INVALID_VALUE, "path"),
+    ((512, 512, 64), dict(tail_slices=3), g.GEMM_ERR_INVALID_VALUE, "tail_slices"),
 ])
 def test_plan_errors(args, cfg, code, text):
     rc, _ = g.gemm_plan(*args, 0, 152, g.GemmConfig(**cfg) if cfg else None)
