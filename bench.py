@@ -60,6 +60,9 @@ METRIC = "BF16 GEMM TFLOP/s at 8192×28672×4096 (% of tensor peak); GB/s at M=1
 MAIN = 3       # index of the 8192x28672x4096 workload
 DECODE = 4     # index of the 16x8192x8192 workload
 KERNEL_SOURCES = ("gemm_api.cu", "gemm_tiled.cu", "gemm_skinny.cu", "ptx.cuh", "kernels.h", "epilogue.cuh")
+# the sources each profiled kernel is built from (its traffic stays valid while they are unchanged)
+TILED_SOURCES = ("gemm_api.cu", "gemm_tiled.cu", "ptx.cuh", "kernels.h", "epilogue.cuh")
+SKINNY_SOURCES = ("gemm_api.cu", "gemm_skinny.cu", "ptx.cuh", "kernels.h", "epilogue.cuh")
 PATH_NAMES = {1: "1sm", 2: "2sm", 3: "skinny"}
 
 
@@ -170,23 +173,31 @@ class ClockSampler:
 # ----------------------------------------------------------------------------- helpers
 
 
-def kernel_source_hash() -> str:
+def kernel_source_hash(sources=KERNEL_SOURCES) -> str:
     h = hashlib.sha256()
-    for f in KERNEL_SOURCES:
+    for f in sources:
         with open(os.path.join(ROOT, "tensor_core_dense_tn_gb300", "csrc", f), "rb") as fh:
             h.update(fh.read())
     return h.hexdigest()[:16]
 
 
 def profiled_traffic(workload_name: str):
-    """DRAM bytes per launch from the committed ncu summary, if the kernels are unchanged."""
+    """DRAM bytes per launch from the committed ncu summary, if the sources of
+    the profiled kernel (the entry's `sources`, else all kernel sources) are
+    unchanged since the capture."""
     p = os.path.join(ROOT, "profiles", "ncu_traffic.json")
     try:
         d = json.load(open(p))
     except (OSError, ValueError):
         return None
     e = d.get(workload_name)
-    if not e or e.get("source_hash") != kernel_source_hash():
+    if not e:
+        return None
+    try:
+        h = kernel_source_hash(tuple(e.get("sources") or KERNEL_SOURCES))
+    except OSError:
+        return None
+    if e.get("source_hash") != h:
         return None
     return e.get("dram_bytes_per_launch")
 
@@ -1165,6 +1176,57 @@ def run_box_rate(args):
                          "launch": "CUDA graph of 40 calls, median of 3 replays", "rows": out}}
 
 
+def run_stream_grid(args):
+    """gemm_stream_read over four copies of a 128 MiB matrix with 8 to 152
+    CTAs streaming, for 64 KiB boxes (128 rows x 4 k-blocks, the decode's)
+    and 16 KiB boxes (128 rows x 1 k-block, the tiled kernels' B box):
+    GB/s in all and per streaming SM.  Shows what one SM's TMA stream can
+    take from HBM, which bounds GEMMs whose tiles occupy few SMs."""
+    import torch
+    import tensor_core_dense_tn_gb300 as g
+    g.load()
+    dev = torch.device("cuda", 0)
+    torch.cuda.set_device(dev)
+    stream = torch.cuda.Stream(dev)
+    sms = torch.cuda.get_device_properties(dev).multi_processor_count
+    rows, row_bytes, copies = 8192, 16384, 4
+    bufs = [torch.zeros(rows * row_bytes, dtype=torch.uint8, device=dev) for _ in range(copies)]
+    out = []
+    for box_rows, kgroup in ((128, 4), (128, 1)):
+        for grid in (8, 16, 32, 64, 96, 128, sms):
+            def step(i, box_rows=box_rows, kgroup=kgroup, grid=grid):
+                rc = g.gemm_stream_read(bufs[i % copies].data_ptr(), rows, row_bytes, box_rows, kgroup, grid,
+                                        stream.cuda_stream)
+                if rc != 0:
+                    raise RuntimeError(g.last_error())
+            n = 8 if grid < 32 else 20
+            with torch.cuda.stream(stream):
+                for i in range(4):
+                    step(i)
+                torch.cuda.synchronize()
+                graph = torch.cuda.CUDAGraph()
+                with torch.cuda.graph(graph, stream=stream):
+                    for i in range(n):
+                        step(i)
+                graph.replay()
+                t = []
+                for _ in range(3):
+                    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+                    e0.record(stream)
+                    graph.replay()
+                    e1.record(stream)
+                    torch.cuda.synchronize()
+                    t.append(e0.elapsed_time(e1) * 1e3 / n)
+            us = statistics.median(t)
+            out.append({"box_rows": box_rows, "k_blocks": kgroup, "grid": grid, "us": round(us, 2),
+                        "gbs": round(rows * row_bytes / us / 1e3, 1),
+                        "gbs_per_sm": round(rows * row_bytes / us / 1e3 / grid, 1)})
+    if g.gemm_get_status(stream.cuda_stream) != 0:
+        raise RuntimeError(g.last_error())
+    return {"stream_grid": {"bytes": rows * row_bytes, "copies": copies,
+                            "launch": "CUDA graph of 8-20 calls, median of 3 replays", "rows": out}}
+
+
 # ----------------------------------------------------------------------------- reference arm
 
 
@@ -1230,6 +1292,8 @@ def main():
     ap.add_argument("--path-check-m", default="1,16,32,64,96,128,192,256,512")
     ap.add_argument("--path-check-n", default="1024,4096,8192,16384,28672")
     ap.add_argument("--path-check-k", default="1024,2048,4096,8192")
+    ap.add_argument("--stream-grid", action="store_true",
+                    help="only the HBM stream rate of gemm_stream_read against the number of streaming SMs")
     ap.add_argument("--box-rate", action="store_true",
                     help="time gemm_stream_read for each TMA box shape and exit")
     ap.add_argument("--no-e2e", action="store_true")
@@ -1244,6 +1308,9 @@ def main():
         return
     if args.box_rate:
         print(json.dumps(run_box_rate(args)), flush=True)
+        return
+    if args.stream_grid:
+        print(json.dumps(run_stream_grid(args)), flush=True)
         return
     if args.impl == "reference":
         res = run_reference(args, dist)
