@@ -1227,6 +1227,83 @@ def run_stream_grid(args):
                             "launch": "CUDA graph of 8-20 calls, median of 3 replays", "rows": out}}
 
 
+def run_sustained(args):
+    """The up-projection (bf16, or --in-dtype e4m3) back to back for
+    --sustained seconds: CUDA graphs of 20 calls replayed without a pause,
+    each replay timed with events, the SM clock, power and throttle reasons
+    sampled by nvidia-smi.  Reports the first replay, the settled rate (the
+    median of the last half) and the clocks of each half: the power-capped
+    regime a seconds-long GEMM settles into."""
+    import torch
+    import tensor_core_dense_tn_gb300 as g
+    g.load()
+    dev = torch.device("cuda", 0)
+    torch.cuda.set_device(dev)
+    fp8 = args.in_dtype != "bf16"
+    w = gi.WORKLOADS[MAIN]
+    M, N, K = w.M, w.N, w.K
+    gen = torch.Generator(device=dev)
+    gen.manual_seed(7)
+    if fp8:
+        A = (torch.randn(M, K, device=dev, generator=gen) * 4).to(torch.float8_e4m3fn)
+        B = (torch.randn(N, K, device=dev, generator=gen) * 4).to(torch.float8_e4m3fn)
+    else:
+        A = torch.randn(M, K, device=dev, generator=gen).bfloat16()
+        B = (torch.randn(N, K, device=dev, generator=gen) / 64).bfloat16()
+    D = torch.empty(M, N, dtype=torch.bfloat16, device=dev)
+    stream = torch.cuda.Stream(dev)
+    sh = stream.cuda_stream
+
+    def call():
+        if fp8:
+            rc = g.gemm_fp8_tn(M, N, K, A.data_ptr(), K, B.data_ptr(), K, gi.FP8_E4M3, 0.25, 0.25, 0, 0,
+                               D.data_ptr(), N, 1.0, 0.0, gi.OUT_BF16, sh)
+        else:
+            rc = g.gemm_bf16_tn(M, N, K, A.data_ptr(), K, B.data_ptr(), K, 0, 0, D.data_ptr(), N, 1.0, 0.0,
+                                gi.OUT_BF16, sh)
+        if rc != 0:
+            raise RuntimeError(g.last_error())
+    n = 20
+    with torch.cuda.stream(stream):
+        call()
+        torch.cuda.synchronize()
+        graph = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(graph, stream=stream):
+            for _ in range(n):
+                call()
+        torch.cuda.synchronize()
+        time.sleep(1.0)   # start from idle
+        clocks = ClockSampler(torch.cuda.current_device(), period_ms=50)
+        clocks.start()
+        t_start = time.time()
+        t_end = t_start + args.sustained
+        evs = []
+        while time.time() < t_end:
+            e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            e0.record(stream)
+            graph.replay()
+            e1.record(stream)
+            evs.append((e0, e1))
+            if len(evs) % 4 == 0:
+                evs[-4][1].synchronize()
+        torch.cuda.synchronize()
+        t_stop = time.time()
+        clocks.stop()
+    if g.gemm_get_status(sh) != 0:
+        raise RuntimeError(g.last_error())
+    us = [e0.elapsed_time(e1) / n * 1e3 for e0, e1 in evs]
+    half = len(us) // 2
+    tf = lambda u: 2 * M * N * K / (u * 1e-6) / 1e12
+    mid = t_start + (t_stop - t_start) / 2
+    first, settled = us[0], statistics.median(us[half:])
+    return {"sustained": {
+        "workload": w.name, "dtype": "e4m3" if fp8 else "bf16", "seconds": round(t_stop - t_start, 2),
+        "calls": len(us) * n, "launch": f"CUDA graph of {n} calls, replayed back to back",
+        "first_replay_us_per_call": round(first, 1), "first_replay_tflops": round(tf(first), 1),
+        "settled_us_per_call": round(settled, 1), "settled_tflops": round(tf(settled), 1),
+        "clocks_first_half": clocks.summary(t_start, mid), "clocks_second_half": clocks.summary(mid, t_stop)}}
+
+
 # ----------------------------------------------------------------------------- reference arm
 
 
@@ -1292,6 +1369,8 @@ def main():
     ap.add_argument("--path-check-m", default="1,16,32,64,96,128,192,256,512")
     ap.add_argument("--path-check-n", default="1024,4096,8192,16384,28672")
     ap.add_argument("--path-check-k", default="1024,2048,4096,8192")
+    ap.add_argument("--sustained", type=float, default=0.0,
+                    help="only: the up-projection back to back for this many seconds, with clocks")
     ap.add_argument("--stream-grid", action="store_true",
                     help="only the HBM stream rate of gemm_stream_read against the number of streaming SMs")
     ap.add_argument("--box-rate", action="store_true",
@@ -1311,6 +1390,9 @@ def main():
         return
     if args.stream_grid:
         print(json.dumps(run_stream_grid(args)), flush=True)
+        return
+    if args.sustained > 0:
+        print(json.dumps(run_sustained(args)), flush=True)
         return
     if args.impl == "reference":
         res = run_reference(args, dist)
