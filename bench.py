@@ -1046,7 +1046,7 @@ def cpu_baseline(w, A, B, C, dD, out_t, torch, seconds):
 
 def run_path_check(args):
     """The automatic path against every forced choice (1-SM and 2-SM tiles,
-    each with and without the tiled k-split, and the streaming kernel) over a
+    each unsplit and in 2 and 4 k-parts, and the streaming kernel) over a
     grid of shapes: M 1..512 tokens, N 1024..28672, K 1024..8192, bf16,
     graph-replayed, B rotated over copies so that large weights stream from
     HBM.  Prints one JSON line: per shape the automatic choice's time and the
@@ -1058,9 +1058,9 @@ def run_path_check(args):
     torch.cuda.set_device(dev)
     stream = torch.cuda.Stream(dev)
     sh = stream.cuda_stream
-    opts = [dict(path=0), dict(path=1, tiled_k_parts=1), dict(path=1, tiled_k_parts=2),
-            dict(path=2, tiled_k_parts=1), dict(path=2, tiled_k_parts=2), dict(path=3)]
-    names = ["auto", "1sm", "1sm_split2", "2sm", "2sm_split2", "skinny"]
+    opts = [dict(path=0), dict(path=1, tiled_k_parts=1), dict(path=1, tiled_k_parts=2), dict(path=1, tiled_k_parts=4),
+            dict(path=2, tiled_k_parts=1), dict(path=2, tiled_k_parts=2), dict(path=2, tiled_k_parts=4), dict(path=3)]
+    names = ["auto", "1sm", "1sm_split2", "1sm_split4", "2sm", "2sm_split2", "2sm_split4", "skinny"]
 
     def timeit(M, N, K, Bs, A, D, opt):
         cfg = g.GemmConfig(**opt)

@@ -252,24 +252,31 @@ constexpr int64_t kStreamedBytes = 32ll << 20;
 
 // k-parts per tile for the tiled kernels (single problem, static schedule),
 // one cluster per (tile, part); part 0 adds the other parts' fp32 partials.
-// Measured on GB300 (graph-replayed, bf16), two parts against none: 256 x
-// 2048 x 8192 (8 pair tiles) 37.4 against 40.7 us, 256 x 4096 x 8192 (16)
-// 38.7 against 41.3; about even at 32 pair tiles (224 x 8192 x 8192: 44.6
-// against 44.0); but 192 x 4096 x 4096 29.5 against 23.8, 512 x 4096 x 4096
-// 30.3 against 23.9 and 1024 x 2048 x 2048 24.8 against 14.1, and four parts
-// were never the fastest.  The partial hand-off costs a few microseconds and
-// the operand stream into the SMs is already near its aggregate rate, so
-// only a long k-range on few tiles pays: two parts where the tiles fill at
-// most a quarter of the clusters and K holds at least 128 k-blocks.  Forced
-// values (tiled_k_parts) go up to four.
+// Measured on GB300 (graph-replayed, bf16, B rotated), none / two / four parts:
+//   256 x 2048 x 8192 (8 pair tiles, 128 k-blocks)   40.0 / 31.7 / 24.6 us
+//   256 x 4096 x 8192 (16)                            41.3 / 32.9 / 27.6
+//   192 x 4096 x 4096 (16, 64 k-blocks)               22.7 / 23.2 / 21.2
+//   256 x 4096 x 4096 (16, 64 k-blocks)               22.6 / 23.3 / 21.4
+//   224 x 8192 x 8192 (32, 128 k-blocks)              41.8 / 38.4 / (does not fit)
+//   512 x 4096 x 4096 (32, 64 k-blocks)               23.5 / 23.8 / (does not fit)
+//   300 x 1096 x 4096 (15 1-SM tiles, 64 k-blocks)    24.0 / 23.9 / 19.9
+//   256 x 2048 x 2048 (8, 32 k-blocks)                13.3 / 18.2 / 17.6
+//   1024 x 2048 x 2048 (64 1-SM tiles, 32 k-blocks)   14.4 / 18.5 / (does not fit)
+// So four parts where they fit one round of clusters and K holds at least 64
+// k-blocks, else two where they fit and K holds at least 128, else none.
+// Every unit needs a co-resident cluster (part 0 waits for the others).
+// Forced values (tiled_k_parts) go up to four.
 constexpr int kMaxTiledParts = 4;
-constexpr int kSplitMinKb = 128;
+constexpr int kSplit4MinKb = 64;
+constexpr int kSplit2MinKb = 128;
 int tiled_parts(long long tiles, int num_kb, int sms, int cg, const gemm_tn_config* cfg) {
   const int req = cfg ? cfg->tiled_k_parts : 0;
   if (req > 0) return req < num_kb ? req : (num_kb > 1 ? num_kb : 1);
   const long long clusters = sms / cg;
-  if (tiles < 1 || 4 * tiles > clusters || num_kb < kSplitMinKb) return 1;
-  return 2;
+  if (tiles < 1) return 1;
+  if (4 * tiles <= clusters && num_kb >= kSplit4MinKb) return 4;
+  if (2 * tiles <= clusters && num_kb >= kSplit2MinKb) return 2;
+  return 1;
 }
 
 // Slices of the last round of a static tiled launch over `clusters`

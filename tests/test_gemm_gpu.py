@@ -553,14 +553,14 @@ def test_tiled_k_split_with_c(path, out_dtype):
 
 def test_tiled_k_split_automatic():
     """Few tiles and a long K split automatically (300 x 1100 x 8192: 15 tiles
-    of 128 x 256 on 152 SMs, 128 k-blocks -> 2 parts), deterministically."""
+    of 128 x 256 on 152 SMs, 128 k-blocks -> 4 parts), deterministically."""
     outs = []
     for _ in range(3):
         got, exp = run_int(300, 1100, 8192, 0, gi.OUT_F32, seed=399)
         assert_same(got, exp)
         outs.append(got.view(np.uint32))
         info = g.last_launch_info()
-        assert info["path"] == P1 and info["k_parts"] == 2 and info["grid"] == 30
+        assert info["path"] == P1 and info["k_parts"] == 4 and info["grid"] == 60
     assert np.array_equal(outs[0], outs[1]) and np.array_equal(outs[0], outs[2])
 
 
@@ -572,7 +572,7 @@ def test_tiled_k_split_normal_inputs_within_bound():
     rc, st = call(M, N, K, to_dev_bf16(A), K, to_dev_bf16(B), K, None, 0, dD, ldd, 1.0, 0.0, gi.OUT_BF16)
     assert rc == 0 and st == 0, g.last_error()
     info = g.last_launch_info()
-    assert info["path"] == P2 and info["k_parts"] == 2
+    assert info["path"] == P2 and info["k_parts"] == 4
     ref, absdot = oracle.gemm_ref(A, B)
     ok, worst, where = oracle.check(from_dev(dD, gi.OUT_BF16), ref, absdot, gi.OUT_BF16)
     assert ok, (worst, where)
@@ -617,7 +617,7 @@ def test_tiled_split_first_used_inside_graph_capture():
     # outside capture the same shape splits
     got, exp = run_int(M, N, K, 0, gi.OUT_F32, seed=422)
     assert_same(got, exp)
-    assert g.last_launch_info()["k_parts"] == 2
+    assert g.last_launch_info()["k_parts"] == 4
 
 
 def test_fused_epilogue_is_never_split():

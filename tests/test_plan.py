@@ -119,10 +119,12 @@ def test_tiled_tile_shape():
 
 
 @pytest.mark.parametrize("M,N,K,path,parts", [
-    (256, 2048, 8192, P2, 2),     # 37.4 us against 42.5 unsplit
-    (224, 8192, 8192, P2, 1),     # 32 pair tiles: even (44.6 against 44.0)
-    (300, 1100, 8192, P1, 2),
-    (192, 4096, 4096, P2, 1),     # split 29.2 against 25.1: K too short
+    (256, 2048, 8192, P2, 4),     # 24.6 us; 2 parts 31.7, none 40.0
+    (224, 8192, 8192, P2, 2),     # 32 pair tiles: 38.4 against 41.8 (4 parts would not fit)
+    (300, 1100, 8192, P1, 4),
+    (192, 4096, 4096, P2, 4),     # 64 k-blocks: 21.2 against 22.7
+    (512, 4096, 4096, P2, 1),     # 32 tiles, 64 k-blocks: 2 parts 23.8 against 23.5
+    (256, 2048, 2048, P1, 1),     # 32 k-blocks: 4 parts 17.6 against 13.3
     (1024, 2048, 2048, P1, 1),
     (96, 28672, 8192, P1, 1),     # 112 tiles: more than half of the SMs
 ])
