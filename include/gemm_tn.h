@@ -130,8 +130,9 @@ typedef struct gemm_tn_config {
                                above 1 apply only when K is a whole number of k-blocks (64 bf16 or
                                128 fp8 elements); otherwise the path uses 1 */
   int tiled_k_parts;        /* tiled paths, single problem, static scheduler: k-parts per tile, 0..4;
-                               0 = auto (2 when the tiles fill at most a quarter of the clusters and K
-                               holds at least 128 k-blocks, else 1), 1 = no split.  Capped at launch
+                               0 = auto (4 when the tiles times 4 fit one round of clusters and K holds
+                               at least 64 k-blocks, else 2 when the tiles times 2 fit and K holds at
+                               least 128, else 1), 1 = no split.  Capped at launch
                                so that every part has a co-resident cluster and at K's k-blocks;
                                ignored with CLC, a grid override or a fused epilogue
                                (gemm_bf16_tn_bias_act).  Inside a stream capture that

@@ -232,22 +232,33 @@ constexpr long long kSmallTileCount = 64;
 long long one_sm_tiles(int64_t M, int64_t N) { return ((M + 127) / 128) * ((N + 255) / 256); }
 
 // Automatic path.  The numbers are GB300 measurements (graph-replayed calls,
-// B rotated over copies so that it streams from HBM where it is large).
-// - Up to 32 tokens: the streaming kernel (swap-AB, tokens as MMA N) is the
-//   fastest at every measured shape, 256 <= N <= 57344, 256 <= K <= 8192.
+// B rotated over copies so that it streams from HBM where it is large), from
+// `bench.py --path-check` (180 shapes against every forced choice) after the
+// tiled k-split's partials were interleaved and grids under one round were
+// sliced, which made the tiled kernels faster on few tiles.
+// - Up to 32 tokens: the streaming kernel (swap-AB, tokens as MMA N), except
+//   for short rows of a small B (K <= 1024, 1024 <= N <= 4096), where sliced
+//   1-SM tiles start and finish sooner (32 x 1024 x 1024: 7.4 against 10.9
+//   us; 16 x 4096 x 1024: 7.6 against 8.9).
 // - 33..128 tokens: streaming where B is too large to stay in L2 between
 //   calls (>= 32 MiB) and the streaming kernel splits each tile into at most
 //   two k-parts.  128 x 8192 x 8192: 38.5 us against 43.6 (2-SM) and 56.6
 //   (1-SM).  Where tiles fall to stream-K (64 x 28672 x 4096: 49.9 against
 //   44.5 us) or B is small (64 x 4096 x 1024: 13.1 against 9.3 us), the
 //   tiled kernels win.  Refinements (see auto_path): up to 64 tokens, four
-//   parts with a long K also stream; above 64, only N <= 8192 with long
-//   rows streams.
+//   parts with a long K also stream, but not for N <= 4096, where tiles in
+//   four k-parts are faster (64 x 1024 x 4096: 17.6 against 22.6 us; 64 x
+//   4096 x 8192: 27.1 against 28.9); above 64 tokens, only 4096 < N <= 8192
+//   with K of at least 64 k-blocks (32 up to 96 tokens) streams (128 x 4096
+//   x 8192: pair tiles in four parts 27.5 against 37.5 us; 128 x 8192 x
+//   2048: 1-SM 14.6 against 16.0; 96 x 8192 x 2048: 14.7 either way).
 // - When B streams from HBM and the tiles are few, pair tiles win over 1-SM
 //   tiles even for M <= 128: each SM of a pair loads half of the B tile, and
-//   twice the SMs stream (96 x 16384 x 8192: 53.5 against 61.6 us).  For
-//   129..256 tokens this holds at any tile count (224 x 8192 x 8192: 44.0
-//   against 56.6 us); with B in L2 the 1-SM kernel's lighter launch wins.
+//   twice the SMs stream (96 x 16384 x 8192: 53.5 against 61.6 us), unless K
+//   is short (32 k-blocks or fewer: 128 x 16384 x 1024 on sliced 1-SM tiles
+//   10.8 against 12.4 us).  For 129..256 tokens this holds at any tile count
+//   (224 x 8192 x 8192: 44.0 against 56.6 us); with B in L2 the 1-SM
+//   kernel's lighter launch wins.
 constexpr int64_t kStreamedBytes = 32ll << 20;
 
 // k-parts per tile for the tiled kernels (single problem, static schedule),
@@ -345,18 +356,19 @@ int auto_path(int64_t M, int64_t N, int64_t K, int in_bytes, int sms) {
   const int parts = M <= 256 ? skinny_parts(N, np, skinny_max_grid(np, sms)) : 0;
   const long long tiles = one_sm_tiles(M, N);
   const long long num_kb = (K + 128 / in_bytes - 1) / (128 / in_bytes);
-  if (M <= 32) return GEMM_PATH_SKINNY;
-  // 33..64 tokens: also on a few tiles split four ways once K is long
-  // (64 x 1024 x 8192: 24.1 against 37.8 us on split 1-SM tiles)
-  if (M <= 64 && parts >= 1 && ((streamed && parts <= 2) || num_kb >= 64)) return GEMM_PATH_SKINNY;
-  // 65..128 tokens (wide form): only up to N = 8192 and with long rows of B
-  // (96 x 4096 x 4096: 25.9 against 23.5 us on pair tiles; 128 x 16384 x K:
-  // pair tiles 4-17% faster; 128 x 4096 x 8192 and 128 x 8192 x 4096: the
-  // streaming kernel is the fastest)
-  if (M > 64 && M <= 128 && streamed && parts >= 1 && parts <= 2 && N <= 8192 && (N >= 8192 || num_kb >= 128))
+  if (M <= 32) return (num_kb <= 16 && N >= 1024 && N <= 4096) ? GEMM_PATH_1SM : GEMM_PATH_SKINNY;
+  // 33..64 tokens: also on a few tiles split four ways once K is long, but
+  // not where N <= 4096 (the tiled k-split in four parts is faster there)
+  if (M <= 64 && parts >= 1 && ((streamed && parts <= 2 && !(N <= 4096 && num_kb >= 64)) ||
+                                (num_kb >= 64 && N > 4096)))
+    return GEMM_PATH_SKINNY;
+  // 65..128 tokens (wide form): only for 4096 < N <= 8192 with long rows of B
+  // (K of 64 k-blocks, or 32 up to 96 tokens)
+  if (M > 64 && M <= 128 && streamed && parts >= 1 && parts <= 2 && N > 4096 && N <= 8192 &&
+      (num_kb >= 64 || (M <= 96 && num_kb >= 32)))
     return GEMM_PATH_SKINNY;
   if (M > 128 && (streamed || tiles > kSmallTileCount)) return GEMM_PATH_2SM;
-  if (M <= 128 && streamed && 2 * tiles <= sms) return GEMM_PATH_2SM;
+  if (M <= 128 && streamed && 2 * tiles <= sms && num_kb > 32) return GEMM_PATH_2SM;
   return GEMM_PATH_1SM;
 }
 
@@ -877,6 +889,7 @@ int gemm_plan(int64_t M, int64_t N, int64_t K, int fp8_inputs, int num_sms, cons
   if (path == GEMM_PATH_SKINNY && (M > 256 || K == 0))
     return fail(GEMM_ERR_NOT_IMPLEMENTED, "skinny path needs 1 <= M <= 256 and K > 0");
   out->path = path;
+  out->tail_slices = 1;
   if (path == GEMM_PATH_SKINNY) {
     SkinnyParams p = {};
     if ((rc = skinny_geometry(&p, M, N, K, 128 / in_bytes, num_sms, cfg))) return rc;

@@ -149,10 +149,10 @@ def test_bias_act_argument_errors():
 
 @pytest.mark.parametrize("act", [0, 1, 3])
 def test_wide_streaming_epilogue(act):
-    """96 tokens against a 4096 x 8192 weight (64 MiB): the auto path is the
+    """96 tokens against a 4608 x 8192 weight (72 MiB): the auto path is the
     streaming kernel's wide form (64-row tiles, two k-parts each).  Checked on
     every row at sampled columns, tile edges included."""
-    M, N, K = 96, 4096, 8192
+    M, N, K = 96, 4608, 8192
     A = gi.draw_bf16(M, K, gi.Dist("int", -4, 4), 4600 + act)
     B = gi.draw_bf16(N, K, gi.Dist("int", -4, 4), 4610 + act)
     bias = gi.draw_bf16(N, 1, gi.Dist("int", -50, 50), 4620).reshape(N)

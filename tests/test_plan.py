@@ -27,11 +27,15 @@ def plan(M, N, K, fp8=0, sms=152, **cfg):
     (16, 8192, 8192, 0, S),      # decode: skinny 25.6 us
     (16, 8192, 8192, 1, S),
     (1, 256, 256, 0, S),         # skinny 3.9 us against 5.9 (1-SM)
-    (32, 1024, 1024, 0, S),
+    (32, 1024, 1024, 0, P1),     # short rows, small B: sliced 1-SM 7.4 us; skinny 10.9
+    (16, 4096, 1024, 0, P1),     # 7.6 us; skinny 8.9
+    (16, 8192, 1024, 0, S),
     (64, 8192, 8192, 0, S),      # 64-row whole tiles 31.4 us; 2-SM 43.1
-    (64, 4096, 4096, 0, S),      # 18.8 us; 2-SM 23.4
-    (64, 1024, 4096, 0, S),      # 4 parts: skinny 20.5 us; 1-SM 21.9
-    (64, 1024, 8192, 0, S),      # skinny 24.1 us; split 1-SM 37.8
+    (64, 4096, 4096, 0, P2),     # tiles in 4 k-parts about 21 us; skinny 22.3
+    (64, 1024, 4096, 0, P1),     # 1-SM in 4 k-parts 17.6 us; skinny 22.6
+    (64, 1024, 8192, 0, P1),     # 1-SM in 4 k-parts 22.8 us; skinny 26.3
+    (64, 4096, 8192, 0, P2),     # pair tiles in 4 k-parts 27.1 us; skinny 28.9
+    (64, 16384, 4096, 0, S),     # skinny 27.1 us
     (64, 1024, 2048, 0, P1),     # K short: 1-SM 13.4 us
     (64, 4096, 1024, 0, P1),     # 8 MiB B: 1-SM 9.3 us; skinny 13.1
     (64, 28672, 4096, 0, P1),    # stream-K skinny 49.9 us; 1-SM 44.5
@@ -40,9 +44,11 @@ def plan(M, N, K, fp8=0, sms=152, **cfg):
     (96, 8192, 4096, 1, S),      # fp8, 32 MiB
     (96, 8192, 2048, 1, P1),     # fp8, 16 MiB stays in L2
     (96, 16384, 8192, 0, P2),    # N > 8192: 2-SM 53.0 us, skinny 53.0
-    (128, 16384, 2048, 0, P2),   # 2-SM 18.0 us; skinny 19.9
+    (128, 16384, 2048, 0, P1),   # sliced 1-SM 17.4 us; 2-SM 18.4; skinny 19.9
+    (128, 16384, 4096, 0, P2),   # 2-SM 30.5 us
     (128, 4096, 4096, 0, P2),    # 2-SM 23.7 us; skinny 29.5
-    (128, 4096, 8192, 0, S),     # skinny 37.6 us
+    (128, 4096, 8192, 0, P2),    # pair tiles in 4 k-parts 27.5 us; skinny 37.5
+    (128, 8192, 2048, 0, P1),    # 1-SM 14.6 us; skinny 16.0
     (128, 8192, 8192, 0, S),     # skinny 38.5 us; 2-SM 43.6; 1-SM 56.6
     (96, 28672, 8192, 0, P1),    # 1-SM 83.1 us; skinny 90.6
     (160, 8192, 8192, 0, P2),    # 2-SM 43.8 us; skinny 46.9
