@@ -709,10 +709,10 @@ __global__ void __launch_bounds__(kThreads, 1)
             }
           }
         }
-        // A split launch never has a fused epilogue (the host runs those
-        // unsplit): compiled into the split instantiation, bias alone made it
-        // 25 us slower at 256 x 2048 x 8192 (61.7 against 37.1 us).
-        if (!SPLIT && (p.epi.bias || p.epi.act)) {
+        // bias and activation, on the finisher's sums in a split launch (the
+        // host splits fused calls only into four long parts, where the split
+        // pays for the epilogue sitting after the hand-off)
+        if (p.epi.bias || p.epi.act) {
           // bias is per column: lane l fetches column col0 + l, every lane
           // then takes the 32 values by shuffle
           if (p.epi.bias) {

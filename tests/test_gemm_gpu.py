@@ -620,11 +620,14 @@ def test_tiled_split_first_used_inside_graph_capture():
     assert g.last_launch_info()["k_parts"] == 4
 
 
-def test_fused_epilogue_is_never_split():
-    """A shape the plain GEMM splits (300 x 1104 x 8192) runs unsplit with a
-    fused bias + ReLU, exactly."""
+@pytest.mark.parametrize("M,N,K,parts", [
+    (300, 1104, 8192, 4),   # 15 1-SM tiles, 128 k-blocks: four parts of 32
+    (192, 4096, 4096, 1),   # plain calls split in four here, fused ones (64 k-blocks) do not
+])
+def test_fused_epilogue_split_rule(M, N, K, parts):
+    """Fused bias + ReLU splits only into four parts of at least 32 k-blocks;
+    exact either way (the bias and activation run on the finisher's sums)."""
     import torch
-    M, N, K = 300, 1104, 8192
     A = gi.draw_bf16(M, K, gi.Dist("int", -4, 4), 430)
     B = gi.draw_bf16(N, K, gi.Dist("int", -4, 4), 431)
     bias = gi.draw_bf16(N, 1, gi.Dist("int", -50, 50), 432).reshape(N)
@@ -635,8 +638,35 @@ def test_fused_epilogue_is_never_split():
     rc = g.gemm_bf16_tn_bias_act(M, N, K, dA.data_ptr(), K, dB.data_ptr(), K, 0, 0,
                                  dD.data_ptr(), ldd, 1.0, 0.0, gi.OUT_F32, dbias.data_ptr(), 0, 1, s)
     assert rc == 0 and g.gemm_get_status(s) == 0, g.last_error()
-    assert g.last_launch_info()["k_parts"] == 1
+    assert g.last_launch_info()["k_parts"] == parts
     assert_same(from_dev(dD, gi.OUT_F32), oracle.exact_f32(oracle.epilogue(ref, bias, 1)))
+
+
+def test_fused_gelu_on_split_tiles_within_bound():
+    """bias + tanh-GELU on tiles split in four parts (256 x 1024 x 8192: 1-SM
+    tiles), real inputs, within the oracle's activation bound, bf16 and fp32
+    outputs."""
+    import torch
+    M, N, K = 256, 1024, 8192
+    A = gi.draw_bf16(M, K, gi.Dist("normal", 1.0), 440)
+    B = gi.draw_bf16(N, K, gi.Dist("normal", 4.0 / K), 441)
+    bias = gi.draw_bf16(N, 1, gi.Dist("normal", 1.0), 442).reshape(N)
+    ref, absdot = oracle.gemm_ref(A, B)
+    z = oracle.epilogue(ref, bias, 0)
+    fz = oracle.epilogue(ref, bias, 3)
+    dA, dB, dbias = to_dev_bf16(A), to_dev_bf16(B), to_dev_bf16(bias)
+    s = torch.cuda.current_stream().cuda_stream
+    for out_dtype in (gi.OUT_BF16, gi.OUT_F32):
+        dD, ldd = empty_out(M, N, out_dtype)
+        rc = g.gemm_bf16_tn_bias_act(M, N, K, dA.data_ptr(), K, dB.data_ptr(), K, 0, 0,
+                                     dD.data_ptr(), ldd, 1.0, 0.0, out_dtype, dbias.data_ptr(), 0, 3, s)
+        assert rc == 0 and g.gemm_get_status(s) == 0, g.last_error()
+        info = g.last_launch_info()
+        assert info["k_parts"] == 4, info
+        got = oracle.decode_out(from_dev(dD, out_dtype), out_dtype)
+        bnd = oracle.bound_act(z, fz, absdot, out_dtype, 3)
+        err = np.abs(got - fz)
+        assert np.all(err <= bnd), float(np.max(err / bnd))
 
 
 @pytest.mark.parametrize("pref", [4, 8])
