@@ -67,3 +67,22 @@ def test_committed_entries_are_consistent():
         assert len(e["source_hash"]) == 16 and int(e["source_hash"], 16) >= 0, name
         assert e["dram_bytes_per_launch"] == e["dram_read_bytes"] + e["dram_write_bytes"], name
         assert "--clock-control none" in e["command"], name
+
+
+def test_clock_summary_reads_only_the_timed_window():
+    """Median SM clock, the maximum clock and every active slowdown reason of
+    the samples inside [t0, t1]; samples outside it and malformed lines do not
+    count."""
+    c = bench.ClockSampler(0)
+    na, a = "Not Active", "Active"
+    c.lines = [
+        (9.0, f"0, 1000, 2070, 500.0, 0x1, {na}, {na}, {a}, {na}"),        # before the window
+        (10.0, f"0, 2070, 2070, 1300.5, 0x0, {na}, {na}, {na}, {na}"),
+        (10.1, f"0, 1965, 2070, 1398.0, 0x4, {na}, {na}, {na}, {a}"),
+        (10.2, "0, [N/A], 2070, 1390.0, 0x4, Not Active"),                  # malformed
+        (10.3, f"0, 1950, 2070, 1401.0, 0x4, {na}, {na}, {na}, {a}"),
+        (12.0, f"0, 900, 2070, 300.0, 0x8, {a}, {na}, {na}, {na}"),         # after the window
+    ]
+    s = c.summary(10.0, 10.3)
+    assert s == {"sm_mhz": 1965.0, "sm_max_mhz": 2070.0, "reasons": ["sw_power_cap"], "samples": 3}
+    assert c.summary(20.0, 21.0) == {"sm_mhz": None, "sm_max_mhz": None, "reasons": [], "samples": 0}
