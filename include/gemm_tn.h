@@ -134,8 +134,11 @@ typedef struct gemm_tn_config {
                                at least 64 k-blocks, else 2 when the tiles times 2 fit and K holds at
                                least 128, else 1), 1 = no split.  Capped at launch
                                so that every part has a co-resident cluster and at K's k-blocks;
-                               ignored with CLC, a grid override or a fused epilogue
-                               (gemm_bf16_tn_bias_act).  Inside a stream capture that
+                               ignored with CLC or a grid override.  The fused-epilogue calls
+                               (gemm_bf16_tn_bias_act, gemm_fp8_tn_bias_act), which take no
+                               config, keep the automatic choice only when it is four parts
+                               and K holds at least 128 k-blocks, and run unsplit otherwise.
+                               Inside a stream capture that
                                would have to grow the stream's split workspace, the call runs
                                unsplit (the skinny path returns an error there instead) */
   int l2_hints;             /* tiled paths, single problem: L2 eviction priorities of the kernel's
