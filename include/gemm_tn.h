@@ -95,15 +95,20 @@ typedef enum {
   GEMM_PATH_AUTO = 0,   /* choose by shape */
   GEMM_PATH_1SM = 1,    /* persistent tiled kernel, 128x256 tile, one CTA per SM */
   GEMM_PATH_2SM = 2,    /* persistent tiled kernel, 256x256 tile per CTA pair */
-  GEMM_PATH_SKINNY = 3  /* M <= 256: swap-AB stream-K HBM streaming of B (the tokens are MMA N);
-                           automatic for M <= 32; for 32 < M <= 64 when each tile is split into
-                           at most two k-parts and B (N x K) is at least 32 MiB, or into at most
-                           four with K at least 64 k-blocks; for 64 < M <= 128 when B is at least
-                           32 MiB, N <= 8192, tiles are split at most in two, and N = 8192 or K
-                           holds at least 128 k-blocks (k-block: 64 bf16 or 128 fp8 elements).
-                           AUTO otherwise takes pair tiles (2SM) when B is at least 32 MiB and
-                           M > 128 or the 1-SM tiles would fill at most half of the SMs, or
-                           when M > 128 with more than 64 tiles of 128x256; else 1SM */
+  GEMM_PATH_SKINNY = 3  /* M <= 256: swap-AB stream-K HBM streaming of B (the tokens are MMA N).
+                           AUTO, with kb = K's k-blocks (64 bf16 or 128 fp8 elements), "B large"
+                           = B (N x K) of at least 32 MiB, and "parts" = the equal k-parts per
+                           tile the streaming kernel would use (0 where it would take stream-K
+                           ranges instead):
+                           - M <= 32: SKINNY, except 1SM for kb <= 16 with 1024 <= N <= 4096;
+                           - 32 < M <= 64, parts >= 1: SKINNY when B is large with parts <= 2
+                             (but not for N <= 4096 with kb >= 64), or when kb >= 64 and
+                             N > 4096;
+                           - 64 < M <= 128: SKINNY when B is large, 1 <= parts <= 2,
+                             4096 < N <= 8192, and kb >= 64 (kb >= 32 up to M = 96);
+                           - otherwise 2SM when M > 128 and B is large or the 128x256 tiles
+                             number more than 64, or when M <= 128, B is large, those tiles
+                             fill at most half of the SMs and kb > 32; else 1SM */
 } gemm_path;
 
 /* Overrides for gemm_bf16_tn_ex (benchmarks, ablations, tests).
