@@ -131,7 +131,9 @@ typedef struct gemm_tn_config {
                                64-row tiles fit one wave and M > 32 (or M > 16 and 128-row tiles would
                                be split into 4 or more k-parts), else 128 */
   int skinny_kgroup;        /* skinny path: k-blocks per ring stage, loaded as one TMA box per operand:
-                               1, 2 or 4; 0 = auto (32 KiB boxes of B while 4 stages fit).  Values
+                               1, 2 or 4; 0 = auto (the largest of 4, 2, 1 that leaves at least 3
+                               ring stages and does not exceed K's k-blocks; 1 for 128-row tiles
+                               with more than 64 tokens).  Values
                                above 1 apply only when K is a whole number of k-blocks (64 bf16 or
                                128 fp8 elements); otherwise the path uses 1 */
   int tiled_k_parts;        /* tiled paths, single problem, static scheduler: k-parts per tile, 0..4;
