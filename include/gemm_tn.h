@@ -34,17 +34,20 @@
  * Degenerate shapes: M == 0 or N == 0 returns GEMM_OK with no launch;
  * K == 0 gives D = beta * C (or zeros).
  *
- * Library-owned memory: the skinny path (M <= 256) uses an fp32 partial-sum
- * workspace and arrival counters, allocated on the first such call for a
- * (device, stream) pair and kept until gemm_shutdown().  That first call
- * must not happen during stream capture.  Calls on different streams use
- * different workspaces.
+ * Library-owned memory: the skinny path (M <= 256) and the tiled k-split
+ * use an fp32 partial-sum workspace and arrival counters, allocated (or
+ * grown) on the first call for a (device, stream) pair that needs them and
+ * kept until gemm_shutdown().  A skinny call that would allocate or grow it
+ * during stream capture returns an error; a tiled call runs unsplit
+ * instead.  Calls on different streams use different workspaces.
  *
  * Launch: kernels are launched with programmatic stream serialisation, so
  * their set-up (barrier initialisation, Tensor Memory allocation) may overlap
  * the tail of the previous kernel on the stream.  Each kernel waits for the
  * previous kernel's completion (griddepcontrol.wait) before its first global
- * memory access, so stream order is preserved for inputs and outputs.
+ * memory access, so stream order is preserved for inputs and outputs.  The
+ * one exception is opt-in: with gemm_tn_config.b_static the skinny kernel
+ * loads its first ring of B before that wait.
  *
  * Thread safety: calls may come from several host threads; the last-error
  * string is per thread.
