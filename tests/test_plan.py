@@ -187,3 +187,55 @@ def test_plan_argument_errors():
     assert g.gemm_plan(16, 64, 64, 2, 152)[0] == g.GEMM_ERR_INVALID_VALUE
     rc, info = g.gemm_plan(0, 64, 64)
     assert rc == 0 and info["path"] == 0
+
+
+# The automatic path as the header (gemm_path) states it, restated here so
+# that the documentation and the code cannot drift apart.
+def _split_parts(tiles, sms):
+    if tiles < 1 or tiles > sms:
+        return 0
+    s = sms // tiles
+    if s >= 4:
+        return 4
+    return s if 5 * tiles * s >= 4 * sms else 0
+
+
+def _equal_parts(N, np_, sms):
+    s64 = _split_parts(-(-N // 64), sms)
+    s128 = _split_parts(-(-N // 128), sms)
+    bm = 64 if (s64 >= 1 and np_ >= 48) or (s64 >= 1 and np_ >= 32 and s128 >= 4) else 128
+    return _split_parts(-(-N // bm), sms)
+
+
+def _documented_path(M, N, K, fp8, sms=152):
+    if K == 0:
+        return P1
+    kb = -(-K // (128 if fp8 else 64))
+    large = N * K * (1 if fp8 else 2) >= 32 << 20
+    parts = _equal_parts(N, -(-M // 16) * 16, sms) if M <= 256 else 0
+    tiles = -(-M // 128) * -(-N // 256)
+    if M <= 32:
+        return P1 if kb <= 16 and 1024 <= N <= 4096 else S
+    if M <= 64 and parts >= 1 and ((large and parts <= 2 and not (N <= 4096 and kb >= 64)) or
+                                   (kb >= 64 and N > 4096)):
+        return S
+    if 64 < M <= 128 and large and 1 <= parts <= 2 and 4096 < N <= 8192 and (kb >= 64 or (M <= 96 and kb >= 32)):
+        return S
+    if M > 128 and (large or tiles > 64):
+        return P2
+    if M <= 128 and large and 2 * tiles <= sms and kb > 32:
+        return P2
+    return P1
+
+
+def test_automatic_path_follows_the_documented_rule():
+    bad = []
+    for fp8 in (0, 1):
+        for M in (1, 16, 31, 32, 33, 48, 64, 65, 80, 96, 97, 112, 128, 129, 192, 256, 257, 1024):
+            for N in (256, 1024, 2048, 4096, 4352, 6144, 8192, 8448, 16384, 28672):
+                for K in (0, 256, 1000, 1024, 2048, 2056, 4096, 8192):
+                    got = plan(M, N, K, fp8)["path"]
+                    want = _documented_path(M, N, K, fp8)
+                    if got != want:
+                        bad.append((M, N, K, fp8, got, want))
+    assert not bad, bad[:10]
