@@ -239,3 +239,31 @@ def test_automatic_path_follows_the_documented_rule():
                     if got != want:
                         bad.append((M, N, K, fp8, got, want))
     assert not bad, bad[:10]
+
+
+def test_tiled_split_and_slices_follow_the_documented_rules():
+    """gemm_tn_config.tiled_k_parts and .tail_slices at 0 (automatic), as the
+    header states them: four k-parts when four per tile fit one round of
+    clusters and K holds at least 64 k-blocks, else two when two fit and K
+    holds at least 128, else none; without a split, tiles that fill less than
+    one round are cut into the most slices (4, then 2) that still fit it."""
+    bad = []
+    for fp8 in (0, 1):
+        for M in (129, 256, 300, 512, 1024, 2048, 4096):
+            for N in (256, 1024, 2048, 4096, 8192, 28672):
+                for K in (64, 1024, 4096, 8192, 16384):
+                    p = plan(M, N, K, fp8)
+                    if p["path"] not in (P1, P2):
+                        continue
+                    cg = p["path"]
+                    clusters = 152 // cg
+                    tiles = -(-M // (128 * cg)) * -(-N // 256)
+                    kb = -(-K // (128 if fp8 else 64))
+                    parts = 4 if 4 * tiles <= clusters and kb >= 64 else (
+                        2 if 2 * tiles <= clusters and kb >= 128 else 1)
+                    slices = 1
+                    if parts == 1 and tiles < clusters:
+                        slices = 4 if 4 * tiles <= clusters else (2 if 2 * tiles <= clusters else 1)
+                    if (p["k_parts"], p["tail_slices"]) != (parts, slices):
+                        bad.append((M, N, K, fp8, cg, p["k_parts"], p["tail_slices"], parts, slices))
+    assert not bad, bad[:10]
