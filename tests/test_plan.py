@@ -267,3 +267,31 @@ def test_tiled_split_and_slices_follow_the_documented_rules():
                     if (p["k_parts"], p["tail_slices"]) != (parts, slices):
                         bad.append((M, N, K, fp8, cg, p["k_parts"], p["tail_slices"], parts, slices))
     assert not bad, bad[:10]
+
+
+def test_skinny_tile_rows_and_kgroup_follow_the_documented_rules():
+    """gemm_tn_config.skinny_bm and .skinny_kgroup at 0, as the header states
+    them: 64-row tiles where they fit one wave and M > 32 (or M > 16 with
+    128-row tiles split into 4 or more parts); k-groups of 4, 2 or 1 k-blocks
+    that leave at least 3 ring stages and do not exceed K's k-blocks, 1 for a
+    partial last k-block and for 128-row tiles of more than 64 tokens."""
+    bad = []
+    for fp8 in (0, 1):
+        kbe = 128 if fp8 else 64
+        for M in (1, 16, 17, 32, 33, 48, 64, 65, 96, 128, 160, 256):
+            for N in (1024, 2048, 4096, 8192, 16384, 28672):
+                for K in (64, 128, 256, 1000, 4096, 8192):
+                    p = plan(M, N, K, fp8, path=S)
+                    np_ = -(-M // 16) * 16
+                    s64 = _split_parts(-(-N // 64), 152)
+                    s128 = _split_parts(-(-N // 128), 152)
+                    bm = 64 if (s64 >= 1 and np_ >= 48) or (s64 >= 1 and np_ >= 32 and s128 >= 4) else 128
+                    kg, kb = p["skinny_kgroup"], -(-K // kbe)
+                    ok = p["tile_m"] == bm and kg in (1, 2, 4) and kg <= max(1, kb) and p["skinny_stages"] >= 2
+                    if K % kbe or (np_ > 64 and bm == 128):
+                        ok = ok and kg == 1
+                    elif kg > 1:
+                        ok = ok and p["skinny_stages"] >= 3
+                    if not ok:
+                        bad.append((M, N, K, fp8, p["tile_m"], kg, p["skinny_stages"], bm))
+    assert not bad, bad[:10]
