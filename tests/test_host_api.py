@@ -62,6 +62,15 @@ def test_no_torch_or_oracle_in_product_sources():
     (dict(ldd=20, N=20), g.GEMM_ERR_MISALIGNED),        # 40 B rows of bf16
     (dict(M=0), g.GEMM_OK),                             # empty: no launch
     (dict(N=0), g.GEMM_OK),
+    (dict(M=1 << 31), g.GEMM_ERR_INVALID_VALUE),        # sizes below 2^31
+    (dict(K=1 << 31, lda=1 << 31, ldb=1 << 31), g.GEMM_ERR_INVALID_VALUE),
+    (dict(B=0), g.GEMM_ERR_INVALID_VALUE),              # K > 0 needs A and B
+    (dict(ldb=48), g.GEMM_ERR_INVALID_VALUE),           # ldb < K
+    (dict(beta=0.5, C=0x4000, ldc=32), g.GEMM_ERR_INVALID_VALUE),   # ldc < N
+    (dict(beta=0.5, C=0x4008, ldc=64), g.GEMM_ERR_MISALIGNED),      # C read: 16-byte base
+    (dict(beta=0.5, C=0x4000, ldc=68), g.GEMM_ERR_MISALIGNED),      # C rows of 136 B
+    (dict(out_dtype=1, ldd=66), g.GEMM_ERR_MISALIGNED), # fp32 rows of 264 B
+    (dict(B=0x2004), g.GEMM_ERR_MISALIGNED),
 ])
 def test_validation_before_any_device_call(lib, kw, code):
     a = dict(M=64, N=64, K=64, A=0x1000, lda=64, B=0x2000, ldb=64, C=0, ldc=0, D=0x3000, ldd=64,
