@@ -236,3 +236,45 @@ def test_fp8_bias_act_rejects_before_any_device_call(lib):
     assert g.gemm_fp8_tn_bias_act(*a, 2, *tail, 0x4000, 0, 1, 0) == g.GEMM_ERR_INVALID_VALUE
     assert g.gemm_fp8_tn_bias_act(*a, 0, *tail, 0x4000, 0, 9, 0) == g.GEMM_ERR_INVALID_VALUE
     assert g.gemm_fp8_tn_bias_act(*a, 0, *tail, 0x4002, 1, 1, 0) == g.GEMM_ERR_MISALIGNED
+
+
+_BASE = (64, 64, 64, 0x1000, 64, 0x2000, 64, 0, 0, 0x3000, 64, 1.0, 0.0, 0)
+
+
+@pytest.mark.parametrize("bias,bias_dtype,act,code", [
+    (0x4000, 0, 7, g.GEMM_ERR_INVALID_VALUE),     # unknown activation
+    (0x4000, 0, -1, g.GEMM_ERR_INVALID_VALUE),
+    (0x4000, 5, 1, g.GEMM_ERR_INVALID_VALUE),     # unknown bias dtype
+    (0x4002, 1, 1, g.GEMM_ERR_MISALIGNED),        # fp32 bias on a 2-byte boundary
+    (0x4001, 0, 1, g.GEMM_ERR_MISALIGNED),        # bf16 bias on an odd address
+])
+def test_bias_act_validation_before_any_device_call(lib, bias, bias_dtype, act, code):
+    assert g.gemm_bf16_tn_bias_act(*_BASE, bias, bias_dtype, act, 0) == code
+    assert g.last_error() != ""
+
+
+@pytest.mark.parametrize("kw,code", [
+    (dict(fp8_format=2), g.GEMM_ERR_INVALID_VALUE),
+    (dict(fp8_format=-1), g.GEMM_ERR_INVALID_VALUE),
+    (dict(lda=72), g.GEMM_ERR_MISALIGNED),          # one-byte rows must be multiples of 16 elements
+    (dict(ldb=88), g.GEMM_ERR_MISALIGNED),
+    (dict(lda=32), g.GEMM_ERR_INVALID_VALUE),       # lda < K
+    (dict(A=0x1008), g.GEMM_ERR_MISALIGNED),
+    (dict(out_dtype=3), g.GEMM_ERR_INVALID_VALUE),
+])
+def test_fp8_validation_before_any_device_call(lib, kw, code):
+    a = dict(M=64, N=64, K=64, A=0x1000, lda=64, B=0x2000, ldb=64, fp8_format=0, scale_a=1.0, scale_b=1.0,
+             C=0, ldc=0, D=0x3000, ldd=64, alpha=1.0, beta=0.0, out_dtype=0, stream=0)
+    a.update(kw)
+    assert g.gemm_fp8_tn(*a.values()) == code
+    assert g.last_error() != ""
+
+
+def test_fp8_bias_act_validation_before_any_device_call(lib):
+    a = (64, 64, 64, 0x1000, 64, 0x2000, 64, 0, 1.0, 1.0, 0, 0, 0x3000, 64, 1.0, 0.0, 0)
+    assert g.gemm_fp8_tn_bias_act(*a, 0x4000, 0, 9, 0) == g.GEMM_ERR_INVALID_VALUE
+    assert g.gemm_fp8_tn_bias_act(*a, 0x4000, 2, 1, 0) == g.GEMM_ERR_INVALID_VALUE
+    assert g.gemm_fp8_tn_bias_act(*a, 0x4002, 1, 1, 0) == g.GEMM_ERR_MISALIGNED
+    b = list(a)
+    b[7] = 3                                        # fp8_format
+    assert g.gemm_fp8_tn_bias_act(*b, 0, 0, 0, 0) == g.GEMM_ERR_INVALID_VALUE
