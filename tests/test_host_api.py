@@ -278,3 +278,23 @@ def test_fp8_bias_act_validation_before_any_device_call(lib):
     b = list(a)
     b[7] = 3                                        # fp8_format
     assert g.gemm_fp8_tn_bias_act(*b, 0, 0, 0, 0) == g.GEMM_ERR_INVALID_VALUE
+
+
+@pytest.mark.parametrize("kw,code", [
+    (dict(M=65), g.GEMM_ERR_INVALID_VALUE),          # 1 <= M <= 64
+    (dict(M=0), g.GEMM_ERR_INVALID_VALUE),
+    (dict(N=131072 + 16, ldd=131072 + 16), g.GEMM_ERR_INVALID_VALUE),   # fixed scratch: N <= 131072
+    (dict(K=0), g.GEMM_ERR_INVALID_VALUE),
+    (dict(out_dtype=2), g.GEMM_ERR_INVALID_VALUE),
+    (dict(B=0), g.GEMM_ERR_INVALID_VALUE),
+    (dict(beta=1.0), g.GEMM_ERR_INVALID_VALUE),        # C is NULL
+    (dict(ldd=32), g.GEMM_ERR_INVALID_VALUE),
+    (dict(lda=68), g.GEMM_ERR_MISALIGNED),
+    (dict(D=0x3008), g.GEMM_ERR_MISALIGNED),
+])
+def test_noalloc_validation_before_any_device_call(lib, kw, code):
+    a = dict(M=16, N=64, K=64, A=0x1000, lda=64, B=0x2000, ldb=64, C=0, ldc=0, D=0x3000, ldd=64,
+             alpha=1.0, beta=0.0, out_dtype=0, stream=0)
+    a.update(kw)
+    assert g.gemm_bf16_tn_skinny_noalloc(*a.values()) == code
+    assert g.last_error() != ""
