@@ -298,3 +298,21 @@ def test_noalloc_validation_before_any_device_call(lib, kw, code):
     a.update(kw)
     assert g.gemm_bf16_tn_skinny_noalloc(*a.values()) == code
     assert g.last_error() != ""
+
+
+@pytest.mark.parametrize("args,code", [
+    ((64, 3, 0, 16, 2, 0x1000), g.GEMM_ERR_INVALID_VALUE),     # cta_group not 1 or 2
+    ((8, 1, 0, 16, 2, 0x1000), g.GEMM_ERR_INVALID_VALUE),      # n below 16
+    ((72, 1, 0, 16, 2, 0x1000), g.GEMM_ERR_INVALID_VALUE),     # n not a multiple of 16
+    ((272, 1, 0, 16, 2, 0x1000), g.GEMM_ERR_INVALID_VALUE),    # n above 256
+    ((64, 1, 0, 0, 2, 0x1000), g.GEMM_ERR_INVALID_VALUE),      # reps below 1
+    ((64, 1, 0, (1 << 24) + 1, 2, 0x1000), g.GEMM_ERR_INVALID_VALUE),
+    ((64, 2, 0, 16, 3, 0x1000), g.GEMM_ERR_INVALID_VALUE),     # grid not a multiple of the pair
+    ((64, 1, 0, 16, 1025, 0x1000), g.GEMM_ERR_INVALID_VALUE),
+    ((64, 1, 0, 16, 2, 0), g.GEMM_ERR_MISALIGNED),             # NULL output
+    ((64, 1, 0, 16, 2, 0x1004), g.GEMM_ERR_MISALIGNED),        # output not 8-byte aligned
+])
+def test_mma_rate_argument_errors(lib, args, code):
+    n, cg, fp8, reps, grid, out = args
+    assert g.gemm_mma_rate(n, cg, fp8, reps, grid, out, 0) == code
+    assert g.last_error() != ""
